@@ -1,0 +1,218 @@
+/*
+ * muonclip.h - C ABI of the GB300 (sm_103a) MuonClip optimizer step.
+ *
+ * MuonClip = the Muon update followed by per-head QK-Clip.  Sources, cited by
+ * page title and section:
+ *   [K2-internals] "Kimi K2 内部机制" (LLM-101-CN): "Algorithm 1 MuonClip
+ *                  Optimizer", "核心数学" (S_max, gamma), "MLA 的特殊处理".
+ *   [K2-notes]     "Kimi K2: Open Agentic Intelligence" notes, section 3.2
+ *                  MuonClip (pseudocode muonclip_step).
+ *   [K2-explained] "Kimi K2, explained": "Pretraining with MuonClip".
+ *   [K2-zhihu]     zhihu Q&A on K2: MuonClip formula written with msign.
+ *
+ * Conventions for every call:
+ *   - All pointers inside mc_mat / mc_attn_desc / mc_clip_seg are DEVICE
+ *     pointers owned by the caller.  Descriptor arrays themselves (mc_mat*,
+ *     mc_clip_seg*, mc_clip_layer*) are HOST memory, read only during the call.
+ *   - Matrices are row-major: element (r, c) lives at ptr[r * ld + c], with
+ *     ld >= cols, ld in elements.  Weights are stored [out, in].
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  The library allocates no device memory: scratch comes
+ *     from the caller's `workspace` (size from the matching *_workspace_size).
+ *   - Argument, shape, dtype and alignment errors are detected on the host
+ *     before any launch; the call then returns MC_ERR_INVALID_ARG or
+ *     MC_ERR_UNSUPPORTED and launches nothing.  A failed launch returns
+ *     MC_ERR_CUDA.  mc_last_error() returns a thread-local message for the last
+ *     non-OK return.
+ *   - Data-dependent conditions (non-finite values, a device wait that ran
+ *     out of time) are reported through the optional device word `status`:
+ *     the kernels OR MC_STATUS_* bits into it; the caller reads it after
+ *     synchronising the stream.  The library never traps or asserts on device.
+ */
+#ifndef MUONCLIP_H
+#define MUONCLIP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* mc_stream_t; /* same object as cudaStream_t */
+
+typedef enum {
+  MC_OK = 0,
+  MC_ERR_INVALID_ARG = 1,  /* bad pointer, shape, dtype, stride or value   */
+  MC_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement  */
+  MC_ERR_WORKSPACE = 3,    /* workspace missing, misaligned or too small   */
+  MC_ERR_CUDA = 4,         /* a CUDA runtime/driver call or launch failed  */
+  MC_ERR_NONFINITE = 5,    /* reserved for host-side reporting of status   */
+  MC_ERR_TIMEOUT = 6       /* reserved for host-side reporting of status   */
+} mc_status;
+
+/* Bits OR-ed into the optional device status word. */
+#define MC_STATUS_NONFINITE_UPDATE 1  /* NaN/Inf in M, G or the NS result  */
+#define MC_STATUS_NONFINITE_LOGIT  2  /* NaN/Inf among the attention logits */
+#define MC_STATUS_NONFINITE_SMAX   4  /* NaN/Inf S_max given to the clip     */
+#define MC_STATUS_TIMEOUT          8  /* a bounded device wait gave up       */
+
+typedef enum { MC_F32 = 0, MC_BF16 = 1 } mc_dtype;
+
+/* Arithmetic of the Newton-Schulz products.
+ *   MC_NS_SPLIT_BF16: tcgen05 tensor cores; every operand is split into a
+ *     bf16 pair (hi + lo) and each product is hi*hi + hi*lo + lo*hi with fp32
+ *     accumulation; iterates are stored as (hi, lo) pairs (~16 significand
+ *     bits).  Default for bf16 weights.
+ *   MC_NS_BF16: tcgen05, one bf16 product, bf16 iterates (fastest, ~1e-1
+ *     max-abs / 1e-2 RMS deviation from exact arithmetic).
+ *   MC_NS_FP32: CUDA-core fp32 products and fp32 iterates.  Default for fp32
+ *     weights.
+ *   MC_NS_AUTO: SPLIT_BF16 when every weight is bf16, else FP32. */
+typedef enum { MC_NS_AUTO = 0, MC_NS_SPLIT_BF16 = 1, MC_NS_BF16 = 2, MC_NS_FP32 = 3 } mc_ns_precision;
+
+typedef struct {
+  void* ptr;      /* device pointer, 16-byte aligned                    */
+  int32_t dtype;  /* mc_dtype                                           */
+  int32_t _pad;
+  int64_t rows;   /* >= 1                                               */
+  int64_t cols;   /* >= 1                                               */
+  int64_t ld;     /* leading dimension in elements, >= cols, ld*size%16==0 */
+} mc_mat;
+
+/* Hyper-parameters of one MuonClip step ([K2-internals] Algorithm 1;
+ * [K2-notes] 3.2 pseudocode defaults: mu 0.95, weight_decay 0.1, tau 100). */
+typedef struct {
+  float mu;            /* momentum coefficient                               */
+  float lr;            /* learning rate eta_t                                */
+  float weight_decay;  /* decoupled weight decay lambda                      */
+  float rms_scale;     /* 0.2: O_t = NS(M_t) * sqrt(max(n,m)) * rms_scale    */
+  int32_t ns_steps;    /* Newton-Schulz iterations (5), 0..32                */
+  float ns_a, ns_b, ns_c; /* X <- a X + (b A + c A^2) X, A = X X^T          */
+  float ns_eps;        /* X0 = M / (||M||_F + ns_eps)                        */
+  float tau;           /* QK-Clip threshold (> 0)                            */
+  float alpha;         /* MHA split: W_q by gamma^alpha, W_k by gamma^(1-alpha) */
+  int32_t ns_precision;/* mc_ns_precision                                    */
+} mc_hparams;
+
+/* One head-blocked row segment of a weight that QK-Clip rescales.  Head h
+ * owns rows [head_row_offset + h*head_row_stride, ... + rows_per_head) of w;
+ * when S_max^h > tau those rows are multiplied by gamma_h^exponent, where
+ * gamma_h = tau / S_max^h ([K2-internals] "核心数学", "MLA 的特殊处理";
+ * Algorithm 1 QK-Clip branch).  MHA: W_q exponent alpha, W_k 1 - alpha.
+ * MLA: q^C rows 0.5, k^C rows 0.5, q^R rows 1.0; the shared rotary key k^R
+ * gets no segment, so it is never touched. */
+typedef struct {
+  mc_mat w;                /* bf16 or f32 weight, updated in place */
+  int64_t head_row_offset;
+  int64_t head_row_stride;
+  int64_t rows_per_head;
+  float exponent;          /* in [0, 4] */
+  int32_t _pad;
+} mc_clip_seg;
+
+/* One attention layer's clip: S_max per head (device, [H]) and its segments. */
+typedef struct {
+  const float* smax;       /* device [H], S_max^h from this step's forward  */
+  int32_t H;
+  int32_t nsegs;
+  const mc_clip_seg* segs; /* host array of nsegs                           */
+  float* gamma_out;        /* device [H] or NULL: gamma_h (1 when no clip)  */
+  int32_t* nclipped;       /* device int or NULL: heads clipped in layer    */
+} mc_clip_layer;
+
+/* Query/key features of one attention layer, for the per-head max logit.
+ * Logit(b, h, i, j) = q_{b,i,h} . k_{b,j,h} with
+ *   q_{b,i,h} = q[b*q_strides[0] + i*q_strides[1] + h*q_strides[2] + t],
+ *               t in [0, d_head + d_shared)
+ *   k_{b,j,h} = [ k[b*k_strides[0] + j*k_strides[1] + h*k_strides[2] + t],
+ *                   t in [0, d_head)  ||
+ *                 k_shared[b*ks_strides[0] + j*ks_strides[1] + t],
+ *                   t in [0, d_shared) ]
+ * MHA: d_shared = 0, k_shared = NULL.  MLA: q = [q^C || q^R] per head,
+ * k = k^C (head-specific), k_shared = k^R (one rotary key for all heads).
+ * Strides are in elements; the feature index is contiguous. */
+typedef struct {
+  int32_t B, S, H;
+  int32_t d_head;          /* head-specific q.k length (MLA: d_nope)        */
+  int32_t d_shared;        /* shared rotary length (MLA: d_rope), or 0      */
+  int32_t dtype;           /* mc_dtype of q, k, k_shared                    */
+  int32_t causal;          /* 1: max over j <= i only                       */
+  float scale;             /* logit scale, 1/sqrt(d_head + d_shared)        */
+  const void* q;
+  const void* k;
+  const void* k_shared;
+  int64_t q_strides[3];    /* batch, sequence, head                         */
+  int64_t k_strides[3];    /* batch, sequence, head                         */
+  int64_t ks_strides[2];   /* batch, sequence                               */
+} mc_attn_desc;
+
+/* Fill *hp with the defaults named above (mu 0.95, lr 2e-4, weight_decay 0.1,
+ * rms_scale 0.2, 5 steps of the quintic (3.4445, -4.7750, 2.0315),
+ * ns_eps 1e-7, tau 100, alpha 0.5, MC_NS_AUTO). */
+void mc_default_hparams(mc_hparams* hp);
+
+/* Bytes of workspace that muon_newton_schulz / muonclip_step need for these
+ * `count` matrices (shapes and dtypes of M, or of W for muonclip_step). */
+mc_status mc_workspace_size(const mc_mat* M, int32_t count, const mc_hparams* hp, size_t* bytes);
+
+/* M_t = mu * M_{t-1} + G_t for each of `count` matrices, in place.
+ * [K2-internals] Algorithm 1, momentum step (M_0 = 0: pass a zeroed M).
+ * M: f32; G: f32 or bf16, same rows/cols as M.  A NaN/Inf in M_t sets
+ * MC_STATUS_NONFINITE_UPDATE. */
+mc_status muon_momentum(mc_mat* M, const mc_mat* G, int32_t count, float mu, int32_t* status,
+                        mc_stream_t stream);
+
+/* O_t = NewtonSchulz(M_t) * sqrt(max(rows, cols)) * rms_scale for each matrix.
+ * [K2-internals] Algorithm 1, orthogonalisation step; [K2-explained] symbol
+ * list (odd matrix polynomial pushing singular values toward 1).  M: f32;
+ * O: f32 or bf16, same shape as M (not in place).  The iteration runs on the
+ * orientation with rows <= cols (transposed internally when rows > cols). */
+mc_status muon_newton_schulz(const mc_mat* M, mc_mat* O, int32_t count, const mc_hparams* hp,
+                             void* workspace, size_t workspace_bytes, int32_t* status,
+                             mc_stream_t stream);
+
+/* Per-head max logit S_max^h = scale * max_{b} max_{i, j(<=i)} q.k.
+ * [K2-internals] "核心数学" (S_max^h over the batch); Algorithm 1 takes it
+ * from the forward pass.  smax: device float[H], written (accumulate = 0) or
+ * max-combined with its current contents (accumulate = 1, for several
+ * micro-batches of one step).  argmax: device int64[H] or NULL; receives the
+ * flat index (b*S + i)*S + j of the maximising pair, ties to the smallest
+ * index (requires B*S*S < 2^32; accumulate must be 0 with argmax).
+ * A NaN/Inf logit sets MC_STATUS_NONFINITE_LOGIT. */
+mc_status qk_max_logit(const mc_attn_desc* attn, float* smax, int64_t* argmax,
+                       int32_t accumulate, int32_t* status, mc_stream_t stream);
+
+/* QK-Clip for one attention layer: for every head with smax[h] > tau,
+ * gamma_h = tau / smax[h] and every segment's rows of head h are multiplied by
+ * gamma_h^exponent.  Heads with smax[h] <= tau (or NaN: also sets
+ * MC_STATUS_NONFINITE_SMAX) are untouched bit for bit.  [K2-internals]
+ * Algorithm 1 QK-Clip branch; "MLA 的特殊处理". gamma_out: device float[H] or
+ * NULL; nclipped: device int or NULL (number of heads clipped). */
+mc_status qk_clip_apply(const float* smax, int32_t H, float tau, const mc_clip_seg* segs,
+                        int32_t nsegs, float* gamma_out, int32_t* nclipped, int32_t* status,
+                        mc_stream_t stream);
+
+/* One MuonClip step ([K2-internals] Algorithm 1): for every matrix
+ * M = mu M + G; O = NS(M) sqrt(max) rms_scale; W = W - lr (O + wd W); then for
+ * every layer the per-head QK-Clip with that layer's smax (computed on the
+ * forward's pre-update weights) applied to the updated weights.
+ * W: bf16 or f32; G: f32 or bf16; M: f32 (the fp32 momentum state).
+ * Segments in `layers` must point into matrices of W (any overlap with W is
+ * allowed: the clip runs after every matrix's update). */
+mc_status muonclip_step(mc_mat* W, const mc_mat* G, mc_mat* M, int32_t count,
+                        const mc_hparams* hp, const mc_clip_layer* layers, int32_t nlayers,
+                        void* workspace, size_t workspace_bytes, int32_t* status,
+                        mc_stream_t stream);
+
+/* Thread-local description of the last non-OK return ("" if none). */
+const char* mc_last_error(void);
+
+/* Library version string. */
+const char* mc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MUONCLIP_H */

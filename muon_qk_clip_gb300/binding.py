@@ -1,0 +1,220 @@
+"""Python binding of the MuonClip C ABI, with the same call names.
+
+Each function converts torch tensors into the C descriptors (device pointers,
+shapes, strides) and calls libmuonclip.so on the current CUDA stream.  Torch
+provides device memory and streams only; no arithmetic of the method happens
+here.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+from . import abi
+from .abi import McAttnDesc, McClipLayer, McClipSeg, McHparams, McMat, check
+
+_DT = {torch.float32: abi.MC_F32, torch.bfloat16: abi.MC_BF16}
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def mat(t: torch.Tensor) -> McMat:
+    """Descriptor of a 2-D row-major tensor (unit column stride)."""
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("expected a 2-D tensor with unit column stride")
+    if t.dtype not in _DT:
+        raise ValueError(f"unsupported dtype {t.dtype}")
+    return McMat(ctypes.c_void_p(t.data_ptr()), _DT[t.dtype], 0, t.shape[0], t.shape[1],
+                 max(t.stride(0), t.shape[1]))
+
+
+def _mats(ts):
+    arr = (McMat * len(ts))()
+    for i, t in enumerate(ts):
+        arr[i] = mat(t)
+    return arr
+
+
+@dataclass
+class Hparams:
+    """Mirror of mc_hparams; defaults follow mc_default_hparams."""
+    mu: float = 0.95
+    lr: float = 2e-4
+    weight_decay: float = 0.1
+    rms_scale: float = 0.2
+    ns_steps: int = 5
+    ns_coeffs: tuple = (3.4445, -4.7750, 2.0315)
+    ns_eps: float = 1e-7
+    tau: float = 100.0
+    alpha: float = 0.5
+    ns_precision: int = abi.MC_NS_AUTO
+
+    def c(self) -> McHparams:
+        a, b, c = self.ns_coeffs
+        return McHparams(self.mu, self.lr, self.weight_decay, self.rms_scale, self.ns_steps,
+                         a, b, c, self.ns_eps, self.tau, self.alpha, self.ns_precision)
+
+
+def default_hparams() -> Hparams:
+    h = McHparams()
+    abi.load().mc_default_hparams(ctypes.byref(h))
+    return Hparams(h.mu, h.lr, h.weight_decay, h.rms_scale, h.ns_steps, (h.ns_a, h.ns_b, h.ns_c),
+                   h.ns_eps, h.tau, h.alpha, h.ns_precision)
+
+
+def workspace_size(shapes_or_tensors, hp: Hparams | None = None) -> int:
+    hp = hp or Hparams()
+    arr = (McMat * len(shapes_or_tensors))()
+    for i, s in enumerate(shapes_or_tensors):
+        r, c = (s.shape if isinstance(s, torch.Tensor) else s)
+        arr[i] = McMat(None, abi.MC_F32, 0, r, c, c)
+    n = ctypes.c_size_t(0)
+    hc = hp.c()
+    check(abi.load().mc_workspace_size(arr, len(arr), ctypes.byref(hc), ctypes.byref(n)),
+          "mc_workspace_size")
+    return n.value
+
+
+def alloc_workspace(shapes_or_tensors, hp=None, device="cuda") -> torch.Tensor:
+    n = workspace_size(shapes_or_tensors, hp)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def muon_momentum(M, G, mu: float, status=None, stream=None):
+    """M_t = mu M_{t-1} + G_t in place for every pair of matrices."""
+    lib = abi.load()
+    check(lib.muon_momentum(_mats(M), _mats(G), len(M), mu, _ptr(status), _stream(stream)),
+          "muon_momentum")
+
+
+def muon_newton_schulz(M, O, hp: Hparams | None = None, workspace=None, status=None, stream=None):
+    """O = NewtonSchulz(M) * sqrt(max(rows, cols)) * rms_scale for every matrix."""
+    hp = hp or Hparams()
+    if workspace is None:
+        workspace = alloc_workspace(M, hp, M[0].device)
+    hc = hp.c()
+    check(abi.load().muon_newton_schulz(_mats(M), _mats(O), len(M), ctypes.byref(hc),
+                                        _ptr(workspace), workspace.numel(), _ptr(status),
+                                        _stream(stream)), "muon_newton_schulz")
+
+
+def attn_desc(q, k, k_shared=None, causal=True, scale=None) -> McAttnDesc:
+    """q: [B,S,H,dq], k: [B,S,H,dk], k_shared: [B,S,dr] (dq = dk + dr); any
+    strides with a contiguous feature axis."""
+    B, S, H, dq = q.shape
+    dk = k.shape[-1]
+    dr = 0 if k_shared is None else k_shared.shape[-1]
+    if dq != dk + dr:
+        raise ValueError("q feature length must equal k + k_shared lengths")
+    if q.stride(3) != 1 or k.stride(3) != 1 or (k_shared is not None and k_shared.stride(2) != 1):
+        raise ValueError("feature axis must be contiguous")
+    if q.dtype not in _DT or k.dtype != q.dtype or (k_shared is not None and k_shared.dtype != q.dtype):
+        raise ValueError("q, k, k_shared must share a supported dtype")
+    d = McAttnDesc()
+    d.B, d.S, d.H, d.d_head, d.d_shared = B, S, H, dk, dr
+    d.dtype = _DT[q.dtype]
+    d.causal = 1 if causal else 0
+    d.scale = (1.0 / math.sqrt(dq)) if scale is None else scale
+    d.q, d.k = q.data_ptr(), k.data_ptr()
+    d.k_shared = None if k_shared is None else k_shared.data_ptr()
+    for i in range(3):
+        d.q_strides[i] = q.stride(i)
+        d.k_strides[i] = k.stride(i)
+    if k_shared is not None:
+        d.ks_strides[0], d.ks_strides[1] = k_shared.stride(0), k_shared.stride(1)
+    return d
+
+
+def qk_max_logit(q, k, k_shared=None, causal=True, scale=None, smax=None, argmax=None,
+                 accumulate=False, status=None, stream=None):
+    """Per-head max logit S_max^h; returns (smax [H] f32, argmax [H] int64 or None)."""
+    H = q.shape[2]
+    if smax is None:
+        smax = torch.empty(H, dtype=torch.float32, device=q.device)
+    d = attn_desc(q, k, k_shared, causal, scale)
+    check(abi.load().qk_max_logit(ctypes.byref(d), _ptr(smax), _ptr(argmax), int(bool(accumulate)),
+                                  _ptr(status), _stream(stream)), "qk_max_logit")
+    return smax, argmax
+
+
+@dataclass
+class ClipSegment:
+    """Rows [offset + h*stride, +rows) of `w` belong to head h; scaled by gamma^exponent."""
+    w: torch.Tensor
+    offset: int
+    stride: int
+    rows: int
+    exponent: float
+
+    def c(self) -> McClipSeg:
+        return McClipSeg(mat(self.w), self.offset, self.stride, self.rows, self.exponent, 0)
+
+
+def _segs(segs):
+    arr = (McClipSeg * max(len(segs), 1))()
+    for i, s in enumerate(segs):
+        arr[i] = s.c()
+    return arr
+
+
+def qk_clip_apply(smax, tau: float, segments, gamma_out=None, nclipped=None, status=None,
+                  stream=None):
+    """Rescale the rows of every head whose smax exceeds tau (in place)."""
+    arr = _segs(segments)
+    check(abi.load().qk_clip_apply(_ptr(smax), smax.numel(), tau, arr, len(segments),
+                                   _ptr(gamma_out), _ptr(nclipped), _ptr(status), _stream(stream)),
+          "qk_clip_apply")
+
+
+@dataclass
+class ClipLayer:
+    smax: torch.Tensor
+    segments: list
+    gamma_out: torch.Tensor | None = None
+    nclipped: torch.Tensor | None = None
+    _keep: list = field(default_factory=list, repr=False)
+
+
+def muonclip_step(W, G, M, hp: Hparams | None = None, layers=(), workspace=None, status=None,
+                  stream=None):
+    """One MuonClip step: Muon on every (W, G, M) triple, then per-head QK-Clip."""
+    hp = hp or Hparams()
+    if workspace is None:
+        workspace = alloc_workspace(W, hp, W[0].device)
+    larr = (McClipLayer * max(len(layers), 1))()
+    keep = []
+    for i, L in enumerate(layers):
+        segs = _segs(L.segments)
+        keep.append(segs)
+        larr[i] = McClipLayer(_ptr(L.smax), L.smax.numel(), len(L.segments),
+                              ctypes.cast(segs, ctypes.POINTER(McClipSeg)),
+                              _ptr(L.gamma_out), _ptr(L.nclipped))
+    hc = hp.c()
+    check(abi.load().muonclip_step(_mats(W), _mats(G), _mats(M), len(W), ctypes.byref(hc), larr,
+                                   len(layers), _ptr(workspace), workspace.numel(), _ptr(status),
+                                   _stream(stream)), "muonclip_step")
+
+
+def mha_segments(Wq, Wk, H: int, alpha: float = 0.5):
+    """QK-Clip segments of an MHA layer: head h owns rows [h d, (h+1) d)."""
+    d = Wq.shape[0] // H
+    return [ClipSegment(Wq, 0, d, d, alpha), ClipSegment(Wk, 0, d, d, 1.0 - alpha)]
+
+
+def mla_segments(W_UQ, W_UKV, H: int, d_nope=128, d_rope=64, d_v=128):
+    """QK-Clip segments of an MLA layer: q^C and k^C by sqrt(gamma), q^R by
+    gamma; the shared rotary key (W_KR) and the value rows get none."""
+    dq, dkv = d_nope + d_rope, d_nope + d_v
+    return [ClipSegment(W_UQ, 0, dq, d_nope, 0.5), ClipSegment(W_UQ, d_nope, dq, d_rope, 1.0),
+            ClipSegment(W_UKV, 0, dkv, d_nope, 0.5)]

@@ -1,0 +1,174 @@
+// Internal launcher interface between the host API (api.cpp) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mc {
+
+inline constexpr int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline constexpr int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+
+// Storage of a Newton-Schulz iterate (and of its Gram / polynomial matrices).
+enum XMode : int {
+  kXSplit = 0,  // two bf16 planes, value = hi + lo
+  kXBf16 = 1,   // one bf16 plane
+  kXF32 = 2     // one fp32 plane (hi pointer is float*)
+};
+
+constexpr int kMaxJobs = 96;     // matrices per streaming-kernel launch
+constexpr int kMaxGroups = 6;    // shape groups per tensor-core GEMM launch
+
+// ---------------------------------------------------------------- streaming
+// One matrix for the momentum / Newton-Schulz preparation kernel.  The
+// iterate is written in the orientation with rows <= cols (transposed when
+// rows > cols).
+struct PrepJob {
+  float* M;            // f32 momentum, updated in place when do_momentum
+  const void* G;       // f32 or bf16 gradient (unused without do_momentum)
+  void* xh;            // oriented iterate planes (see XMode)
+  void* xl;
+  long long ldM, ldG, ldx;
+  int rows, cols;      // original shape
+  int g_bf16;
+  int transpose;
+  int tile_begin;      // first 64x64 tile of this matrix in the launch
+  int tiles_c;         // tiles along cols of the original
+};
+
+struct PrepParams {
+  PrepJob jobs[kMaxJobs];
+  int njobs;
+  int total_tiles;
+  int do_momentum;
+  int write_x;         // 0: momentum only (public muon_momentum)
+  int xmode;
+  float mu;
+  double* partials;    // [total_tiles] sum of squares per tile, or null
+  int32_t* status;
+};
+
+// One matrix for the update / output kernel.
+struct ApplyJob {
+  const void* xh;      // final oriented iterate planes
+  const void* xl;
+  long long ldx;
+  void* out;           // W (update in place) or O (write)
+  long long ldo;
+  int rows, cols;
+  int transpose;
+  int out_bf16;
+  int tile_begin;
+  int tiles_c;
+  int mat;             // index into mat_scale
+  float scale;         // rms_scale * sqrt(max(rows, cols))
+};
+
+struct ApplyParams {
+  ApplyJob jobs[kMaxJobs];
+  int njobs;
+  int total_tiles;
+  int xmode;
+  int write_o;         // 1: out = scale * X; 0: W -= lr (scale X + wd W)
+  float lr, wd;
+  const float* mat_scale;  // per-matrix extra factor on X, or null
+  int32_t* status;
+};
+
+cudaError_t launch_prep(const PrepParams& p, cudaStream_t s);
+cudaError_t launch_apply(const ApplyParams& p, cudaStream_t s);
+// inv_norm[j] = 1 / (sqrt(sum of partials of matrix j) + eps), inv_norm_sq = square.
+// tile_begin / tile_count are HOST arrays (passed to the kernel as parameters).
+constexpr int kMaxNormMats = 1024;
+struct NormParams {
+  int begin[kMaxNormMats];
+  int count[kMaxNormMats];
+  int nmat, mat0;
+  float eps;
+  const double* partials;
+  float* inv_norm;
+  float* inv_norm_sq;
+};
+cudaError_t launch_norms(const double* partials, const int* tile_begin, const int* tile_count,
+                         int nmat, float eps, float* inv_norm, float* inv_norm_sq,
+                         cudaStream_t s);
+
+// ---------------------------------------------------------------- NS GEMMs
+// One batch of same-shape matrices for a Newton-Schulz phase:
+//   D[b] = s_b * (alpha * P[b] + beta * C[b]),  P = A-operand x B-operand
+// with P an M x N product over K.
+struct GemmGroup {
+  int M, N, K, batch;
+  int tiles_m, tiles_n;
+  int tile_begin;
+  int mat_base;           // index of batch item 0 into the s_b array
+  int b_mn_major;         // B operand stored [K, N] (N contiguous)
+  // plain pointers (SIMT path reads operands through these; the tensor-core
+  // path reads operands through tensor maps and uses these for C and D)
+  const void* a_hi; const void* a_lo; long long lda, a_bstride;
+  const void* b_hi; const void* b_lo; long long ldb, b_bstride;
+  const void* c_hi; const void* c_lo; long long ldc, c_bstride;
+  void* d_hi; void* d_lo; long long ldd, d_bstride;
+};
+
+struct alignas(64) GemmTmaps {
+  CUtensorMap a_hi[kMaxGroups], a_lo[kMaxGroups], b_hi[kMaxGroups], b_lo[kMaxGroups];
+};
+
+struct GemmParams {
+  GemmGroup g[kMaxGroups];
+  int ngroups;
+  int total_tiles;
+  int xmode;
+  float alpha, beta;
+  const float* s;         // per-matrix scale, or null
+  int32_t* status;
+};
+
+// Tensor-core path (split bf16 or bf16).  Encodes its own tensor maps.
+cudaError_t launch_ns_gemm_tc(const GemmParams& p, cudaStream_t s, char* err, size_t errlen);
+// CUDA-core fp32 path.
+cudaError_t launch_ns_gemm_f32(const GemmParams& p, cudaStream_t s);
+
+// ---------------------------------------------------------------- QK-Clip
+struct ClipSegDev {
+  void* w;
+  long long ld;
+  long long row_offset, row_stride, rows;
+  int cols;
+  int bf16;
+  float exponent;
+};
+constexpr int kMaxSegs = 16;
+struct ClipParams {
+  ClipSegDev segs[kMaxSegs];
+  int nsegs;
+  int H;
+  float tau;
+  const float* smax;
+  float* gamma_out;
+  int32_t* nclipped;
+  int32_t* status;
+};
+cudaError_t launch_clip(const ClipParams& p, cudaStream_t s);
+
+// ---------------------------------------------------------------- max logit
+struct MaxLogitParams {
+  int B, S, H, d_head, d_shared;
+  int dtype;       // 0 f32, 1 bf16
+  int causal;
+  float scale;
+  const void* q; const void* k; const void* ks;
+  long long qs[3], kst[3], kss[2];
+  float* smax;             // ordered-int scratch view when argmax is null
+  long long* argmax;       // packed (ordered value << 32 | ~index) scratch view
+  int accumulate;
+  int32_t* status;
+};
+cudaError_t launch_max_logit(const MaxLogitParams& p, cudaStream_t s, char* err, size_t errlen);
+
+// Device/properties helpers.
+int sm_count();
+
+}  // namespace mc

@@ -1,0 +1,220 @@
+"""Host-only checks of the C ABI: the library loads, exports every entry point
+include/muonclip.h declares, its struct layouts match the ctypes mirror, and
+argument errors are rejected on the host before any launch (these calls use
+fake, aligned device addresses that are never dereferenced)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from muon_qk_clip_gb300 import abi
+from muon_qk_clip_gb300.abi import McAttnDesc, McClipLayer, McClipSeg, McHparams, McMat
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "muonclip.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from muon_qk_clip_gb300 import build
+    build.build()
+    return abi.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_five_calls():
+    fns = declared_functions()
+    for name in ("muon_momentum", "muon_newton_schulz", "qk_max_logit", "qk_clip_apply",
+                 "muonclip_step", "mc_workspace_size", "mc_last_error"):
+        assert name in fns
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", abi.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r" T (\w+)$", out, flags=re.M))
+    missing = [f for f in declared_functions() if f not in exported]
+    assert not missing, missing
+    assert set(abi.SIGNATURES) <= exported
+
+
+def test_struct_layouts_match_c(tmp_path):
+    src = tmp_path / "layout.c"
+    src.write_text(f'''
+#include <stdio.h>
+#include <stddef.h>
+#include "{HEADER}"
+int main(void) {{
+  printf("%zu %zu %zu %zu %zu\\n", sizeof(mc_mat), sizeof(mc_hparams), sizeof(mc_clip_seg),
+         sizeof(mc_clip_layer), sizeof(mc_attn_desc));
+  printf("%zu %zu %zu %zu\\n", offsetof(mc_attn_desc, q), offsetof(mc_attn_desc, ks_strides),
+         offsetof(mc_clip_seg, exponent), offsetof(mc_hparams, ns_precision));
+  return 0;
+}}''')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", str(src), "-o", str(exe)], check=True)
+    sizes, offs = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")[:2]
+    assert [int(x) for x in sizes.split()] == [ctypes.sizeof(t) for t in
+                                               (McMat, McHparams, McClipSeg, McClipLayer, McAttnDesc)]
+    assert [int(x) for x in offs.split()] == [McAttnDesc.q.offset, McAttnDesc.ks_strides.offset,
+                                              McClipSeg.exponent.offset, McHparams.ns_precision.offset]
+
+
+def test_default_hparams(lib):
+    h = McHparams()
+    lib.mc_default_hparams(ctypes.byref(h))
+    assert (h.mu, h.weight_decay, h.rms_scale, h.ns_steps, h.tau, h.alpha) == pytest.approx(
+        (0.95, 0.1, 0.2, 5, 100.0, 0.5))
+    assert (h.ns_a, h.ns_b, h.ns_c) == pytest.approx((3.4445, -4.7750, 2.0315))
+    assert lib.mc_version().decode().startswith("muonclip")
+
+
+FAKE = 0x7f0000000000   # 256-byte aligned, never dereferenced
+
+
+def m(rows, cols, dtype=abi.MC_F32, ld=None, ptr=FAKE):
+    return McMat(ctypes.c_void_p(ptr), dtype, 0, rows, cols, cols if ld is None else ld)
+
+
+def arr(*ms):
+    a = (McMat * len(ms))()
+    for i, x in enumerate(ms):
+        a[i] = x
+    return a
+
+
+def hp(**kw):
+    h = McHparams()
+    abi.load().mc_default_hparams(ctypes.byref(h))
+    for k, v in kw.items():
+        setattr(h, k, v)
+    return h
+
+
+@pytest.mark.parametrize("bad,code", [
+    (m(4, 8, ptr=0), abi.MC_ERR_INVALID_ARG),                 # null
+    (m(4, 8, ptr=FAKE + 4), abi.MC_ERR_INVALID_ARG),          # misaligned
+    (m(4, 8, ld=6), abi.MC_ERR_INVALID_ARG),                  # ld < cols
+    (m(4, 6, ld=6), abi.MC_ERR_INVALID_ARG),                  # 24-byte pitch
+    (m(0, 8), abi.MC_ERR_INVALID_ARG),                        # empty
+    (m(4, 8, dtype=abi.MC_BF16), abi.MC_ERR_INVALID_ARG),     # momentum must be f32
+    (m(4, 8, dtype=7), abi.MC_ERR_INVALID_ARG),               # unknown dtype
+])
+def test_momentum_rejects_bad_matrix(lib, bad, code):
+    assert lib.muon_momentum(arr(bad), arr(m(4, 8)), 1, 0.9, None, None) == code
+    assert lib.mc_last_error().decode()
+
+
+def test_momentum_rejects_shape_mismatch_and_bad_mu(lib):
+    assert lib.muon_momentum(arr(m(4, 8)), arr(m(4, 16)), 1, 0.9, None, None) == abi.MC_ERR_INVALID_ARG
+    assert lib.muon_momentum(arr(m(4, 8)), arr(m(4, 8)), 1, float("nan"), None, None) == abi.MC_ERR_INVALID_ARG
+    assert lib.muon_momentum(arr(m(4, 8)), arr(m(4, 8)), 0, 0.9, None, None) == abi.MC_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("field,value", [("ns_steps", -1), ("ns_steps", 33), ("tau", 0.0),
+                                         ("tau", -3.0), ("alpha", 1.5), ("ns_eps", -1.0),
+                                         ("lr", float("inf")), ("ns_precision", 9)])
+def test_newton_schulz_rejects_bad_hparams(lib, field, value):
+    h = hp(**{field: value})
+    rc = lib.muon_newton_schulz(arr(m(64, 128)), arr(m(64, 128)), 1, ctypes.byref(h),
+                                ctypes.c_void_p(FAKE), 1 << 30, None, None)
+    assert rc == abi.MC_ERR_INVALID_ARG
+
+
+def test_workspace_size_and_checks(lib):
+    h = hp()
+    n = ctypes.c_size_t(0)
+    assert lib.mc_workspace_size(arr(m(64, 128), m(256, 64)), 2, ctypes.byref(h), ctypes.byref(n)) == 0
+    need = n.value
+    assert need > 4 * (64 * 128 + 64 * 256)
+    hb = hp(ns_precision=abi.MC_NS_BF16)
+    nb = ctypes.c_size_t(0)
+    lib.mc_workspace_size(arr(m(64, 128), m(256, 64)), 2, ctypes.byref(hb), ctypes.byref(nb))
+    assert nb.value < need
+    M, O = arr(m(64, 128), m(256, 64)), arr(m(64, 128), m(256, 64))
+    assert lib.muon_newton_schulz(M, O, 2, ctypes.byref(h), ctypes.c_void_p(FAKE), need - 1,
+                                  None, None) == abi.MC_ERR_WORKSPACE
+    assert lib.muon_newton_schulz(M, O, 2, ctypes.byref(h), None, need, None, None) == abi.MC_ERR_WORKSPACE
+    assert lib.muon_newton_schulz(M, O, 2, ctypes.byref(h), ctypes.c_void_p(FAKE + 16), need,
+                                  None, None) == abi.MC_ERR_WORKSPACE
+    assert lib.muon_newton_schulz(M, arr(m(64, 128), m(64, 256)), 2, ctypes.byref(h),
+                                  ctypes.c_void_p(FAKE), need, None, None) == abi.MC_ERR_INVALID_ARG
+
+
+def attn(**kw):
+    d = McAttnDesc()
+    d.B, d.S, d.H, d.d_head, d.d_shared, d.dtype, d.causal = 1, 16, 2, 64, 0, abi.MC_BF16, 1
+    d.scale = 0.125
+    d.q = d.k = FAKE
+    d.q_strides[:] = [16 * 2 * 64, 2 * 64, 64]
+    d.k_strides[:] = [16 * 2 * 64, 2 * 64, 64]
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(S=0), abi.MC_ERR_INVALID_ARG), (dict(H=0), abi.MC_ERR_INVALID_ARG),
+    (dict(d_head=0), abi.MC_ERR_INVALID_ARG), (dict(scale=0.0), abi.MC_ERR_INVALID_ARG),
+    (dict(dtype=5), abi.MC_ERR_INVALID_ARG), (dict(q=None), abi.MC_ERR_INVALID_ARG),
+    (dict(d_shared=64), abi.MC_ERR_INVALID_ARG),            # k_shared missing
+    (dict(d_head=300), abi.MC_ERR_UNSUPPORTED),
+])
+def test_max_logit_rejects(lib, kw, code):
+    d = attn(**kw)
+    assert lib.qk_max_logit(ctypes.byref(d), ctypes.c_void_p(FAKE), None, 0, None, None) == code
+
+
+def test_max_logit_argmax_rules(lib):
+    d = attn()
+    assert lib.qk_max_logit(ctypes.byref(d), ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 1,
+                            None, None) == abi.MC_ERR_INVALID_ARG          # accumulate + argmax
+    big = attn(B=2, S=65536)
+    assert lib.qk_max_logit(ctypes.byref(big), ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 0,
+                            None, None) == abi.MC_ERR_UNSUPPORTED          # index overflow
+
+
+def seg(w, off, stride, rows, e):
+    return McClipSeg(w, off, stride, rows, e, 0)
+
+
+def segarr(*ss):
+    a = (McClipSeg * len(ss))()
+    for i, s in enumerate(ss):
+        a[i] = s
+    return a
+
+
+@pytest.mark.parametrize("s,H,tau,code", [
+    (seg(m(64, 32), 0, 16, 16, 0.5), 5, 100.0, abi.MC_ERR_INVALID_ARG),   # runs past the rows
+    (seg(m(64, 32), 0, 16, 16, 0.5), 0, 100.0, abi.MC_ERR_INVALID_ARG),   # H = 0
+    (seg(m(64, 32), 0, 16, 16, 5.0), 4, 100.0, abi.MC_ERR_INVALID_ARG),   # exponent
+    (seg(m(64, 32), -1, 16, 16, 0.5), 4, 100.0, abi.MC_ERR_INVALID_ARG),  # negative offset
+    (seg(m(64, 32), 0, 16, 16, 0.5), 4, 0.0, abi.MC_ERR_INVALID_ARG),     # tau
+])
+def test_clip_rejects(lib, s, H, tau, code):
+    assert lib.qk_clip_apply(ctypes.c_void_p(FAKE), H, tau, segarr(s), 1, None, None, None, None) == code
+
+
+def test_step_rejects_mismatch_and_bad_layer(lib):
+    h = hp()
+    W, G, M = arr(m(64, 128, abi.MC_BF16)), arr(m(64, 128)), arr(m(64, 64))
+    assert lib.muonclip_step(W, G, M, 1, ctypes.byref(h), None, 0, ctypes.c_void_p(FAKE), 1 << 30,
+                             None, None) == abi.MC_ERR_INVALID_ARG
+    L = (McClipLayer * 1)()
+    L[0] = McClipLayer(None, 4, 0, None, None, None)
+    assert lib.muonclip_step(W, G, arr(m(64, 128)), 1, ctypes.byref(h), L, 1, ctypes.c_void_p(FAKE),
+                             1 << 30, None, None) == abi.MC_ERR_INVALID_ARG
+
+
+def test_binding_raises_with_message(lib):
+    with pytest.raises(abi.MuonClipError) as ei:
+        abi.check(lib.muon_momentum(arr(m(4, 8, ptr=0)), arr(m(4, 8)), 1, 0.9, None, None), "muon_momentum")
+    assert "null pointer" in str(ei.value)

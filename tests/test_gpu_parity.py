@@ -1,0 +1,385 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.
+
+Tolerances (floating point; see the design doc for their derivation):
+  * momentum:                 within 1 fp32 rounding of the exact mu*M + G
+  * Newton-Schulz, split bf16: |O - O_exact| <= 2e-2 * RMS(O_exact) before the
+                               output rounding (spec bound)
+  * Newton-Schulz, fp32:      1e-5 * RMS(O_exact)
+  * Newton-Schulz, bf16:      2.5e-1 * RMS max, 2.5e-2 * RMS root-mean-square
+  * updated weights:          |W - W_exact| <= tol * RMS(lr O) before the final
+                               rounding to the weight dtype
+  * S_max:                    relative 1e-3 (bf16 features), 1e-5 (fp32)
+  * clip mask / argmax:       exact (argmax where the oracle's top-2 gap is
+                               clear of the fp32 accumulation error)
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from muon_qk_clip_gb300 import abi, build
+from muon_qk_clip_gb300 import binding as mc
+from muon_qk_clip_gb300 import forward, synth
+from tests.gpu_helpers import assert_rounded_within, f64, padded, rms
+
+pytestmark = pytest.mark.gpu
+
+F32, BF16 = torch.float32, torch.bfloat16
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    abi.load()
+
+
+def fp32(x):
+    return float(np.float32(x))
+
+
+def new_status():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+# ------------------------------------------------------------------ momentum
+@pytest.mark.parametrize("shapes", [[(64, 64)], [(100, 77), (3, 5)], [(300, 1000), (1000, 300)]])
+@pytest.mark.parametrize("gdtype", [F32, BF16])
+def test_momentum_parity(shapes, gdtype):
+    mu = 0.95
+    Ms, Gs, ref = [], [], []
+    for i, (r, c) in enumerate(shapes):
+        M0 = synth.normal((r, c), 1.0, f"m{i}", 1)
+        G0 = synth.normal((r, c), 0.5, f"g{i}", 1).to(gdtype)
+        M = padded(r, c, F32); M.copy_(M0)
+        G = padded(r, c, gdtype); G.copy_(G0)
+        Ms.append(M); Gs.append(G)
+        ref.append(O.momentum(f64(M0), f64(G0), fp32(mu)))
+    st = new_status()
+    mc.muon_momentum(Ms, Gs, mu, status=st)
+    torch.cuda.synchronize()
+    for M, want in zip(Ms, ref):
+        assert_rounded_within(M, want, 0.0, "momentum")
+    assert st.item() == 0
+
+
+def test_momentum_flags_nonfinite():
+    M = torch.zeros(64, 64, device="cuda")
+    G = torch.zeros(64, 64, device="cuda")
+    G[3, 5] = float("nan")
+    st = new_status()
+    mc.muon_momentum([M], [G], 0.9, status=st)
+    torch.cuda.synchronize()
+    assert st.item() & abi.MC_STATUS_NONFINITE_UPDATE
+
+
+# ------------------------------------------------------------------ Newton-Schulz
+NS_CASES = {
+    "single": [(256, 512)],
+    "transposed": [(384, 256)],
+    "ragged_groups": [(200, 328), (328, 200), (64, 1000)],
+    "batched": [(512, 512), (512, 512), (512, 512), (256, 768)],
+    "tall_thin": [(1000, 64)],
+}
+
+
+def run_ns(shapes, precision, out_dtype, steps=5, seed=0):
+    Ms, Os, ref = [], [], []
+    hp = mc.Hparams(ns_precision=precision, ns_steps=steps)
+    ohp = O.Hparams(ns_steps=steps, ns_coeffs=tuple(fp32(c) for c in hp.ns_coeffs),
+                    ns_eps=fp32(hp.ns_eps), rms_scale=fp32(hp.rms_scale))
+    for i, (r, c) in enumerate(shapes):
+        M0 = synth.ns_test_matrix(r, c, seed, f"ns{i}")
+        M = M0.cuda()
+        Ms.append(M)
+        Os.append(torch.full((r, c), float("nan"), dtype=out_dtype, device="cuda"))
+        ref.append(O.muon_direction(f64(M0), ohp))
+    st = new_status()
+    mc.muon_newton_schulz(Ms, Os, hp, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    return Os, ref
+
+
+@pytest.mark.parametrize("case", list(NS_CASES))
+@pytest.mark.parametrize("out_dtype", [F32, BF16])
+def test_ns_split_bf16_parity(case, out_dtype):
+    Os, ref = run_ns(NS_CASES[case], abi.MC_NS_SPLIT_BF16, out_dtype)
+    for o, want in zip(Os, ref):
+        assert_rounded_within(o, want, 2e-2 * rms(want), f"NS split {case}")
+
+
+@pytest.mark.parametrize("case", ["single", "transposed", "ragged_groups"])
+def test_ns_fp32_parity(case):
+    Os, ref = run_ns(NS_CASES[case], abi.MC_NS_FP32, F32)
+    for o, want in zip(Os, ref):
+        assert_rounded_within(o, want, 1e-5 * rms(want), f"NS fp32 {case}")
+
+
+@pytest.mark.parametrize("case", ["single", "ragged_groups"])
+def test_ns_bf16_parity(case):
+    Os, ref = run_ns(NS_CASES[case], abi.MC_NS_BF16, F32)
+    for o, want in zip(Os, ref):
+        err = f64(o) - want
+        assert np.abs(err).max() <= 0.25 * rms(want)
+        assert rms(err) <= 2.5e-2 * rms(want)
+
+
+@pytest.mark.parametrize("steps", [0, 1, 2])
+def test_ns_few_steps(steps):
+    Os, ref = run_ns([(128, 320), (320, 128)], abi.MC_NS_SPLIT_BF16, F32, steps=steps)
+    for o, want in zip(Os, ref):
+        assert_rounded_within(o, want, 2e-2 * rms(want), f"NS {steps} steps")
+
+
+def test_ns_zero_matrix():
+    M = torch.zeros(128, 256, device="cuda")
+    Ot = torch.full((128, 256), float("nan"), device="cuda")
+    mc.muon_newton_schulz([M], [Ot])
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(Ot).item() == 0
+
+
+# ------------------------------------------------------------------ full Muon step
+def oracle_muon(W, G, M, hp):
+    ohp = O.Hparams(mu=fp32(hp.mu), lr=fp32(hp.lr), weight_decay=fp32(hp.weight_decay),
+                    rms_scale=fp32(hp.rms_scale), ns_steps=hp.ns_steps,
+                    ns_coeffs=tuple(fp32(c) for c in hp.ns_coeffs), ns_eps=fp32(hp.ns_eps))
+    return O.muon_step(f64(W), f64(G), f64(M), ohp), ohp
+
+
+@pytest.mark.parametrize("wdtype,precision,tol", [(F32, abi.MC_NS_FP32, 1e-5),
+                                                  (BF16, abi.MC_NS_SPLIT_BF16, 2e-2)])
+@pytest.mark.parametrize("warm", [False, True])
+def test_muon_step_parity(wdtype, precision, tol, warm):
+    shapes = [(256, 512), (384, 128), (96, 96)]
+    hp = mc.Hparams(ns_precision=precision)
+    W, G, M, want = [], [], [], []
+    for i, (r, c) in enumerate(shapes):
+        w = synth.normal((r, c), 0.02, f"w{i}", 3).to(wdtype)
+        g = synth.normal((r, c), 1.0, f"g{i}", 3)
+        m = synth.normal((r, c), 3.0, f"m{i}", 3) if warm else torch.zeros(r, c)
+        (Wn, Mn, Od), _ = oracle_muon(w, g, m, hp)
+        want.append((Wn, Mn, Od))
+        W.append(w.cuda()); G.append(g.cuda()); M.append(m.cuda())
+    st = new_status()
+    mc.muonclip_step(W, G, M, hp, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    for (Wn, Mn, Od), w, m in zip(want, W, M):
+        assert_rounded_within(m, Mn, 0.0, "momentum state")
+        assert_rounded_within(w, Wn, tol * rms(fp32(hp.lr) * Od), "updated W")
+
+
+def test_step_is_deterministic_and_resumable():
+    """Two runs from the same state are bit-identical; a step taken after
+    saving and reloading (M, W) equals the uninterrupted second step."""
+    hp = mc.Hparams()
+    shapes = [(256, 384), (384, 256)]
+    base = [(synth.normal(s, 0.02, f"w{i}", 4).to(BF16), synth.normal(s, 1.0, f"g{i}", 4))
+            for i, s in enumerate(shapes)]
+    G2 = [synth.normal(s, 1.0, f"h{i}", 4).cuda() for i, s in enumerate(shapes)]
+
+    def run(two_steps, reload=False):
+        W = [w.cuda() for w, _ in base]
+        G = [g.cuda() for _, g in base]
+        M = [torch.zeros(s, device="cuda") for s in shapes]
+        mc.muonclip_step(W, G, M, hp)
+        if reload:
+            W = [w.cpu().cuda() for w in W]
+            M = [m.cpu().cuda() for m in M]
+        if two_steps:
+            mc.muonclip_step(W, G2, M, hp)
+        torch.cuda.synchronize()
+        return W, M
+
+    a, b = run(True), run(True)
+    c = run(True, reload=True)
+    for x, y, z in zip(a[0] + a[1], b[0] + b[1], c[0] + c[1]):
+        assert torch.equal(x, y) and torch.equal(x, z)
+
+
+# ------------------------------------------------------------------ max logit
+ML_CASES = {
+    "tiny_fp32": dict(B=2, S=128, H=4, dk=64, dr=0, dtype=F32, causal=True),
+    "ragged_bf16": dict(B=1, S=200, H=3, dk=128, dr=0, dtype=BF16, causal=True),
+    "mla_bf16": dict(B=2, S=129, H=2, dk=128, dr=64, dtype=BF16, causal=True),
+    "noncausal": dict(B=1, S=96, H=2, dk=64, dr=0, dtype=BF16, causal=False),
+    "single_token": dict(B=3, S=1, H=2, dk=64, dr=0, dtype=BF16, causal=True),
+    "fp32_mla": dict(B=1, S=70, H=2, dk=32, dr=16, dtype=F32, causal=True),
+}
+
+
+def check_smax(s_gpu, arg_gpu, q, k, ks, causal, dtype):
+    ref, arg = O.max_logit(f64(q), f64(k), None if ks is None else f64(ks), causal=causal)
+    S = q.shape[1]
+    rel = 1e-5 if dtype == F32 else 1e-3
+    np.testing.assert_allclose(f64(s_gpu), ref, rtol=rel, atol=0)
+    if arg_gpu is not None:
+        # compare the argmax where the oracle's best beats every other pair by
+        # more than the fp32 accumulation error
+        got = arg_gpu.cpu().numpy()
+        for h in range(q.shape[2]):
+            b, i, j = arg[h]
+            flat = (b * S + i) * S + j
+            if got[h] != flat:
+                gb, rem = divmod(int(got[h]), S * S)
+                gi, gj = divmod(rem, S)
+                kv = np.concatenate([f64(k)[gb, gj, h]] + ([f64(ks)[gb, gj]] if ks is not None else []))
+                other = float(f64(q)[gb, gi, h] @ kv) / math.sqrt(q.shape[-1])
+                assert abs(other - ref[h]) <= 2e-6 * abs(ref[h]) + 1e-6, (h, got[h], flat)
+
+
+@pytest.mark.parametrize("case", list(ML_CASES))
+@pytest.mark.parametrize("with_argmax", [False, True])
+def test_max_logit_parity(case, with_argmax):
+    c = ML_CASES[case]
+    q, k, ks = synth.attention_features(c["B"], c["S"], c["H"], c["dk"] + c["dr"], c["dk"],
+                                        c["dr"], c["dtype"], seed=5, key=case)
+    qd, kd = q.cuda(), k.cuda()
+    ksd = None if ks is None else ks.cuda()
+    arg = torch.empty(c["H"], dtype=torch.int64, device="cuda") if with_argmax else None
+    st = new_status()
+    s, a = mc.qk_max_logit(qd, kd, ksd, causal=c["causal"], argmax=arg, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    check_smax(s, a, q, k, ks, c["causal"], c["dtype"])
+
+
+def test_max_logit_strided_mla_views():
+    """K^C as a strided view into the [k^C || v] projection, shared K^R."""
+    wl = synth.scaled(synth.workload("k2_mla_layer"), S=80)
+    X, W = synth.attention_inputs(wl, seed=2)
+    q, kc, kr = forward.project_mla(X, W, wl.attention.H)
+    q, kc = q[:, :, :6], kc[:, :, :6]
+    # device K^C keeps the projection's layout: a view with head stride 256
+    kv_d = torch.zeros(kc.shape[:3] + (256,), dtype=kc.dtype, device="cuda")
+    kc_d = kv_d[..., :128]
+    kc_d.copy_(kc)
+    assert kc_d.stride(2) == 256
+    s, a = mc.qk_max_logit(q.cuda(), kc_d, kr.cuda(),
+                           argmax=torch.empty(6, dtype=torch.int64, device="cuda"))
+    torch.cuda.synchronize()
+    check_smax(s, a, q, kc, kr, True, BF16)
+
+
+def test_max_logit_accumulate_over_microbatches():
+    q, k, _ = synth.attention_features(4, 64, 3, 64, 64, 0, BF16, seed=6)
+    qd, kd = q.cuda(), k.cuda()
+    full, _ = mc.qk_max_logit(qd, kd)
+    part, _ = mc.qk_max_logit(qd[:2], kd[:2])
+    mc.qk_max_logit(qd[2:], kd[2:], smax=part, accumulate=True)
+    torch.cuda.synchronize()
+    assert torch.equal(full, part)
+
+
+def test_max_logit_flags_nonfinite():
+    q, k, _ = synth.attention_features(1, 32, 2, 64, 64, 0, BF16, seed=7)
+    q[0, 5, 1, 3] = float("inf")
+    st = new_status()
+    mc.qk_max_logit(q.cuda(), k.cuda(), status=st)
+    torch.cuda.synchronize()
+    assert st.item() & abi.MC_STATUS_NONFINITE_LOGIT
+
+
+# ------------------------------------------------------------------ QK-Clip
+def test_clip_mha_parity_and_untouched_heads():
+    H, d, D, tau = 8, 16, 40, 100.0
+    Wq = synth.normal((H * d, D), 1.0, "cq", 8).to(BF16)
+    Wk = synth.normal((H * d, D), 1.0, "ck", 8).to(BF16)
+    smax = torch.tensor([50.0, 100.0, 150.0, 400.0, 0.0, -3.0, 101.0, 1e4])
+    Wq_d, Wk_d, s_d = Wq.cuda(), Wk.cuda(), smax.cuda()
+    gamma = torch.empty(H, device="cuda")
+    ncl = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mc.qk_clip_apply(s_d, tau, mc.mha_segments(Wq_d, Wk_d, H, 0.5), gamma_out=gamma, nclipped=ncl)
+    torch.cuda.synchronize()
+    out, g, mask = O.qk_clip({"Wq": f64(Wq), "Wk": f64(Wk)}, O.mha_segments(H, d, 0.5),
+                             f64(smax), tau)
+    assert ncl.item() == int(mask.sum()) == 4
+    np.testing.assert_allclose(f64(gamma), g, rtol=1e-6)
+    for name, dev, src in (("Wq", Wq_d, Wq), ("Wk", Wk_d, Wk)):
+        for h in range(H):
+            rows = slice(h * d, (h + 1) * d)
+            if not mask[h]:
+                assert torch.equal(dev[rows].cpu(), src[rows]), f"{name} head {h} changed"
+        assert_rounded_within(dev, out[name], 1e-6 * np.abs(out[name]), f"clip {name}")
+
+
+def test_clip_mla_parity_shared_key_untouched():
+    H, dn, dr, dv, ql, kl, tau = 4, 16, 8, 16, 24, 12, 100.0
+    W_UQ = synth.normal((H * (dn + dr), ql), 1.0, "uq", 9).to(BF16)
+    W_UKV = synth.normal((H * (dn + dv), kl), 1.0, "ukv", 9).to(BF16)
+    W_KR = synth.normal((dr, 40), 1.0, "kr", 9).to(BF16)
+    smax = torch.tensor([300.0, 20.0, 100.5, 99.0])
+    d_uq, d_ukv, d_kr = W_UQ.cuda(), W_UKV.cuda(), W_KR.cuda()
+    mc.qk_clip_apply(smax.cuda(), tau, mc.mla_segments(d_uq, d_ukv, H, dn, dr, dv))
+    torch.cuda.synchronize()
+    out, g, mask = O.qk_clip({"W_UQ": f64(W_UQ), "W_UKV": f64(W_UKV)},
+                             O.mla_segments(H, dn, dr, dv), f64(smax), tau)
+    assert_rounded_within(d_uq, out["W_UQ"], 1e-6 * np.abs(out["W_UQ"]), "W_UQ")
+    assert_rounded_within(d_ukv, out["W_UKV"], 1e-6 * np.abs(out["W_UKV"]), "W_UKV")
+    assert torch.equal(d_kr.cpu(), W_KR)
+    for h in range(H):
+        v = slice(h * (dn + dv) + dn, (h + 1) * (dn + dv))
+        assert torch.equal(d_ukv[v].cpu(), W_UKV[v])
+
+
+def test_clip_fp32_alpha_split():
+    H, d, D = 4, 8, 12
+    Wq = synth.normal((H * d, D), 1.0, "fq", 10)
+    Wk = synth.normal((H * d, D), 1.0, "fk", 10)
+    smax = torch.tensor([1000.0, 10.0, 250.0, 90.0])
+    dq, dk = Wq.cuda(), Wk.cuda()
+    mc.qk_clip_apply(smax.cuda(), 100.0, mc.mha_segments(dq, dk, H, 0.25))
+    torch.cuda.synchronize()
+    out, _, _ = O.qk_clip({"Wq": f64(Wq), "Wk": f64(Wk)}, O.mha_segments(H, d, 0.25),
+                          f64(smax), 100.0)
+    assert_rounded_within(dq, out["Wq"], 1e-6 * np.abs(out["Wq"]), "Wq")
+    assert_rounded_within(dk, out["Wk"], 1e-6 * np.abs(out["Wk"]), "Wk")
+
+
+def test_clip_nan_smax_flags_and_leaves_weights():
+    H, d = 2, 8
+    Wq = synth.normal((H * d, 16), 1.0, "nq", 11).to(BF16).cuda()
+    Wk = synth.normal((H * d, 16), 1.0, "nk", 11).to(BF16).cuda()
+    before = (Wq.clone(), Wk.clone())
+    st = new_status()
+    mc.qk_clip_apply(torch.tensor([float("nan"), 5.0], device="cuda"), 100.0,
+                     mc.mha_segments(Wq, Wk, H), status=st)
+    torch.cuda.synchronize()
+    assert st.item() & abi.MC_STATUS_NONFINITE_SMAX
+    assert torch.equal(Wq, before[0]) and torch.equal(Wk, before[1])
+
+
+# ------------------------------------------------------------------ MuonClip step, tiny MHA
+def test_tiny_mha_fp32_full_step():
+    """The tiny fp32 MHA workload end to end: S_max from the forward features,
+    Muon on the 256x512 matrix, then QK-Clip of heads 1 and 3."""
+    wl = synth.workload("tiny_mha_fp32")
+    X, Wa = synth.attention_inputs(wl)
+    Wm, Gm, Mm = synth.muon_inputs(wl)
+    q, k = forward.project_mha(X, Wa["Wq"], Wa["Wk"], wl.attention.H)
+    hp = mc.Hparams()
+    smax, _ = mc.qk_max_logit(q.cuda(), k.cuda())
+    ref_s, _ = O.max_logit(f64(q), f64(k))
+    np.testing.assert_allclose(f64(smax), ref_s, rtol=1e-5)
+    assert list(ref_s > 100.0) == [False, True, False, True]
+    W, G, M = [Wm["W"].cuda()], [Gm["W"].cuda()], [Mm["W"].cuda()]
+    Wq, Wk = Wa["Wq"].cuda(), Wa["Wk"].cuda()
+    layer = mc.ClipLayer(smax, mc.mha_segments(Wq, Wk, wl.attention.H))
+    mc.muonclip_step(W, G, M, hp, layers=[layer])
+    torch.cuda.synchronize()
+    (Wn, _, Od), _ = oracle_muon(Wm["W"], Gm["W"], Mm["W"], hp)
+    assert_rounded_within(W[0], Wn, 1e-5 * rms(fp32(hp.lr) * Od), "tiny W")
+    out, _, mask = O.qk_clip({"Wq": f64(Wa["Wq"]), "Wk": f64(Wa["Wk"])},
+                             O.mha_segments(4, 64), ref_s, 100.0)
+    assert_rounded_within(Wq, out["Wq"], 1e-6 * np.abs(out["Wq"]), "Wq")
+    assert_rounded_within(Wk, out["Wk"], 1e-6 * np.abs(out["Wk"]), "Wk")
+    # re-measured max logit after the clip is min(S, tau)
+    q2, k2 = forward.project_mha(X, Wq.cpu(), Wk.cpu(), 4)
+    s2, _ = mc.qk_max_logit(q2.cuda(), k2.cuda())
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(f64(s2), np.minimum(ref_s, 100.0), rtol=1e-5)
