@@ -1,0 +1,371 @@
+"""Benchmark of one MuonClip step on GB300 (prints one JSON line on rank 0).
+
+Workload (dense_block): one dense transformer block, d_model 2048, 16 heads x
+128, FFN 2048 -> 5632 -> 2048; bf16 weights, fp32 momentum and gradients;
+attention features of a batch of 4 x 4096 tokens; 3 heads pre-scaled past
+tau = 100.  One step = qk_max_logit on the layer's Q/K (the S_max the forward
+records) + muonclip_step over all 7 matrices (momentum, Newton-Schulz x5,
+RMS-matched update with weight decay, per-head QK-Clip).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the CPU oracle (fp64 numpy) on a bounded sample of the
+same workload on the host cores, scaled to the full step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MuonClip step ms per layer; NS & max-logit TFLOP/s (% BF16 peak); clip GB/s"
+WORKLOAD = "dense_block"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "of measured"
+    return dict(FALLBACK_PEAKS), "of fallback"
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def cpu_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 0) for i in threadpool_info()), default=0)
+        if n:
+            return n
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+# ------------------------------------------------------------------ CPU oracle sample
+def oracle_sample(seed=0, heads=1):
+    """Time the oracle on a bounded sample of the dense_block step and scale
+    it to the full step: Newton-Schulz on one 2048x2048 and one 2048x5632
+    matrix (momentum, NS, update) and the max logit of `heads` head(s) over the
+    4 x 4096 batch.  Returns (ms per full step, description)."""
+    import numpy as np
+
+    import oracle as O
+    from muon_qk_clip_gb300 import synth
+    wl = synth.workload(WORKLOAD)
+    rng = np.random.default_rng(seed)
+    hp = O.Hparams()
+    t0 = time.perf_counter()
+    sample_flops = 0.0
+    for (r, c) in ((2048, 2048), (5632, 2048)):
+        W = rng.standard_normal((r, c)) * 0.02
+        G = rng.standard_normal((r, c)) * 1e-3
+        O.muon_step(W, G, np.zeros((r, c)), hp)
+        sample_flops += synth.flops_ns(r, c)
+    t_ns = time.perf_counter() - t0
+    full_ns = sum(synth.flops_ns(m.rows, m.cols) for m in wl.matrices)
+    att = wl.attention
+    q = rng.standard_normal((att.B, att.S, heads, att.d_head))
+    k = rng.standard_normal((att.B, att.S, heads, att.d_head))
+    t1 = time.perf_counter()
+    O.max_logit(q, k)
+    t_ml = time.perf_counter() - t1
+    ms = 1e3 * (t_ns * full_ns / sample_flops + t_ml * att.H / heads)
+    desc = (f"oracle (fp64 numpy) on a sample: Muon step of one 2048x2048 and one 5632x2048 "
+            f"matrix ({t_ns:.1f} s, scaled by NS flops x{full_ns / sample_flops:.2f}) + max logit "
+            f"of {heads} of {att.H} heads over 4x4096 tokens ({t_ml:.1f} s, scaled x{att.H // heads})")
+    return ms, desc
+
+
+def reference_arm(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_sample(heads=1)
+    vals = []
+    desc = ""
+    for _ in range(args.steps):
+        v, desc = oracle_sample(heads=1)
+        vals.append(v)
+    value = statistics.mean(vals)
+    cores = cpu_cores()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "ms",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": value,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD},
+            "cpu_baseline": {"value": value, "unit": "ms", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_for(kernel_src):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None when the kernel source changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get("ns_gemm")
+    if not d:
+        return None
+    h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    return d["bytes_per_launch"] if d.get("source_sha256_16") == h else None
+
+
+def gpu_arm(args):
+    import torch
+
+    from muon_qk_clip_gb300 import binding as mc
+    from muon_qk_clip_gb300 import forward, synth
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+
+    wl = synth.workload(WORKLOAD)
+    att = wl.attention
+    # ---- inputs resident in HBM (each rank its own layer: weak scaling)
+    seed = 1000 + rank
+    W, G, M = synth.muon_inputs(wl, seed=seed, device=dev)
+    names = [m.name for m in wl.matrices]
+    Wl, Gl, Ml = [W[n] for n in names], [G[n] for n in names], [M[n] for n in names]
+    X = synth.normal((att.B, att.S, att.d_model), 1.0, "X", seed, torch.bfloat16, dev)
+    q, k = forward.project_mha(X, W["Wq"], W["Wk"], att.H)          # setup (untimed)
+    q, k = q.contiguous(), k.contiguous()
+    del X
+    hp = mc.Hparams()
+    ws = mc.alloc_workspace(Wl, hp, dev)
+    smax = torch.zeros(att.H, dtype=torch.float32, device=dev)
+    gamma = torch.zeros(att.H, dtype=torch.float32, device=dev)
+    ncl = torch.zeros(1, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    layer = mc.ClipLayer(smax, mc.mha_segments(W["Wq"], W["Wk"], att.H, hp.alpha), gamma, ncl)
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)   # > 129 MB L2
+    stream = torch.cuda.current_stream()
+
+    def step():
+        mc.qk_max_logit(q, k, smax=smax, status=status, stream=stream)
+        mc.muonclip_step(Wl, Gl, Ml, hp, layers=[layer], workspace=ws, status=status, stream=stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    barrier()
+
+    # ---- timed region: K steps, L2 flushed before each (outside the events)
+    mc.profiler_enable(True)
+    mc.profiler_read(reset=True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        barrier()
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        barrier()
+        wall = time.perf_counter() - wall0
+    prof = mc.profiler_read(reset=True)
+    mc.profiler_enable(False)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    t_local = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([t_local], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_local = float(t.item())
+    ms_per_step = t_local / args.steps
+    stat = int(status.item())
+
+    # ---- end to end through the public API: pinned host G, Q, K in, metrics out
+    Gh = [g.to("cpu").pin_memory() for g in Gl]
+    qh, kh = q.to("cpu").pin_memory(), k.to("cpu").pin_memory()
+    out_h = torch.empty(2 * att.H + 1, dtype=torch.float32).pin_memory()
+    h2d = sum(g.numel() * g.element_size() for g in Gh) + qh.numel() * 2 + kh.numel() * 2
+    d2h = out_h.numel() * 4
+    res = torch.empty(2 * att.H + 1, dtype=torch.float32, device=dev)
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+
+    def e2e_step():
+        for gd, gh in zip(Gl, Gh):
+            gd.copy_(gh, non_blocking=True)
+        q.copy_(qh, non_blocking=True)
+        k.copy_(kh, non_blocking=True)
+        step()
+        res[:att.H].copy_(smax)
+        res[att.H:2 * att.H].copy_(gamma)
+        res[2 * att.H:].copy_(ncl.float())
+        out_h.copy_(res, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    for i in range(args.steps):
+        flush.zero_()
+        e2e_ev[i][0].record(stream)
+        e2e_step()
+        e2e_ev[i][1].record(stream)
+    barrier()
+    e2e_local = sum(a.elapsed_time(b) for a, b in e2e_ev)
+    if dist is not None:
+        t = torch.tensor([e2e_local], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_local = float(t.item())
+
+    # ---- algorithmic work
+    ns_flops = sum(synth.flops_ns(m.rows, m.cols, hp.ns_steps) for m in wl.matrices)
+    ml_flops = synth.flops_max_logit(att.B, att.S, att.H, att.d_head)
+    pk, pk_src = peaks()
+    n_gemm, t_gemm = prof.get("ns_gemm", (0, 0.0))
+    n_ml, t_ml = prof.get("max_logit", (0, 0.0))
+    n_clip, t_clip = prof.get("clip", (0, 0.0))
+    ns_tflops = ns_flops * args.steps / (t_gemm * 1e-3) / 1e12 if t_gemm else None
+    ml_tflops = ml_flops * args.steps / (t_ml * 1e-3) / 1e12 if t_ml else None
+    clipped_heads = len(att.scaled_heads)
+    clip_bytes = 2 * 2 * clipped_heads * att.d_head * att.d_model * 2   # Wq+Wk rows, read+write bf16
+    clip_gbs = clip_bytes * args.steps / (t_clip * 1e-3) / 1e9 if t_clip else None
+    peak_t = pk["bf16_tflops"]
+    per_launch_flops = ns_flops / (n_gemm / args.steps) if n_gemm else None
+    achieved = per_launch_flops / (t_gemm / n_gemm * 1e-3) / 1e12 if n_gemm else None
+    launches = sum(v[0] for v in prof.values())
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    value = ms_per_step / world
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": "ms", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "matrices": "4x2048x2048, 2x5632x2048, 1x2048x5632",
+                   "attention": "B4 S4096 H16 d128 causal", "ns_steps": hp.ns_steps,
+                   "ns_precision": "split-bf16 (hi*hi+hi*lo+lo*hi), fp32 accumulate",
+                   "clipped_heads": clipped_heads, "l2": "flushed (512 MB write) before each step",
+                   "parallelism": f"dp{world} (one layer per rank)"},
+        "clocks": clk.summary(),
+        "e2e": {"value": round(e2e_local / args.steps / world, 4), "unit": "ms",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "roofline": {"bound": "tensor", "kernel": "ns_gemm (tcgen05 split-bf16 Newton-Schulz phase)",
+                     "achieved": round(achieved, 2) if achieved else None,
+                     "peak": peak_t, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak_t, 4) if achieved else None,
+                     "peak_source": f"bf16_tflops {pk_src}",
+                     "traffic": traffic_for(os.path.join(ROOT, "muon_qk_clip_gb300", "csrc", "ns_tc.cu"))},
+        "components": {
+            "ns_algorithmic_tflops": round(ns_tflops, 2) if ns_tflops else None,
+            "ns_frac_bf16_peak": round(ns_tflops / peak_t, 4) if ns_tflops else None,
+            "max_logit_tflops": round(ml_tflops, 2) if ml_tflops else None,
+            "max_logit_frac_bf16_peak": round(ml_tflops / peak_t, 4) if ml_tflops else None,
+            "clip_gbs": round(clip_gbs, 1) if clip_gbs else None,
+            "kernel_ms_per_step": {k: round(v[1] / args.steps, 4) for k, v in prof.items()},
+            "kernel_launches_per_step": {k: v[0] // args.steps for k, v in prof.items()},
+            "step_ms_min": round(min(step_ms), 4), "step_ms_max": round(max(step_ms), 4),
+            "wall_s_timed_loop": round(wall, 3), "device_status": stat,
+        },
+    }
+    if not args.no_cpu_baseline:
+        v, desc = oracle_sample(heads=1)
+        line["cpu_baseline"] = {"value": round(v, 1), "unit": "ms", "cores": cpu_cores(),
+                                "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        from muon_qk_clip_gb300 import build
+        build.build()
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

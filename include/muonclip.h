@@ -206,6 +206,21 @@ mc_status muonclip_step(mc_mat* W, const mc_mat* G, mc_mat* M, int32_t count,
                         void* workspace, size_t workspace_bytes, int32_t* status,
                         mc_stream_t stream);
 
+/* Optional launch timing (observability).  While enabled, every kernel
+ * launch of the library is bracketed by CUDA events recorded on the launch's
+ * stream, accumulated per kernel class ("prep", "norms", "ns_gemm", "apply",
+ * "clip", "max_logit").  mc_profiler_read synchronises on the recorded
+ * events, writes up to `max` entries (class name, launches, total
+ * milliseconds) and returns the number written; reset = 1 clears the totals.
+ * Process-wide; not meant for use while several threads launch. */
+typedef struct {
+  char name[24];
+  int32_t launches;
+  float ms;
+} mc_kernel_time;
+void mc_profiler_enable(int32_t on);
+int32_t mc_profiler_read(mc_kernel_time* out, int32_t max, int32_t reset);
+
 /* Thread-local description of the last non-OK return ("" if none). */
 const char* mc_last_error(void);
 

@@ -54,6 +54,10 @@ class McAttnDesc(ctypes.Structure):
                 ("q_strides", c_int64 * 3), ("k_strides", c_int64 * 3), ("ks_strides", c_int64 * 2)]
 
 
+class McKernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 24), ("launches", c_int32), ("ms", c_float)]
+
+
 # name -> (restype, argtypes), exactly the declarations of include/muonclip.h
 SIGNATURES = {
     "mc_default_hparams": (None, [POINTER(McHparams)]),
@@ -67,6 +71,8 @@ SIGNATURES = {
     "muonclip_step": (c_int32, [POINTER(McMat), POINTER(McMat), POINTER(McMat), c_int32,
                                 POINTER(McHparams), POINTER(McClipLayer), c_int32, c_void_p,
                                 c_size_t, c_void_p, c_void_p]),
+    "mc_profiler_enable": (None, [c_int32]),
+    "mc_profiler_read": (c_int32, [POINTER(McKernelTime), c_int32, c_int32]),
     "mc_last_error": (c_char_p, []),
     "mc_version": (c_char_p, []),
 }

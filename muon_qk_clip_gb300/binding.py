@@ -206,6 +206,18 @@ def muonclip_step(W, G, M, hp: Hparams | None = None, layers=(), workspace=None,
                                    _stream(stream)), "muonclip_step")
 
 
+def profiler_enable(on: bool = True):
+    """Bracket every library launch with CUDA events (per kernel class)."""
+    abi.load().mc_profiler_enable(1 if on else 0)
+
+
+def profiler_read(reset: bool = True) -> dict:
+    """{class: (launches, milliseconds)} accumulated since the last reset."""
+    buf = (abi.McKernelTime * 16)()
+    n = abi.load().mc_profiler_read(buf, 16, 1 if reset else 0)
+    return {buf[i].name.decode(): (buf[i].launches, buf[i].ms) for i in range(n)}
+
+
 def mha_segments(Wq, Wk, H: int, alpha: float = 0.5):
     """QK-Clip segments of an MHA layer: head h owns rows [h d, (h+1) d)."""
     d = Wq.shape[0] // H

@@ -39,6 +39,54 @@ mc_status cuda_fail(cudaError_t e, const char* what) {
   return fail(MC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// ------------------------------------------------------------------ profiler
+enum ProfClass { kPrep, kNorms, kGemm, kApply, kClip, kMaxLogit, kNumProf };
+const char* kProfNames[kNumProf] = {"prep", "norms", "ns_gemm", "apply", "clip", "max_logit"};
+
+struct Profiler {
+  bool on = false;
+  struct Rec { int cls; int launches; cudaEvent_t a, b; };
+  std::vector<Rec> pending;
+  std::vector<cudaEvent_t> pool;
+  double ms[kNumProf] = {0};
+  long long launches[kNumProf] = {0};
+  cudaEvent_t get() {
+    if (!pool.empty()) { cudaEvent_t e = pool.back(); pool.pop_back(); return e; }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+  void drain() {
+    for (Rec& r : pending) {
+      float t = 0.f;
+      if (cudaEventSynchronize(r.b) == cudaSuccess && cudaEventElapsedTime(&t, r.a, r.b) == cudaSuccess)
+        ms[r.cls] += t;
+      launches[r.cls] += r.launches;
+      pool.push_back(r.a);
+      pool.push_back(r.b);
+    }
+    pending.clear();
+  }
+};
+Profiler g_prof;
+
+struct ProfScope {
+  int cls, n;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr;
+  ProfScope(int cls_, int n_, cudaStream_t s_) : cls(cls_), n(n_), s(s_) {
+    if (g_prof.on) { a = g_prof.get(); cudaEventRecord(a, s); }
+  }
+  ~ProfScope() {
+    if (a) {
+      cudaEvent_t b = g_prof.get();
+      cudaEventRecord(b, s);
+      g_prof.pending.push_back({cls, n, a, b});
+      if (g_prof.pending.size() > 4096) g_prof.drain();
+    }
+  }
+};
+
 size_t dtype_size(int32_t d) { return d == MC_BF16 ? 2 : 4; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -207,6 +255,7 @@ mc_status run_prep(const Plan& P, void* ws, mc_mat* M, const mc_mat* G, bool do_
       t += (int)(cdiv(jb.rows, 64) * jb.tiles_c);
     }
     pp.total_tiles = t;
+    ProfScope ps(kPrep, 1, s);
     cudaError_t e = launch_prep(pp, s);
     if (e != cudaSuccess) return cuda_fail(e, "momentum/prep launch");
   }
@@ -214,6 +263,7 @@ mc_status run_prep(const Plan& P, void* ws, mc_mat* M, const mc_mat* G, bool do_
 }
 
 mc_status run_norms(const Plan& P, void* ws, float eps, cudaStream_t s) {
+  ProfScope ps(kNorms, (P.count + kMaxNormMats - 1) / kMaxNormMats, s);
   cudaError_t e = launch_norms(reinterpret_cast<double*>(wsp(ws, P.off_partials)),
                                P.tile_begin.data(), P.tile_count.data(), P.count, eps,
                                reinterpret_cast<float*>(wsp(ws, P.off_inv)),
@@ -295,6 +345,7 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
         gp.s = it == 0 ? reinterpret_cast<const float*>(wsp(ws, P.off_inv)) : nullptr;
         break;
     }
+    ProfScope ps(kGemm, 1, s);
     cudaError_t e;
     if (P.xmode == kXF32) {
       e = launch_ns_gemm_f32(gp, s);
@@ -356,6 +407,7 @@ mc_status run_apply(const Plan& P, void* ws, mc_mat* out, bool write_o, const mc
       t += (int)(cdiv(jb.rows, 64) * jb.tiles_c);
     }
     ap.total_tiles = t;
+    ProfScope ps(kApply, 1, s);
     cudaError_t e = launch_apply(ap, s);
     if (e != cudaSuccess) return cuda_fail(e, "apply launch");
   }
@@ -406,6 +458,7 @@ mc_status run_clip(const float* smax, int H, float tau, const mc_clip_seg* segs,
     d.bf16 = segs[i].w.dtype == MC_BF16;
     d.exponent = segs[i].exponent;
   }
+  ProfScope ps(kClip, (gamma_out || nclipped || status) ? 2 : 1, s);
   cudaError_t e = launch_clip(cp, s);
   if (e != cudaSuccess) return cuda_fail(e, "clip launch");
   return MC_OK;
@@ -467,6 +520,24 @@ void mc_default_hparams(mc_hparams* hp) {
 }
 
 const char* mc_last_error(void) { return g_last_error.c_str(); }
+
+void mc_profiler_enable(int32_t on) { g_prof.on = on != 0; }
+
+int32_t mc_profiler_read(mc_kernel_time* out, int32_t max, int32_t reset) {
+  g_prof.drain();
+  int n = 0;
+  for (int c = 0; c < kNumProf && out && n < max; ++c) {
+    if (g_prof.launches[c] == 0) continue;
+    memset(out[n].name, 0, sizeof out[n].name);
+    strncpy(out[n].name, kProfNames[c], sizeof out[n].name - 1);
+    out[n].launches = (int32_t)g_prof.launches[c];
+    out[n].ms = (float)g_prof.ms[c];
+    ++n;
+  }
+  if (reset)
+    for (int c = 0; c < kNumProf; ++c) { g_prof.ms[c] = 0; g_prof.launches[c] = 0; }
+  return n;
+}
 
 const char* mc_version(void) { return "muonclip-gb300 0.1 (sm_103a)"; }
 
@@ -568,7 +639,11 @@ mc_status qk_max_logit(const mc_attn_desc* a, float* smax, int64_t* argmax, int3
   p.accumulate = accumulate != 0;
   p.status = status;
   char err[256] = {0};
-  cudaError_t e = launch_max_logit(p, (cudaStream_t)stream, err, sizeof err);
+  cudaError_t e;
+  {
+    ProfScope ps(kMaxLogit, 3, (cudaStream_t)stream);
+    e = launch_max_logit(p, (cudaStream_t)stream, err, sizeof err);
+  }
   if (e != cudaSuccess) {
     if (err[0]) return fail(MC_ERR_CUDA, "max logit: %s", err);
     return cuda_fail(e, "max logit launch");

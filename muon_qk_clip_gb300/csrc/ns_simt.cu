@@ -2,7 +2,9 @@
 //   D[b] = s_b * (alpha * A[b] x op(B[b]) + beta * C[b])
 // op(B) = B^T when B is stored [N, K] (K contiguous), B when stored [K, N].
 // Used for fp32 weights, where the update must match exact arithmetic to
-// ~1e-5 of its RMS, beyond what bf16 tensor-core operands give.
+// ~1e-5 of its RMS, beyond what bf16 tensor-core operands give.  Each 16-wide
+// k-tile is summed in fp32 and folded into fp64 accumulators, so rounding
+// error grows with sqrt(16) rather than sqrt(K); the epilogue runs in fp64.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -30,8 +32,9 @@ __global__ void __launch_bounds__(NT) sgemm_kernel(const __grid_constant__ GemmP
     const int m0 = (rem % g.tiles_m) * BM, n0 = (rem / g.tiles_m) * BN;
     const float* A = reinterpret_cast<const float*>(g.a_hi) + (long long)b * g.a_bstride;
     const float* B = reinterpret_cast<const float*>(g.b_hi) + (long long)b * g.b_bstride;
-    float acc[4][4] = {};
+    double acc64[4][4] = {};
     for (int k0 = 0; k0 < g.K; k0 += BK) {
+      float acc[4][4] = {};
       // A tile [BM x BK] -> As[k][m]; 1024 elements, 4 per thread
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -66,6 +69,10 @@ __global__ void __launch_bounds__(NT) sgemm_kernel(const __grid_constant__ GemmP
 #pragma unroll
           for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
       }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc64[i][j] += (double)acc[i][j];
       __syncthreads();
     }
     const float s = p.s ? p.s[g.mat_base + b] : 1.f;
@@ -80,11 +87,12 @@ __global__ void __launch_bounds__(NT) sgemm_kernel(const __grid_constant__ GemmP
       for (int j = 0; j < 4; ++j) {
         const int c = n0 + tx * 4 + j;
         if (c >= g.N) continue;
-        float v = p.alpha * acc[i][j];
-        if (p.beta != 0.f) v = fmaf(p.beta, C[(long long)b * g.c_bstride + (long long)r * g.ldc + c], v);
-        v *= s;
-        bad |= !finite_f(v);
-        D[(long long)r * g.ldd + c] = v;
+        double v = (double)p.alpha * acc64[i][j];
+        if (p.beta != 0.f)
+          v += (double)p.beta * (double)C[(long long)b * g.c_bstride + (long long)r * g.ldc + c];
+        const float vf = (float)(v * (double)s);
+        bad |= !finite_f(vf);
+        D[(long long)r * g.ldd + c] = vf;
       }
     }
     if (bad) set_status(p.status, MC_STATUS_NONFINITE_UPDATE);

@@ -1,0 +1,68 @@
+"""One-shot cases for profilers (ncu): run a single call of the library on
+the dense_block shapes and exit.
+
+  python -m muon_qk_clip_gb300.profile_cases step        # one full MuonClip step
+  python -m muon_qk_clip_gb300.profile_cases ns          # Newton-Schulz of the 7 matrices
+  python -m muon_qk_clip_gb300.profile_cases max_logit   # S_max of B4 S4096 H16 d128
+  python -m muon_qk_clip_gb300.profile_cases momentum    # momentum of the 7 matrices
+
+Each case warms up once (so the profiled launch is not the first) and runs
+`--repeat` more times.
+"""
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+from . import binding as mc
+from . import build, forward, synth
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=["step", "ns", "max_logit", "momentum"])
+    ap.add_argument("--repeat", type=int, default=1)
+    ap.add_argument("--precision", type=int, default=0, help="mc_ns_precision")
+    args = ap.parse_args()
+    build.build()
+    dev = torch.device("cuda", 0)
+    wl = synth.workload("dense_block")
+    att = wl.attention
+    W, G, M = synth.muon_inputs(wl, device=dev)
+    names = [m.name for m in wl.matrices]
+    Wl, Gl, Ml = [W[n] for n in names], [G[n] for n in names], [M[n] for n in names]
+    hp = mc.Hparams(ns_precision=args.precision)
+    if args.case in ("step", "max_logit"):
+        X = synth.normal((att.B, att.S, att.d_model), 1.0, "X", 0, torch.bfloat16, dev)
+        q, k = forward.project_mha(X, W["Wq"], W["Wk"], att.H)
+        q, k = q.contiguous(), k.contiguous()
+        del X
+        smax = torch.zeros(att.H, device=dev)
+    if args.case in ("step", "ns"):
+        ws = mc.alloc_workspace(Wl, hp, dev)
+    if args.case == "ns":
+        Ol = [torch.empty_like(w) for w in Wl]
+
+    def once():
+        if args.case == "step":
+            mc.qk_max_logit(q, k, smax=smax)
+            mc.muonclip_step(Wl, Gl, Ml, hp, workspace=ws,
+                             layers=[mc.ClipLayer(smax, mc.mha_segments(W["Wq"], W["Wk"], att.H))])
+        elif args.case == "ns":
+            mc.muon_newton_schulz(Gl, Ol, hp, workspace=ws)
+        elif args.case == "max_logit":
+            mc.qk_max_logit(q, k, smax=smax)
+        else:
+            mc.muon_momentum(Ml, Gl, hp.mu)
+
+    once()
+    torch.cuda.synchronize()
+    for _ in range(args.repeat):
+        once()
+    torch.cuda.synchronize()
+    print(f"profile case {args.case} done")
+
+
+if __name__ == "__main__":
+    main()

@@ -309,7 +309,7 @@ def test_clip_mha_parity_and_untouched_heads():
 
 
 def test_clip_mla_parity_shared_key_untouched():
-    H, dn, dr, dv, ql, kl, tau = 4, 16, 8, 16, 24, 12, 100.0
+    H, dn, dr, dv, ql, kl, tau = 4, 16, 8, 16, 24, 16, 100.0
     W_UQ = synth.normal((H * (dn + dr), ql), 1.0, "uq", 9).to(BF16)
     W_UKV = synth.normal((H * (dn + dv), kl), 1.0, "ukv", 9).to(BF16)
     W_KR = synth.normal((dr, 40), 1.0, "kr", 9).to(BF16)
