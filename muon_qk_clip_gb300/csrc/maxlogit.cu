@@ -10,6 +10,9 @@
 //                    (ordered value << 32 | (0xffffffff - flat index)) so one
 //                    atomicMax keeps the largest value and, among equal
 //                    values, the smallest flat index (b*S + i)*S + j.
+#include <stdio.h>
+#include <string.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -151,6 +154,357 @@ __global__ void __launch_bounds__(256) ml_simt_kernel(const __grid_constant__ Ma
   }
 }
 
+
+// ---------------------------------------------------------------- tensor cores
+// bf16 features, q.k length in 64-wide chunks.  One work item = (b, h, 128
+// query rows); its Q chunks are loaded once (double-buffered across items) and
+// 256-row key blocks stream through a ring of 64-feature chunk stages.  For
+// MLA the key chunks come first from the head's k^C, then from the shared k^R.
+// Each key block is one 128 x 256 x d product accumulated in TMEM (double
+// buffered); 8 epilogue warps take running row maxima straight out of TMEM.
+namespace tcml {
+
+constexpr int BM = 128, BN = 256;
+constexpr int kThreads = 320;            // producer, MMA, 8 epilogue warps
+constexpr int Q_CHUNK = BM * 64 * 2;     // 16 KB
+constexpr int K_CHUNK = BN * 64 * 2;     // 32 KB
+constexpr int kMaxStages = 6;
+constexpr uint32_t kTmemCols = 512;
+
+struct Maps {
+  CUtensorMap q, k, ks;
+};
+
+struct Geo {
+  int nch, nck;        // chunks of q.k and of the head-specific key part
+  int stages;
+  int nqb;             // query blocks per (b, h)
+  long long items;
+};
+
+__device__ inline float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+__device__ inline void item_coords(const MaxLogitParams& p, const Geo& g, long long t, int& b,
+                                   int& h, int& ib) {
+  const long long bh = (long long)p.B * p.H;
+  ib = g.nqb - 1 - (int)(t / bh);        // heaviest query blocks first
+  const int r = (int)(t % bh);
+  h = r % p.H;
+  b = r / p.H;
+}
+
+__device__ inline int kblocks(const MaxLogitParams& p, int ib) {
+  const int hi = p.causal ? min(p.S, (ib + 1) * BM) : p.S;
+  return (hi + BN - 1) / BN;
+}
+
+template <bool ARG>
+__global__ void __launch_bounds__(kThreads, 1)
+    ml_tc_kernel(const __grid_constant__ MaxLogitParams p, const __grid_constant__ Maps mp,
+                 const Geo g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* qbuf = smem;                                   // [2][nch] x 16 KB
+  uint8_t* kbuf = smem + 2 * g.nch * Q_CHUNK;             // [stages] x 32 KB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(kbuf + g.stages * K_CHUNK);
+  uint64_t* q_full = bars;            // [2]
+  uint64_t* q_empty = bars + 2;       // [2]
+  uint64_t* t_full = bars + 4;        // [2]
+  uint64_t* t_empty = bars + 6;       // [2]
+  uint64_t* drain = bars + 8;         // [1]
+  uint64_t* k_full = bars + 9;        // [stages]
+  uint64_t* k_empty = k_full + kMaxStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(k_empty + kMaxStages);
+  __shared__ volatile int abort_flag;
+  __shared__ float red_v[8];
+  __shared__ uint32_t red_i[8];
+  __shared__ int red_bad[8];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1);
+      mbar_init(&t_full[i], 1); mbar_init(&t_empty[i], 8);
+    }
+    mbar_init(drain, 1);
+    for (int s = 0; s < g.stages; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&mp.q); prefetch_tmap(&mp.k);
+    if (g.nch > g.nck) prefetch_tmap(&mp.ks);
+  }
+  if (warp == 1) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  auto fail = [&]() { abort_flag = 1; set_status(p.status, MC_STATUS_TIMEOUT); };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t it = 0, li = 0;
+      bool used_q[2] = {false, false}, used_k[kMaxStages] = {};
+      uint32_t par_q[2] = {0, 0}, par_k[kMaxStages] = {};
+      for (long long t = blockIdx.x; t < g.items && !abort_flag; t += gridDim.x, ++li) {
+        int b, h, ib;
+        item_coords(p, g, t, b, h, ib);
+        const int qb = li & 1;
+        if (!mbar_wait(&q_empty[qb], ((li >> 1) & 1) ^ 1, &abort_flag)) { fail(); break; }
+        mbar_arrive_expect_tx(&q_full[qb], g.nch * Q_CHUNK);
+        for (int c = 0; c < g.nch; ++c)
+          tma_load_4d(qbuf + (qb * g.nch + c) * Q_CHUNK, &mp.q, &q_full[qb], 64 * c, h, ib * BM, b);
+        used_q[qb] = true; par_q[qb] = (li >> 1) & 1;
+        const int nkb = kblocks(p, ib);
+        bool ok = true;
+        for (int kb = 0; kb < nkb && ok; ++kb) {
+          for (int c = 0; c < g.nch; ++c, ++it) {
+            const int s = it % g.stages;
+            const uint32_t use = it / g.stages;
+            if (!mbar_wait(&k_empty[s], (use & 1) ^ 1, &abort_flag)) { fail(); ok = false; break; }
+            mbar_arrive_expect_tx(&k_full[s], K_CHUNK);
+            if (c < g.nck)
+              tma_load_4d(kbuf + s * K_CHUNK, &mp.k, &k_full[s], 64 * c, h, kb * BN, b);
+            else
+              tma_load_3d(kbuf + s * K_CHUNK, &mp.ks, &k_full[s], 64 * (c - g.nck), kb * BN, b);
+            used_k[s] = true; par_k[s] = use & 1;
+          }
+        }
+        if (!ok) break;
+      }
+      for (int i = 0; i < 2; ++i) if (used_q[i]) mbar_wait(&q_full[i], par_q[i], nullptr);
+      for (int s = 0; s < g.stages; ++s) if (used_k[s]) mbar_wait(&k_full[s], par_k[s], nullptr);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc_bf16(BM, BN, 0, 0);
+      uint32_t it = 0, li = 0, tcount = 0;
+      bool issued = false;
+      for (long long t = blockIdx.x; t < g.items && !abort_flag; t += gridDim.x, ++li) {
+        int b, h, ib;
+        item_coords(p, g, t, b, h, ib);
+        const int qb = li & 1;
+        if (!mbar_wait(&q_full[qb], (li >> 1) & 1, &abort_flag)) { fail(); break; }
+        const int nkb = kblocks(p, ib);
+        bool ok = true;
+        for (int kb = 0; kb < nkb && ok; ++kb, ++tcount) {
+          const int acc = tcount & 1;
+          if (!mbar_wait(&t_empty[acc], ((tcount >> 1) & 1) ^ 1, &abort_flag)) { fail(); ok = false; break; }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + acc * BN;
+          for (int c = 0; c < g.nch; ++c, ++it) {
+            const int s = it % g.stages;
+            if (!mbar_wait(&k_full[s], (it / g.stages) & 1, &abort_flag)) { fail(); ok = false; break; }
+            tc_fence_after();
+            const uint32_t qa = smem_u32(qbuf + (qb * g.nch + c) * Q_CHUNK);
+            const uint32_t ka = smem_u32(kbuf + s * K_CHUNK);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma(d_tmem, make_sdesc_sw128(qa + kk * 32, 16, 1024),
+                     make_sdesc_sw128(ka + kk * 32, 16, 1024), idesc, (c > 0 || kk > 0) ? 1u : 0u);
+            issued = true;
+            tc_commit(&k_empty[s]);
+          }
+          if (ok) tc_commit(&t_full[acc]);
+        }
+        if (!ok) break;
+        tc_commit(&q_empty[qb]);
+      }
+      if (issued) { tc_commit(drain); mbar_wait(drain, 0, nullptr); }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int e = warp - 2;              // 0..7
+    const int q = warp & 3;              // TMEM lane quadrant
+    const int half = e >> 2;             // columns [half*128, half*128 + 128)
+    uint32_t tcount = 0;
+    for (long long t = blockIdx.x; t < g.items; t += gridDim.x) {
+      int b, h, ib;
+      item_coords(p, g, t, b, h, ib);
+      const int nkb = kblocks(p, ib);
+      const int i = ib * BM + q * 32 + lane;          // this thread's query row
+      const int i_lo = ib * BM + q * 32;              // warp's first row
+      float best = -INFINITY;
+      uint32_t bidx = 0xffffffffu;
+      float nanacc = 0.f;
+      int failed = 0;                    // warp-uniform
+      for (int kb = 0; kb < nkb; ++kb, ++tcount) {
+        if (failed) continue;            // every later wait would fail too
+        const int acc = tcount & 1;
+        int w = 1;
+        if (lane == 0) w = mbar_wait(&t_full[acc], (tcount >> 1) & 1, &abort_flag) ? 1 : 0;
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (!w) { failed = 1; if (lane == 0) fail(); continue; }
+        tc_fence_after();
+        const int j0 = kb * BN + half * 128;
+        // every element of this warp's 32 x 128 block valid?
+        const bool interior = (j0 + 127 < p.S) && (i_lo + 31 < p.S) && (!p.causal || j0 + 127 <= i_lo);
+        const bool empty = (j0 >= p.S) || (i_lo >= p.S) || (p.causal && j0 > i_lo + 31);
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          float v[32];
+          tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + half * 128 + ch * 32, v);
+          if (empty) continue;
+          const int jc = j0 + ch * 32;
+          if (!interior) {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+              const int j = jc + x;
+              const bool valid = j < p.S && i < p.S && (!p.causal || j <= i);
+              v[x] = valid ? v[x] : -3.402823466e38f;   // finite: keeps the NaN check exact
+            }
+          }
+#pragma unroll
+          for (int x = 0; x < 32; ++x) nanacc = fmaf(v[x], 0.f, nanacc);
+          float m = max3(v[0], v[1], v[2]);
+#pragma unroll
+          for (int x = 3; x < 31; x += 2) m = max3(m, v[x], v[x + 1]);
+          m = fmaxf(m, v[31]);
+          if (m > best) {
+            best = m;
+            if (ARG) {
+              uint32_t jx = 31;
+#pragma unroll
+              for (int x = 31; x >= 0; --x) jx = (v[x] == m) ? (uint32_t)x : jx;
+              bidx = (uint32_t)(((long long)b * p.S + i) * p.S + jc + (int)jx);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&t_empty[acc]);
+      }
+      // nanacc became NaN iff some unmasked logit was NaN or infinite.
+      // Reduce (best, bidx) over the warp, then over the 8 epilogue warps.  All
+      // 8 warps reach both named barriers for every item, failed or not, and
+      // all leave after the same item.
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_down_sync(0xffffffffu, best, o);
+        const uint32_t oi = __shfl_down_sync(0xffffffffu, bidx, o);
+        if (ov > best || (ov == best && oi < bidx)) { best = ov; bidx = oi; }
+      }
+      const int badw = __any_sync(0xffffffffu, nanacc != 0.f);
+      if (lane == 0) { red_v[e] = best; red_i[e] = bidx; red_bad[e] = badw | (failed << 1); }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      int any_fail = 0, bad = 0;
+      for (int x = 0; x < 8; ++x) { any_fail |= red_bad[x] >> 1; bad |= red_bad[x] & 1; }
+      if (e == 0 && lane == 0 && !any_fail) {
+        for (int x = 1; x < 8; ++x)
+          if (red_v[x] > best || (red_v[x] == best && red_i[x] < bidx)) { best = red_v[x]; bidx = red_i[x]; }
+        if (bad) set_status(p.status, MC_STATUS_NONFINITE_LOGIT);
+        if (best > -INFINITY) publish(p, h, best * p.scale, bidx);
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (any_fail) break;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult qr;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &qr) == cudaSuccess && qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+            const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return false;
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides_bytes,
+             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace tcml
+
+// The tensor-core path takes bf16 features whose rows TMA can address
+// (16-byte aligned bases and strides) and whose head/shared split falls on a
+// 64-feature chunk boundary.
+bool tc_eligible(const MaxLogitParams& p) {
+  if (p.dtype != MC_BF16) return false;
+  const int D = p.d_head + p.d_shared;
+  if (D > 256) return false;
+  if (p.d_shared > 0 && (p.d_head % 64) != 0) return false;
+  auto al16 = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
+  if (!al16(p.q) || !al16(p.k) || (p.d_shared > 0 && !al16(p.ks))) return false;
+  for (int i = 0; i < 3; ++i)
+    if ((p.qs[i] % 8) != 0 || (p.kst[i] % 8) != 0) return false;
+  if (p.d_shared > 0 && ((p.kss[0] % 8) != 0 || (p.kss[1] % 8) != 0)) return false;
+  return true;
+}
+
+cudaError_t launch_ml_tc(const MaxLogitParams& p, cudaStream_t s, char* err, size_t errlen) {
+  using namespace tcml;
+  Maps mp;
+  memset(&mp, 0, sizeof mp);
+  const int D = p.d_head + p.d_shared;
+  Geo g;
+  g.nck = (p.d_head + 63) / 64;
+  g.nch = p.d_shared > 0 ? g.nck + (p.d_shared + 63) / 64 : g.nck;
+  g.nqb = (p.S + BM - 1) / BM;
+  g.items = (long long)p.B * p.H * g.nqb;
+  const int smem_cap = 227 * 1024 - 2048;
+  g.stages = (smem_cap - 2 * g.nch * Q_CHUNK) / K_CHUNK;
+  if (g.stages > kMaxStages) g.stages = kMaxStages;
+  if (g.stages < 2) { snprintf(err, errlen, "q.k length %d leaves no room for key stages", D); return cudaErrorInvalidValue; }
+  {
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)p.H, (cuuint64_t)p.S, (cuuint64_t)p.B};
+    cuuint64_t st[3] = {(cuuint64_t)p.qs[2] * 2, (cuuint64_t)p.qs[1] * 2, (cuuint64_t)p.qs[0] * 2};
+    cuuint32_t box[4] = {64, 1, BM, 1};
+    if (!encode(&mp.q, p.q, 4, dims, st, box)) { snprintf(err, errlen, "tensor map for q failed"); return cudaErrorInvalidValue; }
+  }
+  {
+    cuuint64_t dims[4] = {(cuuint64_t)p.d_head, (cuuint64_t)p.H, (cuuint64_t)p.S, (cuuint64_t)p.B};
+    cuuint64_t st[3] = {(cuuint64_t)p.kst[2] * 2, (cuuint64_t)p.kst[1] * 2, (cuuint64_t)p.kst[0] * 2};
+    cuuint32_t box[4] = {64, 1, BN, 1};
+    if (!encode(&mp.k, p.k, 4, dims, st, box)) { snprintf(err, errlen, "tensor map for k failed"); return cudaErrorInvalidValue; }
+  }
+  if (p.d_shared > 0) {
+    cuuint64_t dims[3] = {(cuuint64_t)p.d_shared, (cuuint64_t)p.S, (cuuint64_t)p.B};
+    cuuint64_t st[2] = {(cuuint64_t)p.kss[1] * 2, (cuuint64_t)p.kss[0] * 2};
+    cuuint32_t box[3] = {64, BN, 1};
+    if (!encode(&mp.ks, p.ks, 3, dims, st, box)) { snprintf(err, errlen, "tensor map for k_shared failed"); return cudaErrorInvalidValue; }
+  }
+  const size_t smem = 1024 + 2 * g.nch * Q_CHUNK + g.stages * K_CHUNK + 256;
+  const int grid = (int)(g.items < sm_count() ? g.items : sm_count());
+  cudaError_t e;
+  if (p.argmax) {
+    e = cudaFuncSetAttribute(ml_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    ml_tc_kernel<true><<<grid, kThreads, smem, s>>>(p, mp, g);
+  } else {
+    e = cudaFuncSetAttribute(ml_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    ml_tc_kernel<false><<<grid, kThreads, smem, s>>>(p, mp, g);
+  }
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_max_logit(const MaxLogitParams& p, cudaStream_t s, char* err, size_t errlen) {
@@ -158,6 +512,12 @@ cudaError_t launch_max_logit(const MaxLogitParams& p, cudaStream_t s, char* err,
   ml_init_kernel<<<hb, 128, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (tc_eligible(p)) {
+    e = launch_ml_tc(p, s, err, errlen);
+    if (e != cudaSuccess) return e;
+    ml_final_kernel<<<hb, 128, 0, s>>>(p);
+    return cudaGetLastError();
+  }
   const int D = p.d_head + p.d_shared;
   const size_t smem = 2 * (size_t)D * (kT + 1) * sizeof(float);
   const int nib = (p.S + kT - 1) / kT;

@@ -44,3 +44,18 @@ def padded(rows, cols, dtype, pad_to=8, fill=float("nan")):
     ld = (cols + pad_to - 1) // pad_to * pad_to
     base = torch.full((rows, ld), fill, dtype=dtype, device="cuda")
     return base[:, :cols]
+
+
+def update_then_clip_band(w_exact, tol, row_factor, rn, gamma_rel=1e-6):
+    """Band of the stored weight after the Muon update (stored, i.e. rounded,
+    in the weight dtype) and then the clip (multiply by row_factor > 0,
+    rounded again).  w_exact: exact updated weights; tol: update tolerance;
+    row_factor: per-row factor gamma^e (1 for untouched rows); gamma_rel:
+    relative uncertainty of the device's gamma (its S_max is an fp32 sum)."""
+    lo, hi = rn(w_exact - tol), rn(w_exact + tol)
+    f = np.asarray(row_factor, np.float64).reshape(-1, 1)
+    lo, hi = lo * f, hi * f
+    clipped = f != 1.0
+    lo = np.where(clipped, lo - gamma_rel * np.abs(lo), lo)
+    hi = np.where(clipped, hi + gamma_rel * np.abs(hi), hi)
+    return rn(lo), rn(hi)

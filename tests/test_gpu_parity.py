@@ -23,7 +23,7 @@ import oracle as O
 from muon_qk_clip_gb300 import abi, build
 from muon_qk_clip_gb300 import binding as mc
 from muon_qk_clip_gb300 import forward, synth
-from tests.gpu_helpers import assert_rounded_within, f64, padded, rms
+from tests.gpu_helpers import assert_rounded_within, f64, padded, rms, update_then_clip_band
 
 pytestmark = pytest.mark.gpu
 
@@ -383,3 +383,38 @@ def test_tiny_mha_fp32_full_step():
     s2, _ = mc.qk_max_logit(q2.cuda(), k2.cuda())
     torch.cuda.synchronize()
     np.testing.assert_allclose(f64(s2), np.minimum(ref_s, 100.0), rtol=1e-5)
+
+
+def test_dense_block_step_reduced_tokens():
+    """dense_block weights (full 2048-wide Wq/Wk and one FFN matrix) updated by
+    Muon and then clipped in the same muonclip_step call, with S_max from a
+    reduced batch (1 x 512 tokens) of the layer's features."""
+    wl = synth.scaled(synth.workload("dense_block"), B=1, S=512)
+    W, G, M = synth.muon_inputs(wl, seed=12, only=("Wq", "Wk", "W_down"))
+    X, _ = synth.attention_inputs(wl, seed=12)
+    q, k = forward.project_mha(X, W["Wq"], W["Wk"], 16)
+    hp = mc.Hparams()
+    names = ["Wq", "Wk", "W_down"]
+    Wd = [W[n].cuda() for n in names]
+    smax, _ = mc.qk_max_logit(q.cuda(), k.cuda())
+    ncl = torch.zeros(1, dtype=torch.int32, device="cuda")
+    layer = mc.ClipLayer(smax, mc.mha_segments(Wd[0], Wd[1], 16), nclipped=ncl)
+    mc.muonclip_step(Wd, [G[n].cuda() for n in names], [M[n].cuda() for n in names], hp,
+                     layers=[layer])
+    torch.cuda.synchronize()
+    s_ref, _ = O.max_logit(f64(q), f64(k))
+    np.testing.assert_allclose(f64(smax), s_ref, rtol=1e-3)
+    gamma, mask = O.clip_factors(s_ref, 100.0)
+    assert sorted(np.nonzero(mask)[0].tolist()) == [2, 7, 11] and ncl.item() == 3
+    assert np.all(np.abs(s_ref - 100.0) > 5.0)          # clear margin for the mask
+    for i, n in enumerate(names):
+        (Wn, _, Od), _ = oracle_muon(W[n], G[n], M[n], hp)
+        tol = 2e-2 * rms(fp32(hp.lr) * Od)
+        if n == "W_down":
+            assert_rounded_within(Wd[i], Wn, tol, n)
+            continue
+        factor = np.repeat(np.where(mask, np.sqrt(gamma), 1.0), 128)
+        s_rel = float(np.max(np.abs(f64(smax) / s_ref - 1.0))) + 1e-7   # device gamma error
+        lo, hi = update_then_clip_band(Wn, tol, factor, O.round_to_bf16, gamma_rel=s_rel)
+        g = f64(Wd[i])
+        assert np.all((g >= lo) & (g <= hi)), n
