@@ -173,6 +173,29 @@ mc_status muon_newton_schulz(const mc_mat* M, mc_mat* O, int32_t count, const mc
                              void* workspace, size_t workspace_bytes, int32_t* status,
                              mc_stream_t stream);
 
+/* muon_newton_schulz without a workspace argument, for callers that cannot
+ * give this library device memory: a framework whose caching allocator owns
+ * the GPU's memory and must not see foreign cudaMalloc calls, a training loop
+ * that cannot afford the device-wide synchronisation of cudaFree, or a plugin
+ * whose host application provides no allocator.  The pages have no
+ * counterpart to this call; it exists for those callers only.
+ *   - Scratch comes from one fixed device array inside the library,
+ *     MC_NOALLOC_SCRATCH_BYTES long, held on every GPU that loads the library
+ *     until the process exits.  The call allocates nothing.
+ *   - Requests whose workspace (mc_workspace_size) exceeds that size return
+ *     MC_ERR_WORKSPACE with a message; use muon_newton_schulz for them.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array.  Nothing in it needs to start at zero
+ *     (each value a kernel reads was written earlier in the same call), but
+ *     calls that overlap on the GPU (different streams, or several host
+ *     threads) race on it: serialise them.
+ * Arguments, results and errors are otherwise those of muon_newton_schulz. */
+#define MC_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+mc_status muon_newton_schulz_noalloc(const mc_mat* M, mc_mat* O, int32_t count,
+                                     const mc_hparams* hp, int32_t* status, mc_stream_t stream);
+
 /* Per-head max logit S_max^h = scale * max_{b} max_{i, j(<=i)} q.k.
  * [K2-internals] "核心数学" (S_max^h over the batch); Algorithm 1 takes it
  * from the forward pass.  smax: device float[H], written (accumulate = 0) or

@@ -22,6 +22,8 @@ MC_STATUS_NONFINITE_LOGIT = 2
 MC_STATUS_NONFINITE_SMAX = 4
 MC_STATUS_TIMEOUT = 8
 
+MC_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
 MC_F32, MC_BF16 = 0, 1
 MC_NS_AUTO, MC_NS_SPLIT_BF16, MC_NS_BF16, MC_NS_FP32 = 0, 1, 2, 3
 
@@ -65,6 +67,8 @@ SIGNATURES = {
     "muon_momentum": (c_int32, [POINTER(McMat), POINTER(McMat), c_int32, c_float, c_void_p, c_void_p]),
     "muon_newton_schulz": (c_int32, [POINTER(McMat), POINTER(McMat), c_int32, POINTER(McHparams),
                                      c_void_p, c_size_t, c_void_p, c_void_p]),
+    "muon_newton_schulz_noalloc": (c_int32, [POINTER(McMat), POINTER(McMat), c_int32,
+                                             POINTER(McHparams), c_void_p, c_void_p]),
     "qk_max_logit": (c_int32, [POINTER(McAttnDesc), c_void_p, c_void_p, c_int32, c_void_p, c_void_p]),
     "qk_clip_apply": (c_int32, [c_void_p, c_int32, c_float, POINTER(McClipSeg), c_int32, c_void_p,
                                 c_void_p, c_void_p, c_void_p]),

@@ -500,6 +500,13 @@ std::vector<T> permute(const T* v, const std::vector<int>& idx) {
 
 }  // namespace
 
+namespace mc {
+mc_status record_error(mc_status s, const char* msg) {
+  g_last_error = msg;
+  return s;
+}
+}  // namespace mc
+
 // ==================================================================== C ABI
 extern "C" {
 

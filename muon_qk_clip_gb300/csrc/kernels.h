@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/muonclip.h"
+
 namespace mc {
 
 inline constexpr int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -170,5 +172,8 @@ cudaError_t launch_max_logit(const MaxLogitParams& p, cudaStream_t s, char* err,
 
 // Device/properties helpers.
 int sm_count();
+
+// Record `msg` as the thread's last error (mc_last_error) and return `s`.
+mc_status record_error(mc_status s, const char* msg);
 
 }  // namespace mc
