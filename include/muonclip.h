@@ -94,6 +94,10 @@ typedef struct {
   float tau;           /* QK-Clip threshold (> 0)                            */
   float alpha;         /* MHA split: W_q by gamma^alpha, W_k by gamma^(1-alpha) */
   int32_t ns_precision;/* mc_ns_precision                                    */
+  int32_t ns_fast_steps;/* MC_NS_SPLIT_BF16 only: this many leading iterations
+                          use one bf16 product (hi operands only) on the split
+                          iterate; the last three iterations always use the
+                          three-term split product.  Default 2.              */
 } mc_hparams;
 
 /* One head-blocked row segment of a weight that QK-Clip rescales.  Head h
@@ -150,7 +154,7 @@ typedef struct {
 
 /* Fill *hp with the defaults named above (mu 0.95, lr 2e-4, weight_decay 0.1,
  * rms_scale 0.2, 5 steps of the quintic (3.4445, -4.7750, 2.0315),
- * ns_eps 1e-7, tau 100, alpha 0.5, MC_NS_AUTO). */
+ * ns_eps 1e-7, tau 100, alpha 0.5, MC_NS_AUTO, ns_fast_steps 2). */
 void mc_default_hparams(mc_hparams* hp);
 
 /* Bytes of workspace that muon_newton_schulz / muonclip_step need for these

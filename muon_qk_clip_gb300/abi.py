@@ -36,7 +36,8 @@ class McMat(ctypes.Structure):
 class McHparams(ctypes.Structure):
     _fields_ = [("mu", c_float), ("lr", c_float), ("weight_decay", c_float), ("rms_scale", c_float),
                 ("ns_steps", c_int32), ("ns_a", c_float), ("ns_b", c_float), ("ns_c", c_float),
-                ("ns_eps", c_float), ("tau", c_float), ("alpha", c_float), ("ns_precision", c_int32)]
+                ("ns_eps", c_float), ("tau", c_float), ("alpha", c_float), ("ns_precision", c_int32),
+                ("ns_fast_steps", c_int32)]
 
 
 class McClipSeg(ctypes.Structure):

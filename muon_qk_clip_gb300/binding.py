@@ -59,18 +59,20 @@ class Hparams:
     tau: float = 100.0
     alpha: float = 0.5
     ns_precision: int = abi.MC_NS_AUTO
+    ns_fast_steps: int = 2
 
     def c(self) -> McHparams:
         a, b, c = self.ns_coeffs
         return McHparams(self.mu, self.lr, self.weight_decay, self.rms_scale, self.ns_steps,
-                         a, b, c, self.ns_eps, self.tau, self.alpha, self.ns_precision)
+                         a, b, c, self.ns_eps, self.tau, self.alpha, self.ns_precision,
+                         self.ns_fast_steps)
 
 
 def default_hparams() -> Hparams:
     h = McHparams()
     abi.load().mc_default_hparams(ctypes.byref(h))
     return Hparams(h.mu, h.lr, h.weight_decay, h.rms_scale, h.ns_steps, (h.ns_a, h.ns_b, h.ns_c),
-                   h.ns_eps, h.tau, h.alpha, h.ns_precision)
+                   h.ns_eps, h.tau, h.alpha, h.ns_precision, h.ns_fast_steps)
 
 
 def workspace_size(shapes_or_tensors, hp: Hparams | None = None) -> int:

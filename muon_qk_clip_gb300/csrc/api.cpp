@@ -125,6 +125,8 @@ mc_status check_hparams(const mc_hparams* hp) {
     return fail(MC_ERR_INVALID_ARG, "hparams: alpha outside [0, 1]");
   if (hp->ns_precision < MC_NS_AUTO || hp->ns_precision > MC_NS_FP32)
     return fail(MC_ERR_INVALID_ARG, "hparams: unknown ns_precision %d", hp->ns_precision);
+  if (hp->ns_fast_steps < 0 || hp->ns_fast_steps > 32)
+    return fail(MC_ERR_INVALID_ARG, "hparams: ns_fast_steps %d outside [0, 32]", hp->ns_fast_steps);
   return MC_OK;
 }
 
@@ -326,12 +328,24 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
       }
       G.tiles_m = (int)cdiv(G.M, tileM);
       G.tiles_n = (int)cdiv(G.N, tileN);
+      G.tiles_per_item = G.tiles_m * G.tiles_n;
+      // Gram and polynomial outputs are symmetric: the tensor-core path
+      // computes only the tiles touching the upper triangle
+      if (P.xmode != kXF32 && (ph == kGram || ph == kPoly)) {
+        G.symmetric = 1;
+        G.tiles_per_item = 0;
+        for (int tn = 0; tn < G.tiles_n; ++tn) G.tiles_per_item += std::min(G.tiles_m, 2 * tn + 2);
+      }
       G.tile_begin = t;
-      t += G.tiles_m * G.tiles_n * G.batch;
+      t += G.tiles_per_item * G.batch;
       (void)es;
     }
     gp.ngroups = ng;
     gp.total_tiles = t;
+    // split iterate: leading "fast" iterations take one bf16 product per
+    // k-step; the last three iterations always take the three-term product
+    const int fast = std::min(hp->ns_fast_steps, std::max(0, hp->ns_steps - 3));
+    gp.terms = (P.xmode == kXSplit && it >= fast) ? 3 : 1;
     switch (ph) {
       case kGram:
         gp.alpha = 1.f; gp.beta = 0.f;
@@ -524,6 +538,7 @@ void mc_default_hparams(mc_hparams* hp) {
   hp->tau = 100.f;
   hp->alpha = 0.5f;
   hp->ns_precision = MC_NS_AUTO;
+  hp->ns_fast_steps = 2;
 }
 
 const char* mc_last_error(void) { return g_last_error.c_str(); }

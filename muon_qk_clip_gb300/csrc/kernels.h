@@ -106,6 +106,9 @@ struct GemmGroup {
   int tile_begin;
   int mat_base;           // index of batch item 0 into the s_b array
   int b_mn_major;         // B operand stored [K, N] (N contiguous)
+  int symmetric;          // D is symmetric (M == N): compute only tiles that touch
+                          // the upper triangle and write each element's mirror
+  int tiles_per_item;     // output tiles per batch item
   // plain pointers (SIMT path reads operands through these; the tensor-core
   // path reads operands through tensor maps and uses these for C and D)
   const void* a_hi; const void* a_lo; long long lda, a_bstride;
@@ -123,6 +126,7 @@ struct GemmParams {
   int ngroups;
   int total_tiles;
   int xmode;
+  int terms;              // tensor-core products per k-step: 1 (hi*hi) or 3 (split)
   float alpha, beta;
   const float* s;         // per-matrix scale, or null
   int32_t* status;

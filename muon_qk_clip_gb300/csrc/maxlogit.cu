@@ -345,33 +345,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         // every element of this warp's 32 x 128 block valid?
         const bool interior = (j0 + 127 < p.S) && (i_lo + 31 < p.S) && (!p.causal || j0 + 127 <= i_lo);
         const bool empty = (j0 >= p.S) || (i_lo >= p.S) || (p.causal && j0 > i_lo + 31);
-#pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-          float v[32];
-          tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + half * 128 + ch * 32, v);
-          if (empty) continue;
-          const int jc = j0 + ch * 32;
-          if (!interior) {
+        // all four 32-column loads in flight before one wait
+        uint32_t r[4][32];
+        const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + half * 128;
 #pragma unroll
-            for (int x = 0; x < 32; ++x) {
-              const int j = jc + x;
-              const bool valid = j < p.S && i < p.S && (!p.causal || j <= i);
-              v[x] = valid ? v[x] : -3.402823466e38f;   // finite: keeps the NaN check exact
+        for (int ch = 0; ch < 4; ++ch) tmem_ld_32x32b_x32_async(tbase + ch * 32, r[ch]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) reg_fence32(r[ch]);
+        if (!empty) {
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            float* v = reinterpret_cast<float*>(r[ch]);
+            const int jc = j0 + ch * 32;
+            if (!interior) {
+#pragma unroll
+              for (int x = 0; x < 32; ++x) {
+                const int j = jc + x;
+                const bool valid = j < p.S && i < p.S && (!p.causal || j <= i);
+                v[x] = valid ? v[x] : -3.402823466e38f;   // finite: keeps the NaN check exact
+              }
             }
-          }
 #pragma unroll
-          for (int x = 0; x < 32; ++x) nanacc = fmaf(v[x], 0.f, nanacc);
-          float m = max3(v[0], v[1], v[2]);
+            for (int x = 0; x < 32; ++x) nanacc = fmaf(v[x], 0.f, nanacc);
+            float m = max3(v[0], v[1], v[2]);
 #pragma unroll
-          for (int x = 3; x < 31; x += 2) m = max3(m, v[x], v[x + 1]);
-          m = fmaxf(m, v[31]);
-          if (m > best) {
-            best = m;
-            if (ARG) {
-              uint32_t jx = 31;
+            for (int x = 3; x < 31; x += 2) m = max3(m, v[x], v[x + 1]);
+            m = fmaxf(m, v[31]);
+            if (m > best) {
+              best = m;
+              if (ARG) {
+                uint32_t jx = 31;
 #pragma unroll
-              for (int x = 31; x >= 0; --x) jx = (v[x] == m) ? (uint32_t)x : jx;
-              bidx = (uint32_t)(((long long)b * p.S + i) * p.S + jc + (int)jx);
+                for (int x = 31; x >= 0; --x) jx = (v[x] == m) ? (uint32_t)x : jx;
+                bidx = (uint32_t)(((long long)b * p.S + i) * p.S + jc + (int)jx);
+              }
             }
           }
         }

@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(NT) sgemm_kernel(const __grid_constant__ GemmP
   for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
     const int gi = find_group(p, t);
     const GemmGroup& g = p.g[gi];
-    const int per = g.tiles_m * g.tiles_n;
+    const int per = g.tiles_per_item;
     const int lt = t - g.tile_begin;
     const int b = lt / per, rem = lt % per;
     const int m0 = (rem % g.tiles_m) * BM, n0 = (rem / g.tiles_m) * BN;

@@ -56,6 +56,58 @@ __device__ inline float load_x(const void* xh, const void* xl, long long idx) {
   return reinterpret_cast<const float*>(xh)[idx];
 }
 
+// Four consecutive elements (16-byte aligned fp32 or 8-byte aligned bf16).
+__device__ inline void load4(const void* base, long long idx, int bf16, float (&o)[4]) {
+  if (bf16) {
+    const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(base) + idx);
+    const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&u);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] = __bfloat162float(b[e]);
+  } else {
+    const float4 f = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + idx);
+    o[0] = f.x; o[1] = f.y; o[2] = f.z; o[3] = f.w;
+  }
+}
+__device__ inline void store4(void* base, long long idx, int bf16, const float (&v)[4]) {
+  if (bf16) {
+    uint2 u;
+    __nv_bfloat16* b = reinterpret_cast<__nv_bfloat16*>(&u);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) b[e] = __float2bfloat16_rn(v[e]);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(base) + idx) = u;
+  } else {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + idx) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+}
+template <int XM>
+__device__ inline void store_x4(void* xh, void* xl, long long idx, const float (&v)[4]) {
+  if (XM == kXSplit) {
+    uint2 uh, ul;
+    __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(&uh);
+    __nv_bfloat16* l = reinterpret_cast<__nv_bfloat16*>(&ul);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) split_bf16(v[e], h[e], l[e]);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(xh) + idx) = uh;
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(xl) + idx) = ul;
+  } else if (XM == kXBf16) {
+    store4(xh, idx, 1, v);
+  } else {
+    store4(xh, idx, 0, v);
+  }
+}
+template <int XM>
+__device__ inline void load_x4(const void* xh, const void* xl, long long idx, float (&o)[4]) {
+  if (XM == kXSplit) {
+    float h[4], l[4];
+    load4(xh, idx, 1, h);
+    load4(xl, idx, 1, l);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] = h[e] + l[e];
+  } else {
+    load4(xh, idx, XM == kXBf16, o);
+  }
+}
+
 // Deterministic block sum (fixed shuffle tree, then fixed order over warps).
 __device__ inline double block_sum(double v, double* red) {
 #pragma unroll
@@ -83,24 +135,40 @@ __global__ void __launch_bounds__(kThreads) prep_kernel(const __grid_constant__ 
     const int r0 = (lt / jb.tiles_c) * kTile, c0 = (lt % jb.tiles_c) * kTile;
     float ss = 0.f;
     bool bad = false;
+    const int cl0 = tx * 4, cbase = c0 + cl0;
+    const bool vec = cbase + 3 < jb.cols;        // 4 in-range columns: one vector access
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int rl = ty + 16 * k, r = r0 + rl;
+      float m[4] = {0.f, 0.f, 0.f, 0.f};
+      if (r < jb.rows) {
+        const long long im = (long long)r * jb.ldM + cbase;
+        if (vec) {
+          load4(jb.M, im, 0, m);
+          if (p.do_momentum) {
+            float g[4];
+            load4(jb.G, (long long)r * jb.ldG + cbase, jb.g_bf16, g);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) m[e] = fmaf(p.mu, m[e], g[e]);
+            store4(jb.M, im, 0, m);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (cbase + e >= jb.cols) continue;
+            m[e] = jb.M[im + e];
+            if (p.do_momentum) {
+              m[e] = fmaf(p.mu, m[e], load_elem(jb.G, (long long)r * jb.ldG + cbase + e, jb.g_bf16));
+              jb.M[im + e] = m[e];
+            }
+          }
+        }
+      }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int cl = tx * 4 + e, c = c0 + cl;
-        float m = 0.f;
-        if (r < jb.rows && c < jb.cols) {
-          const long long im = (long long)r * jb.ldM + c;
-          m = jb.M[im];
-          if (p.do_momentum) {
-            m = fmaf(p.mu, m, load_elem(jb.G, (long long)r * jb.ldG + c, jb.g_bf16));
-            jb.M[im] = m;
-          }
-          bad |= !finite_f(m);
-        }
-        ss = fmaf(m, m, ss);
-        tile[rl][cl] = m;
+        bad |= !finite_f(m[e]);
+        ss = fmaf(m[e], m[e], ss);
+        tile[rl][cl0 + e] = m[e];
       }
     }
     if (bad) set_status(p.status, MC_STATUS_NONFINITE_UPDATE);
@@ -109,24 +177,36 @@ __global__ void __launch_bounds__(kThreads) prep_kernel(const __grid_constant__ 
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int rl = ty + 16 * k, r = r0 + rl;
+          if (r >= jb.rows) continue;
+          const long long ix = (long long)r * jb.ldx + cbase;
+          if (vec) {
+            float v[4] = {tile[rl][cl0], tile[rl][cl0 + 1], tile[rl][cl0 + 2], tile[rl][cl0 + 3]};
+            store_x4<XM>(jb.xh, jb.xl, ix, v);
+          } else {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = c0 + tx * 4 + e;
-            if (r < jb.rows && c < jb.cols)
-              store_x<XM>(jb.xh, jb.xl, (long long)r * jb.ldx + c, tile[rl][tx * 4 + e]);
+            for (int e = 0; e < 4; ++e)
+              if (cbase + e < jb.cols) store_x<XM>(jb.xh, jb.xl, ix + e, tile[rl][cl0 + e]);
           }
         }
       } else {
         __syncthreads();
         // oriented row = original column, oriented column = original row
+        const int rbase = r0 + tx * 4;
+        const bool rvec = rbase + 3 < jb.rows;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int cl = ty + 16 * k, c = c0 + cl;
+          if (c >= jb.cols) continue;
+          const long long ix = (long long)c * jb.ldx + rbase;
+          float v[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int rl = tx * 4 + e, r = r0 + rl;
-            if (r < jb.rows && c < jb.cols)
-              store_x<XM>(jb.xh, jb.xl, (long long)c * jb.ldx + r, tile[rl][cl]);
+          for (int e = 0; e < 4; ++e) v[e] = tile[tx * 4 + e][cl];
+          if (rvec) {
+            store_x4<XM>(jb.xh, jb.xl, ix, v);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (rbase + e < jb.rows) store_x<XM>(jb.xh, jb.xl, ix + e, v[e]);
           }
         }
       }
@@ -163,43 +243,73 @@ __global__ void __launch_bounds__(kThreads) apply_kernel(const __grid_constant__
     const int lt = t - jb.tile_begin;
     const int r0 = (lt / jb.tiles_c) * kTile, c0 = (lt % jb.tiles_c) * kTile;
     const float s = jb.scale * (p.mat_scale ? p.mat_scale[jb.mat] : 1.f);
+    const int cl0 = tx * 4, cbase = c0 + cl0;
     if (jb.transpose) {
       // stage X^T tile: oriented rows c0.., oriented cols r0..
+      const int rbase = r0 + tx * 4;
+      const bool rvec = rbase + 3 < jb.rows;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int cl = ty + 16 * k, c = c0 + cl;
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (c < jb.cols) {
+          const long long ix = (long long)c * jb.ldx + rbase;
+          if (rvec) {
+            load_x4<XM>(jb.xh, jb.xl, ix, x);
+          } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int rl = tx * 4 + e, r = r0 + rl;
-          tile[rl][cl] = (r < jb.rows && c < jb.cols)
-                             ? load_x<XM>(jb.xh, jb.xl, (long long)c * jb.ldx + r)
-                             : 0.f;
+            for (int e = 0; e < 4; ++e)
+              if (rbase + e < jb.rows) x[e] = load_x<XM>(jb.xh, jb.xl, ix + e);
+          }
         }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) tile[tx * 4 + e][cl] = x[e];
       }
       __syncthreads();
     }
     bool bad = false;
+    const bool vec = cbase + 3 < jb.cols;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int rl = ty + 16 * k, r = r0 + rl;
+      if (r >= jb.rows) continue;
+      float x[4];
+      const long long ixo = (long long)r * jb.ldx + cbase;
+      if (jb.transpose) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] = tile[rl][cl0 + e];
+      } else if (vec) {
+        load_x4<XM>(jb.xh, jb.xl, ixo, x);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] = cbase + e < jb.cols ? load_x<XM>(jb.xh, jb.xl, ixo + e) : 0.f;
+      }
+      const long long io = (long long)r * jb.ldo + cbase;
+      float w[4] = {0.f, 0.f, 0.f, 0.f}, v[4];
+      if (!p.write_o) {
+        if (vec) {
+          load4(jb.out, io, jb.out_bf16, w);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (cbase + e < jb.cols) w[e] = load_elem(jb.out, io + e, jb.out_bf16);
+        }
+      }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int cl = tx * 4 + e, c = c0 + cl;
-        if (r >= jb.rows || c >= jb.cols) continue;
-        const float x = jb.transpose ? tile[rl][cl]
-                                     : load_x<XM>(jb.xh, jb.xl, (long long)r * jb.ldx + c);
-        const float o = s * x;
-        const long long io = (long long)r * jb.ldo + c;
-        float v;
-        if (p.write_o) {
-          v = o;
-        } else {
-          const float w = load_elem(jb.out, io, jb.out_bf16);
-          v = fmaf(-p.lr, fmaf(p.wd, w, o), w);   // w - lr (o + wd w), one rounding
+        const float o = s * x[e];
+        v[e] = p.write_o ? o : fmaf(-p.lr, fmaf(p.wd, w[e], o), w[e]);   // w - lr (o + wd w)
+        bad |= !finite_f(v[e]) && (cbase + e < jb.cols);
+      }
+      if (vec) {
+        store4(jb.out, io, jb.out_bf16, v);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (cbase + e >= jb.cols) continue;
+          if (jb.out_bf16) reinterpret_cast<__nv_bfloat16*>(jb.out)[io + e] = __float2bfloat16_rn(v[e]);
+          else reinterpret_cast<float*>(jb.out)[io + e] = v[e];
         }
-        bad |= !finite_f(v);
-        if (jb.out_bf16) reinterpret_cast<__nv_bfloat16*>(jb.out)[io] = __float2bfloat16_rn(v);
-        else reinterpret_cast<float*>(jb.out)[io] = v;
       }
     }
     if (bad) set_status(p.status, MC_STATUS_NONFINITE_UPDATE);

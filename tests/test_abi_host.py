@@ -73,6 +73,7 @@ def test_default_hparams(lib):
     assert (h.mu, h.weight_decay, h.rms_scale, h.ns_steps, h.tau, h.alpha) == pytest.approx(
         (0.95, 0.1, 0.2, 5, 100.0, 0.5))
     assert (h.ns_a, h.ns_b, h.ns_c) == pytest.approx((3.4445, -4.7750, 2.0315))
+    assert h.ns_fast_steps == 2
     assert lib.mc_version().decode().startswith("muonclip")
 
 
@@ -120,7 +121,8 @@ def test_momentum_rejects_shape_mismatch_and_bad_mu(lib):
 
 @pytest.mark.parametrize("field,value", [("ns_steps", -1), ("ns_steps", 33), ("tau", 0.0),
                                          ("tau", -3.0), ("alpha", 1.5), ("ns_eps", -1.0),
-                                         ("lr", float("inf")), ("ns_precision", 9)])
+                                         ("lr", float("inf")), ("ns_precision", 9),
+                                         ("ns_fast_steps", -1), ("ns_fast_steps", 40)])
 def test_newton_schulz_rejects_bad_hparams(lib, field, value):
     h = hp(**{field: value})
     rc = lib.muon_newton_schulz(arr(m(64, 128)), arr(m(64, 128)), 1, ctypes.byref(h),

@@ -86,9 +86,9 @@ NS_CASES = {
 }
 
 
-def run_ns(shapes, precision, out_dtype, steps=5, seed=0):
+def run_ns(shapes, precision, out_dtype, steps=5, seed=0, fast_steps=2):
     Ms, Os, ref = [], [], []
-    hp = mc.Hparams(ns_precision=precision, ns_steps=steps)
+    hp = mc.Hparams(ns_precision=precision, ns_steps=steps, ns_fast_steps=fast_steps)
     ohp = O.Hparams(ns_steps=steps, ns_coeffs=tuple(fp32(c) for c in hp.ns_coeffs),
                     ns_eps=fp32(hp.ns_eps), rms_scale=fp32(hp.rms_scale))
     for i, (r, c) in enumerate(shapes):
@@ -110,6 +110,16 @@ def test_ns_split_bf16_parity(case, out_dtype):
     Os, ref = run_ns(NS_CASES[case], abi.MC_NS_SPLIT_BF16, out_dtype)
     for o, want in zip(Os, ref):
         assert_rounded_within(o, want, 2e-2 * rms(want), f"NS split {case}")
+
+
+@pytest.mark.parametrize("fast_steps", [0, 1, 2])
+@pytest.mark.parametrize("case", ["batched", "ragged_groups"])
+def test_ns_split_fast_steps(case, fast_steps):
+    """Leading iterations with one bf16 product (hi operands) on the split
+    iterate, the last three always split: every setting stays in tolerance."""
+    Os, ref = run_ns(NS_CASES[case], abi.MC_NS_SPLIT_BF16, F32, fast_steps=fast_steps)
+    for o, want in zip(Os, ref):
+        assert_rounded_within(o, want, 2e-2 * rms(want), f"NS fast={fast_steps} {case}")
 
 
 @pytest.mark.parametrize("case", ["single", "transposed", "ragged_groups"])
