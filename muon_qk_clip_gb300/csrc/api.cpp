@@ -288,7 +288,8 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
     const Group &a = P.groups[x], &b = P.groups[y];
     return (ph == kGram ? a.n : a.m) > (ph == kGram ? b.n : b.m);
   });
-  const int tileM = P.xmode == kXF32 ? 64 : 128, tileN = P.xmode == kXF32 ? 64 : 256;
+  int tileM = 64, tileN = 64, sym_step = 1;
+  if (P.xmode != kXF32) ns_tc_tile_shape(&tileM, &tileN, &sym_step);
   for (size_t g0 = 0; g0 < order.size(); g0 += kMaxGroups) {
     GemmParams gp;
     memset(&gp, 0, sizeof gp);
@@ -334,7 +335,8 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
       if (P.xmode != kXF32 && (ph == kGram || ph == kPoly)) {
         G.symmetric = 1;
         G.tiles_per_item = 0;
-        for (int tn = 0; tn < G.tiles_n; ++tn) G.tiles_per_item += std::min(G.tiles_m, 2 * tn + 2);
+        for (int tn = 0; tn < G.tiles_n; ++tn)
+          G.tiles_per_item += std::min(G.tiles_m, (tn + 1) * sym_step);
       }
       G.tile_begin = t;
       t += G.tiles_per_item * G.batch;

@@ -119,6 +119,7 @@ struct GemmGroup {
 
 struct alignas(64) GemmTmaps {
   CUtensorMap a_hi[kMaxGroups], a_lo[kMaxGroups], b_hi[kMaxGroups], b_lo[kMaxGroups];
+  CUtensorMap c_hi[kMaxGroups], c_lo[kMaxGroups], d_hi[kMaxGroups], d_lo[kMaxGroups];
 };
 
 struct GemmParams {
@@ -134,6 +135,10 @@ struct GemmParams {
 
 // Tensor-core path (split bf16 or bf16).  Encodes its own tensor maps.
 cudaError_t launch_ns_gemm_tc(const GemmParams& p, cudaStream_t s, char* err, size_t errlen);
+// Output tile of one tensor-core work unit (bm x bn) and, for symmetric
+// outputs, how many row tiles column tile tn holds per step (rows touching the
+// upper triangle: min(tiles_m, (tn + 1) * sym_rows_per_col_block)).
+void ns_tc_tile_shape(int* bm, int* bn, int* sym_rows_per_col_block);
 // CUDA-core fp32 path.
 cudaError_t launch_ns_gemm_f32(const GemmParams& p, cudaStream_t s);
 

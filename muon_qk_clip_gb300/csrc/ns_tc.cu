@@ -16,10 +16,12 @@
 //   warp 0      TMA producer (one elected lane)
 //   warp 1      TMEM allocator + MMA issuer (one elected lane)
 //   warps 2..5  epilogue: TMEM -> registers -> fused polynomial -> global
-// Tiles are 128 x 256; K advances by BKT (64: 128-byte swizzle rows, or 32:
-// 64-byte swizzle rows and twice the stages); the accumulator is
-// double-buffered in TMEM (2 x 256 columns) so the epilogue of tile t overlaps
-// the MMAs of tile t+1.
+// Tiles are 128 x 256 with K advancing by 32 (64-byte swizzle rows); the
+// accumulator is double-buffered in TMEM (2 x 256 columns) so the epilogue of
+// tile t overlaps the MMAs of tile t+1.  The epilogue stages every 32 x 32
+// chunk through shared memory: C is prefetched there by TMA, D (and, for
+// symmetric outputs, its transpose) leaves by TMA bulk stores, so global
+// memory only sees whole 64-byte rows.
 //
 // Symmetric outputs (phases 1 and 2) are computed only on tiles that touch
 // the upper triangle.  Per 128 x 128 block (I, J) of such a tile: I < J is
@@ -40,25 +42,31 @@
 namespace mc {
 namespace {
 
-constexpr int BM = 128, BN = 256;
+constexpr int BM = 128, BN = 256, BKT = 32;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;    // two 128 x 256 fp32 accumulators
-constexpr int kOperandSmem = 192 * 1024;
+constexpr int kEpiWarpBytes = 16384;   // per epilogue warp: C x2, D, mirror (hi+lo each)
+constexpr int kEpiBytes = 4 * kEpiWarpBytes;
+constexpr int kBarBytes = 256;
+constexpr int kSmemCap = 227 * 1024;
+
+// K-major operand rows of 32 bf16 = 64 bytes: 64-byte swizzle (layout type 4),
+// 8-row atoms of 512 bytes.
+constexpr uint32_t kLayout = 4u;
+constexpr uint32_t kSbo = 8 * BKT * 2;
 
 // TERMS: tensor-core products per k-step (1: hi*hi, 3: hi*hi + hi*lo + lo*hi).
 // LO: the iterate is stored as (hi, lo) planes (the epilogue reads and writes
 // both), independently of how many products the k-loop takes.
-template <int TERMS, int BKT>
-struct Cfg {
-  static constexpr int kABytes = BM * BKT * 2;
-  static constexpr int kBBytes = BN * BKT * 2;
+template <int TERMS, int AROWS, int BROWS>
+struct Stages {
+  static constexpr int kABytes = AROWS * BKT * 2;
+  static constexpr int kBBytes = BROWS * BKT * 2;
   static constexpr int kStageBytes = TERMS == 3 ? 2 * (kABytes + kBBytes) : (kABytes + kBBytes);
-  static constexpr int kStages = kOperandSmem / kStageBytes;
-  static constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
-  // K-major operands: rows of BKT bf16 = 128 B (swizzle 128) or 64 B (swizzle 64)
-  static constexpr uint32_t kLayout = BKT == 64 ? 2u : 4u;
-  static constexpr uint32_t kSbo = 8 * BKT * 2;   // one 8-row swizzle atom
-  static_assert(kStages >= 2 && kStages <= 8, "stage count");
+  static constexpr int kAvail = kSmemCap - kEpiBytes - 1024 - kBarBytes - 64;
+  static constexpr int kStages = kAvail / kStageBytes > 8 ? 8 : kAvail / kStageBytes;
+  static constexpr int kSmem = kStages * kStageBytes + kEpiBytes + 1024 + kBarBytes;
+  static_assert(kStages >= 2, "stage count");
 };
 
 struct TmaArgs {
@@ -74,6 +82,10 @@ __device__ inline int find_group(const GemmParams& p, int t) {
 struct TileCoord {
   int g, b, m0, n0;
 };
+
+// Tiles of tm_rows x 256.  Symmetric outputs keep only tiles touching the
+// upper triangle: column tile tn holds row tiles tm < (tn + 1) * 256 / tm_rows.
+template <int TM_ROWS>
 __device__ inline TileCoord tile_coord(const GemmParams& p, int t) {
   TileCoord c;
   c.g = find_group(p, t);
@@ -82,43 +94,176 @@ __device__ inline TileCoord tile_coord(const GemmParams& p, int t) {
   c.b = lt / G.tiles_per_item;
   int rem = lt % G.tiles_per_item;
   if (!G.symmetric) {
-    c.m0 = (rem % G.tiles_m) * BM;   // consecutive tiles share the B column block
+    c.m0 = (rem % G.tiles_m) * TM_ROWS;   // consecutive tiles share the B column block
     c.n0 = (rem / G.tiles_m) * BN;
   } else {
-    // column block tn holds row blocks tm <= 2 tn + 1 (those touching i <= j)
     int tn = 0;
     for (;; ++tn) {
-      const int rows = min(G.tiles_m, 2 * tn + 2);
+      const int rows = min(G.tiles_m, (tn + 1) * (BN / TM_ROWS));
       if (rem < rows) break;
       rem -= rows;
     }
-    c.m0 = rem * BM;
+    c.m0 = rem * TM_ROWS;
     c.n0 = tn * BN;
   }
   return c;
 }
 
-template <int TERMS, bool LO, int BKT>
+// Byte offset of (row, byte b) in a 32 x 64-byte plane with the 64-byte TMA
+// swizzle: 16-byte unit index XOR ((row >> 1) & 3).
+__device__ inline uint32_t swz64(int row, int b) {
+  return (uint32_t)(row * 64 + ((((b >> 4) ^ ((row >> 1) & 3)) & 3) << 4) + (b & 15));
+}
+
+// ------------------------------------------------------------ epilogue
+// One warp's 32 rows [r0, r0 + 32) of an output tile whose accumulator sits in
+// TMEM at `tacc` (lane quadrant q).  D = s_b * (alpha * acc + beta * C).
+// Symmetric outputs: 32-column chunks in blocks I < J are also stored
+// transposed (mirror); I > J are dropped.  Returns false on a wait timeout.
+template <bool LO>
+__device__ bool epilogue_rows(const GemmParams& p, const TmaArgs& tm, const TileCoord& tc, int r0,
+                              uint32_t tacc, int q, int lane, uint8_t* ebuf, uint64_t* cbar,
+                              uint32_t& cpar, bool& bad, volatile int* abort_flag) {
+  const GemmGroup& G = p.g[tc.g];
+  if (r0 >= G.M) return true;                       // no valid row in this warp
+  const float sb = p.s ? p.s[G.mat_base + tc.b] : 1.f;
+  const float al = p.alpha * sb, be = p.beta * sb;
+  const bool use_c = p.beta != 0.f;
+  uint8_t* cb[2] = {ebuf, ebuf + 4096};
+  uint8_t* db = ebuf + 8192;
+  uint8_t* mb = ebuf + 12288;
+  const int I = r0 / 128;
+  auto mode_of = [&](int ch) -> int {             // 0 skip, 1 store, 2 store + mirror
+    const int col0 = tc.n0 + ch * 32;
+    if (col0 >= G.N) return 0;
+    if (!G.symmetric) return 1;
+    const int J = col0 / 128;
+    return I < J ? 2 : (I == J ? 1 : 0);
+  };
+  auto next_live = [&](int ch) -> int {
+    for (int c = ch + 1; c < BN / 32; ++c)
+      if (mode_of(c)) return c;
+    return BN / 32;
+  };
+  auto issue_c = [&](int ch, int buf) {
+    const int col0 = tc.n0 + ch * 32;
+    mbar_arrive_expect_tx(&cbar[buf], LO ? 4096 : 2048);
+    tma_load_3d(cb[buf], &tm.maps.c_hi[tc.g], &cbar[buf], col0, r0, tc.b);
+    if (LO) tma_load_3d(cb[buf] + 2048, &tm.maps.c_lo[tc.g], &cbar[buf], col0, r0, tc.b);
+  };
+  const int row = r0 + lane;
+  int ch = next_live(-1);
+  if (use_c && ch < BN / 32 && lane == 0) issue_c(ch, 0);
+  int k = 0;
+  for (; ch < BN / 32; ch = next_live(ch), ++k) {
+    const int mode = mode_of(ch);
+    const int col0 = tc.n0 + ch * 32;
+    const int buf = k & 1;
+    if (use_c && lane == 0) {
+      const int nx = next_live(ch);
+      if (nx < BN / 32) issue_c(nx, buf ^ 1);
+    }
+    float v[32];
+    tmem_ld_32x32b_x32(tacc + ((uint32_t)(q * 32) << 16) + ch * 32, v);
+    if (use_c) {
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&cbar[buf], (cpar >> buf) & 1, abort_flag) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      cpar ^= 1u << buf;
+      if (!ok) return false;
+      const uint8_t* ch_hi = cb[buf];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 h = *reinterpret_cast<const uint4*>(ch_hi + swz64(lane, j * 16));
+        const __nv_bfloat16* hh = reinterpret_cast<const __nv_bfloat16*>(&h);
+        if (LO) {
+          const uint4 l = *reinterpret_cast<const uint4*>(ch_hi + 2048 + swz64(lane, j * 16));
+          const __nv_bfloat16* ll = reinterpret_cast<const __nv_bfloat16*>(&l);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            v[j * 8 + e] = fmaf(al, v[j * 8 + e], be * (__bfloat162float(hh[e]) + __bfloat162float(ll[e])));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[j * 8 + e] = fmaf(al, v[j * 8 + e], be * __bfloat162float(hh[e]));
+        }
+      }
+      fence_async_smem();            // these reads precede the TMA refill of the buffer
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] *= al;
+    }
+    __nv_bfloat16 hb[32], lb[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      bad |= !finite_f(v[e]) && (col0 + e < G.N) && (row < G.M);
+      if (LO) split_bf16(v[e], hb[e], lb[e]);
+      else hb[e] = __float2bfloat16_rn(v[e]);
+    }
+    // the previous chunk's stores must have finished reading D/mirror buffers
+    if (lane == 0) bulk_wait_read0();
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      *reinterpret_cast<uint4*>(db + swz64(lane, j * 16)) = *reinterpret_cast<const uint4*>(hb + j * 8);
+      if (LO)
+        *reinterpret_cast<uint4*>(db + 2048 + swz64(lane, j * 16)) = *reinterpret_cast<const uint4*>(lb + j * 8);
+    }
+    if (mode == 2) {
+      // mirror tile: row c holds column c of this chunk, i.e. lane (row) r -> byte 2r
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        *reinterpret_cast<__nv_bfloat16*>(mb + swz64(c, 2 * lane)) = hb[c];
+        if (LO) *reinterpret_cast<__nv_bfloat16*>(mb + 2048 + swz64(c, 2 * lane)) = lb[c];
+      }
+    }
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(&tm.maps.d_hi[tc.g], db, col0, r0, tc.b);
+      if (LO) tma_store_3d(&tm.maps.d_lo[tc.g], db + 2048, col0, r0, tc.b);
+      if (mode == 2) {
+        tma_store_3d(&tm.maps.d_hi[tc.g], mb, r0, col0, tc.b);
+        if (LO) tma_store_3d(&tm.maps.d_lo[tc.g], mb + 2048, r0, col0, tc.b);
+      }
+      bulk_commit();
+    }
+  }
+  return true;
+}
+
+// ------------------------------------------------------------ 1-CTA kernel
+// CL = 1: every CTA streams its own operands.  CL = 2: clusters of two CTAs
+// take the two 128-row halves of a 256 x 256 super-tile; they need the same
+// 256 B rows, so each CTA loads one 128-row half of B and multicasts it to
+// both (half the B traffic from L2).  A stage is refilled only when both
+// CTAs' MMAs have released it (each MMA thread's commit arrives on both).
+template <int TERMS, bool LO, int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     ns_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ TmaArgs tm) {
-  using C = Cfg<TERMS, BKT>;
-  constexpr bool SPLIT = TERMS == 3;      // lo operands are loaded and multiplied
+  using C = Stages<TERMS, BM, BN>;
+  constexpr bool SPLIT = TERMS == 3;
+  constexpr int TM_ROWS = BM * CL;
+  const uint32_t crank = CL > 1 ? cluster_ctarank() : 0;
+  const int unit = blockIdx.x / CL, nunits = gridDim.x / CL;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
-  uint64_t* empty = full + C::kStages;
-  uint64_t* tfull = empty + C::kStages;   // [2]
+  uint8_t* epi = smem + C::kStages * C::kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(epi + kEpiBytes);
+  uint64_t* empty = full + 8;
+  uint64_t* tfull = empty + 8;             // [2]
   uint64_t* tempty = tfull + 2;            // [2]
   uint64_t* drain = tempty + 2;            // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* cbar = drain + 1;              // [4][2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cbar + 8);
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int s = 0; s < C::kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int s = 0; s < C::kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], CL); }
     for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 4); }
     mbar_init(drain, 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&cbar[i], 1);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -129,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
   tc_fence_before();
-  __syncthreads();
+  if (CL > 1) { __syncwarp(); cluster_sync_all(); } else { __syncthreads(); }
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -144,10 +289,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0;
       uint32_t last_par[8] = {};
       bool used[8] = {};
-      for (int t = blockIdx.x; t < p.total_tiles && !abort_flag; t += gridDim.x) {
-        const TileCoord tc = tile_coord(p, t);
+      for (int t = unit; t < p.total_tiles && !abort_flag; t += nunits) {
+        const TileCoord tc = tile_coord<TM_ROWS>(p, t);
         const GemmGroup& G = p.g[tc.g];
         const int nk = (G.K + BKT - 1) / BKT;
+        const int m0 = tc.m0 + BM * (int)crank;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % C::kStages;
@@ -160,17 +306,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* b_lo = b_hi + C::kBBytes;
           mbar_arrive_expect_tx(&full[s], C::kStageBytes);
           const int k0 = kb * BKT;
-          tma_load_3d(a_hi, &tm.maps.a_hi[tc.g], &full[s], k0, tc.m0, tc.b);
-          if (SPLIT) tma_load_3d(a_lo, &tm.maps.a_lo[tc.g], &full[s], k0, tc.m0, tc.b);
-          if (!G.b_mn_major) {
-            tma_load_3d(b_hi, &tm.maps.b_hi[tc.g], &full[s], k0, tc.n0, tc.b);
-            if (SPLIT) tma_load_3d(b_lo, &tm.maps.b_lo[tc.g], &full[s], k0, tc.n0, tc.b);
-          } else {
+          tma_load_3d(a_hi, &tm.maps.a_hi[tc.g], &full[s], k0, m0, tc.b);
+          if (SPLIT) tma_load_3d(a_lo, &tm.maps.a_lo[tc.g], &full[s], k0, m0, tc.b);
+          if (CL == 1) {
+            if (!G.b_mn_major) {
+              tma_load_3d(b_hi, &tm.maps.b_hi[tc.g], &full[s], k0, tc.n0, tc.b);
+              if (SPLIT) tma_load_3d(b_lo, &tm.maps.b_lo[tc.g], &full[s], k0, tc.n0, tc.b);
+            } else {
 #pragma unroll
-            for (int q = 0; q < BN / 64; ++q) {
-              tma_load_3d(b_hi + q * (64 * BKT * 2), &tm.maps.b_hi[tc.g], &full[s], tc.n0 + 64 * q, k0, tc.b);
+              for (int qq = 0; qq < BN / 64; ++qq) {
+                tma_load_3d(b_hi + qq * (64 * BKT * 2), &tm.maps.b_hi[tc.g], &full[s], tc.n0 + 64 * qq, k0, tc.b);
+                if (SPLIT)
+                  tma_load_3d(b_lo + qq * (64 * BKT * 2), &tm.maps.b_lo[tc.g], &full[s], tc.n0 + 64 * qq, k0, tc.b);
+              }
+            }
+          } else {
+            // this CTA's half of B (128 of the 256 rows), to both CTAs
+            constexpr uint16_t kAll = (1u << CL) - 1;
+            if (!G.b_mn_major) {
+              const int off = (int)crank * 128 * BKT * 2;     // 128 K-major rows of 64 bytes
+              tma_load_3d_mc(b_hi + off, &tm.maps.b_hi[tc.g], &full[s], k0, tc.n0 + 128 * (int)crank, tc.b, kAll);
               if (SPLIT)
-                tma_load_3d(b_lo + q * (64 * BKT * 2), &tm.maps.b_lo[tc.g], &full[s], tc.n0 + 64 * q, k0, tc.b);
+                tma_load_3d_mc(b_lo + off, &tm.maps.b_lo[tc.g], &full[s], k0, tc.n0 + 128 * (int)crank, tc.b, kAll);
+            } else {
+#pragma unroll
+              for (int qq = 2 * (int)crank; qq < 2 * (int)crank + 2; ++qq) {
+                tma_load_3d_mc(b_hi + qq * (64 * BKT * 2), &tm.maps.b_hi[tc.g], &full[s], tc.n0 + 64 * qq, k0, tc.b, kAll);
+                if (SPLIT)
+                  tma_load_3d_mc(b_lo + qq * (64 * BKT * 2), &tm.maps.b_lo[tc.g], &full[s], tc.n0 + 64 * qq, k0, tc.b, kAll);
+              }
             }
           }
           used[s] = true;
@@ -189,8 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_mn = make_idesc_bf16(BM, BN, 0, 1);
       uint32_t it = 0, tcount = 0;
       bool issued = false;
-      for (int t = blockIdx.x; t < p.total_tiles && !abort_flag; t += gridDim.x, ++tcount) {
-        const TileCoord tc = tile_coord(p, t);
+      for (int t = unit; t < p.total_tiles && !abort_flag; t += nunits, ++tcount) {
+        const TileCoord tc = tile_coord<TM_ROWS>(p, t);
         const GemmGroup& G = p.g[tc.g];
         const int nk = (G.K + BKT - 1) / BKT;
         const int acc = tcount & 1;
@@ -211,11 +375,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < BKT / 16; ++kk) {
             // K-major: 16 elements = 32 bytes further along the swizzled row
-            const uint64_t dah = make_sdesc(a_hi + kk * 32, 16, C::kSbo, C::kLayout);
+            const uint64_t dah = make_sdesc(a_hi + kk * 32, 16, kSbo, kLayout);
             uint64_t dbh, dbl = 0, dal = 0;
             if (!G.b_mn_major) {
-              dbh = make_sdesc(b_hi + kk * 32, 16, C::kSbo, C::kLayout);
-              if (SPLIT) dbl = make_sdesc(b_lo + kk * 32, 16, C::kSbo, C::kLayout);
+              dbh = make_sdesc(b_hi + kk * 32, 16, kSbo, kLayout);
+              if (SPLIT) dbl = make_sdesc(b_lo + kk * 32, 16, kSbo, kLayout);
             } else {
               // MN-major (128-byte swizzle): 16 K-rows = two 1024-byte atoms;
               // 64-wide N blocks are 64*BKT*2 bytes apart
@@ -225,13 +389,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
             tc_mma(d_tmem, dah, dbh, idesc, accum);
             if (SPLIT) {
-              dal = make_sdesc(a_lo + kk * 32, 16, C::kSbo, C::kLayout);
+              dal = make_sdesc(a_lo + kk * 32, 16, kSbo, kLayout);
               tc_mma(d_tmem, dah, dbl, idesc, 1u);
               tc_mma(d_tmem, dal, dbh, idesc, 1u);
             }
           }
           issued = true;
-          tc_commit(&empty[s]);          // stage free once these MMAs have read it
+          // stage free once these MMAs have read it (in both CTAs of a cluster:
+          // the peer multicasts into this stage too)
+          if (CL > 1) tc_commit_mc(&empty[s], (1u << CL) - 1);
+          else tc_commit(&empty[s]);
         }
         if (!ok) break;
         tc_commit(&tfull[acc]);          // accumulator ready for the epilogue
@@ -243,104 +410,231 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    const int e = warp - 2;
     const int q = warp & 3;              // TMEM lane quadrant of this warp
+    uint8_t* ebuf = epi + e * kEpiWarpBytes;
+    uint32_t cpar = 0;
+    bool bad = false;
     uint32_t tcount = 0;
-    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++tcount) {
-      const TileCoord tc = tile_coord(p, t);
-      const GemmGroup& G = p.g[tc.g];
+    for (int t = unit; t < p.total_tiles; t += nunits, ++tcount) {
+      const TileCoord tc = tile_coord<TM_ROWS>(p, t);
       const int acc = tcount & 1;
-      const uint32_t ause = tcount >> 1;
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(&tfull[acc], ause & 1, &abort_flag) ? 1 : 0;
+      if (lane == 0) ok = mbar_wait(&tfull[acc], (tcount >> 1) & 1, &abort_flag) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) { if (lane == 0) fail(); break; }
       tc_fence_after();
-      const int row = tc.m0 + q * 32 + lane;
-      const float sb = p.s ? p.s[G.mat_base + tc.b] : 1.f;
-      const float al = p.alpha * sb, be = p.beta * sb;
-      const bool row_ok = row < G.M;
-      const long long crow = (long long)tc.b * G.c_bstride + (long long)row * G.ldc;
-      const long long drow = (long long)tc.b * G.d_bstride + (long long)row * G.ldd;
-      const long long mbase = (long long)tc.b * G.d_bstride + row;     // mirror column
-      __nv_bfloat16* dh = reinterpret_cast<__nv_bfloat16*>(G.d_hi);
-      __nv_bfloat16* dl = reinterpret_cast<__nv_bfloat16*>(G.d_lo);
-      bool bad = false;
-#pragma unroll 1
-      for (int ch = 0; ch < BN / 32; ++ch) {
-        float v[32];
-        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + ch * 32, v);
-        const int col0 = tc.n0 + ch * 32;
-        // block ownership of this 32-column chunk (symmetric outputs)
-        bool store = true, mirror = false;
-        if (G.symmetric) {
-          const int I = tc.m0 / 128, J = col0 / 128;
-          store = I <= J;
-          mirror = I < J;
-        }
-        if (!row_ok || col0 >= G.N || !store) continue;
-#pragma unroll
-        for (int v8 = 0; v8 < 4; ++v8) {
-          const int col = col0 + v8 * 8;
-          float* o = v + v8 * 8;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] *= al;
-          if (p.beta != 0.f && col < G.N) {
-            const uint4 ch4 = *reinterpret_cast<const uint4*>(
-                reinterpret_cast<const __nv_bfloat16*>(G.c_hi) + crow + col);
-            const __nv_bfloat16* chb = reinterpret_cast<const __nv_bfloat16*>(&ch4);
-            if (LO) {
-              const uint4 cl4 = *reinterpret_cast<const uint4*>(
-                  reinterpret_cast<const __nv_bfloat16*>(G.c_lo) + crow + col);
-              const __nv_bfloat16* clb = reinterpret_cast<const __nv_bfloat16*>(&cl4);
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                o[e] = fmaf(be, __bfloat162float(chb[e]) + __bfloat162float(clb[e]), o[e]);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 8; ++e) o[e] = fmaf(be, __bfloat162float(chb[e]), o[e]);
-            }
-          }
-        }
-        __nv_bfloat16 hb[32], lb[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          bad |= !finite_f(v[e]) && (col0 + e < G.N);
-          if (LO) split_bf16(v[e], hb[e], lb[e]);
-          else hb[e] = __float2bfloat16_rn(v[e]);
-        }
-#pragma unroll
-        for (int v8 = 0; v8 < 4; ++v8) {
-          const int col = col0 + v8 * 8;
-          if (col >= G.N) break;
-          *reinterpret_cast<uint4*>(dh + drow + col) = *reinterpret_cast<const uint4*>(hb + v8 * 8);
-          if (LO)
-            *reinterpret_cast<uint4*>(dl + drow + col) = *reinterpret_cast<const uint4*>(lb + v8 * 8);
-        }
-        if (mirror) {
-          // (row, col) also lands at (col, row); lanes hold consecutive rows,
-          // so each store instruction covers 64 contiguous bytes
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int col = col0 + e;
-            if (col < G.N) {
-              dh[mbase + (long long)col * G.ldd] = hb[e];
-              if (LO) dl[mbase + (long long)col * G.ldd] = lb[e];
-            }
-          }
-        }
-      }
-      if (bad) set_status(p.status, MC_STATUS_NONFINITE_UPDATE);
+      const bool done = epilogue_rows<LO>(p, tm, tc, tc.m0 + BM * (int)crank + q * 32, tmem_base + acc * BN, q, lane, ebuf,
+                                          cbar + 2 * e, cpar, bad, &abort_flag);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (!done) { if (lane == 0) fail(); break; }
     }
+    if (lane == 0) bulk_wait0();         // all TMA stores of this warp complete
+    if (bad) set_status(p.status, MC_STATUS_NONFINITE_UPDATE);
   }
 
   tc_fence_before();
-  __syncthreads();
+  if (CL > 1) { __syncwarp(); cluster_sync_all(); } else { __syncthreads(); }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- CTA pairs
+// The same GEMM on CTA pairs (cluster of 2, tcgen05 .cta_group::2): one
+// 256 x 256 output tile per pair, each CTA holding 128 rows of A and 128 rows
+// (N values) of B, so each SM receives half the B operand of a 1-CTA 128 x 256
+// tile for the same MMA work.  The even CTA issues the MMAs; both CTAs' TMA
+// copies count on its full barrier; commits multicast to both CTAs.
+constexpr int PBM = 256, PBN = 256;
+
+template <int TERMS, bool LO>
+__global__ void __launch_bounds__(kThreads, 1)
+    ns_gemm_pair_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ TmaArgs tm) {
+  using C = Stages<TERMS, 128, 128>;
+  constexpr bool SPLIT = TERMS == 3;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* epi = smem + C::kStages * C::kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(epi + kEpiBytes);
+  uint64_t* empty = full + 8;
+  uint64_t* tfull = empty + 8;             // [2]
+  uint64_t* tempty = tfull + 2;            // [2]
+  uint64_t* drain = tempty + 2;            // [1]
+  uint64_t* cbar = drain + 1;              // [4][2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cbar + 8);
+  __shared__ volatile int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < C::kStages; ++s) { mbar_init(&full[s], 2); mbar_init(&empty[s], 1); }
+    for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 8); }
+    mbar_init(drain, 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&cbar[i], 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int g = 0; g < p.ngroups; ++g) {
+      prefetch_tmap(&tm.maps.a_hi[g]); prefetch_tmap(&tm.maps.b_hi[g]);
+      if (SPLIT) { prefetch_tmap(&tm.maps.a_lo[g]); prefetch_tmap(&tm.maps.b_lo[g]); }
+    }
+  }
+  if (warp == 1) { tmem_alloc_pair(tmem_slot, kTmemCols); tmem_relinquish_pair(); }
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync_all();              // barriers and TMEM of both CTAs are ready
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  auto fail = [&]() {
+    abort_flag = 1;
+    set_status(p.status, MC_STATUS_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      uint32_t it = 0;
+      uint32_t last_par[8] = {};
+      bool used[8] = {};
+      for (int t = pair; t < p.total_tiles && !abort_flag; t += npairs) {
+        const TileCoord tc = tile_coord<PBM>(p, t);
+        const GemmGroup& G = p.g[tc.g];
+        const int nk = (G.K + BKT - 1) / BKT;
+        const int ma = tc.m0 + 128 * (int)rank, nb = tc.n0 + 128 * (int)rank;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % C::kStages;
+          const uint32_t use = it / C::kStages;
+          if (!mbar_wait(&empty[s], (use & 1) ^ 1, &abort_flag)) { fail(); ok = false; break; }
+          uint8_t* st = smem + s * C::kStageBytes;
+          uint8_t* a_hi = st;
+          uint8_t* a_lo = st + C::kABytes;
+          uint8_t* b_hi = st + (SPLIT ? 2 * C::kABytes : C::kABytes);
+          uint8_t* b_lo = b_hi + C::kBBytes;
+          const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);   // the even CTA's barrier
+          mbar_arrive_expect_tx_cluster(fb, C::kStageBytes);
+          const int k0 = kb * BKT;
+          tma_load_3d_pair(a_hi, &tm.maps.a_hi[tc.g], fb, k0, ma, tc.b);
+          if (SPLIT) tma_load_3d_pair(a_lo, &tm.maps.a_lo[tc.g], fb, k0, ma, tc.b);
+          if (!G.b_mn_major) {
+            tma_load_3d_pair(b_hi, &tm.maps.b_hi[tc.g], fb, k0, nb, tc.b);
+            if (SPLIT) tma_load_3d_pair(b_lo, &tm.maps.b_lo[tc.g], fb, k0, nb, tc.b);
+          } else {
+#pragma unroll
+            for (int qq = 0; qq < 2; ++qq) {
+              tma_load_3d_pair(b_hi + qq * (64 * BKT * 2), &tm.maps.b_hi[tc.g], fb, nb + 64 * qq, k0, tc.b);
+              if (SPLIT)
+                tma_load_3d_pair(b_lo + qq * (64 * BKT * 2), &tm.maps.b_lo[tc.g], fb, nb + 64 * qq, k0, tc.b);
+            }
+          }
+          used[s] = true;
+          last_par[s] = use & 1;
+        }
+        if (!ok) break;
+      }
+      // the even CTA's full barriers count both CTAs' copies: drain them there
+      if (leader)
+        for (int s = 0; s < C::kStages; ++s)
+          if (used[s]) mbar_wait(&full[s], last_par[s], nullptr);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc_k = make_idesc_bf16(PBM, PBN, 0, 0);
+      constexpr uint32_t idesc_mn = make_idesc_bf16(PBM, PBN, 0, 1);
+      uint32_t it = 0, tcount = 0;
+      bool issued = false;
+      for (int t = pair; t < p.total_tiles && !abort_flag; t += npairs, ++tcount) {
+        const TileCoord tc = tile_coord<PBM>(p, t);
+        const GemmGroup& G = p.g[tc.g];
+        const int nk = (G.K + BKT - 1) / BKT;
+        const int acc = tcount & 1;
+        const uint32_t ause = tcount >> 1;
+        if (!mbar_wait(&tempty[acc], (ause & 1) ^ 1, &abort_flag)) { fail(); break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * PBN;
+        const uint32_t idesc = G.b_mn_major ? idesc_mn : idesc_k;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % C::kStages;
+          const uint32_t use = it / C::kStages;
+          if (!mbar_wait(&full[s], use & 1, &abort_flag)) { fail(); ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + s * C::kStageBytes);
+          const uint32_t a_hi = st, a_lo = st + C::kABytes;
+          const uint32_t b_hi = st + (SPLIT ? 2 * C::kABytes : C::kABytes), b_lo = b_hi + C::kBBytes;
+#pragma unroll
+          for (int kk = 0; kk < BKT / 16; ++kk) {
+            const uint64_t dah = make_sdesc(a_hi + kk * 32, 16, kSbo, kLayout);
+            uint64_t dbh, dbl = 0, dal = 0;
+            if (!G.b_mn_major) {
+              dbh = make_sdesc(b_hi + kk * 32, 16, kSbo, kLayout);
+              if (SPLIT) dbl = make_sdesc(b_lo + kk * 32, 16, kSbo, kLayout);
+            } else {
+              dbh = make_sdesc(b_hi + kk * 2048, 64 * BKT * 2, 1024, 2);
+              if (SPLIT) dbl = make_sdesc(b_lo + kk * 2048, 64 * BKT * 2, 1024, 2);
+            }
+            const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+            tc_mma_pair(d_tmem, dah, dbh, idesc, accum);
+            if (SPLIT) {
+              dal = make_sdesc(a_lo + kk * 32, 16, kSbo, kLayout);
+              tc_mma_pair(d_tmem, dah, dbl, idesc, 1u);
+              tc_mma_pair(d_tmem, dal, dbh, idesc, 1u);
+            }
+          }
+          issued = true;
+          tc_commit_pair_mc(&empty[s], 0x3);     // both CTAs' stage s is free
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(&tfull[acc], 0x3);     // both CTAs' accumulators ready
+      }
+      if (issued) {
+        tc_commit_pair_mc(drain, 0x1);
+        mbar_wait(drain, 0, nullptr);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int e = warp - 2;
+    const int q = warp & 3;
+    uint8_t* ebuf = epi + e * kEpiWarpBytes;
+    const uint32_t te_l[2] = {mapa_shared(smem_u32(&tempty[0]), 0), mapa_shared(smem_u32(&tempty[1]), 0)};
+    uint32_t cpar = 0;
+    bool bad = false;
+    uint32_t tcount = 0;
+    for (int t = pair; t < p.total_tiles; t += npairs, ++tcount) {
+      const TileCoord tc = tile_coord<PBM>(p, t);
+      const int acc = tcount & 1;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&tfull[acc], (tcount >> 1) & 1, &abort_flag) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) { if (lane == 0) fail(); break; }
+      tc_fence_after();
+      const bool done = epilogue_rows<LO>(p, tm, tc, tc.m0 + 128 * (int)rank + q * 32, tmem_base + acc * PBN,
+                                          q, lane, ebuf, cbar + 2 * e, cpar, bad, &abort_flag);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(te_l[acc]);   // the even CTA's MMA may reuse it
+      if (!done) { if (lane == 0) fail(); break; }
+    }
+    if (lane == 0) bulk_wait0();
+    if (bad) set_status(p.status, MC_STATUS_NONFINITE_UPDATE);
+  }
+
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync_all();              // no MMA of the pair is still writing either TMEM
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
@@ -365,8 +659,8 @@ EncodeTiledFn get_encode() {
 
 // 3D bf16 map over `batch` row-major [rows, cols] planes (row stride ld,
 // plane stride bstride, both in elements); box = box_cols x box_rows x 1,
-// swizzle 128 B (box_cols 64) or 64 B (box_cols 32), zero fill outside
-// [cols, rows, batch].
+// swizzle 128 B (box_cols 64) or 64 B (box_cols 32), zero fill (loads) and
+// clipping (stores) outside [cols, rows, batch].
 bool encode_3d(CUtensorMap* m, const void* base, int cols, int rows, int batch, long long ld,
                long long bstride, int box_cols, int box_rows, char* err, size_t errlen) {
   EncodeTiledFn enc = get_encode();
@@ -387,61 +681,137 @@ bool encode_3d(CUtensorMap* m, const void* base, int cols, int rows, int batch, 
   return true;
 }
 
-template <int TERMS, bool LO, int BKT>
-cudaError_t launch_variant(const GemmParams& p, cudaStream_t s, char* err, size_t errlen) {
-  constexpr bool SPLIT = TERMS == 3;
-  TmaArgs tm;
+// Operand maps (A rows of a_rows, B rows of b_rows per box) and the 32 x 32
+// epilogue maps for C and D.
+bool encode_all(const GemmParams& p, TmaArgs& tm, bool split, bool lo, int a_rows, int b_rows,
+                char* err, size_t errlen) {
   memset(&tm, 0, sizeof(tm));
   for (int g = 0; g < p.ngroups; ++g) {
     const GemmGroup& G = p.g[g];
-    // A operand: rows of an [M, K] plane (K contiguous)
-    if (!encode_3d(&tm.maps.a_hi[g], G.a_hi, G.K, G.M, G.batch, G.lda, G.a_bstride, BKT, BM, err, errlen))
-      return cudaErrorInvalidValue;
-    if (SPLIT && !encode_3d(&tm.maps.a_lo[g], G.a_lo, G.K, G.M, G.batch, G.lda, G.a_bstride, BKT, BM, err, errlen))
-      return cudaErrorInvalidValue;
+    if (!encode_3d(&tm.maps.a_hi[g], G.a_hi, G.K, G.M, G.batch, G.lda, G.a_bstride, BKT, a_rows, err, errlen)) return false;
+    if (split && !encode_3d(&tm.maps.a_lo[g], G.a_lo, G.K, G.M, G.batch, G.lda, G.a_bstride, BKT, a_rows, err, errlen)) return false;
     if (!G.b_mn_major) {   // B operand: rows of an [N, K] plane
-      if (!encode_3d(&tm.maps.b_hi[g], G.b_hi, G.K, G.N, G.batch, G.ldb, G.b_bstride, BKT, BN, err, errlen))
-        return cudaErrorInvalidValue;
-      if (SPLIT && !encode_3d(&tm.maps.b_lo[g], G.b_lo, G.K, G.N, G.batch, G.ldb, G.b_bstride, BKT, BN, err, errlen))
-        return cudaErrorInvalidValue;
+      if (!encode_3d(&tm.maps.b_hi[g], G.b_hi, G.K, G.N, G.batch, G.ldb, G.b_bstride, BKT, b_rows, err, errlen)) return false;
+      if (split && !encode_3d(&tm.maps.b_lo[g], G.b_lo, G.K, G.N, G.batch, G.ldb, G.b_bstride, BKT, b_rows, err, errlen)) return false;
     } else {               // B operand: [K, N] plane, 64-wide N boxes of BKT rows
-      if (!encode_3d(&tm.maps.b_hi[g], G.b_hi, G.N, G.K, G.batch, G.ldb, G.b_bstride, 64, BKT, err, errlen))
-        return cudaErrorInvalidValue;
-      if (SPLIT && !encode_3d(&tm.maps.b_lo[g], G.b_lo, G.N, G.K, G.batch, G.ldb, G.b_bstride, 64, BKT, err, errlen))
-        return cudaErrorInvalidValue;
+      if (!encode_3d(&tm.maps.b_hi[g], G.b_hi, G.N, G.K, G.batch, G.ldb, G.b_bstride, 64, BKT, err, errlen)) return false;
+      if (split && !encode_3d(&tm.maps.b_lo[g], G.b_lo, G.N, G.K, G.batch, G.ldb, G.b_bstride, 64, BKT, err, errlen)) return false;
     }
+    if (p.beta != 0.f) {
+      if (!encode_3d(&tm.maps.c_hi[g], G.c_hi, G.N, G.M, G.batch, G.ldc, G.c_bstride, 32, 32, err, errlen)) return false;
+      if (lo && !encode_3d(&tm.maps.c_lo[g], G.c_lo, G.N, G.M, G.batch, G.ldc, G.c_bstride, 32, 32, err, errlen)) return false;
+    }
+    if (!encode_3d(&tm.maps.d_hi[g], G.d_hi, G.N, G.M, G.batch, G.ldd, G.d_bstride, 32, 32, err, errlen)) return false;
+    if (lo && !encode_3d(&tm.maps.d_lo[g], G.d_lo, G.N, G.M, G.batch, G.ldd, G.d_bstride, 32, 32, err, errlen)) return false;
   }
-  const int grid = p.total_tiles < sm_count() ? p.total_tiles : sm_count();
-  auto k = ns_gemm_tc_kernel<TERMS, LO, BKT>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Cfg<TERMS, BKT>::kSmem);
+  return true;
+}
+
+template <int TERMS, bool LO, int CL>
+cudaError_t launch_single(const GemmParams& p, cudaStream_t s, char* err, size_t errlen) {
+  TmaArgs tm;
+  // with clusters each CTA's B box is one 128-row half (multicast to both)
+  if (!encode_all(p, tm, TERMS == 3, LO, BM, CL > 1 ? 128 : BN, err, errlen)) return cudaErrorInvalidValue;
+  auto k = ns_gemm_tc_kernel<TERMS, LO, CL>;
+  const int smem = Stages<TERMS, BM, BN>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, kThreads, Cfg<TERMS, BKT>::kSmem, s>>>(p, tm);
+  if (CL == 1) {
+    const int grid = p.total_tiles < sm_count() ? p.total_tiles : sm_count();
+    k<<<grid, kThreads, smem, s>>>(p, tm);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static int max_clusters = 0;
+  if (max_clusters == 0) {
+    cfg.gridDim = dim3(CL * (sm_count() / CL));
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, k, &cfg) != cudaSuccess || max_clusters <= 0)
+      max_clusters = sm_count() / CL;
+  }
+  const int units = p.total_tiles < max_clusters ? p.total_tiles : max_clusters;
+  cfg.gridDim = dim3(CL * units);
+  e = cudaLaunchKernelEx(&cfg, k, p, tm);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-// K step of the tensor-core GEMM: 64 (default) or 32 (MC_NS_BK=32).
-int k_step() {
-  static int bk = 0;
-  if (bk == 0) {
-    const char* e = getenv("MC_NS_BK");
-    bk = (e && atoi(e) == 32) ? 32 : 64;
+template <int TERMS, bool LO>
+cudaError_t launch_pair(const GemmParams& p, cudaStream_t s, char* err, size_t errlen) {
+  TmaArgs tm;
+  if (!encode_all(p, tm, TERMS == 3, LO, 128, 128, err, errlen)) return cudaErrorInvalidValue;
+  auto k = ns_gemm_pair_kernel<TERMS, LO>;
+  const int smem = Stages<TERMS, 128, 128>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static int max_clusters = 0;
+  if (max_clusters == 0) {
+    cfg.gridDim = dim3(2 * (sm_count() / 2));
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, k, &cfg) != cudaSuccess || max_clusters <= 0)
+      max_clusters = sm_count() / 2;
   }
-  return bk;
+  const int pairs = p.total_tiles < max_clusters ? p.total_tiles : max_clusters;
+  cfg.gridDim = dim3(2 * pairs);
+  e = cudaLaunchKernelEx(&cfg, k, p, tm);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
+
+// Work-unit layout of the tensor-core GEMM: MC_NS_CTA=1 single CTAs,
+// 2 = CTA pairs (cta_group::2), 3 = clusters of two CTAs sharing B by
+// multicast (default).
+int cta_mode() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("MC_NS_CTA");
+    v = e ? atoi(e) : 3;
+    if (v < 1 || v > 3) v = 3;
+  }
+  return v;
+}
+bool use_pairs() { return cta_mode() == 2; }
 
 }  // namespace
 
-template <int BKT>
-cudaError_t launch_bk(const GemmParams& p, cudaStream_t s, char* err, size_t errlen) {
-  if (p.xmode != kXSplit) return launch_variant<1, false, BKT>(p, s, err, errlen);
-  if (p.terms == 3) return launch_variant<3, true, BKT>(p, s, err, errlen);
-  return launch_variant<1, true, BKT>(p, s, err, errlen);
-}
-
 cudaError_t launch_ns_gemm_tc(const GemmParams& p, cudaStream_t s, char* err, size_t errlen) {
   if (p.total_tiles <= 0) return cudaSuccess;
-  return k_step() == 32 ? launch_bk<32>(p, s, err, errlen) : launch_bk<64>(p, s, err, errlen);
+  const bool lo = p.xmode == kXSplit;
+  const bool three = lo && p.terms == 3;
+  if (use_pairs()) {
+    if (three) return launch_pair<3, true>(p, s, err, errlen);
+    return lo ? launch_pair<1, true>(p, s, err, errlen) : launch_pair<1, false>(p, s, err, errlen);
+  }
+  if (cta_mode() == 3) {
+    if (three) return launch_single<3, true, 2>(p, s, err, errlen);
+    return lo ? launch_single<1, true, 2>(p, s, err, errlen) : launch_single<1, false, 2>(p, s, err, errlen);
+  }
+  if (three) return launch_single<3, true, 1>(p, s, err, errlen);
+  return lo ? launch_single<1, true, 1>(p, s, err, errlen) : launch_single<1, false, 1>(p, s, err, errlen);
+}
+
+void ns_tc_tile_shape(int* bm, int* bn, int* sym_rows_per_col_block) {
+  if (cta_mode() != 1) { *bm = 256; *bn = 256; *sym_rows_per_col_block = 1; }
+  else { *bm = 128; *bn = 256; *sym_rows_per_col_block = 2; }
 }
 
 }  // namespace mc
