@@ -29,6 +29,16 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MuonClip step ms per layer; NS & max-logit TFLOP/s (% BF16 peak); clip GB/s"
 WORKLOAD = "dense_block"
+WORKLOAD_CONFIG = {
+    "tiny_mha_fp32": {"matrices": "1x256x512 (fp32)", "attention": "B2 S128 H4 d64 causal (fp32)"},
+    "dense_block": {"matrices": "4x2048x2048, 2x5632x2048, 1x2048x5632",
+                    "attention": "B4 S4096 H16 d128 causal"},
+    "k2_mla_layer": {"matrices": "W_DQ 1536x7168, W_UQ 12288x1536, W_DKV 512x7168, W_KR 64x7168, "
+                                 "W_UKV 16384x512, W_O 7168x8192",
+                     "attention": "MLA B1 S4096 H64 q.k 128+64 (shared k^R) causal"},
+    "moe_experts": {"matrices": "64x2048x7168 + 64x7168x2048", "attention": "none"},
+    "long_mla": {"matrices": "as k2_mla_layer", "attention": "MLA B1 S32768 H64 q.k 128+64 causal"},
+}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -128,7 +138,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -191,30 +201,44 @@ def gpu_arm(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
 
-    wl = synth.workload(WORKLOAD)
+    wl = synth.workload(args.workload)
     att = wl.attention
     # ---- inputs resident in HBM (each rank its own layer: weak scaling)
     seed = 1000 + rank
     W, G, M = synth.muon_inputs(wl, seed=seed, device=dev)
     names = [m.name for m in wl.matrices]
     Wl, Gl, Ml = [W[n] for n in names], [G[n] for n in names], [M[n] for n in names]
-    X = synth.normal((att.B, att.S, att.d_model), 1.0, "X", seed, torch.bfloat16, dev)
-    q, k = forward.project_mha(X, W["Wq"], W["Wk"], att.H)          # setup (untimed)
-    q, k = q.contiguous(), k.contiguous()
-    del X
     hp = mc.Hparams()
+    q = k = ks = None
+    segs = []
+    if att is not None:                                 # setup forward (untimed)
+        X, Wa = synth.attention_inputs(wl, seed=seed, device=dev)
+        if att.kind == "mha":
+            q, k = forward.project_mha(X, Wa["Wq"], Wa["Wk"], att.H)
+            q, k = q.contiguous(), k.contiguous()
+            Wq = W["Wq"] if "Wq" in W else Wa["Wq"]
+            Wk = W["Wk"] if "Wk" in W else Wa["Wk"]
+            segs = mc.mha_segments(Wq, Wk, att.H, hp.alpha)
+        else:
+            q, kc, ks = forward.project_mla(X, Wa, att.H, att.d_nope, att.d_rope, att.d_v)
+            q, ks = q.contiguous(), ks.contiguous()
+            k = kc                                      # strided view of [k^C || v]
+            segs = mc.mla_segments(W["W_UQ"], W["W_UKV"], att.H, att.d_nope, att.d_rope, att.d_v)
+        del X
     ws = mc.alloc_workspace(Wl, hp, dev)
-    smax = torch.zeros(att.H, dtype=torch.float32, device=dev)
-    gamma = torch.zeros(att.H, dtype=torch.float32, device=dev)
+    H = att.H if att is not None else 1
+    smax = torch.zeros(H, dtype=torch.float32, device=dev)
+    gamma = torch.zeros(H, dtype=torch.float32, device=dev)
     ncl = torch.zeros(1, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    layer = mc.ClipLayer(smax, mc.mha_segments(W["Wq"], W["Wk"], att.H, hp.alpha), gamma, ncl)
+    layers = [mc.ClipLayer(smax, segs, gamma, ncl)] if att is not None else []
     flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)   # > 129 MB L2
     stream = torch.cuda.current_stream()
 
     def step():
-        mc.qk_max_logit(q, k, smax=smax, status=status, stream=stream)
-        mc.muonclip_step(Wl, Gl, Ml, hp, layers=[layer], workspace=ws, status=status, stream=stream)
+        if att is not None:
+            mc.qk_max_logit(q, k, ks, smax=smax, status=status, stream=stream)
+        mc.muonclip_step(Wl, Gl, Ml, hp, layers=layers, workspace=ws, status=status, stream=stream)
 
     def barrier():
         if dist is not None:
@@ -252,25 +276,28 @@ def gpu_arm(args):
     ms_per_step = t_local / args.steps
     stat = int(status.item())
 
-    # ---- end to end through the public API: pinned host G, Q, K in, metrics out
+    # ---- end to end through the public API: pinned host G (and Q, K) in, metrics out
     Gh = [g.to("cpu").pin_memory() for g in Gl]
-    qh, kh = q.to("cpu").pin_memory(), k.to("cpu").pin_memory()
-    out_h = torch.empty(2 * att.H + 1, dtype=torch.float32).pin_memory()
-    h2d = sum(g.numel() * g.element_size() for g in Gh) + qh.numel() * 2 + kh.numel() * 2
+    feats = [t for t in (q, ks) if t is not None]
+    if k is not None:
+        feats.append(k)
+    fh = [t.to("cpu").pin_memory() for t in feats]
+    out_h = torch.empty(2 * H + 1, dtype=torch.float32).pin_memory()
+    h2d = sum(g.numel() * g.element_size() for g in Gh) + sum(t.numel() * t.element_size() for t in fh)
     d2h = out_h.numel() * 4
-    res = torch.empty(2 * att.H + 1, dtype=torch.float32, device=dev)
+    res = torch.empty(2 * H + 1, dtype=torch.float32, device=dev)
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
 
     def e2e_step():
         for gd, gh in zip(Gl, Gh):
             gd.copy_(gh, non_blocking=True)
-        q.copy_(qh, non_blocking=True)
-        k.copy_(kh, non_blocking=True)
+        for td, th in zip(feats, fh):
+            td.copy_(th, non_blocking=True)
         step()
-        res[:att.H].copy_(smax)
-        res[att.H:2 * att.H].copy_(gamma)
-        res[2 * att.H:].copy_(ncl.float())
+        res[:H].copy_(smax)
+        res[H:2 * H].copy_(gamma)
+        res[2 * H:].copy_(ncl.float())
         out_h.copy_(res, non_blocking=True)
 
     for _ in range(2):
@@ -290,20 +317,35 @@ def gpu_arm(args):
 
     # ---- algorithmic work
     ns_flops = sum(synth.flops_ns(m.rows, m.cols, hp.ns_steps) for m in wl.matrices)
-    ml_flops = synth.flops_max_logit(att.B, att.S, att.H, att.d_head)
+    ml_flops = 0.0
+    clip_bytes = 0
+    if att is not None:
+        d_qk = att.d_head if att.kind == "mha" else att.d_nope + att.d_rope
+        ml_flops = synth.flops_max_logit(att.B, att.S, att.H, d_qk)
+        esz = 2 if wl.dtype == torch.bfloat16 else 4
+        clipped_heads = len(att.scaled_heads)
+        per_head_rows = (2 * att.d_head if att.kind == "mha"
+                         else att.d_nope + att.d_rope + att.d_nope)
+        row_len = {s_.w.shape[1] for s_ in segs}
+        clip_bytes = 2 * clipped_heads * per_head_rows * max(row_len) * esz   # read + write
     pk, pk_src = peaks()
     n_gemm, t_gemm = prof.get("ns_gemm", (0, 0.0))
     n_ml, t_ml = prof.get("max_logit", (0, 0.0))
     n_clip, t_clip = prof.get("clip", (0, 0.0))
     ns_tflops = ns_flops * args.steps / (t_gemm * 1e-3) / 1e12 if t_gemm else None
     ml_tflops = ml_flops * args.steps / (t_ml * 1e-3) / 1e12 if t_ml else None
-    clipped_heads = len(att.scaled_heads)
-    clip_bytes = 2 * 2 * clipped_heads * att.d_head * att.d_model * 2   # Wq+Wk rows, read+write bf16
-    clip_gbs = clip_bytes * args.steps / (t_clip * 1e-3) / 1e9 if t_clip else None
+    clip_gbs = clip_bytes * args.steps / (t_clip * 1e-3) / 1e9 if t_clip and clip_bytes else None
     peak_t = pk["bf16_tflops"]
     per_launch_flops = ns_flops / (n_gemm / args.steps) if n_gemm else None
     achieved = per_launch_flops / (t_gemm / n_gemm * 1e-3) / 1e12 if n_gemm else None
     launches = sum(v[0] for v in prof.values())
+    cfg = {"workload": args.workload, **WORKLOAD_CONFIG[args.workload], "ns_steps": hp.ns_steps,
+           "ns_precision": ("split-bf16 (hi*hi+hi*lo+lo*hi) for the last 3 iterations, hi*hi for "
+                            "the first 2, fp32 accumulate" if wl.dtype == torch.bfloat16
+                            else "fp32 CUDA cores"),
+           "clipped_heads": len(att.scaled_heads) if att is not None else 0,
+           "l2": "flushed (512 MB write) before each step",
+           "parallelism": f"dp{world} (one layer per rank)"}
 
     if rank != 0:
         if dist is not None:
@@ -313,13 +355,9 @@ def gpu_arm(args):
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": "ms", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": WORKLOAD, "matrices": "4x2048x2048, 2x5632x2048, 1x2048x5632",
-                   "attention": "B4 S4096 H16 d128 causal", "ns_steps": hp.ns_steps,
-                   "ns_precision": "split-bf16 (hi*hi+hi*lo+lo*hi), fp32 accumulate",
-                   "clipped_heads": clipped_heads, "l2": "flushed (512 MB write) before each step",
-                   "parallelism": f"dp{world} (one layer per rank)"},
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if wl.dtype == torch.bfloat16 else "f32", "data": "synthetic",
+        "config": cfg,
         "clocks": clk.summary(),
         "e2e": {"value": round(e2e_local / args.steps / world, 4), "unit": "ms",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -342,7 +380,7 @@ def gpu_arm(args):
             "wall_s_timed_loop": round(wall, 3), "device_status": stat,
         },
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and args.workload == WORKLOAD:
         v, desc = oracle_sample(heads=1)
         line["cpu_baseline"] = {"value": round(v, 1), "unit": "ms", "cores": cpu_cores(),
                                 "kind": "oracle", "sample": desc}
@@ -354,10 +392,12 @@ def gpu_arm(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(WORKLOAD_CONFIG),
+                    help="dense_block is the reported workload; the others for exploration")
     args = ap.parse_args()
     if args.impl == "reference":
         reference_arm(args)
