@@ -72,6 +72,19 @@ typedef enum { MC_F32 = 0, MC_BF16 = 1 } mc_dtype;
  *   MC_NS_AUTO: SPLIT_BF16 when every weight is bf16, else FP32. */
 typedef enum { MC_NS_AUTO = 0, MC_NS_SPLIT_BF16 = 1, MC_NS_BF16 = 2, MC_NS_FP32 = 3 } mc_ns_precision;
 
+/* Factor applied to NewtonSchulz(M) for a weight stored [rows=out, cols=in].
+ *   MC_SCALE_RMS: rms_scale * sqrt(max(rows, cols)) (AdamW-matched update RMS,
+ *     [K2-internals] Algorithm 1; the default).
+ *   MC_SCALE_SPECTRAL: sqrt(max(1, rows / cols)) (the MuP-style scale of the
+ *     zhihu answer's section 3.2); rms_scale is ignored. */
+typedef enum { MC_SCALE_RMS = 0, MC_SCALE_SPECTRAL = 1 } mc_scale_mode;
+
+/* QK-Clip granularity.
+ *   MC_CLIP_PER_HEAD: gamma_h = tau / S_max^h for each head over tau (K2).
+ *   MC_CLIP_TOTAL: one gamma = tau / max_h S_max^h for every head when that
+ *     max exceeds tau (the naive form of [K2-internals] "核心数学"). */
+typedef enum { MC_CLIP_PER_HEAD = 0, MC_CLIP_TOTAL = 1 } mc_clip_mode;
+
 typedef struct {
   void* ptr;      /* device pointer, 16-byte aligned                    */
   int32_t dtype;  /* mc_dtype                                           */
@@ -98,6 +111,7 @@ typedef struct {
                           use one bf16 product (hi operands only) on the split
                           iterate; the last three iterations always use the
                           three-term split product.  Default 2.              */
+  int32_t scale_mode;  /* mc_scale_mode: factor on NewtonSchulz(M)            */
 } mc_hparams;
 
 /* One head-blocked row segment of a weight that QK-Clip rescales.  Head h
@@ -124,6 +138,8 @@ typedef struct {
   const mc_clip_seg* segs; /* host array of nsegs                           */
   float* gamma_out;        /* device [H] or NULL: gamma_h (1 when no clip)  */
   int32_t* nclipped;       /* device int or NULL: heads clipped in layer    */
+  int32_t mode;            /* mc_clip_mode                                  */
+  int32_t _pad;
 } mc_clip_layer;
 
 /* Query/key features of one attention layer, for the per-head max logit.
@@ -154,7 +170,7 @@ typedef struct {
 
 /* Fill *hp with the defaults named above (mu 0.95, lr 2e-4, weight_decay 0.1,
  * rms_scale 0.2, 5 steps of the quintic (3.4445, -4.7750, 2.0315),
- * ns_eps 1e-7, tau 100, alpha 0.5, MC_NS_AUTO, ns_fast_steps 2). */
+ * ns_eps 1e-7, tau 100, alpha 0.5, MC_NS_AUTO, ns_fast_steps 2, MC_SCALE_RMS). */
 void mc_default_hparams(mc_hparams* hp);
 
 /* Bytes of workspace that muon_newton_schulz / muonclip_step need for these
@@ -211,15 +227,17 @@ mc_status muon_newton_schulz_noalloc(const mc_mat* M, mc_mat* O, int32_t count,
 mc_status qk_max_logit(const mc_attn_desc* attn, float* smax, int64_t* argmax,
                        int32_t accumulate, int32_t* status, mc_stream_t stream);
 
-/* QK-Clip for one attention layer: for every head with smax[h] > tau,
- * gamma_h = tau / smax[h] and every segment's rows of head h are multiplied by
- * gamma_h^exponent.  Heads with smax[h] <= tau (or NaN: also sets
- * MC_STATUS_NONFINITE_SMAX) are untouched bit for bit.  [K2-internals]
- * Algorithm 1 QK-Clip branch; "MLA 的特殊处理". gamma_out: device float[H] or
- * NULL; nclipped: device int or NULL (number of heads clipped). */
-mc_status qk_clip_apply(const float* smax, int32_t H, float tau, const mc_clip_seg* segs,
-                        int32_t nsegs, float* gamma_out, int32_t* nclipped, int32_t* status,
-                        mc_stream_t stream);
+/* QK-Clip for one attention layer.  MC_CLIP_PER_HEAD: for every head with
+ * smax[h] > tau, gamma_h = tau / smax[h] and every segment's rows of head h are
+ * multiplied by gamma_h^exponent; heads with smax[h] <= tau are untouched bit
+ * for bit.  MC_CLIP_TOTAL: when max_h smax[h] > tau, every head's rows take
+ * gamma = tau / max_h smax[h].  A NaN S_max sets MC_STATUS_NONFINITE_SMAX and
+ * is never clipped on (in total mode nothing is clipped).  [K2-internals]
+ * Algorithm 1 QK-Clip branch; "核心数学"; "MLA 的特殊处理".  gamma_out:
+ * device float[H] or NULL; nclipped: device int or NULL (heads clipped). */
+mc_status qk_clip_apply(const float* smax, int32_t H, float tau, int32_t mode,
+                        const mc_clip_seg* segs, int32_t nsegs, float* gamma_out,
+                        int32_t* nclipped, int32_t* status, mc_stream_t stream);
 
 /* One MuonClip step ([K2-internals] Algorithm 1): for every matrix
  * M = mu M + G; O = NS(M) sqrt(max) rms_scale; W = W - lr (O + wd W); then for

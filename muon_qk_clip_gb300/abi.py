@@ -26,6 +26,8 @@ MC_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 MC_F32, MC_BF16 = 0, 1
 MC_NS_AUTO, MC_NS_SPLIT_BF16, MC_NS_BF16, MC_NS_FP32 = 0, 1, 2, 3
+MC_SCALE_RMS, MC_SCALE_SPECTRAL = 0, 1
+MC_CLIP_PER_HEAD, MC_CLIP_TOTAL = 0, 1
 
 
 class McMat(ctypes.Structure):
@@ -37,7 +39,7 @@ class McHparams(ctypes.Structure):
     _fields_ = [("mu", c_float), ("lr", c_float), ("weight_decay", c_float), ("rms_scale", c_float),
                 ("ns_steps", c_int32), ("ns_a", c_float), ("ns_b", c_float), ("ns_c", c_float),
                 ("ns_eps", c_float), ("tau", c_float), ("alpha", c_float), ("ns_precision", c_int32),
-                ("ns_fast_steps", c_int32)]
+                ("ns_fast_steps", c_int32), ("scale_mode", c_int32)]
 
 
 class McClipSeg(ctypes.Structure):
@@ -47,7 +49,8 @@ class McClipSeg(ctypes.Structure):
 
 class McClipLayer(ctypes.Structure):
     _fields_ = [("smax", c_void_p), ("H", c_int32), ("nsegs", c_int32),
-                ("segs", POINTER(McClipSeg)), ("gamma_out", c_void_p), ("nclipped", c_void_p)]
+                ("segs", POINTER(McClipSeg)), ("gamma_out", c_void_p), ("nclipped", c_void_p),
+                ("mode", c_int32), ("_pad", c_int32)]
 
 
 class McAttnDesc(ctypes.Structure):
@@ -71,8 +74,8 @@ SIGNATURES = {
     "muon_newton_schulz_noalloc": (c_int32, [POINTER(McMat), POINTER(McMat), c_int32,
                                              POINTER(McHparams), c_void_p, c_void_p]),
     "qk_max_logit": (c_int32, [POINTER(McAttnDesc), c_void_p, c_void_p, c_int32, c_void_p, c_void_p]),
-    "qk_clip_apply": (c_int32, [c_void_p, c_int32, c_float, POINTER(McClipSeg), c_int32, c_void_p,
-                                c_void_p, c_void_p, c_void_p]),
+    "qk_clip_apply": (c_int32, [c_void_p, c_int32, c_float, c_int32, POINTER(McClipSeg), c_int32,
+                                c_void_p, c_void_p, c_void_p, c_void_p]),
     "muonclip_step": (c_int32, [POINTER(McMat), POINTER(McMat), POINTER(McMat), c_int32,
                                 POINTER(McHparams), POINTER(McClipLayer), c_int32, c_void_p,
                                 c_size_t, c_void_p, c_void_p]),

@@ -9,7 +9,7 @@ from __future__ import annotations
 
 import ctypes
 import math
-from dataclasses import dataclass, field
+from dataclasses import dataclass
 
 import torch
 
@@ -60,19 +60,20 @@ class Hparams:
     alpha: float = 0.5
     ns_precision: int = abi.MC_NS_AUTO
     ns_fast_steps: int = 2
+    scale_mode: int = abi.MC_SCALE_RMS
 
     def c(self) -> McHparams:
         a, b, c = self.ns_coeffs
         return McHparams(self.mu, self.lr, self.weight_decay, self.rms_scale, self.ns_steps,
                          a, b, c, self.ns_eps, self.tau, self.alpha, self.ns_precision,
-                         self.ns_fast_steps)
+                         self.ns_fast_steps, self.scale_mode)
 
 
 def default_hparams() -> Hparams:
     h = McHparams()
     abi.load().mc_default_hparams(ctypes.byref(h))
     return Hparams(h.mu, h.lr, h.weight_decay, h.rms_scale, h.ns_steps, (h.ns_a, h.ns_b, h.ns_c),
-                   h.ns_eps, h.tau, h.alpha, h.ns_precision, h.ns_fast_steps)
+                   h.ns_eps, h.tau, h.alpha, h.ns_precision, h.ns_fast_steps, h.scale_mode)
 
 
 def workspace_size(shapes_or_tensors, hp: Hparams | None = None) -> int:
@@ -171,10 +172,11 @@ def _segs(segs):
 
 
 def qk_clip_apply(smax, tau: float, segments, gamma_out=None, nclipped=None, status=None,
-                  stream=None):
-    """Rescale the rows of every head whose smax exceeds tau (in place)."""
+                  stream=None, mode: int = abi.MC_CLIP_PER_HEAD):
+    """Rescale the rows of every head whose smax exceeds tau (in place); with
+    mode=MC_CLIP_TOTAL every head takes one gamma from the layer's max."""
     arr = _segs(segments)
-    check(abi.load().qk_clip_apply(_ptr(smax), smax.numel(), tau, arr, len(segments),
+    check(abi.load().qk_clip_apply(_ptr(smax), smax.numel(), tau, mode, arr, len(segments),
                                    _ptr(gamma_out), _ptr(nclipped), _ptr(status), _stream(stream)),
           "qk_clip_apply")
 
@@ -185,7 +187,7 @@ class ClipLayer:
     segments: list
     gamma_out: torch.Tensor | None = None
     nclipped: torch.Tensor | None = None
-    _keep: list = field(default_factory=list, repr=False)
+    mode: int = abi.MC_CLIP_PER_HEAD
 
 
 def muonclip_step(W, G, M, hp: Hparams | None = None, layers=(), workspace=None, status=None,
@@ -201,7 +203,7 @@ def muonclip_step(W, G, M, hp: Hparams | None = None, layers=(), workspace=None,
         keep.append(segs)
         larr[i] = McClipLayer(_ptr(L.smax), L.smax.numel(), len(L.segments),
                               ctypes.cast(segs, ctypes.POINTER(McClipSeg)),
-                              _ptr(L.gamma_out), _ptr(L.nclipped))
+                              _ptr(L.gamma_out), _ptr(L.nclipped), L.mode, 0)
     hc = hp.c()
     check(abi.load().muonclip_step(_mats(W), _mats(G), _mats(M), len(W), ctypes.byref(hc), larr,
                                    len(layers), _ptr(workspace), workspace.numel(), _ptr(status),

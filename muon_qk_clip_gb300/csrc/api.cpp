@@ -125,6 +125,8 @@ mc_status check_hparams(const mc_hparams* hp) {
     return fail(MC_ERR_INVALID_ARG, "hparams: alpha outside [0, 1]");
   if (hp->ns_precision < MC_NS_AUTO || hp->ns_precision > MC_NS_FP32)
     return fail(MC_ERR_INVALID_ARG, "hparams: unknown ns_precision %d", hp->ns_precision);
+  if (hp->scale_mode != MC_SCALE_RMS && hp->scale_mode != MC_SCALE_SPECTRAL)
+    return fail(MC_ERR_INVALID_ARG, "hparams: unknown scale_mode %d", hp->scale_mode);
   if (hp->ns_fast_steps < 0 || hp->ns_fast_steps > 32)
     return fail(MC_ERR_INVALID_ARG, "hparams: ns_fast_steps %d outside [0, 32]", hp->ns_fast_steps);
   return MC_OK;
@@ -419,7 +421,9 @@ mc_status run_apply(const Plan& P, void* ws, mc_mat* out, bool write_o, const mc
       jb.tile_begin = t;
       jb.tiles_c = (int)cdiv(jb.cols, 64);
       jb.mat = j;
-      jb.scale = (float)((double)hp->rms_scale * std::sqrt((double)std::max(jb.rows, jb.cols)));
+      jb.scale = hp->scale_mode == MC_SCALE_SPECTRAL
+                     ? (float)std::sqrt(std::max(1.0, (double)jb.rows / (double)jb.cols))
+                     : (float)((double)hp->rms_scale * std::sqrt((double)std::max(jb.rows, jb.cols)));
       t += (int)(cdiv(jb.rows, 64) * jb.tiles_c);
     }
     ap.total_tiles = t;
@@ -452,12 +456,13 @@ mc_status check_segments(const mc_clip_seg* segs, int nsegs, int H, const char* 
   return MC_OK;
 }
 
-mc_status run_clip(const float* smax, int H, float tau, const mc_clip_seg* segs, int nsegs,
-                   float* gamma_out, int32_t* nclipped, int32_t* status, cudaStream_t s) {
+mc_status run_clip(const float* smax, int H, float tau, int mode, const mc_clip_seg* segs,
+                   int nsegs, float* gamma_out, int32_t* nclipped, int32_t* status, cudaStream_t s) {
   ClipParams cp;
   memset(&cp, 0, sizeof cp);
   cp.nsegs = nsegs;
   cp.H = H;
+  cp.total = mode == MC_CLIP_TOTAL;
   cp.tau = tau;
   cp.smax = smax;
   cp.gamma_out = gamma_out;
@@ -541,6 +546,7 @@ void mc_default_hparams(mc_hparams* hp) {
   hp->alpha = 0.5f;
   hp->ns_precision = MC_NS_AUTO;
   hp->ns_fast_steps = 2;
+  hp->scale_mode = MC_SCALE_RMS;
 }
 
 const char* mc_last_error(void) { return g_last_error.c_str(); }
@@ -675,14 +681,16 @@ mc_status qk_max_logit(const mc_attn_desc* a, float* smax, int64_t* argmax, int3
   return ok();
 }
 
-mc_status qk_clip_apply(const float* smax, int32_t H, float tau, const mc_clip_seg* segs,
-                        int32_t nsegs, float* gamma_out, int32_t* nclipped, int32_t* status,
-                        mc_stream_t stream) {
+mc_status qk_clip_apply(const float* smax, int32_t H, float tau, int32_t mode,
+                        const mc_clip_seg* segs, int32_t nsegs, float* gamma_out,
+                        int32_t* nclipped, int32_t* status, mc_stream_t stream) {
   if (!smax) return fail(MC_ERR_INVALID_ARG, "smax: null");
   if (!(tau > 0.f) || !std::isfinite(tau)) return fail(MC_ERR_INVALID_ARG, "tau must be finite and > 0");
+  if (mode != MC_CLIP_PER_HEAD && mode != MC_CLIP_TOTAL)
+    return fail(MC_ERR_INVALID_ARG, "qk_clip_apply: unknown mode %d", mode);
   mc_status st = check_segments(segs, nsegs, H, "qk_clip_apply");
   if (st != MC_OK) return st;
-  st = run_clip(smax, H, tau, segs, nsegs, gamma_out, nclipped, status, (cudaStream_t)stream);
+  st = run_clip(smax, H, tau, mode, segs, nsegs, gamma_out, nclipped, status, (cudaStream_t)stream);
   return st == MC_OK ? ok() : st;
 }
 
@@ -706,6 +714,8 @@ mc_status muonclip_step(mc_mat* W, const mc_mat* G, mc_mat* M, int32_t count,
   }
   for (int l = 0; l < nlayers; ++l) {
     if (!layers[l].smax) return fail(MC_ERR_INVALID_ARG, "layer %d: smax null", l);
+    if (layers[l].mode != MC_CLIP_PER_HEAD && layers[l].mode != MC_CLIP_TOTAL)
+      return fail(MC_ERR_INVALID_ARG, "layer %d: unknown clip mode %d", l, layers[l].mode);
     if ((st = check_segments(layers[l].segs, layers[l].nsegs, layers[l].H, "muonclip_step")) != MC_OK)
       return st;
   }
@@ -722,7 +732,7 @@ mc_status muonclip_step(mc_mat* W, const mc_mat* G, mc_mat* M, int32_t count,
   // Algorithm 1, part 2: per-head QK-Clip on the updated weights
   for (int l = 0; l < nlayers; ++l) {
     const mc_clip_layer& L = layers[l];
-    if ((st = run_clip(L.smax, L.H, hp->tau, L.segs, L.nsegs, L.gamma_out, L.nclipped, status, s)) != MC_OK)
+    if ((st = run_clip(L.smax, L.H, hp->tau, L.mode, L.segs, L.nsegs, L.gamma_out, L.nclipped, status, s)) != MC_OK)
       return st;
   }
   return ok();

@@ -156,6 +156,7 @@ struct ClipParams {
   ClipSegDev segs[kMaxSegs];
   int nsegs;
   int H;
+  int total;               // 1: one gamma from max_h smax for every head
   float tau;
   const float* smax;
   float* gamma_out;

@@ -325,13 +325,31 @@ __device__ inline float clip_power(float gamma, float e) {
   return powf(gamma, e);
 }
 
+// Total mode: the layer's max S_max (NaN if any head's is NaN).
+__device__ inline float total_smax(const ClipParams& p) {
+  float mx = -INFINITY;
+  bool nan = false;
+  for (int h = 0; h < p.H; ++h) {
+    const float s = p.smax[h];
+    nan |= s != s;
+    mx = fmaxf(mx, s);
+  }
+  return nan ? NAN : mx;
+}
+
 __global__ void clip_stats_kernel(const __grid_constant__ ClipParams p) {
   // one block: gamma_out, nclipped and the NaN flag
+  __shared__ float s_total;
+  if (p.total) {
+    if (threadIdx.x == 0) s_total = total_smax(p);
+    __syncthreads();
+  }
   int local = 0;
   for (int h = threadIdx.x; h < p.H; h += blockDim.x) {
-    const float s = p.smax[h];
+    const float sh = p.smax[h];
+    const float s = p.total ? s_total : sh;
     const bool clip = s > p.tau;
-    if (s != s) set_status(p.status, MC_STATUS_NONFINITE_SMAX);
+    if (sh != sh) set_status(p.status, MC_STATUS_NONFINITE_SMAX);
     if (p.gamma_out) p.gamma_out[h] = clip ? p.tau / s : 1.f;
     local += clip;
   }
@@ -350,7 +368,10 @@ __global__ void __launch_bounds__(kThreads) clip_rows_kernel(const __grid_consta
   const int pair = blockIdx.x;
   const int seg = pair / p.H, h = pair % p.H;
   if (seg >= p.nsegs) return;
-  const float s = p.smax[h];
+  __shared__ float s_blk;
+  if (threadIdx.x == 0) s_blk = p.total ? total_smax(p) : p.smax[h];
+  __syncthreads();
+  const float s = s_blk;
   if (!(s > p.tau)) return;                       // untouched head (and NaN)
   const ClipSegDev& sg = p.segs[seg];
   const float f = clip_power(p.tau / s, sg.exponent);

@@ -63,6 +63,7 @@ class Hparams:
     ns_eps: float = 1e-7
     tau: float = 100.0
     alpha: float = 0.5
+    scale_mode: str = "rms"        # "rms": 0.2 sqrt(max(n, m)); "spectral": sqrt(max(1, out/in))
 
 
 # ---------------------------------------------------------------------------
@@ -110,15 +111,26 @@ def newton_schulz(M: np.ndarray, steps: int = 5, coeffs=DEFAULT_NS_COEFFS,
     return X.T if transpose else X
 
 
+def update_scale(rows: int, cols: int, hp: Hparams) -> float:
+    """Factor on NewtonSchulz(M) for a weight stored [out=rows, in=cols].
+
+    "rms": sqrt(max(n, m)) * 0.2, matching AdamW's update RMS ([K2-internals]
+    Algorithm 1, "Match Adam RMS"; [K2-zhihu] MuonClip formula).
+    "spectral": sqrt(max(1, d_out / d_in)), the MuP-style scale the zhihu
+    answer's section 3.2 describes for later Muon versions."""
+    if hp.scale_mode == "spectral":
+        return math.sqrt(max(1.0, rows / cols))
+    return math.sqrt(max(rows, cols)) * hp.rms_scale
+
+
 def muon_direction(M: np.ndarray, hp: Hparams) -> np.ndarray:
-    """O_t = NewtonSchulz(M_t) * sqrt(max(n, m)) * 0.2.
+    """O_t = NewtonSchulz(M_t) * update_scale (default sqrt(max(n, m)) * 0.2).
 
     [K2-internals] Algorithm 1, orthogonalisation step ("Match Adam RMS");
     [K2-zhihu] MuonClip formula (second row).
     """
     r, c = M.shape
-    return newton_schulz(M, hp.ns_steps, hp.ns_coeffs, hp.ns_eps) * (
-        math.sqrt(max(r, c)) * hp.rms_scale)
+    return newton_schulz(M, hp.ns_steps, hp.ns_coeffs, hp.ns_eps) * update_scale(r, c, hp)
 
 
 def muon_apply(W_prev: np.ndarray, O: np.ndarray, lr: float, weight_decay: float) -> np.ndarray:
@@ -246,9 +258,25 @@ def total_clip_factor(smax: np.ndarray, tau: float) -> float:
     """The naive all-head variant: one gamma = min(1, tau / max_h S_max^h).
 
     [K2-internals] "核心数学" (朴素实现); [K2-zhihu] (Total Clip before Per-Head).
+    A NaN among the S_max values means no clip.
     """
     s = float(np.max(smax))
-    return min(1.0, tau / s) if s > 0 else 1.0
+    return tau / s if s > tau else 1.0
+
+
+def qk_clip_total(weights: dict, segments, smax: np.ndarray, tau: float):
+    """Total QK-Clip: every head's segment rows scale by gamma^exponent with the
+    one gamma of total_clip_factor.  Returns (new weights, gamma)."""
+    g = total_clip_factor(smax, tau)
+    out = {k: np.array(v, np.float64) for k, v in weights.items()}
+    if g < 1.0:
+        H = len(smax)
+        for seg in segments:
+            W = out[seg.name]
+            for h in range(H):
+                r0 = seg.offset + h * seg.stride
+                W[r0:r0 + seg.rows] *= g ** seg.exponent
+    return out, g
 
 
 def mha_segments(H: int, d: int, alpha: float = 0.5):

@@ -122,7 +122,8 @@ def test_momentum_rejects_shape_mismatch_and_bad_mu(lib):
 @pytest.mark.parametrize("field,value", [("ns_steps", -1), ("ns_steps", 33), ("tau", 0.0),
                                          ("tau", -3.0), ("alpha", 1.5), ("ns_eps", -1.0),
                                          ("lr", float("inf")), ("ns_precision", 9),
-                                         ("ns_fast_steps", -1), ("ns_fast_steps", 40)])
+                                         ("ns_fast_steps", -1), ("ns_fast_steps", 40),
+                                         ("scale_mode", 3)])
 def test_newton_schulz_rejects_bad_hparams(lib, field, value):
     h = hp(**{field: value})
     rc = lib.muon_newton_schulz(arr(m(64, 128)), arr(m(64, 128)), 1, ctypes.byref(h),
@@ -202,7 +203,13 @@ def segarr(*ss):
     (seg(m(64, 32), 0, 16, 16, 0.5), 4, 0.0, abi.MC_ERR_INVALID_ARG),     # tau
 ])
 def test_clip_rejects(lib, s, H, tau, code):
-    assert lib.qk_clip_apply(ctypes.c_void_p(FAKE), H, tau, segarr(s), 1, None, None, None, None) == code
+    assert lib.qk_clip_apply(ctypes.c_void_p(FAKE), H, tau, 0, segarr(s), 1, None, None, None, None) == code
+
+
+def test_clip_rejects_unknown_mode(lib):
+    s = seg(m(64, 32), 0, 16, 16, 0.5)
+    assert lib.qk_clip_apply(ctypes.c_void_p(FAKE), 4, 100.0, 7, segarr(s), 1, None, None, None,
+                             None) == abi.MC_ERR_INVALID_ARG
 
 
 def test_step_rejects_mismatch_and_bad_layer(lib):
@@ -211,7 +218,7 @@ def test_step_rejects_mismatch_and_bad_layer(lib):
     assert lib.muonclip_step(W, G, M, 1, ctypes.byref(h), None, 0, ctypes.c_void_p(FAKE), 1 << 30,
                              None, None) == abi.MC_ERR_INVALID_ARG
     L = (McClipLayer * 1)()
-    L[0] = McClipLayer(None, 4, 0, None, None, None)
+    L[0] = McClipLayer(None, 4, 0, None, None, None, 0, 0)
     assert lib.muonclip_step(W, G, arr(m(64, 128)), 1, ctypes.byref(h), L, 1, ctypes.c_void_p(FAKE),
                              1 << 30, None, None) == abi.MC_ERR_INVALID_ARG
 

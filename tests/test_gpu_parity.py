@@ -157,7 +157,8 @@ def test_ns_zero_matrix():
 def oracle_muon(W, G, M, hp):
     ohp = O.Hparams(mu=fp32(hp.mu), lr=fp32(hp.lr), weight_decay=fp32(hp.weight_decay),
                     rms_scale=fp32(hp.rms_scale), ns_steps=hp.ns_steps,
-                    ns_coeffs=tuple(fp32(c) for c in hp.ns_coeffs), ns_eps=fp32(hp.ns_eps))
+                    ns_coeffs=tuple(fp32(c) for c in hp.ns_coeffs), ns_eps=fp32(hp.ns_eps),
+                    scale_mode="spectral" if hp.scale_mode == abi.MC_SCALE_SPECTRAL else "rms")
     return O.muon_step(f64(W), f64(G), f64(M), ohp), ohp
 
 
@@ -181,6 +182,30 @@ def test_muon_step_parity(wdtype, precision, tol, warm):
     assert st.item() == 0
     for (Wn, Mn, Od), w, m in zip(want, W, M):
         assert_rounded_within(m, Mn, 0.0, "momentum state")
+        assert_rounded_within(w, Wn, tol * rms(fp32(hp.lr) * Od), "updated W")
+
+
+@pytest.mark.parametrize("wdtype,precision,tol", [(F32, abi.MC_NS_FP32, 1e-5),
+                                                  (BF16, abi.MC_NS_SPLIT_BF16, 2e-2)])
+def test_muon_step_spectral_scale(wdtype, precision, tol):
+    """The MuP-style update scale sqrt(max(1, out/in)): tall, wide and square
+    weights in one call (factor 3, 1 and 1)."""
+    shapes = [(576, 64), (128, 320), (96, 96)]
+    hp = mc.Hparams(ns_precision=precision, scale_mode=abi.MC_SCALE_SPECTRAL)
+    W, G, M, want = [], [], [], []
+    for i, (r, c) in enumerate(shapes):
+        w = synth.normal((r, c), 0.02, f"sw{i}", 13).to(wdtype)
+        g = synth.normal((r, c), 1.0, f"sg{i}", 13)
+        m = synth.normal((r, c), 2.0, f"sm{i}", 13)
+        (Wn, Mn, Od), ohp = oracle_muon(w, g, m, hp)
+        assert ohp.scale_mode == "spectral"
+        want.append((Wn, Od))
+        W.append(w.cuda()); G.append(g.cuda()); M.append(m.cuda())
+    st = new_status()
+    mc.muonclip_step(W, G, M, hp, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    for (Wn, Od), w in zip(want, W):
         assert_rounded_within(w, Wn, tol * rms(fp32(hp.lr) * Od), "updated W")
 
 
@@ -362,6 +387,72 @@ def test_clip_nan_smax_flags_and_leaves_weights():
     torch.cuda.synchronize()
     assert st.item() & abi.MC_STATUS_NONFINITE_SMAX
     assert torch.equal(Wq, before[0]) and torch.equal(Wk, before[1])
+
+
+@pytest.mark.parametrize("smax_vals,clipped", [([50.0, 100.0, 150.0, 400.0], True),
+                                               ([50.0, 99.0, 100.0, -1.0], False)])
+def test_clip_total_mode_parity(smax_vals, clipped):
+    """Total clip: one gamma = tau / max_h S_max^h on every head's rows."""
+    H, d, D, tau = 4, 16, 40, 100.0
+    Wq = synth.normal((H * d, D), 1.0, "tq", 14).to(BF16)
+    Wk = synth.normal((H * d, D), 1.0, "tk", 14).to(BF16)
+    smax = torch.tensor(smax_vals)
+    dq, dk = Wq.cuda(), Wk.cuda()
+    gamma = torch.empty(H, device="cuda")
+    ncl = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mc.qk_clip_apply(smax.cuda(), tau, mc.mha_segments(dq, dk, H, 0.5), gamma_out=gamma,
+                     nclipped=ncl, mode=abi.MC_CLIP_TOTAL)
+    torch.cuda.synchronize()
+    out, g = O.qk_clip_total({"Wq": f64(Wq), "Wk": f64(Wk)}, O.mha_segments(H, d, 0.5),
+                             f64(smax), tau)
+    assert (g < 1.0) == clipped
+    assert ncl.item() == (H if clipped else 0)
+    np.testing.assert_allclose(f64(gamma), np.full(H, g), rtol=1e-6)
+    if clipped:
+        assert_rounded_within(dq, out["Wq"], 1e-6 * np.abs(out["Wq"]), "Wq")
+        assert_rounded_within(dk, out["Wk"], 1e-6 * np.abs(out["Wk"]), "Wk")
+    else:
+        assert torch.equal(dq.cpu(), Wq) and torch.equal(dk.cpu(), Wk)
+
+
+def test_clip_total_mode_mla_in_step():
+    """Total clip of an MLA layer inside muonclip_step (beside one unrelated
+    Muon matrix): q^C and k^C by sqrt(gamma), q^R by gamma, v rows untouched."""
+    H, dn, dr, dv, ql, kl, tau = 4, 16, 8, 16, 24, 16, 100.0
+    W_UQ = synth.normal((H * (dn + dr), ql), 1.0, "tuq", 15).to(BF16)
+    W_UKV = synth.normal((H * (dn + dv), kl), 1.0, "tukv", 15).to(BF16)
+    smax = torch.tensor([30.0, 250.0, 99.0, 120.0])
+    d_uq, d_ukv = W_UQ.cuda(), W_UKV.cuda()
+    layer = mc.ClipLayer(smax.cuda(), mc.mla_segments(d_uq, d_ukv, H, dn, dr, dv),
+                         mode=abi.MC_CLIP_TOTAL)
+    w = synth.normal((64, 96), 0.02, "tw", 15).to(BF16).cuda()
+    mc.muonclip_step([w], [torch.ones(64, 96, device="cuda")], [torch.zeros(64, 96, device="cuda")],
+                     mc.Hparams(), layers=[layer])
+    torch.cuda.synchronize()
+    out, g = O.qk_clip_total({"W_UQ": f64(W_UQ), "W_UKV": f64(W_UKV)},
+                             O.mla_segments(H, dn, dr, dv), f64(smax), tau)
+    assert g == pytest.approx(0.4)
+    assert_rounded_within(d_uq, out["W_UQ"], 1e-6 * np.abs(out["W_UQ"]), "W_UQ")
+    assert_rounded_within(d_ukv, out["W_UKV"], 1e-6 * np.abs(out["W_UKV"]), "W_UKV")
+    for h in range(H):
+        v = slice(h * (dn + dv) + dn, (h + 1) * (dn + dv))
+        assert torch.equal(d_ukv[v].cpu(), W_UKV[v])
+
+
+def test_clip_total_mode_nan_clips_nothing():
+    H, d = 3, 8
+    Wq = synth.normal((H * d, 16), 1.0, "tnq", 16).to(BF16).cuda()
+    Wk = synth.normal((H * d, 16), 1.0, "tnk", 16).to(BF16).cuda()
+    before = (Wq.clone(), Wk.clone())
+    st = new_status()
+    gamma = torch.empty(H, device="cuda")
+    mc.qk_clip_apply(torch.tensor([500.0, float("nan"), 5.0], device="cuda"), 100.0,
+                     mc.mha_segments(Wq, Wk, H), gamma_out=gamma, status=st,
+                     mode=abi.MC_CLIP_TOTAL)
+    torch.cuda.synchronize()
+    assert st.item() & abi.MC_STATUS_NONFINITE_SMAX
+    assert torch.equal(Wq, before[0]) and torch.equal(Wk, before[1])
+    assert torch.equal(gamma.cpu(), torch.ones(H))
 
 
 # ------------------------------------------------------------------ MuonClip step, tiny MHA

@@ -377,6 +377,36 @@ def test_clip_mla_remeasured_and_shared_key_untouched():
 def test_total_clip_variant():
     assert O.total_clip_factor(np.array([10.0, 250.0, 50.0]), 100.0) == pytest.approx(0.4)
     assert O.total_clip_factor(np.array([10.0, 50.0]), 100.0) == 1.0
+    assert O.total_clip_factor(np.array([100.0, 50.0]), 100.0) == 1.0
+    assert O.total_clip_factor(np.array([np.nan, 500.0]), 100.0) == 1.0
+
+
+def test_total_clip_scales_every_head_and_caps_the_max():
+    """Total clip ([K2-internals] 核心数学, naive form): all heads share one
+    gamma, so the largest re-measured max logit becomes exactly tau and the
+    others shrink by the same factor."""
+    rng = np.random.default_rng(25)
+    H, d, tau = 4, 8, 100.0
+    X, Wq, Wk = mha_layer(rng, H=H, d=d)
+    S0, _ = O.max_logit(*O.project_mha(X, Wq, Wk, H))
+    out, g = O.qk_clip_total({"Wq": Wq, "Wk": Wk}, O.mha_segments(H, d), S0, tau)
+    S1, _ = O.max_logit(*O.project_mha(X, out["Wq"], out["Wk"], H))
+    assert g == pytest.approx(tau / S0.max())
+    np.testing.assert_allclose(S1, S0 * g, rtol=1e-12)
+    assert S1.max() == pytest.approx(tau, rel=1e-12)
+
+
+@pytest.mark.parametrize("shape", [(20, 50), (50, 20)])
+def test_spectral_scale_gives_unit_or_aspect_norm(shape):
+    """MuP-style scale sqrt(max(1, out/in)): with converged msign every singular
+    value of O equals the scale (zhihu answer, section 3.2)."""
+    rng = np.random.default_rng(26)
+    s = rng.uniform(0.3, 1.0, min(shape))
+    M, _, _ = svd_built(*shape, s, rng)
+    hp = O.Hparams(ns_steps=60, ns_coeffs=CUBIC, ns_eps=0.0, scale_mode="spectral")
+    sv = np.linalg.svd(O.muon_direction(M, hp), compute_uv=False)
+    want = math.sqrt(max(1.0, shape[0] / shape[1]))
+    np.testing.assert_allclose(sv, want, rtol=1e-12)
 
 
 def test_muonclip_step_order_muon_then_clip():
