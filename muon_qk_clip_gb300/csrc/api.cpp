@@ -350,6 +350,11 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
     // k-step; the last three iterations always take the three-term product
     const int fast = std::min(hp->ns_fast_steps, std::max(0, hp->ns_steps - 3));
     gp.terms = (P.xmode == kXSplit && it >= fast) ? 3 : 1;
+    // Three-term iterations fold a X into the polynomial: B' = c A^2 + b A + a I
+    // and X' = B' X, so the last phase reads no C.  (B' holds ~16 significand
+    // bits there; a one-plane bf16 B' would lose the small singular values, so
+    // the other iterations keep X' = B X + a X.)
+    const bool fold = P.xmode == kXSplit && gp.terms == 3;
     switch (ph) {
       case kGram:
         gp.alpha = 1.f; gp.beta = 0.f;
@@ -357,9 +362,10 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
         break;
       case kPoly:
         gp.alpha = hp->ns_c; gp.beta = hp->ns_b; gp.s = nullptr;
+        gp.diag = fold ? hp->ns_a : 0.f;
         break;
       case kNext:
-        gp.alpha = 1.f; gp.beta = hp->ns_a;
+        gp.alpha = 1.f; gp.beta = fold ? 0.f : hp->ns_a;
         gp.s = it == 0 ? reinterpret_cast<const float*>(wsp(ws, P.off_inv)) : nullptr;
         break;
     }

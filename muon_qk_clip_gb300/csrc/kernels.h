@@ -98,8 +98,8 @@ cudaError_t launch_norms(const double* partials, const int* tile_begin, const in
 
 // ---------------------------------------------------------------- NS GEMMs
 // One batch of same-shape matrices for a Newton-Schulz phase:
-//   D[b] = s_b * (alpha * P[b] + beta * C[b]),  P = A-operand x B-operand
-// with P an M x N product over K.
+//   D[b] = s_b * (alpha * P[b] + beta * C[b] + diag * I),  P = A-operand x B-operand
+// with P an M x N product over K (diag is nonzero only for square outputs).
 struct GemmGroup {
   int M, N, K, batch;
   int tiles_m, tiles_n;
@@ -119,7 +119,7 @@ struct GemmGroup {
 
 struct alignas(64) GemmTmaps {
   CUtensorMap a_hi[kMaxGroups], a_lo[kMaxGroups], b_hi[kMaxGroups], b_lo[kMaxGroups];
-  CUtensorMap c_hi[kMaxGroups], c_lo[kMaxGroups], d_hi[kMaxGroups], d_lo[kMaxGroups];
+  CUtensorMap d_hi[kMaxGroups], d_lo[kMaxGroups];
 };
 
 struct GemmParams {
@@ -129,6 +129,7 @@ struct GemmParams {
   int xmode;
   int terms;              // tensor-core products per k-step: 1 (hi*hi) or 3 (split)
   float alpha, beta;
+  float diag;             // added on the diagonal of each output item
   const float* s;         // per-matrix scale, or null
   int32_t* status;
 };

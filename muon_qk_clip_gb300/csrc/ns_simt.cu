@@ -1,5 +1,5 @@
 // CUDA-core fp32 GEMM for the fp32 Newton-Schulz path (MC_NS_FP32):
-//   D[b] = s_b * (alpha * A[b] x op(B[b]) + beta * C[b])
+//   D[b] = s_b * (alpha * A[b] x op(B[b]) + beta * C[b] + diag * I)
 // op(B) = B^T when B is stored [N, K] (K contiguous), B when stored [K, N].
 // Used for fp32 weights, where the update must match exact arithmetic to
 // ~1e-5 of its RMS, beyond what bf16 tensor-core operands give.  Each 16-wide
@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(NT) sgemm_kernel(const __grid_constant__ GemmP
         double v = (double)p.alpha * acc64[i][j];
         if (p.beta != 0.f)
           v += (double)p.beta * (double)C[(long long)b * g.c_bstride + (long long)r * g.ldc + c];
+        if (r == c) v += (double)p.diag;
         const float vf = (float)(v * (double)s);
         bad |= !finite_f(vf);
         D[(long long)r * g.ldd + c] = vf;

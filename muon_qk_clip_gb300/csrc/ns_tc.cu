@@ -6,7 +6,9 @@
 //   phase 2  B  = c * A A + b * A      (A symmetric: its rows serve as B^T)
 //   phase 3  X' = s * (B X + a * X)    (B operand X stored [K, N]: MN-major)
 //
-// All three are D = s_b * (alpha * P + beta * C) with P = A_op x B_op^T.
+// All three are D = s_b * (alpha * P + beta * C + diag * I) with
+// P = A_op x B_op^T.  In three-term iterations phase 2 adds a I and phase 3
+// reads no C (X' = s * (B + a I) X).
 // Split mode (default): every operand is a bf16 pair (hi, lo) and
 // P = hi*hi + hi*lo + lo*hi accumulated in fp32 in TMEM, so products carry
 // ~16 significand bits; D is stored again as a (hi, lo) pair.  Plain mode:
@@ -18,10 +20,11 @@
 //   warps 2..5  epilogue: TMEM -> registers -> fused polynomial -> global
 // Tiles are 128 x 256 with K advancing by 32 (64-byte swizzle rows); the
 // accumulator is double-buffered in TMEM (2 x 256 columns) so the epilogue of
-// tile t overlaps the MMAs of tile t+1.  The epilogue stages every 32 x 32
-// chunk through shared memory: C is prefetched there by TMA, D (and, for
-// symmetric outputs, its transpose) leaves by TMA bulk stores, so global
-// memory only sees whole 64-byte rows.
+// tile t overlaps the MMAs of tile t+1.  The epilogue reads C straight into
+// registers and stages every 32 x 32 chunk of D (and, for symmetric outputs,
+// its transpose) through 8 KB of shared memory per warp, from where TMA bulk
+// stores write whole 64-byte rows; the small epilogue footprint leaves room
+// for 4 operand stages in split mode and 8 in one-product mode.
 //
 // Symmetric outputs (phases 1 and 2) are computed only on tiles that touch
 // the upper triangle.  Per 128 x 128 block (I, J) of such a tile: I < J is
@@ -45,7 +48,7 @@ namespace {
 constexpr int BM = 128, BN = 256, BKT = 32;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;    // two 128 x 256 fp32 accumulators
-constexpr int kEpiWarpBytes = 16384;   // per epilogue warp: C x2, D, mirror (hi+lo each)
+constexpr int kEpiWarpBytes = 8192;    // per epilogue warp: two 32 x 32 hi+lo slots
 constexpr int kEpiBytes = 4 * kEpiWarpBytes;
 constexpr int kBarBytes = 256;
 constexpr int kSmemCap = 227 * 1024;
@@ -117,21 +120,28 @@ __device__ inline uint32_t swz64(int row, int b) {
 
 // ------------------------------------------------------------ epilogue
 // One warp's 32 rows [r0, r0 + 32) of an output tile whose accumulator sits in
-// TMEM at `tacc` (lane quadrant q).  D = s_b * (alpha * acc + beta * C).
+// TMEM at `tacc` (lane quadrant q).  D = s_b * (alpha * acc + beta * C + diag I).
 // Symmetric outputs: 32-column chunks in blocks I < J are also stored
-// transposed (mirror); I > J are dropped.  Returns false on a wait timeout.
+// transposed (mirror); I > J are dropped.
+//
+// The warp's 8 KB of shared memory is two 4 KB slots (a 32 x 32 chunk of hi
+// and lo planes each): D and its mirror for symmetric outputs, else a ring of
+// two D chunks, so a chunk waits only for the store group that last used its
+// slot.  `ek` counts this warp's store groups across tiles.  C is read by each
+// lane straight from global memory (its row's 64 contiguous bytes per plane),
+// one chunk ahead, and the next chunk's TMEM load is in flight while the
+// current one is converted.
 template <bool LO>
-__device__ bool epilogue_rows(const GemmParams& p, const TmaArgs& tm, const TileCoord& tc, int r0,
-                              uint32_t tacc, int q, int lane, uint8_t* ebuf, uint64_t* cbar,
-                              uint32_t& cpar, bool& bad, volatile int* abort_flag) {
+__device__ void epilogue_rows(const GemmParams& p, const TmaArgs& tm, const TileCoord& tc, int r0,
+                              uint32_t tacc, int q, int lane, uint8_t* ebuf, uint32_t& ek,
+                              bool& bad) {
   const GemmGroup& G = p.g[tc.g];
-  if (r0 >= G.M) return true;                       // no valid row in this warp
+  if (r0 >= G.M) return;                            // no valid row in this warp
   const float sb = p.s ? p.s[G.mat_base + tc.b] : 1.f;
-  const float al = p.alpha * sb, be = p.beta * sb;
+  const float al = p.alpha * sb, be = p.beta * sb, dg = p.diag * sb;
   const bool use_c = p.beta != 0.f;
-  uint8_t* cb[2] = {ebuf, ebuf + 4096};
-  uint8_t* db = ebuf + 8192;
-  uint8_t* mb = ebuf + 12288;
+  const int per = G.symmetric ? 2 : 1;              // slots per store group
+  const int depth = 2 / per;                        // store groups in flight
   const int I = r0 / 128;
   auto mode_of = [&](int ch) -> int {             // 0 skip, 1 store, 2 store + mirror
     const int col0 = tc.n0 + ch * 32;
@@ -145,62 +155,74 @@ __device__ bool epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
       if (mode_of(c)) return c;
     return BN / 32;
   };
-  auto issue_c = [&](int ch, int buf) {
-    const int col0 = tc.n0 + ch * 32;
-    mbar_arrive_expect_tx(&cbar[buf], LO ? 4096 : 2048);
-    tma_load_3d(cb[buf], &tm.maps.c_hi[tc.g], &cbar[buf], col0, r0, tc.b);
-    if (LO) tma_load_3d(cb[buf] + 2048, &tm.maps.c_lo[tc.g], &cbar[buf], col0, r0, tc.b);
-  };
   const int row = r0 + lane;
+  const bool row_ok = row < G.M;
+  const __nv_bfloat16* c_hi = reinterpret_cast<const __nv_bfloat16*>(G.c_hi) +
+                              (long long)tc.b * G.c_bstride + (long long)row * G.ldc;
+  const __nv_bfloat16* c_lo = reinterpret_cast<const __nv_bfloat16*>(G.c_lo) +
+                              (long long)tc.b * G.c_bstride + (long long)row * G.ldc;
+  // C of one chunk for this lane: 4 x 8 columns per plane (zero past the edges)
+  auto load_c = [&](int ch, uint4 (&h)[4], uint4 (&l)[4]) {
+    const int col0 = tc.n0 + ch * 32;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const bool ok = row_ok && col0 + 8 * j < G.N;
+      h[j] = ok ? __ldg(reinterpret_cast<const uint4*>(c_hi + col0 + 8 * j)) : make_uint4(0, 0, 0, 0);
+      if (LO) l[j] = ok ? __ldg(reinterpret_cast<const uint4*>(c_lo + col0 + 8 * j)) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  const uint32_t trow = tacc + ((uint32_t)(q * 32) << 16);
   int ch = next_live(-1);
-  if (use_c && ch < BN / 32 && lane == 0) issue_c(ch, 0);
-  int k = 0;
-  for (; ch < BN / 32; ch = next_live(ch), ++k) {
+  if (ch >= BN / 32) return;
+  uint4 ch_h[4], ch_l[4], cn_h[4], cn_l[4];
+  if (use_c) load_c(ch, ch_h, ch_l);
+  // every async TMEM load is waited for within the iteration that issued it
+  uint32_t nr[32];
+  float v[32];
+  tmem_ld_32x32b_x32_async(trow + ch * 32, nr);
+  tmem_ld_wait();
+  reg_fence32(nr);
+#pragma unroll
+  for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(nr[e]);
+  while (ch < BN / 32) {
     const int mode = mode_of(ch);
     const int col0 = tc.n0 + ch * 32;
-    const int buf = k & 1;
-    if (use_c && lane == 0) {
-      const int nx = next_live(ch);
-      if (nx < BN / 32) issue_c(nx, buf ^ 1);
+    const int nx = next_live(ch);
+    if (nx < BN / 32) {
+      tmem_ld_32x32b_x32_async(trow + nx * 32, nr);
+      if (use_c) load_c(nx, cn_h, cn_l);
     }
-    float v[32];
-    tmem_ld_32x32b_x32(tacc + ((uint32_t)(q * 32) << 16) + ch * 32, v);
     if (use_c) {
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait(&cbar[buf], (cpar >> buf) & 1, abort_flag) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      cpar ^= 1u << buf;
-      if (!ok) return false;
-      const uint8_t* ch_hi = cb[buf];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const uint4 h = *reinterpret_cast<const uint4*>(ch_hi + swz64(lane, j * 16));
-        const __nv_bfloat16* hh = reinterpret_cast<const __nv_bfloat16*>(&h);
-        if (LO) {
-          const uint4 l = *reinterpret_cast<const uint4*>(ch_hi + 2048 + swz64(lane, j * 16));
-          const __nv_bfloat16* ll = reinterpret_cast<const __nv_bfloat16*>(&l);
+        const __nv_bfloat16* hh = reinterpret_cast<const __nv_bfloat16*>(&ch_h[j]);
+        const __nv_bfloat16* ll = reinterpret_cast<const __nv_bfloat16*>(&ch_l[j]);
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            v[j * 8 + e] = fmaf(al, v[j * 8 + e], be * (__bfloat162float(hh[e]) + __bfloat162float(ll[e])));
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) v[j * 8 + e] = fmaf(al, v[j * 8 + e], be * __bfloat162float(hh[e]));
+        for (int e = 0; e < 8; ++e) {
+          const float cv = LO ? __bfloat162float(hh[e]) + __bfloat162float(ll[e]) : __bfloat162float(hh[e]);
+          v[j * 8 + e] = fmaf(al, v[j * 8 + e], be * cv);
         }
       }
-      fence_async_smem();            // these reads precede the TMA refill of the buffer
     } else {
 #pragma unroll
       for (int e = 0; e < 32; ++e) v[e] *= al;
     }
+    if (dg != 0.f && row >= col0 && row < col0 + 32) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (col0 + e == row) v[e] += dg;
+    }
     __nv_bfloat16 hb[32], lb[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
-      bad |= !finite_f(v[e]) && (col0 + e < G.N) && (row < G.M);
+      bad |= !finite_f(v[e]) && (col0 + e < G.N) && row_ok;
       if (LO) split_bf16(v[e], hb[e], lb[e]);
       else hb[e] = __float2bfloat16_rn(v[e]);
     }
-    // the previous chunk's stores must have finished reading D/mirror buffers
-    if (lane == 0) bulk_wait_read0();
+    uint8_t* db = ebuf + (int)(ek % (uint32_t)depth) * per * 4096;
+    uint8_t* mb = db + 4096;
+    // the store group that last used these slots must have read them
+    if (lane == 0) bulk_wait_read_upto(depth - 1);
     __syncwarp();
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -227,8 +249,19 @@ __device__ bool epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
       }
       bulk_commit();
     }
+    ++ek;
+    if (nx < BN / 32) {
+      tmem_ld_wait();
+      reg_fence32(nr);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(nr[e]);
+      if (use_c) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) { ch_h[j] = cn_h[j]; ch_l[j] = cn_l[j]; }
+      }
+    }
+    ch = nx;
   }
-  return true;
 }
 
 // ------------------------------------------------------------ 1-CTA kernel
@@ -253,8 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = empty + 8;             // [2]
   uint64_t* tempty = tfull + 2;            // [2]
   uint64_t* drain = tempty + 2;            // [1]
-  uint64_t* cbar = drain + 1;              // [4][2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cbar + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -263,7 +295,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < C::kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], CL); }
     for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 4); }
     mbar_init(drain, 1);
-    for (int i = 0; i < 8; ++i) mbar_init(&cbar[i], 1);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -413,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int e = warp - 2;
     const int q = warp & 3;              // TMEM lane quadrant of this warp
     uint8_t* ebuf = epi + e * kEpiWarpBytes;
-    uint32_t cpar = 0;
+    uint32_t ek = 0;
     bool bad = false;
     uint32_t tcount = 0;
     for (int t = unit; t < p.total_tiles; t += nunits, ++tcount) {
@@ -424,12 +455,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) { if (lane == 0) fail(); break; }
       tc_fence_after();
-      const bool done = epilogue_rows<LO>(p, tm, tc, tc.m0 + BM * (int)crank + q * 32, tmem_base + acc * BN, q, lane, ebuf,
-                                          cbar + 2 * e, cpar, bad, &abort_flag);
+      epilogue_rows<LO>(p, tm, tc, tc.m0 + BM * (int)crank + q * 32, tmem_base + acc * BN, q, lane, ebuf,
+                        ek, bad);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
-      if (!done) { if (lane == 0) fail(); break; }
     }
     if (lane == 0) bulk_wait0();         // all TMA stores of this warp complete
     if (bad) set_status(p.status, MC_STATUS_NONFINITE_UPDATE);
@@ -464,8 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = empty + 8;             // [2]
   uint64_t* tempty = tfull + 2;            // [2]
   uint64_t* drain = tempty + 2;            // [1]
-  uint64_t* cbar = drain + 1;              // [4][2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cbar + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -477,7 +506,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < C::kStages; ++s) { mbar_init(&full[s], 2); mbar_init(&empty[s], 1); }
     for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 8); }
     mbar_init(drain, 1);
-    for (int i = 0; i < 8; ++i) mbar_init(&cbar[i], 1);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -607,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     uint8_t* ebuf = epi + e * kEpiWarpBytes;
     const uint32_t te_l[2] = {mapa_shared(smem_u32(&tempty[0]), 0), mapa_shared(smem_u32(&tempty[1]), 0)};
-    uint32_t cpar = 0;
+    uint32_t ek = 0;
     bool bad = false;
     uint32_t tcount = 0;
     for (int t = pair; t < p.total_tiles; t += npairs, ++tcount) {
@@ -618,12 +646,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) { if (lane == 0) fail(); break; }
       tc_fence_after();
-      const bool done = epilogue_rows<LO>(p, tm, tc, tc.m0 + 128 * (int)rank + q * 32, tmem_base + acc * PBN,
-                                          q, lane, ebuf, cbar + 2 * e, cpar, bad, &abort_flag);
+      epilogue_rows<LO>(p, tm, tc, tc.m0 + 128 * (int)rank + q * 32, tmem_base + acc * PBN,
+                        q, lane, ebuf, ek, bad);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(te_l[acc]);   // the even CTA's MMA may reuse it
-      if (!done) { if (lane == 0) fail(); break; }
     }
     if (lane == 0) bulk_wait0();
     if (bad) set_status(p.status, MC_STATUS_NONFINITE_UPDATE);
@@ -682,7 +709,7 @@ bool encode_3d(CUtensorMap* m, const void* base, int cols, int rows, int batch, 
 }
 
 // Operand maps (A rows of a_rows, B rows of b_rows per box) and the 32 x 32
-// epilogue maps for C and D.
+// epilogue store maps for D.
 bool encode_all(const GemmParams& p, TmaArgs& tm, bool split, bool lo, int a_rows, int b_rows,
                 char* err, size_t errlen) {
   memset(&tm, 0, sizeof(tm));
@@ -696,10 +723,6 @@ bool encode_all(const GemmParams& p, TmaArgs& tm, bool split, bool lo, int a_row
     } else {               // B operand: [K, N] plane, 64-wide N boxes of BKT rows
       if (!encode_3d(&tm.maps.b_hi[g], G.b_hi, G.N, G.K, G.batch, G.ldb, G.b_bstride, 64, BKT, err, errlen)) return false;
       if (split && !encode_3d(&tm.maps.b_lo[g], G.b_lo, G.N, G.K, G.batch, G.ldb, G.b_bstride, 64, BKT, err, errlen)) return false;
-    }
-    if (p.beta != 0.f) {
-      if (!encode_3d(&tm.maps.c_hi[g], G.c_hi, G.N, G.M, G.batch, G.ldc, G.c_bstride, 32, 32, err, errlen)) return false;
-      if (lo && !encode_3d(&tm.maps.c_lo[g], G.c_lo, G.N, G.M, G.batch, G.ldc, G.c_bstride, 32, 32, err, errlen)) return false;
     }
     if (!encode_3d(&tm.maps.d_hi[g], G.d_hi, G.N, G.M, G.batch, G.ldd, G.d_bstride, 32, 32, err, errlen)) return false;
     if (lo && !encode_3d(&tm.maps.d_lo[g], G.d_lo, G.N, G.M, G.batch, G.ldd, G.d_bstride, 32, 32, err, errlen)) return false;
