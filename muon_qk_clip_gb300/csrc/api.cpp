@@ -151,6 +151,8 @@ struct Plan {
   std::vector<int> tile_begin, tile_count;        // prep tiles per matrix
   int total_tiles = 0;
   size_t off_partials = 0, off_inv = 0, off_inv_sq = 0, bytes = 0;
+  size_t off_sched = 0;                           // tile counters, one per NS GEMM launch
+  int nsched = 0;
 };
 
 int resolve_xmode(int prec, bool any_f32_output) {
@@ -211,6 +213,9 @@ Plan make_plan(const mc_mat* mats, int count, int xmode) {
   P.off_partials = off; off += al((size_t)P.total_tiles * sizeof(double));
   P.off_inv = off; off += al((size_t)count * sizeof(float));
   P.off_inv_sq = off; off += al((size_t)count * sizeof(float));
+  // up to 32 iterations x 3 phases x ceil(groups / kMaxGroups) launches
+  P.nsched = 3 * 32 * (int)cdiv((long long)P.groups.size(), kMaxGroups);
+  P.off_sched = off; off += al((size_t)P.nsched * sizeof(int));
   P.bytes = off;
   return P;
 }
@@ -280,7 +285,7 @@ mc_status run_norms(const Plan& P, void* ws, float eps, cudaStream_t s) {
 enum Phase { kGram = 1, kPoly = 2, kNext = 3 };
 
 mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams* hp,
-                    int32_t* status, cudaStream_t s) {
+                    int32_t* status, int& launch, cudaStream_t s) {
   const int cur = it & 1, nxt = cur ^ 1;
   const size_t es = P.xmode == kXF32 ? 4 : 2;
   // heavier K first for a better tail
@@ -346,6 +351,10 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
     }
     gp.ngroups = ng;
     gp.total_tiles = t;
+    // tensor-core launches claim tiles from a zeroed counter of their own
+    if (P.xmode != kXF32 && ns_dynamic_schedule() && launch < P.nsched)
+      gp.sched = reinterpret_cast<int*>(wsp(ws, P.off_sched)) + launch;
+    ++launch;
     // split iterate: leading "fast" iterations take one bf16 product per
     // k-step; the last three iterations always take the three-term product
     const int fast = std::min(hp->ns_fast_steps, std::max(0, hp->ns_steps - 3));
@@ -388,11 +397,16 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
 // (group_order), which makes every group's members consecutive.
 mc_status run_newton_schulz(Plan& P, void* ws, const mc_hparams* hp, int32_t* status,
                             cudaStream_t s) {
+  if (P.nsched > 0 && hp->ns_steps > 0) {
+    cudaError_t e = cudaMemsetAsync(wsp(ws, P.off_sched), 0, (size_t)P.nsched * sizeof(int), s);
+    if (e != cudaSuccess) return cuda_fail(e, "tile counters");
+  }
+  int launch = 0;
   for (int it = 0; it < hp->ns_steps; ++it) {
     mc_status st;
-    if ((st = run_phase(P, ws, kGram, it, hp, status, s)) != MC_OK) return st;
-    if ((st = run_phase(P, ws, kPoly, it, hp, status, s)) != MC_OK) return st;
-    if ((st = run_phase(P, ws, kNext, it, hp, status, s)) != MC_OK) return st;
+    if ((st = run_phase(P, ws, kGram, it, hp, status, launch, s)) != MC_OK) return st;
+    if ((st = run_phase(P, ws, kPoly, it, hp, status, launch, s)) != MC_OK) return st;
+    if ((st = run_phase(P, ws, kNext, it, hp, status, launch, s)) != MC_OK) return st;
   }
   return MC_OK;
 }

@@ -273,6 +273,35 @@ __device__ inline void mbar_arrive_expect_tx_cluster(uint32_t cl_addr, uint32_t 
 __device__ inline void mbar_arrive_cluster(uint32_t cl_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr) : "memory");
 }
+// store to a shared::cluster address (this CTA's or a peer's shared memory)
+__device__ inline void st_shared_cluster_u32(uint32_t cl_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cl_addr), "r"(v) : "memory");
+}
+// try_wait with acquire at cluster scope: for phases completed by arrivals
+// (with release.cluster) from other CTAs of the cluster that also wrote data
+// this thread reads next
+__device__ inline bool mbar_try_wait_acq_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ inline bool mbar_wait_acq_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait_acq_cluster(bar, parity)) return true;
+  unsigned long long t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_acq_cluster(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (abort_flag && *abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitBudgetNs) return false;
+    }
+  }
+}
 // TMA load into this CTA's shared memory whose completion is counted on an
 // mbarrier that may live in the peer CTA (cl_bar: shared::cluster address).
 __device__ inline void tma_load_3d_pair(void* smem_dst, const CUtensorMap* map, uint32_t cl_bar,

@@ -132,10 +132,13 @@ struct GemmParams {
   float diag;             // added on the diagonal of each output item
   const float* s;         // per-matrix scale, or null
   int32_t* status;
+  int* sched;             // zeroed tile counter (dynamic schedule), or null (static)
 };
 
 // Tensor-core path (split bf16 or bf16).  Encodes its own tensor maps.
 cudaError_t launch_ns_gemm_tc(const GemmParams& p, cudaStream_t s, char* err, size_t errlen);
+// false when MC_NS_SCHED=static: the tensor-core GEMM hands tiles out round robin
+bool ns_dynamic_schedule();
 // Output tile of one tensor-core work unit (bm x bn) and, for symmetric
 // outputs, how many row tiles column tile tn holds per step (rows touching the
 // upper triangle: min(tiles_m, (tn + 1) * sym_rows_per_col_block)).

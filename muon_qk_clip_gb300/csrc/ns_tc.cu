@@ -50,7 +50,8 @@ constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;    // two 128 x 256 fp32 accumulators
 constexpr int kEpiWarpBytes = 8192;    // per epilogue warp: two 32 x 32 hi+lo slots
 constexpr int kEpiBytes = 4 * kEpiWarpBytes;
-constexpr int kBarBytes = 256;
+constexpr int kBarBytes = 512;
+constexpr int kTS = 4;                 // tile-id ring (dynamic schedule)
 constexpr int kSmemCap = 227 * 1024;
 
 // K-major operand rows of 32 bf16 = 64 bytes: 64-byte swizzle (layout type 4),
@@ -286,7 +287,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = empty + 8;             // [2]
   uint64_t* tempty = tfull + 2;            // [2]
   uint64_t* drain = tempty + 2;            // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* sfull = drain + 1;             // [kTS] tile id published
+  uint64_t* sempty = sfull + kTS;          // [kTS] tile id read by every role
+  int* sid = reinterpret_cast<int*>(sempty + kTS);   // [kTS]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sid + kTS);
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -295,6 +299,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < C::kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], CL); }
     for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 4); }
     mbar_init(drain, 1);
+    // readers of a ring slot: MMA + 4 epilogue warps of each CTA, and the
+    // second CTA's producer
+    for (int i = 0; i < kTS; ++i) { mbar_init(&sfull[i], 1); mbar_init(&sempty[i], CL > 1 ? 11 : 5); }
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -314,13 +321,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     set_status(p.status, MC_STATUS_TIMEOUT);
   };
 
+  // Tile schedule.  Static: unit u takes tiles u, u + nunits, ...  Dynamic
+  // (p.sched set): the first CTA's producer claims the next tile from a global
+  // counter and publishes its id in a kTS-deep ring (in both CTAs of a
+  // cluster); every role reads the seq-th id from the ring.  Tiles are
+  // numbered heaviest group first, so claiming in order approximates
+  // longest-processing-time-first scheduling.  -1 ends the sequence, -2 is a
+  // wait timeout.
+  const bool dyn = p.sched != nullptr;
+  const uint32_t sempty_r0 = CL > 1 ? mapa_shared(smem_u32(&sempty[0]), 0) : smem_u32(&sempty[0]);
+  auto take = [&](uint32_t seq) -> int {
+    if (!dyn) {
+      const int t = unit + (int)seq * nunits;
+      return t < p.total_tiles ? t : -1;
+    }
+    const int slot = (int)(seq % kTS);
+    if (!mbar_wait_acq_cluster(&sfull[slot], (seq / kTS) & 1, &abort_flag)) return -2;
+    const int t = reinterpret_cast<volatile int*>(sid)[slot];
+    if (CL > 1) mbar_arrive_cluster(sempty_r0 + slot * 8);
+    else mbar_arrive(&sempty[slot]);
+    return t;
+  };
+  auto claim = [&](uint32_t seq) -> int {      // first CTA's producer
+    if (!dyn) return take(seq);
+    const int slot = (int)(seq % kTS);
+    if (!mbar_wait_acq_cluster(&sempty[slot], ((seq / kTS) & 1) ^ 1, &abort_flag)) return -2;
+    int t = atomicAdd(p.sched, 1);
+    if (t >= p.total_tiles) t = -1;
+    sid[slot] = t;
+    if (CL > 1) {
+      st_shared_cluster_u32(mapa_shared(smem_u32(&sid[slot]), 1), (uint32_t)t);
+      mbar_arrive_cluster(mapa_shared(smem_u32(&sfull[slot]), 1));
+    }
+    mbar_arrive(&sfull[slot]);
+    return t;
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t it = 0;
       uint32_t last_par[8] = {};
       bool used[8] = {};
-      for (int t = unit; t < p.total_tiles && !abort_flag; t += nunits) {
+      for (uint32_t seq = 0; !abort_flag; ++seq) {
+        const int t = crank == 0 ? claim(seq) : take(seq);
+        if (t == -2) { fail(); break; }
+        if (t < 0) break;
         const TileCoord tc = tile_coord<TM_ROWS>(p, t);
         const GemmGroup& G = p.g[tc.g];
         const int nk = (G.K + BKT - 1) / BKT;
@@ -384,7 +430,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_mn = make_idesc_bf16(BM, BN, 0, 1);
       uint32_t it = 0, tcount = 0;
       bool issued = false;
-      for (int t = unit; t < p.total_tiles && !abort_flag; t += nunits, ++tcount) {
+      for (uint32_t seq = 0; !abort_flag; ++seq, ++tcount) {
+        const int t = take(seq);
+        if (t == -2) { fail(); break; }
+        if (t < 0) break;
         const TileCoord tc = tile_coord<TM_ROWS>(p, t);
         const GemmGroup& G = p.g[tc.g];
         const int nk = (G.K + BKT - 1) / BKT;
@@ -447,7 +496,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ek = 0;
     bool bad = false;
     uint32_t tcount = 0;
-    for (int t = unit; t < p.total_tiles; t += nunits, ++tcount) {
+    for (uint32_t seq = 0;; ++seq, ++tcount) {
+      int t = 0;
+      if (lane == 0) t = take(seq);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      if (t == -2) { if (lane == 0) fail(); break; }
+      if (t < 0) break;
       const TileCoord tc = tile_coord<TM_ROWS>(p, t);
       const int acc = tcount & 1;
       int ok = 1;
@@ -815,6 +869,15 @@ int cta_mode() {
 bool use_pairs() { return cta_mode() == 2; }
 
 }  // namespace
+
+bool ns_dynamic_schedule() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("MC_NS_SCHED");
+    v = (e && strcmp(e, "static") == 0) ? 0 : 1;
+  }
+  return v == 1;
+}
 
 cudaError_t launch_ns_gemm_tc(const GemmParams& p, cudaStream_t s, char* err, size_t errlen) {
   if (p.total_tiles <= 0) return cudaSuccess;
