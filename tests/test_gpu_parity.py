@@ -519,3 +519,32 @@ def test_dense_block_step_reduced_tokens():
         lo, hi = update_then_clip_band(Wn, tol, factor, O.round_to_bf16, gamma_rel=s_rel)
         g = f64(Wd[i])
         assert np.all((g >= lo) & (g <= hi)), n
+
+
+# ------------------------------------------------------------------ ZeRO-1 ranks on the library
+def test_zero1_single_rank_equals_direct_step():
+    """A ZeRO-1 step on one rank (momentum on the flat slice, then
+    muonclip_step with mu = 0 on the full momentum) is bit-identical to the
+    direct step, clip included."""
+    from muon_qk_clip_gb300.dist import LibraryOps, Zero1Layout, zero1_state, zero1_step
+    shapes = [(64, 96), (128, 40), (96, 64), (64, 32), (64, 32)]
+    W0 = [synth.normal(s, 0.02, f"zw{i}", 17).to(BF16) for i, s in enumerate(shapes)]
+    hp = mc.Hparams()
+    W1 = [w.cuda() for w in W0]
+    W2 = [w.cuda() for w in W0]
+    M1 = [torch.zeros(s, device="cuda") for s in shapes]
+    L = Zero1Layout(shapes, 1)
+    M2 = zero1_state(L, device="cuda")
+    smax = torch.tensor([150.0, 20.0, 400.0, 99.0], device="cuda")
+    for step in range(2):
+        G = [synth.normal(s, 1.0, f"zg{i}_{step}", 17).cuda() for i, s in enumerate(shapes)]
+        layer = mc.ClipLayer(smax.clone(), mc.mha_segments(W1[3], W1[4], 4))
+        mc.muonclip_step(W1, G, M1, hp, layers=[layer])
+        zero1_step(W2, G, M2, L, [(smax.clone(), [(3, 0, 16, 16, 0.5), (4, 0, 16, 16, 0.5)])],
+                   LibraryOps(W2), hp)
+    torch.cuda.synchronize()
+    for a, b in zip(W1, W2):
+        assert torch.equal(a, b)
+    for i, m in enumerate(M1):
+        a = L.offsets[i]
+        assert torch.equal(M2[a:a + m.numel()].view(m.shape), m)
