@@ -207,6 +207,47 @@ def max_logit(Q: np.ndarray, K: np.ndarray, K_shared=None, causal: bool = True,
     return smax, arg
 
 
+def attention_forward(Q: np.ndarray, K: np.ndarray, V: np.ndarray, K_shared=None,
+                      causal: bool = True, scale=None, row_chunk: int = 1024):
+    """Attention output with the per-head max logit taken along the way.
+
+    O^h = softmax(scale * Q^h K^h^T) V^h with scale = 1/sqrt(d)
+    ([K2-internals] "核心数学"), the softmax over j <= i when `causal`; the
+    max logit S_max^h is the max_logit definition above, i.e. the largest
+    entry of the same scaled logit matrix before the softmax.
+
+    Q: [B, S, H, dq]; K: [B, S, H, dk]; K_shared: [B, S, dr] or None (dq = dk + dr);
+    V: [B, S, H, dv].  Returns (O [B, S, H, dv], lse [B, H, S], smax [H]) in
+    float64, lse being the natural log of each row's softmax denominator.
+    """
+    Bsz, S, H, dq = Q.shape
+    dv = V.shape[3]
+    if scale is None:
+        scale = 1.0 / math.sqrt(dq)
+    O = np.zeros((Bsz, S, H, dv))
+    lse = np.zeros((Bsz, H, S))
+    smax = np.full(H, -np.inf)
+    jj = np.arange(S)
+    for b in range(Bsz):
+        for h in range(H):
+            k = head_keys(K, K_shared, b, h)
+            v = np.asarray(V[b, :, h, :], np.float64)
+            q_all = np.asarray(Q[b, :, h, :], np.float64)
+            for i0 in range(0, S, row_chunk):
+                q = q_all[i0:i0 + row_chunk]
+                L = scale * (q @ k.T)
+                if causal:
+                    ii = np.arange(i0, i0 + q.shape[0])
+                    L = np.where(jj[None, :] <= ii[:, None], L, -np.inf)
+                smax[h] = max(smax[h], float(np.max(L)))
+                m = np.max(L, axis=1, keepdims=True)
+                E = np.exp(L - m)
+                den = np.sum(E, axis=1, keepdims=True)
+                O[b, i0:i0 + q.shape[0], h, :] = (E / den) @ v
+                lse[b, h, i0:i0 + q.shape[0]] = (m + np.log(den))[:, 0]
+    return O, lse, smax
+
+
 def clip_factors(smax: np.ndarray, tau: float):
     """gamma_h = min(1, tau / S_max^h); a head clips only when S_max^h > tau.
 

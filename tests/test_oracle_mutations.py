@@ -72,6 +72,27 @@ def _momentum_nesterov(M_prev, G, mu):
     return mu * (mu * M_prev + G) + G
 
 
+def _attention_unmasked(Q, K, V, K_shared=None, causal=True, scale=None, row_chunk=1024):
+    return _attn_real(Q, K, V, K_shared, False, scale, row_chunk)         # causal mask dropped
+
+
+def _attention_scale_one_over_d(Q, K, V, K_shared=None, causal=True, scale=None, row_chunk=1024):
+    return _attn_real(Q, K, V, K_shared, causal, 1.0 / Q.shape[3], row_chunk)
+
+
+def _attention_values_of_query(Q, K, V, K_shared=None, causal=True, scale=None, row_chunk=1024):
+    Out, lse, smax = _attn_real(Q, K, V, K_shared, causal, scale, row_chunk)
+    return Out[:, ::-1], lse, smax                                        # rows reversed
+
+
+def _attention_unnormalised(Q, K, V, K_shared=None, causal=True, scale=None, row_chunk=1024):
+    Out, lse, smax = _attn_real(Q, K, V, K_shared, causal, scale, row_chunk)
+    den = np.exp(lse).transpose(0, 2, 1)[..., None]
+    return Out * den, lse, smax                                           # no division by the sum
+
+
+_attn_real = OM.attention_forward
+
 MUTATIONS = [
     ("ns_iterate", _ns_dropped_quintic, [P.test_golden_newton_schulz_one_step]),
     ("ns_iterate", _ns_wrong_sign, [P.test_golden_newton_schulz_one_step]),
@@ -80,6 +101,10 @@ MUTATIONS = [
     ("mla_segments", _mla_segments_gamma_on_qc, [P.test_golden_clip_mla]),
     ("max_logit", _max_logit_strict_causal, [P.test_max_logit_single_token]),
     ("momentum", _momentum_nesterov, [P.test_golden_momentum]),
+    ("attention_forward", _attention_unmasked, [P.test_attention_zero_queries_average_the_prefix]),
+    ("attention_forward", _attention_scale_one_over_d, [P.test_attention_one_hot_key_closed_form]),
+    ("attention_forward", _attention_values_of_query, [P.test_attention_one_hot_key_closed_form]),
+    ("attention_forward", _attention_unnormalised, [P.test_attention_constant_values_pass_through]),
 ]
 
 

@@ -441,3 +441,85 @@ def test_round_to_bf16_ties_and_exact_values():
 def test_bf16_decode():
     bits = np.array([0x3F80, 0xC000, 0x3F81, 0x0000], np.uint16)
     np.testing.assert_array_equal(O.bf16_bits_to_f64(bits), [1.0, -2.0, 1.0 + 2 ** -7, 0.0])
+
+
+# ------------------------------------------------------------------ attention forward (S_max fused)
+def _attn_inputs(B, S, H, dq, dv, seed, dr=0):
+    rng = np.random.default_rng(seed)
+    Q = rng.standard_normal((B, S, H, dq))
+    K = rng.standard_normal((B, S, H, dq - dr))
+    Ks = rng.standard_normal((B, S, dr)) if dr else None
+    V = rng.standard_normal((B, S, H, dv))
+    return Q, K, Ks, V
+
+
+def test_attention_zero_queries_average_the_prefix():
+    """Q = 0: every logit is 0, so row i averages V_0..V_i and lse_i = log(i + 1)."""
+    _, K, _, V = _attn_inputs(2, 9, 3, 8, 5, 40)
+    Q = np.zeros((2, 9, 3, 8))
+    Out, lse, smax = O.attention_forward(Q, K, V)
+    prefix_mean = np.cumsum(V, axis=1) / np.arange(1, 10)[None, :, None, None]
+    np.testing.assert_allclose(Out, prefix_mean, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, np.broadcast_to(np.log(np.arange(1, 10)), (2, 3, 9)), atol=1e-14)
+    np.testing.assert_array_equal(smax, np.zeros(3))
+    Out_nc, lse_nc, _ = O.attention_forward(Q, K, V, causal=False)
+    np.testing.assert_allclose(Out_nc, np.broadcast_to(V.mean(axis=1, keepdims=True), V.shape), atol=1e-14)
+    np.testing.assert_allclose(lse_nc, np.log(9.0), atol=1e-14)
+
+
+def test_attention_one_hot_key_closed_form():
+    """One key j* with q.k = c, every other logit 0: row i >= j* gets
+    (e^{c s} V_j* + sum_{j != j*, j <= i} V_j) / (e^{c s} + i), s the scale."""
+    S, d, dv, js, c = 7, 4, 3, 2, 3.0
+    Q = np.zeros((1, S, 1, d)); Q[0, :, 0, 0] = 1.0
+    K = np.zeros((1, S, 1, d)); K[0, js, 0, 0] = c
+    V = np.random.default_rng(41).standard_normal((1, S, 1, dv))
+    Out, lse, smax = O.attention_forward(Q, K, V)
+    s = 1.0 / math.sqrt(d)
+    for i in range(S):
+        others = [V[0, j, 0] for j in range(i + 1) if j != js]
+        if i >= js:
+            w = math.exp(c * s)
+            want = (w * V[0, js, 0] + sum(others, np.zeros(dv))) / (w + i)
+            np.testing.assert_allclose(lse[0, 0, i], math.log(w + i), atol=1e-14)
+        else:
+            want = sum(others, np.zeros(dv)) / (i + 1)
+        np.testing.assert_allclose(Out[0, i, 0], want, atol=1e-14)
+    assert smax[0] == pytest.approx(c * s, abs=1e-15)
+
+
+def test_attention_constant_values_pass_through():
+    Q, K, Ks, _ = _attn_inputs(1, 12, 2, 10, 4, 42, dr=3)
+    V = np.broadcast_to(np.array([1.5, -2.0, 0.25, 7.0]), (1, 12, 2, 4)).copy()
+    Out, _, _ = O.attention_forward(Q, K, V, Ks)
+    np.testing.assert_allclose(Out, V, rtol=1e-13)
+
+
+def test_attention_row_shift_changes_only_lse():
+    """Adding u to every key adds scale * q_i . u to row i's logits: O is
+    unchanged (softmax shift invariance) and lse moves by exactly that."""
+    Q, K, _, V = _attn_inputs(1, 10, 2, 6, 3, 43)
+    u = np.random.default_rng(44).standard_normal(6)
+    O1, l1, _ = O.attention_forward(Q, K, V)
+    O2, l2, _ = O.attention_forward(Q, K + u, V)
+    np.testing.assert_allclose(O2, O1, atol=1e-12)
+    shift = np.einsum("bshd,d->bhs", Q, u) / math.sqrt(6)
+    np.testing.assert_allclose(l2 - l1, shift, atol=1e-12)
+
+
+def test_attention_key_permutation_invariance_without_mask():
+    Q, K, Ks, V = _attn_inputs(2, 11, 2, 8, 4, 45, dr=2)
+    perm = np.random.default_rng(46).permutation(11)
+    O1, l1, s1 = O.attention_forward(Q, K, V, Ks, causal=False)
+    O2, l2, s2 = O.attention_forward(Q, K[:, perm], V[:, perm], Ks[:, perm], causal=False)
+    np.testing.assert_allclose(O2, O1, atol=1e-13)
+    np.testing.assert_allclose(l2, l1, atol=1e-13)
+    np.testing.assert_array_equal(s2, s1)
+
+
+@pytest.mark.parametrize("mla", [False, True])
+def test_attention_smax_is_the_max_logit(mla):
+    Q, K, Ks, V = _attn_inputs(2, 13, 3, 12, 5, 47, dr=4 if mla else 0)
+    _, _, smax = O.attention_forward(Q, K, V, Ks, row_chunk=5)
+    ref, _ = O.max_logit(Q, K, Ks)
+    np.testing.assert_allclose(smax, ref, rtol=1e-15)
