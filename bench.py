@@ -209,20 +209,24 @@ def gpu_arm(args):
     names = [m.name for m in wl.matrices]
     Wl, Gl, Ml = [W[n] for n in names], [G[n] for n in names], [M[n] for n in names]
     hp = mc.Hparams()
-    q = k = ks = None
+    q = k = ks = v = None
     segs = []
     if att is not None:                                 # setup forward (untimed)
         X, Wa = synth.attention_inputs(wl, seed=seed, device=dev)
         if att.kind == "mha":
             q, k = forward.project_mha(X, Wa["Wq"], Wa["Wk"], att.H)
             q, k = q.contiguous(), k.contiguous()
+            Wv = W["Wv"] if "Wv" in W else Wa["Wv"]
+            v, _ = forward.project_mha(X, Wv, Wv, att.H)
+            v = v.contiguous()
             Wq = W["Wq"] if "Wq" in W else Wa["Wq"]
             Wk = W["Wk"] if "Wk" in W else Wa["Wk"]
             segs = mc.mha_segments(Wq, Wk, att.H, hp.alpha)
         else:
-            q, kc, ks = forward.project_mla(X, Wa, att.H, att.d_nope, att.d_rope, att.d_v)
+            q, kc, ks, v = forward.project_mla(X, Wa, att.H, att.d_nope, att.d_rope, att.d_v,
+                                               with_v=True)
             q, ks = q.contiguous(), ks.contiguous()
-            k = kc                                      # strided view of [k^C || v]
+            k = kc                                      # strided views of [k^C || v]
             segs = mc.mla_segments(W["W_UQ"], W["W_UKV"], att.H, att.d_nope, att.d_rope, att.d_v)
         del X
     ws = mc.alloc_workspace(Wl, hp, dev)
@@ -275,6 +279,32 @@ def gpu_arm(args):
         t_local = float(t.item())
     ms_per_step = t_local / args.steps
     stat = int(status.item())
+
+    # ---- the attention forward with S_max fused in (its production placement;
+    # timed apart from the step, L2 flushed before each launch)
+    attn_fwd = None
+    if att is not None and q.dtype == torch.bfloat16:
+        o_buf = torch.empty(v.shape, dtype=v.dtype, device=dev)
+        smax_f = torch.empty(H, dtype=torch.float32, device=dev)
+        for _ in range(2):
+            mc.qk_attention_forward(q, k, v, ks, out=o_buf, smax=smax_f, status=status, stream=stream)
+        barrier()
+        mc.profiler_enable(True)
+        mc.profiler_read(reset=True)
+        for _ in range(args.steps):
+            flush.zero_()
+            mc.qk_attention_forward(q, k, v, ks, out=o_buf, smax=smax_f, status=status, stream=stream)
+        barrier()
+        pf = mc.profiler_read(reset=True).get("attn_fwd", (0, 0.0))
+        mc.profiler_enable(False)
+        d_qk = q.shape[-1]
+        fwd_flops = 2.0 * (d_qk + v.shape[-1]) * att.B * att.H * att.S * (att.S + 1) / 2
+        fwd_ms = pf[1] / args.steps
+        attn_fwd = {"ms": round(fwd_ms, 4),
+                    "tflops": round(fwd_flops / (fwd_ms * 1e-3) / 1e12, 2) if fwd_ms else None,
+                    "algorithmic_flops": fwd_flops,
+                    "smax_equals_max_logit": bool(torch.allclose(smax_f, smax, rtol=1e-6, atol=0.0)),
+                    "launches_per_call": pf[0] // args.steps}
 
     # ---- end to end through the public API: pinned host G (and Q, K) in, metrics out
     Gh = [g.to("cpu").pin_memory() for g in Gl]
@@ -369,6 +399,8 @@ def gpu_arm(args):
                      "peak_source": f"bf16_tflops {pk_src}",
                      "traffic": traffic_for(os.path.join(ROOT, "muon_qk_clip_gb300", "csrc", "ns_tc.cu"))},
         "components": {
+            "attn_fwd_fused_smax": dict(attn_fwd, frac_bf16_peak=round(attn_fwd["tflops"] / peak_t, 4))
+            if attn_fwd and attn_fwd.get("tflops") else attn_fwd,
             "ns_algorithmic_tflops": round(ns_tflops, 2) if ns_tflops else None,
             "ns_frac_bf16_peak": round(ns_tflops / peak_t, 4) if ns_tflops else None,
             "max_logit_tflops": round(ml_tflops, 2) if ml_tflops else None,

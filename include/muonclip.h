@@ -227,6 +227,34 @@ mc_status muon_newton_schulz_noalloc(const mc_mat* M, mc_mat* O, int32_t count,
 mc_status qk_max_logit(const mc_attn_desc* attn, float* smax, int64_t* argmax,
                        int32_t accumulate, int32_t* status, mc_stream_t stream);
 
+/* Values and outputs of an attention forward ([K2-internals] "核心数学":
+ * O^h = softmax(scale * Q^h K^h^T) V^h).  Layout [B, S, H, d_v] with unit
+ * feature stride, bf16 like q and k; strides in elements, multiples of 8, and
+ * 16-byte aligned pointers.  o must not overlap q, k, k_shared or v. */
+typedef struct {
+  const void* v;           /* device values [B, S, H, d_v]                          */
+  int32_t d_v;             /* value width, 16..128                                  */
+  int32_t _pad;
+  int64_t v_strides[3];    /* batch, sequence, head                                 */
+  void* o;                 /* device output [B, S, H, d_v] (written)                */
+  int64_t o_strides[3];
+  float* lse;              /* device [B, H, S]: natural log of each row's softmax
+                              denominator (of the scaled logits), or NULL           */
+} mc_attn_out;
+
+/* Attention forward with the per-head max logit fused in: the S_max that
+ * training takes "already computed during forward" ([K2-internals]
+ * Algorithm 1).  The softmax needs each row's largest logit anyway; smax
+ * receives S_max^h exactly as qk_max_logit defines it (written, or
+ * max-combined when accumulate = 1).  bf16 only (MC_ERR_UNSUPPORTED
+ * otherwise); q.k length d_head + d_shared in 16..192 (with a shared part,
+ * d_head a multiple of 64); causal or not as attn->causal says; scale > 0.
+ * Tensor cores: S = Q K^T and O += P V in fp32, P rounded to bf16 (softmax
+ * numerators relative to a running row maximum), O rounded to bf16 once.
+ * A NaN/Inf logit sets MC_STATUS_NONFINITE_LOGIT. */
+mc_status qk_attention_forward(const mc_attn_desc* attn, const mc_attn_out* out, float* smax,
+                               int32_t accumulate, int32_t* status, mc_stream_t stream);
+
 /* QK-Clip for one attention layer.  MC_CLIP_PER_HEAD: for every head with
  * smax[h] > tau, gamma_h = tau / smax[h] and every segment's rows of head h are
  * multiplied by gamma_h^exponent; heads with smax[h] <= tau are untouched bit

@@ -60,6 +60,11 @@ class McAttnDesc(ctypes.Structure):
                 ("q_strides", c_int64 * 3), ("k_strides", c_int64 * 3), ("ks_strides", c_int64 * 2)]
 
 
+class McAttnOut(ctypes.Structure):
+    _fields_ = [("v", c_void_p), ("d_v", c_int32), ("_pad", c_int32), ("v_strides", c_int64 * 3),
+                ("o", c_void_p), ("o_strides", c_int64 * 3), ("lse", c_void_p)]
+
+
 class McKernelTime(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 24), ("launches", c_int32), ("ms", c_float)]
 
@@ -74,6 +79,8 @@ SIGNATURES = {
     "muon_newton_schulz_noalloc": (c_int32, [POINTER(McMat), POINTER(McMat), c_int32,
                                              POINTER(McHparams), c_void_p, c_void_p]),
     "qk_max_logit": (c_int32, [POINTER(McAttnDesc), c_void_p, c_void_p, c_int32, c_void_p, c_void_p]),
+    "qk_attention_forward": (c_int32, [POINTER(McAttnDesc), POINTER(McAttnOut), c_void_p, c_int32,
+                                       c_void_p, c_void_p]),
     "qk_clip_apply": (c_int32, [c_void_p, c_int32, c_float, c_int32, POINTER(McClipSeg), c_int32,
                                 c_void_p, c_void_p, c_void_p, c_void_p]),
     "muonclip_step": (c_int32, [POINTER(McMat), POINTER(McMat), POINTER(McMat), c_int32,

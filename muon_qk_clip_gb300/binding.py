@@ -14,7 +14,7 @@ from dataclasses import dataclass
 import torch
 
 from . import abi
-from .abi import McAttnDesc, McClipLayer, McClipSeg, McHparams, McMat, check
+from .abi import McAttnDesc, McAttnOut, McClipLayer, McClipSeg, McHparams, McMat, check
 
 _DT = {torch.float32: abi.MC_F32, torch.bfloat16: abi.MC_BF16}
 
@@ -149,6 +149,40 @@ def qk_max_logit(q, k, k_shared=None, causal=True, scale=None, smax=None, argmax
     check(abi.load().qk_max_logit(ctypes.byref(d), _ptr(smax), _ptr(argmax), int(bool(accumulate)),
                                   _ptr(status), _stream(stream)), "qk_max_logit")
     return smax, argmax
+
+
+def qk_attention_forward(q, k, v, k_shared=None, causal=True, scale=None, out=None, lse=None,
+                         smax=None, accumulate=False, status=None, stream=None):
+    """Attention forward O = softmax(scale Q K^T) V with the per-head max logit
+    fused in.  q: [B,S,H,dq], k: [B,S,H,dk], k_shared: [B,S,dr] or None,
+    v: [B,S,H,dv] (bf16, contiguous feature axes).  Returns (out [B,S,H,dv],
+    lse [B,H,S] f32 or None, smax [H] f32); pass lse=True to allocate it."""
+    B, S, H, _ = q.shape
+    dv = v.shape[-1]
+    if v.shape[:3] != (B, S, H) or v.stride(3) != 1 or v.dtype != q.dtype:
+        raise ValueError("v must be [B, S, H, d_v] with a contiguous feature axis and q's dtype")
+    if out is None:
+        out = torch.empty((B, S, H, dv), dtype=q.dtype, device=q.device)
+    if out.shape != v.shape or out.stride(3) != 1 or out.dtype != q.dtype:
+        raise ValueError("out must be [B, S, H, d_v] with a contiguous feature axis")
+    if lse is True:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    if lse is not None and (tuple(lse.shape) != (B, H, S) or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous [B, H, S] float32 tensor")
+    if smax is None:
+        smax = torch.empty(H, dtype=torch.float32, device=q.device)
+    d = attn_desc(q, k, k_shared, causal, scale)
+    o = McAttnOut()
+    o.v, o.d_v = v.data_ptr(), dv
+    o.o = out.data_ptr()
+    for i in range(3):
+        o.v_strides[i] = v.stride(i)
+        o.o_strides[i] = out.stride(i)
+    o.lse = None if lse is None else lse.data_ptr()
+    check(abi.load().qk_attention_forward(ctypes.byref(d), ctypes.byref(o), _ptr(smax),
+                                          int(bool(accumulate)), _ptr(status), _stream(stream)),
+          "qk_attention_forward")
+    return out, lse, smax
 
 
 @dataclass

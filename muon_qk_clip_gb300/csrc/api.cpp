@@ -40,8 +40,8 @@ mc_status cuda_fail(cudaError_t e, const char* what) {
 }
 
 // ------------------------------------------------------------------ profiler
-enum ProfClass { kPrep, kNorms, kGemm, kApply, kClip, kMaxLogit, kNumProf };
-const char* kProfNames[kNumProf] = {"prep", "norms", "ns_gemm", "apply", "clip", "max_logit"};
+enum ProfClass { kPrep, kNorms, kGemm, kApply, kClip, kMaxLogit, kAttnFwd, kNumProf };
+const char* kProfNames[kNumProf] = {"prep", "norms", "ns_gemm", "apply", "clip", "max_logit", "attn_fwd"};
 
 struct Profiler {
   bool on = false;
@@ -697,6 +697,53 @@ mc_status qk_max_logit(const mc_attn_desc* a, float* smax, int64_t* argmax, int3
   if (e != cudaSuccess) {
     if (err[0]) return fail(MC_ERR_CUDA, "max logit: %s", err);
     return cuda_fail(e, "max logit launch");
+  }
+  return ok();
+}
+
+mc_status qk_attention_forward(const mc_attn_desc* a, const mc_attn_out* out, float* smax,
+                               int32_t accumulate, int32_t* status, mc_stream_t stream) {
+  if (!a || !out || !smax) return fail(MC_ERR_INVALID_ARG, "need attn, out and smax");
+  if (a->B < 1 || a->S < 1 || a->H < 1 || a->d_head < 1 || a->d_shared < 0)
+    return fail(MC_ERR_INVALID_ARG, "attn: B, S, H, d_head must be >= 1 and d_shared >= 0");
+  if (a->dtype != MC_F32 && a->dtype != MC_BF16)
+    return fail(MC_ERR_INVALID_ARG, "attn: unknown dtype %d", a->dtype);
+  if (a->dtype != MC_BF16) return fail(MC_ERR_UNSUPPORTED, "attention forward: bf16 only");
+  if (!a->q || !a->k || (a->d_shared > 0 && !a->k_shared) || !out->v || !out->o)
+    return fail(MC_ERR_INVALID_ARG, "attention forward: null pointer");
+  if (!(a->scale > 0.f) || !std::isfinite(a->scale))
+    return fail(MC_ERR_INVALID_ARG, "attn: scale must be finite and > 0");
+  for (int i = 0; i < 3; ++i)
+    if (a->q_strides[i] < 0 || a->k_strides[i] < 0 || out->v_strides[i] < 0 || out->o_strides[i] < 0)
+      return fail(MC_ERR_INVALID_ARG, "attention forward: negative stride");
+  if ((reinterpret_cast<uintptr_t>(smax) & 3u) != 0 ||
+      (out->lse && (reinterpret_cast<uintptr_t>(out->lse) & 3u) != 0))
+    return fail(MC_ERR_INVALID_ARG, "smax and lse must be 4-byte aligned");
+  AttnFwdParams p;
+  memset(&p, 0, sizeof p);
+  p.B = a->B; p.S = a->S; p.H = a->H; p.d_head = a->d_head; p.d_shared = a->d_shared;
+  p.d_v = out->d_v;
+  p.causal = a->causal != 0; p.scale = a->scale;
+  p.q = a->q; p.k = a->k; p.ks = a->k_shared; p.v = out->v; p.o = out->o;
+  for (int i = 0; i < 3; ++i) {
+    p.qs[i] = a->q_strides[i]; p.kst[i] = a->k_strides[i];
+    p.vs[i] = out->v_strides[i]; p.os[i] = out->o_strides[i];
+  }
+  for (int i = 0; i < 2; ++i) p.kss[i] = a->ks_strides[i];
+  p.lse = out->lse;
+  p.smax = smax;
+  p.accumulate = accumulate != 0;
+  p.status = status;
+  char err[256] = {0};
+  if (!attn_fwd_supported(p, err, sizeof err)) return fail(MC_ERR_UNSUPPORTED, "attention forward: %s", err);
+  cudaError_t e;
+  {
+    ProfScope ps(kAttnFwd, 3, (cudaStream_t)stream);
+    e = launch_attn_fwd(p, (cudaStream_t)stream, err, sizeof err);
+  }
+  if (e != cudaSuccess) {
+    if (err[0]) return fail(MC_ERR_CUDA, "attention forward: %s", err);
+    return cuda_fail(e, "attention forward launch");
   }
   return ok();
 }

@@ -1,0 +1,537 @@
+// Causal attention forward with the per-head max logit taken on the way:
+//
+//   O^h = softmax(scale * Q^h K^h^T) V^h          ([K2-internals] "核心数学")
+//   S_max^h = scale * max_b max_{i, j <= i} q_{b,i,h} . k_{b,j,h}
+//
+// This is where training finds S_max ("already computed during forward",
+// [K2-internals] Algorithm 1): the softmax already needs each row's maximum
+// logit, so the per-head max costs one max per row and one atomic per warp.
+//
+// Tiles: one work item = (b, h, 128 query rows); key/value blocks of 128.
+//   warp 0      TMA producer (Q once per item; K and V rings per block)
+//   warp 1      TMEM allocator + MMA issuer: S_j = Q K_j^T into one of two
+//               128-column TMEM buffers, then O += P_{j-1} V_{j-1} (O: 128 x d_v
+//               fp32 in TMEM, P: bf16 in shared memory)
+//   warps 2..5  softmax: one thread per query row reads its S row from TMEM,
+//               masks, takes the row maximum, writes P = 2^(s log2e scale - m)
+//               in bf16; at the end of the item it normalises O by the row sum
+//               and stores it through shared memory with TMA.
+// The running maximum m used for the exponentials is updated lazily: only
+// when a block's maximum exceeds it by more than 8 (log2 units) are O and the
+// row sum rescaled (read, scale and write back the row's O in TMEM), so
+// P <= 2^8 and the result is exact either way.  S_max uses the true maximum.
+//
+// MLA: the q.k length is d_head + d_shared; the key chunks of a block come from
+// the head's k^C and then from the rotary key shared by every head, as in the
+// max-logit kernel.
+//
+// Every mbarrier wait is bounded (MC_STATUS_TIMEOUT; the kernel drains its
+// copies and MMAs, frees TMEM and returns).
+#include <stdio.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mc {
+namespace {
+namespace fa {
+
+constexpr int BM = 128, BN = 128;
+constexpr int kThreads = 192;
+constexpr int CH = 128 * 64 * 2;         // one 128-row x 64-feature bf16 chunk (128-byte swizzle)
+constexpr uint32_t kTmemCols = 512;      // S x 2 (cols 0, 128), O (cols 256 ..)
+constexpr uint32_t kOCol = 256;
+constexpr int kMaxStages = 2;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLazy = 8.f;             // rescale O when the max grows by more than 2^8
+
+struct Maps {
+  CUtensorMap q, k, ks, v, o;
+};
+
+struct Geo {
+  int nch, nck, ncv;   // chunks of q.k, of its head-specific part, of d_v
+  int kst, vst;        // K and V stages
+  int nqb;
+  long long items;
+};
+
+__device__ inline void item_coords(const AttnFwdParams& p, const Geo& g, long long t, int& b,
+                                   int& h, int& ib) {
+  const long long bh = (long long)p.B * p.H;
+  ib = g.nqb - 1 - (int)(t / bh);        // longest (causal) items first
+  const int r = (int)(t % bh);
+  h = r % p.H;
+  b = r / p.H;
+}
+
+__device__ inline int kv_blocks(const AttnFwdParams& p, int ib) {
+  const int hi = p.causal ? min(p.S, (ib + 1) * BM) : p.S;
+  return (hi + BN - 1) / BN;
+}
+
+// byte offset of (row, 16-byte unit u) in a 128-row chunk with 128-byte rows
+// and the 128-byte TMA swizzle (unit index XOR row mod 8)
+__device__ inline uint32_t sw128(int row, int u) {
+  return (uint32_t)(row * 128 + ((u ^ (row & 7)) << 4));
+}
+
+__global__ void smax_init_kernel(float* smax, int H, int accumulate) {
+  const int h = blockIdx.x * blockDim.x + threadIdx.x;
+  if (h < H) reinterpret_cast<int32_t*>(smax)[h] = float_to_ordered(accumulate ? smax[h] : -INFINITY);
+}
+__global__ void smax_final_kernel(float* smax, int H) {
+  const int h = blockIdx.x * blockDim.x + threadIdx.x;
+  if (h < H) smax[h] = ordered_to_float(reinterpret_cast<int32_t*>(smax)[h]);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ AttnFwdParams p, const __grid_constant__ Maps mp,
+                    const Geo g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* qbuf = smem;                                   // nch chunks
+  uint8_t* kbuf = qbuf + g.nch * CH;                      // kst x nch chunks
+  uint8_t* vbuf = kbuf + g.kst * g.nch * CH;              // vst x ncv chunks
+  uint8_t* pbuf = vbuf + g.vst * g.ncv * CH;              // 2 chunks: P, then O staging
+  uint64_t* bars = reinterpret_cast<uint64_t*>(pbuf + 2 * CH);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* s_full = bars + 2;     // [2]
+  uint64_t* s_empty = bars + 4;    // [2]
+  uint64_t* p_full = bars + 6;
+  uint64_t* p_empty = bars + 7;
+  uint64_t* o_full = bars + 8;
+  uint64_t* o_empty = bars + 9;
+  uint64_t* drain = bars + 10;
+  uint64_t* k_full = bars + 11;    // [kMaxStages]
+  uint64_t* k_empty = k_full + kMaxStages;
+  uint64_t* v_full = k_empty + kMaxStages;
+  uint64_t* v_empty = v_full + kMaxStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(v_empty + kMaxStages);
+  __shared__ volatile int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(q_full, 1); mbar_init(q_empty, 1);
+    for (int i = 0; i < 2; ++i) { mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], 4); }
+    mbar_init(p_full, 4); mbar_init(p_empty, 1);
+    mbar_init(o_full, 1); mbar_init(o_empty, 4);
+    mbar_init(drain, 1);
+    for (int s = 0; s < g.kst; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
+    for (int s = 0; s < g.vst; ++s) { mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1); }
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&mp.q); prefetch_tmap(&mp.k); prefetch_tmap(&mp.v); prefetch_tmap(&mp.o);
+    if (g.nch > g.nck) prefetch_tmap(&mp.ks);
+  }
+  if (warp == 1) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  auto fail = [&]() { abort_flag = 1; set_status(p.status, MC_STATUS_TIMEOUT); };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t ik = 0, iv = 0, li = 0;
+      bool used_q = false, used_k[kMaxStages] = {}, used_v[kMaxStages] = {};
+      uint32_t par_q = 0, par_k[kMaxStages] = {}, par_v[kMaxStages] = {};
+      for (long long t = blockIdx.x; t < g.items && !abort_flag; t += gridDim.x, ++li) {
+        int b, h, ib;
+        item_coords(p, g, t, b, h, ib);
+        if (!mbar_wait(q_empty, (li & 1) ^ 1, &abort_flag)) { fail(); break; }
+        mbar_arrive_expect_tx(q_full, g.nch * CH);
+        for (int c = 0; c < g.nch; ++c) tma_load_4d(qbuf + c * CH, &mp.q, q_full, 64 * c, h, ib * BM, b);
+        used_q = true; par_q = li & 1;
+        const int nkb = kv_blocks(p, ib);
+        bool ok = true;
+        for (int j = 0; j < nkb && ok; ++j) {
+          {
+            const int s = ik % g.kst;
+            if (!mbar_wait(&k_empty[s], ((ik / g.kst) & 1) ^ 1, &abort_flag)) { fail(); ok = false; break; }
+            mbar_arrive_expect_tx(&k_full[s], g.nch * CH);
+            uint8_t* dst = kbuf + s * g.nch * CH;
+            for (int c = 0; c < g.nch; ++c) {
+              if (c < g.nck) tma_load_4d(dst + c * CH, &mp.k, &k_full[s], 64 * c, h, j * BN, b);
+              else tma_load_3d(dst + c * CH, &mp.ks, &k_full[s], 64 * (c - g.nck), j * BN, b);
+            }
+            used_k[s] = true; par_k[s] = (ik / g.kst) & 1; ++ik;
+          }
+          {
+            const int s = iv % g.vst;
+            if (!mbar_wait(&v_empty[s], ((iv / g.vst) & 1) ^ 1, &abort_flag)) { fail(); ok = false; break; }
+            mbar_arrive_expect_tx(&v_full[s], g.ncv * CH);
+            uint8_t* dst = vbuf + s * g.ncv * CH;
+            for (int c = 0; c < g.ncv; ++c) tma_load_4d(dst + c * CH, &mp.v, &v_full[s], 64 * c, h, j * BN, b);
+            used_v[s] = true; par_v[s] = (iv / g.vst) & 1; ++iv;
+          }
+        }
+        if (!ok) break;
+      }
+      // every issued copy must have landed before the CTA may exit
+      if (used_q) mbar_wait(q_full, par_q, nullptr);
+      for (int s = 0; s < g.kst; ++s) if (used_k[s]) mbar_wait(&k_full[s], par_k[s], nullptr);
+      for (int s = 0; s < g.vst; ++s) if (used_v[s]) mbar_wait(&v_full[s], par_v[s], nullptr);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = make_idesc_bf16(BM, BN, 0, 0);   // Q (K-major) x K (K-major)
+      const uint32_t idesc_o = make_idesc_bf16(BM, 64 * g.ncv, 0, 1);  // P (K-major) x V (MN-major)
+      uint32_t ik = 0, iv = 0, sc = 0, pc = 0, li = 0;
+      bool issued = false;
+      for (long long t = blockIdx.x; t < g.items && !abort_flag; t += gridDim.x, ++li) {
+        int b, h, ib;
+        item_coords(p, g, t, b, h, ib);
+        const int nkb = kv_blocks(p, ib);
+        if (!mbar_wait(q_full, li & 1, &abort_flag)) { fail(); break; }
+        bool ok = true;
+        for (int j = 0; j <= nkb && ok; ++j) {
+          if (j < nkb) {                 // S_j = Q K_j^T
+            const int buf = sc & 1;
+            if (!mbar_wait(&s_empty[buf], ((sc >> 1) & 1) ^ 1, &abort_flag)) { fail(); ok = false; break; }
+            const int s = ik % g.kst;
+            if (!mbar_wait(&k_full[s], (ik / g.kst) & 1, &abort_flag)) { fail(); ok = false; break; }
+            tc_fence_after();
+            const uint32_t qa = smem_u32(qbuf), ka = smem_u32(kbuf + s * g.nch * CH);
+            for (int c = 0; c < g.nch; ++c)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                tc_mma(tmem_base + buf * BN, make_sdesc_sw128(qa + c * CH + kk * 32, 16, 1024),
+                       make_sdesc_sw128(ka + c * CH + kk * 32, 16, 1024), idesc_s,
+                       (c > 0 || kk > 0) ? 1u : 0u);
+            issued = true;
+            tc_commit(&k_empty[s]);
+            tc_commit(&s_full[buf]);
+            if (j == nkb - 1) tc_commit(q_empty);
+            ++ik; ++sc;
+          }
+          if (j >= 1) {                  // O += P_{j-1} V_{j-1}
+            if (j == 1 && !mbar_wait(o_empty, (li & 1) ^ 1, &abort_flag)) { fail(); ok = false; break; }
+            if (!mbar_wait(p_full, pc & 1, &abort_flag)) { fail(); ok = false; break; }
+            const int s = iv % g.vst;
+            if (!mbar_wait(&v_full[s], (iv / g.vst) & 1, &abort_flag)) { fail(); ok = false; break; }
+            tc_fence_after();
+            const uint32_t pa = smem_u32(pbuf), va = smem_u32(vbuf + s * g.ncv * CH);
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              // A: P rows, 64-key chunks of 128-byte rows; B: V rows of 64
+              // features (MN-major), 16 key rows = 2048 bytes per k-step, the
+              // 64-wide feature blocks one chunk apart
+              tc_mma(tmem_base + kOCol, make_sdesc_sw128(pa + (kk >> 2) * CH + (kk & 3) * 32, 16, 1024),
+                     make_sdesc(va + kk * 2048, CH, 1024, 2), idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
+            tc_commit(&v_empty[s]);
+            tc_commit(p_empty);
+            ++iv; ++pc;
+          }
+        }
+        if (!ok) break;
+        tc_commit(o_full);
+      }
+      if (issued) { tc_commit(drain); mbar_wait(drain, 0, nullptr); }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int q = warp & 3;                          // TMEM lane quadrant = 32-row slice
+    const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16);
+    const float c2 = p.scale * kLog2e;
+    uint32_t sc = 0, pc = 0, li = 0;
+    bool bad = false;
+    for (long long t = blockIdx.x; t < g.items; t += gridDim.x, ++li) {
+      int b, h, ib;
+      item_coords(p, g, t, b, h, ib);
+      const int nkb = kv_blocks(p, ib);
+      const int i = ib * BM + q * 32 + lane;         // this thread's query row
+      float m_run = -INFINITY, l = 0.f, raw_max = -INFINITY, nanacc = 0.f;
+      int failed = 0;
+      for (int j = 0; j < nkb && !failed; ++j, ++sc, ++pc) {
+        const int buf = sc & 1;
+        int w = 1;
+        if (lane == 0) w = mbar_wait(&s_full[buf], (sc >> 1) & 1, &abort_flag) ? 1 : 0;
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (!w) { failed = 1; break; }
+        tc_fence_after();
+        uint32_t r[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32_async(trow + buf * BN + c * 32, r[c]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) reg_fence32(r[c]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[buf]);   // S buffer free for block j + 2
+        float v[BN];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int x = 0; x < 32; ++x) v[c * 32 + x] = __uint_as_float(r[c][x]);
+        const int j0 = j * BN;
+        const bool full = (j0 + BN - 1 < p.S) && (i < p.S) && (!p.causal || j0 + BN - 1 <= ib * BM);
+        // nanacc turns NaN iff a valid logit is NaN or infinite
+        if (full) {
+#pragma unroll
+          for (int x = 0; x < BN; ++x) nanacc = fmaf(v[x], 0.f, nanacc);
+        } else {
+#pragma unroll
+          for (int x = 0; x < BN; ++x) {
+            const int jj = j0 + x;
+            const bool valid = jj < p.S && i < p.S && (!p.causal || jj <= i);
+            if (valid) nanacc = fmaf(v[x], 0.f, nanacc);
+            v[x] = valid ? v[x] : -INFINITY;
+          }
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int x = 0; x < BN; ++x) mx = fmaxf(mx, v[x]);
+        raw_max = fmaxf(raw_max, mx);
+        // lazy running max (log2 units)
+        float alpha = 1.f;
+        bool rescale = false;
+        if (mx != -INFINITY) {
+          const float m_new = mx * c2;
+          if (m_run == -INFINITY || m_new > m_run + kLazy) {
+            alpha = m_run == -INFINITY ? 0.f : ex2_approx(m_run - m_new);
+            rescale = j > 0 && m_run != -INFINITY;
+            m_run = m_new;
+            l *= alpha;
+          }
+        }
+        float sum = 0.f;
+        uint32_t pk[BN / 2];
+#pragma unroll
+        for (int x = 0; x < BN; x += 2) {
+          const float e0 = m_run == -INFINITY ? 0.f : ex2_approx(fmaf(v[x], c2, -m_run));
+          const float e1 = m_run == -INFINITY ? 0.f : ex2_approx(fmaf(v[x + 1], c2, -m_run));
+          sum += e0 + e1;
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
+          pk[x / 2] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+        l += sum;
+        // P buffer free and O updated once the previous block's P V is done
+        if (lane == 0) w = mbar_wait(p_empty, (pc & 1) ^ 1, &abort_flag) ? 1 : 0;
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (!w) { failed = 1; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, rescale)) {
+          const float a = rescale ? alpha : 1.f;
+          for (int c = 0; c < 2 * g.ncv; ++c) {
+            uint32_t o[32];
+            tmem_ld_32x32b_x32_async(trow + kOCol + c * 32, o);
+            tmem_ld_wait();
+            reg_fence32(o);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * a);
+            tmem_st_32x32b_x32(trow + kOCol + c * 32, o);
+          }
+          tmem_st_wait();
+        }
+        // the previous item's O store must have read the staging buffer
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
+        const int row = q * 32 + lane;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const uint4 val = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          *reinterpret_cast<uint4*>(pbuf + (u >> 3) * CH + sw128(row, u & 7)) = val;
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
+      }
+      // ---- epilogue of the item: O / l -> bf16 -> TMA store; lse; S_max
+      int w = failed ? 0 : 1;
+      if (!failed && lane == 0) w = mbar_wait(o_full, li & 1, &abort_flag) ? 1 : 0;
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (!w) { if (lane == 0) fail(); break; }
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int row = q * 32 + lane;
+      for (int c = 0; c < 2 * g.ncv; ++c) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32_async(trow + kOCol + c * 32, o);
+        tmem_ld_wait();
+        reg_fence32(o);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint32_t pk4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(o[8 * u + 2 * e]) * inv,
+                                                      __uint_as_float(o[8 * u + 2 * e + 1]) * inv);
+            pk4[e] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          // 32 columns = four 16-byte units; chunk (c >> 1) holds 64 features
+          const int unit = ((c & 1) << 2) + u;
+          *reinterpret_cast<uint4*>(pbuf + (c >> 1) * CH + sw128(row, unit)) =
+              make_uint4(pk4[0], pk4[1], pk4[2], pk4[3]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_empty);           // the MMA warp may overwrite O
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        for (int c = 0; c < g.ncv; ++c)
+          tma_store_4d(&mp.o, pbuf + c * CH + q * 32 * 128, 64 * c, h, ib * BM + q * 32, b);
+        bulk_commit();
+      }
+      if (p.lse && i < p.S)
+        p.lse[((long long)b * p.H + h) * p.S + i] = l > 0.f ? (m_run + log2f(l)) * kLn2 : -INFINITY;
+      bad |= nanacc != 0.f;
+      float wm = raw_max;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+      if (lane == 0 && wm > -INFINITY)
+        atomicMax(reinterpret_cast<int32_t*>(p.smax) + h, float_to_ordered(wm * p.scale));
+    }
+    if (lane == 0) bulk_wait0();
+    if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(p.status, MC_STATUS_NONFINITE_LOGIT);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult qr;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &qr) == cudaSuccess && qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+            const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return false;
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides_bytes,
+             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool geometry(const AttnFwdParams& p, Geo& g, size_t& smem, char* err, size_t errlen) {
+  g.nck = (p.d_head + 63) / 64;
+  g.nch = p.d_shared > 0 ? g.nck + (p.d_shared + 63) / 64 : g.nck;
+  g.ncv = (p.d_v + 63) / 64;
+  g.nqb = (p.S + BM - 1) / BM;
+  g.items = (long long)p.B * p.H * g.nqb;
+  const size_t cap = 227 * 1024 - 1024 - 256;
+  const size_t fixed = (size_t)(g.nch + 2) * CH;      // Q, P
+  g.kst = g.vst = 0;
+  for (int ks = kMaxStages; ks >= 1 && !g.kst; --ks)
+    for (int vs = kMaxStages; vs >= 1; --vs)
+      if (fixed + (size_t)ks * g.nch * CH + (size_t)vs * g.ncv * CH <= cap) { g.kst = ks; g.vst = vs; break; }
+  if (!g.kst) {
+    snprintf(err, errlen, "q.k length %d and d_v %d leave no room for key/value stages",
+             p.d_head + p.d_shared, p.d_v);
+    return false;
+  }
+  smem = 1024 + fixed + (size_t)g.kst * g.nch * CH + (size_t)g.vst * g.ncv * CH + 256;
+  return true;
+}
+
+}  // namespace fa
+}  // namespace
+
+bool attn_fwd_supported(const AttnFwdParams& p, char* err, size_t errlen) {
+  const int D = p.d_head + p.d_shared;
+  if (D < 16 || D > 192) { snprintf(err, errlen, "q.k length %d outside [16, 192]", D); return false; }
+  if (p.d_v < 16 || p.d_v > 128) { snprintf(err, errlen, "d_v %d outside [16, 128]", p.d_v); return false; }
+  if (p.d_shared > 0 && (p.d_head % 64) != 0) {
+    snprintf(err, errlen, "with a shared key part d_head must be a multiple of 64 (got %d)", p.d_head);
+    return false;
+  }
+  auto al16 = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
+  if (!al16(p.q) || !al16(p.k) || !al16(p.v) || !al16(p.o) || (p.d_shared > 0 && !al16(p.ks))) {
+    snprintf(err, errlen, "q, k, k_shared, v and o must be 16-byte aligned");
+    return false;
+  }
+  for (int i = 0; i < 3; ++i)
+    if ((p.qs[i] % 8) || (p.kst[i] % 8) || (p.vs[i] % 8) || (p.os[i] % 8)) {
+      snprintf(err, errlen, "strides must be multiples of 8 elements");
+      return false;
+    }
+  if (p.d_shared > 0 && ((p.kss[0] % 8) || (p.kss[1] % 8))) {
+    snprintf(err, errlen, "k_shared strides must be multiples of 8 elements");
+    return false;
+  }
+  fa::Geo g;
+  size_t smem;
+  return fa::geometry(p, g, smem, err, errlen);
+}
+
+cudaError_t launch_attn_fwd(const AttnFwdParams& p, cudaStream_t s, char* err, size_t errlen) {
+  using namespace fa;
+  Geo g;
+  size_t smem;
+  if (!geometry(p, g, smem, err, errlen)) return cudaErrorInvalidValue;
+  Maps mp;
+  memset(&mp, 0, sizeof mp);
+  const int D = p.d_head + p.d_shared;
+  {
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)p.H, (cuuint64_t)p.S, (cuuint64_t)p.B};
+    cuuint64_t st[3] = {(cuuint64_t)p.qs[2] * 2, (cuuint64_t)p.qs[1] * 2, (cuuint64_t)p.qs[0] * 2};
+    cuuint32_t box[4] = {64, 1, BM, 1};
+    if (!encode(&mp.q, p.q, 4, dims, st, box)) { snprintf(err, errlen, "tensor map for q failed"); return cudaErrorInvalidValue; }
+  }
+  {
+    cuuint64_t dims[4] = {(cuuint64_t)p.d_head, (cuuint64_t)p.H, (cuuint64_t)p.S, (cuuint64_t)p.B};
+    cuuint64_t st[3] = {(cuuint64_t)p.kst[2] * 2, (cuuint64_t)p.kst[1] * 2, (cuuint64_t)p.kst[0] * 2};
+    cuuint32_t box[4] = {64, 1, BN, 1};
+    if (!encode(&mp.k, p.k, 4, dims, st, box)) { snprintf(err, errlen, "tensor map for k failed"); return cudaErrorInvalidValue; }
+  }
+  if (p.d_shared > 0) {
+    cuuint64_t dims[3] = {(cuuint64_t)p.d_shared, (cuuint64_t)p.S, (cuuint64_t)p.B};
+    cuuint64_t st[2] = {(cuuint64_t)p.kss[1] * 2, (cuuint64_t)p.kss[0] * 2};
+    cuuint32_t box[3] = {64, BN, 1};
+    if (!encode(&mp.ks, p.ks, 3, dims, st, box)) { snprintf(err, errlen, "tensor map for k_shared failed"); return cudaErrorInvalidValue; }
+  }
+  {
+    cuuint64_t dims[4] = {(cuuint64_t)p.d_v, (cuuint64_t)p.H, (cuuint64_t)p.S, (cuuint64_t)p.B};
+    cuuint64_t st[3] = {(cuuint64_t)p.vs[2] * 2, (cuuint64_t)p.vs[1] * 2, (cuuint64_t)p.vs[0] * 2};
+    cuuint32_t box[4] = {64, 1, BN, 1};
+    if (!encode(&mp.v, p.v, 4, dims, st, box)) { snprintf(err, errlen, "tensor map for v failed"); return cudaErrorInvalidValue; }
+  }
+  {
+    cuuint64_t dims[4] = {(cuuint64_t)p.d_v, (cuuint64_t)p.H, (cuuint64_t)p.S, (cuuint64_t)p.B};
+    cuuint64_t st[3] = {(cuuint64_t)p.os[2] * 2, (cuuint64_t)p.os[1] * 2, (cuuint64_t)p.os[0] * 2};
+    cuuint32_t box[4] = {64, 1, 32, 1};               // one warp's 32 rows
+    if (!encode(&mp.o, p.o, 4, dims, st, box)) { snprintf(err, errlen, "tensor map for o failed"); return cudaErrorInvalidValue; }
+  }
+  const int hb = (p.H + 127) / 128;
+  smax_init_kernel<<<hb, 128, 0, s>>>(p.smax, p.H, p.accumulate);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int grid = (int)(g.items < sm_count() ? g.items : sm_count());
+  attn_fwd_kernel<<<grid, kThreads, smem, s>>>(p, mp, g);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  smax_final_kernel<<<hb, 128, 0, s>>>(p.smax, p.H);
+  return cudaGetLastError();
+}
+
+}  // namespace mc

@@ -117,7 +117,7 @@ struct GemmGroup {
   void* d_hi; void* d_lo; long long ldd, d_bstride;
 };
 
-struct alignas(64) GemmTmaps {
+struct GemmTmaps {
   CUtensorMap a_hi[kMaxGroups], a_lo[kMaxGroups], b_hi[kMaxGroups], b_lo[kMaxGroups];
   CUtensorMap d_hi[kMaxGroups], d_lo[kMaxGroups];
 };
@@ -183,6 +183,23 @@ struct MaxLogitParams {
   int32_t* status;
 };
 cudaError_t launch_max_logit(const MaxLogitParams& p, cudaStream_t s, char* err, size_t errlen);
+
+// Attention forward (bf16, tensor cores) with the per-head max logit.
+struct AttnFwdParams {
+  int B, S, H, d_head, d_shared, d_v;
+  int causal;
+  float scale;
+  const void* q; const void* k; const void* ks; const void* v; void* o;
+  long long qs[3], kst[3], kss[2], vs[3], os[3];   // element strides (batch, seq, head)
+  float* lse;              // [B, H, S] or null
+  float* smax;             // [H]; ordered-int view during the launch
+  int accumulate;
+  int32_t* status;
+};
+// Returns cudaErrorInvalidValue with a message in err for shapes outside the
+// kernel's tiles (checked by the caller first).
+cudaError_t launch_attn_fwd(const AttnFwdParams& p, cudaStream_t s, char* err, size_t errlen);
+bool attn_fwd_supported(const AttnFwdParams& p, char* err, size_t errlen);
 
 // Device/properties helpers.
 int sm_count();

@@ -39,10 +39,11 @@ def _rope(x, theta=10000.0):
     return out
 
 
-def project_mla(X, W, H: int, d_nope=128, d_rope=64, d_v=128, chunk=4096):
+def project_mla(X, W, H: int, d_nope=128, d_rope=64, d_v=128, chunk=4096, with_v=False):
     """MLA features: Q [B,S,H,d_nope+d_rope] = [q^C || q^R], K^C a [B,S,H,d_nope]
     strided view into the [B,S,H,d_nope+d_v] key/value projection, and the
-    shared rotary key K^R [B,S,d_rope]."""
+    shared rotary key K^R [B,S,d_rope]; with_v adds the values V, the other
+    strided view [B,S,H,d_v] of that projection."""
     B, S, D = X.shape
     dt = X.dtype
     mm = (lambda a, w: a.float() @ w.float().t()) if X.device.type == "cpu" else (lambda a, w: a @ w.t())
@@ -53,4 +54,6 @@ def project_mla(X, W, H: int, d_nope=128, d_rope=64, d_v=128, chunk=4096):
     ckv = _rms(mm(x2, W["W_DKV"])).to(dt)
     kv = mm(ckv, W["W_UKV"]).to(dt).reshape(B, S, H, d_nope + d_v)
     kr = _rope(mm(x2, W["W_KR"]).float().reshape(B, S, d_rope)).to(dt)
+    if with_v:
+        return q.to(dt), kv[..., :d_nope], kr, kv[..., d_nope:]
     return q.to(dt), kv[..., :d_nope], kr

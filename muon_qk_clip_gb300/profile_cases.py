@@ -4,6 +4,7 @@ the dense_block shapes and exit.
   python -m muon_qk_clip_gb300.profile_cases step        # one full MuonClip step
   python -m muon_qk_clip_gb300.profile_cases ns          # Newton-Schulz of the 7 matrices
   python -m muon_qk_clip_gb300.profile_cases max_logit   # S_max of B4 S4096 H16 d128
+  python -m muon_qk_clip_gb300.profile_cases attn_fwd    # attention forward + fused S_max, same layer
   python -m muon_qk_clip_gb300.profile_cases momentum    # momentum of the 7 matrices
 
 Each case warms up once (so the profiled launch is not the first) and runs
@@ -21,7 +22,7 @@ from . import build, forward, synth
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["step", "ns", "max_logit", "momentum"])
+    ap.add_argument("case", choices=["step", "ns", "max_logit", "attn_fwd", "momentum"])
     ap.add_argument("--repeat", type=int, default=1)
     ap.add_argument("--precision", type=int, default=0, help="mc_ns_precision")
     args = ap.parse_args()
@@ -33,10 +34,14 @@ def main():
     names = [m.name for m in wl.matrices]
     Wl, Gl, Ml = [W[n] for n in names], [G[n] for n in names], [M[n] for n in names]
     hp = mc.Hparams(ns_precision=args.precision)
-    if args.case in ("step", "max_logit"):
+    if args.case in ("step", "max_logit", "attn_fwd"):
         X = synth.normal((att.B, att.S, att.d_model), 1.0, "X", 0, torch.bfloat16, dev)
         q, k = forward.project_mha(X, W["Wq"], W["Wk"], att.H)
         q, k = q.contiguous(), k.contiguous()
+        if args.case == "attn_fwd":
+            v, _ = forward.project_mha(X, W["Wv"], W["Wv"], att.H)
+            v = v.contiguous()
+            out = torch.empty_like(v)
         del X
         smax = torch.zeros(att.H, device=dev)
     if args.case in ("step", "ns"):
@@ -53,6 +58,8 @@ def main():
             mc.muon_newton_schulz(Gl, Ol, hp, workspace=ws)
         elif args.case == "max_logit":
             mc.qk_max_logit(q, k, smax=smax)
+        elif args.case == "attn_fwd":
+            mc.qk_attention_forward(q, k, v, out=out, smax=smax)
         else:
             mc.muon_momentum(Ml, Gl, hp.mu)
 

@@ -10,7 +10,7 @@ import subprocess
 import pytest
 
 from muon_qk_clip_gb300 import abi
-from muon_qk_clip_gb300.abi import McAttnDesc, McClipLayer, McClipSeg, McHparams, McMat
+from muon_qk_clip_gb300.abi import McAttnDesc, McAttnOut, McClipLayer, McClipSeg, McHparams, McMat
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "muonclip.h")
@@ -32,7 +32,7 @@ def declared_functions():
 def test_header_declares_the_five_calls():
     fns = declared_functions()
     for name in ("muon_momentum", "muon_newton_schulz", "qk_max_logit", "qk_clip_apply",
-                 "muonclip_step", "mc_workspace_size", "mc_last_error"):
+                 "muonclip_step", "qk_attention_forward", "mc_workspace_size", "mc_last_error"):
         assert name in fns
 
 
@@ -52,19 +52,22 @@ def test_struct_layouts_match_c(tmp_path):
 #include <stddef.h>
 #include "{HEADER}"
 int main(void) {{
-  printf("%zu %zu %zu %zu %zu\\n", sizeof(mc_mat), sizeof(mc_hparams), sizeof(mc_clip_seg),
-         sizeof(mc_clip_layer), sizeof(mc_attn_desc));
-  printf("%zu %zu %zu %zu\\n", offsetof(mc_attn_desc, q), offsetof(mc_attn_desc, ks_strides),
-         offsetof(mc_clip_seg, exponent), offsetof(mc_hparams, ns_precision));
+  printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(mc_mat), sizeof(mc_hparams), sizeof(mc_clip_seg),
+         sizeof(mc_clip_layer), sizeof(mc_attn_desc), sizeof(mc_attn_out));
+  printf("%zu %zu %zu %zu %zu %zu\\n", offsetof(mc_attn_desc, q), offsetof(mc_attn_desc, ks_strides),
+         offsetof(mc_clip_seg, exponent), offsetof(mc_hparams, ns_precision),
+         offsetof(mc_attn_out, o), offsetof(mc_attn_out, lse));
   return 0;
 }}''')
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-std=c99", str(src), "-o", str(exe)], check=True)
     sizes, offs = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")[:2]
     assert [int(x) for x in sizes.split()] == [ctypes.sizeof(t) for t in
-                                               (McMat, McHparams, McClipSeg, McClipLayer, McAttnDesc)]
+                                               (McMat, McHparams, McClipSeg, McClipLayer, McAttnDesc,
+                                                McAttnOut)]
     assert [int(x) for x in offs.split()] == [McAttnDesc.q.offset, McAttnDesc.ks_strides.offset,
-                                              McClipSeg.exponent.offset, McHparams.ns_precision.offset]
+                                              McClipSeg.exponent.offset, McHparams.ns_precision.offset,
+                                              McAttnOut.o.offset, McAttnOut.lse.offset]
 
 
 def test_default_hparams(lib):
@@ -173,6 +176,34 @@ def attn(**kw):
 def test_max_logit_rejects(lib, kw, code):
     d = attn(**kw)
     assert lib.qk_max_logit(ctypes.byref(d), ctypes.c_void_p(FAKE), None, 0, None, None) == code
+
+
+def attn_out(**kw):
+    o = McAttnOut()
+    o.v = o.o = FAKE
+    o.d_v = 64
+    o.v_strides[:] = [16 * 2 * 64, 2 * 64, 64]
+    o.o_strides[:] = [16 * 2 * 64, 2 * 64, 64]
+    for k, v in kw.items():
+        setattr(o, k, v)
+    return o
+
+
+@pytest.mark.parametrize("dkw,okw,code", [
+    (dict(dtype=abi.MC_F32), {}, abi.MC_ERR_UNSUPPORTED),           # bf16 only
+    (dict(S=0), {}, abi.MC_ERR_INVALID_ARG),
+    (dict(scale=-1.0), {}, abi.MC_ERR_INVALID_ARG),
+    ({}, dict(v=None), abi.MC_ERR_INVALID_ARG),
+    ({}, dict(o=None), abi.MC_ERR_INVALID_ARG),
+    (dict(d_head=256), {}, abi.MC_ERR_UNSUPPORTED),                 # q.k length > 192
+    ({}, dict(d_v=256), abi.MC_ERR_UNSUPPORTED),
+    (dict(d_head=96, d_shared=64, k_shared=FAKE), {}, abi.MC_ERR_UNSUPPORTED),  # split off a chunk
+    ({}, dict(o=FAKE + 8), abi.MC_ERR_UNSUPPORTED),                 # misaligned output
+])
+def test_attention_forward_rejects(lib, dkw, okw, code):
+    d, o = attn(**dkw), attn_out(**okw)
+    assert lib.qk_attention_forward(ctypes.byref(d), ctypes.byref(o), ctypes.c_void_p(FAKE), 0,
+                                    None, None) == code
 
 
 def test_max_logit_argmax_rules(lib):
