@@ -174,17 +174,20 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def traffic_for(kernel_src):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, or None when the kernel source changed since the capture."""
+def traffic_for(kernel_src, launches_per_call):
+    """DRAM bytes per launch of the dominant kernel: the committed ncu total
+    per Newton-Schulz call divided by this run's launches per call, or None
+    when the kernel source changed since the capture."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(p):
+    if not os.path.exists(p) or not launches_per_call:
         return None
     d = json.load(open(p)).get("ns_gemm")
     if not d:
         return None
     h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
-    return d["bytes_per_launch"] if d.get("source_sha256_16") == h else None
+    if d.get("source_sha256_16") != h:
+        return None
+    return int(d["bytes_per_ns_call"] / launches_per_call)
 
 
 def gpu_arm(args):
@@ -397,7 +400,9 @@ def gpu_arm(args):
                      "peak": peak_t, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_t, 4) if achieved else None,
                      "peak_source": f"bf16_tflops {pk_src}",
-                     "traffic": traffic_for(os.path.join(ROOT, "muon_qk_clip_gb300", "csrc", "ns_tc.cu"))},
+                     "traffic": traffic_for(os.path.join(ROOT, "muon_qk_clip_gb300", "csrc", "ns_tc.cu"),
+                                            n_gemm // args.steps if n_gemm else 0)
+                     if args.workload == WORKLOAD else None},
         "components": {
             "attn_fwd_fused_smax": dict(attn_fwd, frac_bf16_peak=round(attn_fwd["tflops"] / peak_t, 4))
             if attn_fwd and attn_fwd.get("tflops") else attn_fwd,

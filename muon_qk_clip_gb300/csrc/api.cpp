@@ -213,8 +213,9 @@ Plan make_plan(const mc_mat* mats, int count, int xmode) {
   P.off_partials = off; off += al((size_t)P.total_tiles * sizeof(double));
   P.off_inv = off; off += al((size_t)count * sizeof(float));
   P.off_inv_sq = off; off += al((size_t)count * sizeof(float));
-  // up to 32 iterations x 3 phases x ceil(groups / kMaxGroups) launches
-  P.nsched = 3 * 32 * (int)cdiv((long long)P.groups.size(), kMaxGroups);
+  // up to 32 iterations x 3 phases x (ceil(groups / kMaxGroups) + 1) launches
+  // (the groups may be split over two streams)
+  P.nsched = 3 * 32 * ((int)cdiv((long long)P.groups.size(), kMaxGroups) + 1);
   P.off_sched = off; off += al((size_t)P.nsched * sizeof(int));
   P.bytes = off;
   return P;
@@ -285,12 +286,11 @@ mc_status run_norms(const Plan& P, void* ws, float eps, cudaStream_t s) {
 enum Phase { kGram = 1, kPoly = 2, kNext = 3 };
 
 mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams* hp,
-                    int32_t* status, int& launch, cudaStream_t s) {
+                    int32_t* status, int& launch, const std::vector<int>& groups, cudaStream_t s) {
   const int cur = it & 1, nxt = cur ^ 1;
   const size_t es = P.xmode == kXF32 ? 4 : 2;
   // heavier K first for a better tail
-  std::vector<int> order(P.groups.size());
-  for (size_t i = 0; i < order.size(); ++i) order[i] = (int)i;
+  std::vector<int> order(groups);
   std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
     const Group &a = P.groups[x], &b = P.groups[y];
     return (ph == kGram ? a.n : a.m) > (ph == kGram ? b.n : b.m);
@@ -378,7 +378,6 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
         gp.s = it == 0 ? reinterpret_cast<const float*>(wsp(ws, P.off_inv)) : nullptr;
         break;
     }
-    ProfScope ps(kGemm, 1, s);
     cudaError_t e;
     if (P.xmode == kXF32) {
       e = launch_ns_gemm_f32(gp, s);
@@ -395,18 +394,88 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
 // The GEMM epilogue addresses per-matrix scales as s[mat_base + slot], so the
 // entry points first permute the matrices into shape-group order
 // (group_order), which makes every group's members consecutive.
+// A second stream for Newton-Schulz (one per host thread and device, created
+// on first use and kept): shape groups are independent chains of launches, so
+// running two sets of them side by side lets one set's launches fill the SMs
+// that the other's launch tails leave idle.  MC_NS_STREAMS=1 keeps one stream.
+struct AuxStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+bool ns_two_streams() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("MC_NS_STREAMS");
+    v = (e && atoi(e) == 1) ? 1 : 2;
+  }
+  return v == 2;
+}
+
+cudaError_t aux_stream(AuxStream*& out) {
+  thread_local std::map<int, AuxStream> cache;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  AuxStream& a = cache[dev];
+  if (!a.s) {
+    if ((e = cudaStreamCreateWithFlags(&a.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+  }
+  out = &a;
+  return cudaSuccess;
+}
+
 mc_status run_newton_schulz(Plan& P, void* ws, const mc_hparams* hp, int32_t* status,
                             cudaStream_t s) {
   if (P.nsched > 0 && hp->ns_steps > 0) {
     cudaError_t e = cudaMemsetAsync(wsp(ws, P.off_sched), 0, (size_t)P.nsched * sizeof(int), s);
     if (e != cudaSuccess) return cuda_fail(e, "tile counters");
   }
+  // split the shape groups into two sets of about equal Newton-Schulz work
+  // (largest first onto the lighter set)
+  std::vector<int> set[2];
+  const int ng = (int)P.groups.size();
+  if (ng >= 2 && P.xmode != kXF32 && ns_two_streams()) {
+    std::vector<int> idx(ng);
+    for (int g = 0; g < ng; ++g) idx[g] = g;
+    auto work = [&](int g) {
+      const double m = P.groups[g].m, n = P.groups[g].n;
+      return P.groups[g].batch * (4.0 * m * m * n + 2.0 * m * m * m);
+    };
+    std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return work(a) > work(b); });
+    double load[2] = {0.0, 0.0};
+    for (int g : idx) {
+      const int k = load[1] < load[0] ? 1 : 0;
+      set[k].push_back(g);
+      load[k] += work(g);
+    }
+  } else {
+    for (int g = 0; g < ng; ++g) set[0].push_back(g);
+  }
+  AuxStream* aux = nullptr;
+  if (!set[1].empty()) {
+    cudaError_t e = aux_stream(aux);
+    if (e == cudaSuccess) e = cudaEventRecord(aux->fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(aux->s, aux->fork, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "Newton-Schulz second stream");
+  }
+  // the profiler times the whole Newton-Schulz section (launches overlap)
+  ProfScope ps(kGemm, 0, s);
   int launch = 0;
   for (int it = 0; it < hp->ns_steps; ++it) {
-    mc_status st;
-    if ((st = run_phase(P, ws, kGram, it, hp, status, launch, s)) != MC_OK) return st;
-    if ((st = run_phase(P, ws, kPoly, it, hp, status, launch, s)) != MC_OK) return st;
-    if ((st = run_phase(P, ws, kNext, it, hp, status, launch, s)) != MC_OK) return st;
+    for (Phase ph : {kGram, kPoly, kNext}) {
+      mc_status st;
+      if ((st = run_phase(P, ws, ph, it, hp, status, launch, set[0], s)) != MC_OK) return st;
+      if (aux && (st = run_phase(P, ws, ph, it, hp, status, launch, set[1], aux->s)) != MC_OK) return st;
+    }
+  }
+  ps.n = launch;
+  if (aux) {
+    cudaError_t e = cudaEventRecord(aux->join, aux->s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, aux->join, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "Newton-Schulz stream join");
   }
   return MC_OK;
 }

@@ -12,10 +12,13 @@
 //   warp 1      TMEM allocator + MMA issuer: S_j = Q K_j^T into one of two
 //               128-column TMEM buffers, then O += P_{j-1} V_{j-1} (O: 128 x d_v
 //               fp32 in TMEM, P: bf16 in shared memory)
-//   warps 2..5  softmax: one thread per query row reads its S row from TMEM,
-//               masks, takes the row maximum, writes P = 2^(s log2e scale - m)
-//               in bf16; at the end of the item it normalises O by the row sum
-//               and stores it through shared memory with TMA.
+//   warps 2..9  softmax: two threads per query row (warps w and w + 4 share a
+//               TMEM lane quadrant; each takes 64 keys and half of O's
+//               columns) read S from TMEM, mask, take the row maximum
+//               (exchanging half-row maxima through shared memory), write
+//               P = 2^(s log2e scale - m) in bf16; at the end of the item they
+//               normalise O by the row sum and store it through shared memory
+//               with TMA.
 // The running maximum m used for the exponentials is updated lazily: only
 // when a block's maximum exceeds it by more than 8 (log2 units) are O and the
 // row sum rescaled (read, scale and write back the row's O in TMEM), so
@@ -38,7 +41,7 @@ namespace {
 namespace fa {
 
 constexpr int BM = 128, BN = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;            // producer, MMA, 8 softmax warps
 constexpr int CH = 128 * 64 * 2;         // one 128-row x 64-feature bf16 chunk (128-byte swizzle)
 constexpr uint32_t kTmemCols = 512;      // S x 2 (cols 0, 128), O (cols 256 ..)
 constexpr uint32_t kOCol = 256;
@@ -54,17 +57,34 @@ struct Maps {
 struct Geo {
   int nch, nck, ncv;   // chunks of q.k, of its head-specific part, of d_v
   int kst, vst;        // K and V stages
-  int nqb;
-  long long items;
+  int nqb;             // query blocks per (b, h)
+  int nunit;           // units per (b, h) (pairs of query blocks when causal)
+  long long units;
 };
 
-__device__ inline void item_coords(const AttnFwdParams& p, const Geo& g, long long t, int& b,
-                                   int& h, int& ib) {
-  const long long bh = (long long)p.B * p.H;
-  ib = g.nqb - 1 - (int)(t / bh);        // longest (causal) items first
-  const int r = (int)(t % bh);
-  h = r % p.H;
-  b = r / p.H;
+// Work order.  Causal: a unit is a pair of query blocks (ib, nqb - 1 - ib) of
+// one (b, h), nqb + 1 key blocks in all whatever ib is, so a static round robin
+// over units is balanced; the heavy block runs first and the light one re-reads
+// the same keys from L2.  Units are numbered (b, h)-major so the CTAs in flight
+// share a few heads' keys and values.  Without the mask each unit is one block.
+// Iteration n of a CTA is half n & 1 of its (n >> 1)-th unit: returns 1 with
+// the item's coordinates, 0 for the missing half of an unpaired middle block,
+// -1 when the CTA has no units left.
+__device__ inline int next_item(const AttnFwdParams& p, const Geo& g, uint32_t n, int& b, int& h,
+                                int& ib) {
+  const long long u = blockIdx.x + (long long)(n >> 1) * gridDim.x;
+  if (u >= g.units) return -1;
+  const long long bh = u / g.nunit;
+  const int pu = (int)(u % g.nunit);
+  h = (int)(bh % p.H);
+  b = (int)(bh / p.H);
+  if (!p.causal) {
+    ib = pu;
+    return (n & 1) ? 0 : 1;
+  }
+  if ((n & 1) == 0) { ib = g.nqb - 1 - pu; return 1; }
+  ib = pu;
+  return pu < g.nqb - 1 - pu ? 1 : 0;
 }
 
 __device__ inline int kv_blocks(const AttnFwdParams& p, int ib) {
@@ -76,6 +96,17 @@ __device__ inline int kv_blocks(const AttnFwdParams& p, int ib) {
 // and the 128-byte TMA swizzle (unit index XOR row mod 8)
 __device__ inline uint32_t sw128(int row, int u) {
   return (uint32_t)(row * 128 + ((u ^ (row & 7)) << 4));
+}
+
+__device__ inline float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ inline float min3f(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 __global__ void smax_init_kernel(float* smax, int H, int accumulate) {
@@ -106,21 +137,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* o_full = bars + 8;
   uint64_t* o_empty = bars + 9;
   uint64_t* drain = bars + 10;
-  uint64_t* k_full = bars + 11;    // [kMaxStages]
+  uint64_t* xbar = bars + 11;      // [4] half-row exchange per 32-row range
+  uint64_t* k_full = bars + 15;    // [kMaxStages]
   uint64_t* k_empty = k_full + kMaxStages;
   uint64_t* v_full = k_empty + kMaxStages;
   uint64_t* v_empty = v_full + kMaxStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(v_empty + kMaxStages);
   __shared__ volatile int abort_flag;
+  __shared__ float red[2][2][BM];    // [block parity][half][row] exchanged values
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(q_full, 1); mbar_init(q_empty, 1);
-    for (int i = 0; i < 2; ++i) { mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], 4); }
-    mbar_init(p_full, 4); mbar_init(p_empty, 1);
-    mbar_init(o_full, 1); mbar_init(o_empty, 4);
+    for (int i = 0; i < 2; ++i) { mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], 8); }
+    mbar_init(p_full, 8); mbar_init(p_empty, 1);
+    mbar_init(o_full, 1); mbar_init(o_empty, 8);
     mbar_init(drain, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&xbar[i], 64);
     for (int s = 0; s < g.kst; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
     for (int s = 0; s < g.vst; ++s) { mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1); }
     fence_mbar_init();
@@ -142,9 +176,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ik = 0, iv = 0, li = 0;
       bool used_q = false, used_k[kMaxStages] = {}, used_v[kMaxStages] = {};
       uint32_t par_q = 0, par_k[kMaxStages] = {}, par_v[kMaxStages] = {};
-      for (long long t = blockIdx.x; t < g.items && !abort_flag; t += gridDim.x, ++li) {
+      for (uint32_t n = 0; !abort_flag; ++n) {
         int b, h, ib;
-        item_coords(p, g, t, b, h, ib);
+        const int st = next_item(p, g, n, b, h, ib);
+        if (st < 0) break;
+        if (st == 0) continue;
         if (!mbar_wait(q_empty, (li & 1) ^ 1, &abort_flag)) { fail(); break; }
         mbar_arrive_expect_tx(q_full, g.nch * CH);
         for (int c = 0; c < g.nch; ++c) tma_load_4d(qbuf + c * CH, &mp.q, q_full, 64 * c, h, ib * BM, b);
@@ -173,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
+        ++li;
       }
       // every issued copy must have landed before the CTA may exit
       if (used_q) mbar_wait(q_full, par_q, nullptr);
@@ -186,9 +223,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_o = make_idesc_bf16(BM, 64 * g.ncv, 0, 1);  // P (K-major) x V (MN-major)
       uint32_t ik = 0, iv = 0, sc = 0, pc = 0, li = 0;
       bool issued = false;
-      for (long long t = blockIdx.x; t < g.items && !abort_flag; t += gridDim.x, ++li) {
+      for (uint32_t n = 0; !abort_flag; ++n) {
         int b, h, ib;
-        item_coords(p, g, t, b, h, ib);
+        const int st = next_item(p, g, n, b, h, ib);
+        if (st < 0) break;
+        if (st == 0) continue;
         const int nkb = kv_blocks(p, ib);
         if (!mbar_wait(q_full, li & 1, &abort_flag)) { fail(); break; }
         bool ok = true;
@@ -233,22 +272,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         tc_commit(o_full);
+        ++li;
       }
       if (issued) { tc_commit(drain); mbar_wait(drain, 0, nullptr); }
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const int q = warp & 3;                          // TMEM lane quadrant = 32-row slice
+    // Warps 2..9: warp e = warp - 2 takes rows 32q .. 32q + 31 (q = warp & 3,
+    // its TMEM lane quadrant) and keys / O columns of half hf = e >> 2.  The
+    // two warps of a row range exchange their half-row maxima once per block
+    // through shared memory behind a bounded mbarrier (xbar[q], both slots of
+    // red alternating with the block parity); their row sums stay separate
+    // until the end of the item.
+    const int e = warp - 2;
+    const int q = warp & 3, hf = e >> 2;
+    const int row = q * 32 + lane;
     const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16);
+    const int ocols = 32 * g.ncv;                  // O columns of this half
+    uint8_t* mine = pbuf + hf * CH + q * 32 * 128;  // this warp's P rows / O staging (4 KB)
     const float c2 = p.scale * kLog2e;
-    uint32_t sc = 0, pc = 0, li = 0;
+    uint32_t sc = 0, pc = 0, li = 0, xc = 0;
     bool bad = false;
-    for (long long t = blockIdx.x; t < g.items; t += gridDim.x, ++li) {
+    auto exchange = [&](float v_mine, float& v_other) -> bool {
+      const int slot = xc & 1;
+      red[slot][hf][row] = v_mine;
+      mbar_arrive(&xbar[q]);
+      const bool ok = mbar_wait(&xbar[q], xc & 1, &abort_flag);
+      v_other = red[slot][hf ^ 1][row];
+      ++xc;
+      return ok;
+    };
+    for (uint32_t n = 0;; ++n) {
       int b, h, ib;
-      item_coords(p, g, t, b, h, ib);
+      const int st = next_item(p, g, n, b, h, ib);
+      if (st < 0) break;
+      if (st == 0) continue;
       const int nkb = kv_blocks(p, ib);
-      const int i = ib * BM + q * 32 + lane;         // this thread's query row
-      float m_run = -INFINITY, l = 0.f, raw_max = -INFINITY, nanacc = 0.f;
+      const int i = ib * BM + row;                   // this thread's query row
+      float m_run = -INFINITY, l = 0.f, raw_max = -INFINITY;
       int failed = 0;
       for (int j = 0; j < nkb && !failed; ++j, ++sc, ++pc) {
         const int buf = sc & 1;
@@ -257,40 +318,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         w = __shfl_sync(0xffffffffu, w, 0);
         if (!w) { failed = 1; break; }
         tc_fence_after();
-        uint32_t r[4][32];
+        uint32_t r[2][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32_async(trow + buf * BN + c * 32, r[c]);
+        for (int c = 0; c < 2; ++c) tmem_ld_32x32b_x32_async(trow + buf * BN + hf * 64 + c * 32, r[c]);
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) reg_fence32(r[c]);
+        for (int c = 0; c < 2; ++c) reg_fence32(r[c]);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_empty[buf]);   // S buffer free for block j + 2
-        float v[BN];
+        float v[64];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int x = 0; x < 32; ++x) v[c * 32 + x] = __uint_as_float(r[c][x]);
-        const int j0 = j * BN;
-        const bool full = (j0 + BN - 1 < p.S) && (i < p.S) && (!p.causal || j0 + BN - 1 <= ib * BM);
-        // nanacc turns NaN iff a valid logit is NaN or infinite
+        const int j0 = j * BN + hf * 64;
+        const bool full = (j0 + 63 < p.S) && (i < p.S) && (!p.causal || j0 + 63 <= ib * BM);
+        // half-row max and min over the valid logits, four independent chains
+        // each (a non-finite valid logit shows as max = +inf, min = -inf, or a
+        // NaN sum below)
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        float mn4[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
         if (full) {
 #pragma unroll
-          for (int x = 0; x < BN; ++x) nanacc = fmaf(v[x], 0.f, nanacc);
+          for (int x = 0; x < 64; x += 8)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              mx4[c] = max3f(mx4[c], v[x + 2 * c], v[x + 2 * c + 1]);
+              mn4[c] = min3f(mn4[c], v[x + 2 * c], v[x + 2 * c + 1]);
+            }
         } else {
 #pragma unroll
-          for (int x = 0; x < BN; ++x) {
+          for (int x = 0; x < 64; ++x) {
             const int jj = j0 + x;
             const bool valid = jj < p.S && i < p.S && (!p.causal || jj <= i);
-            if (valid) nanacc = fmaf(v[x], 0.f, nanacc);
+            mn4[x & 3] = fminf(mn4[x & 3], valid ? v[x] : INFINITY);
             v[x] = valid ? v[x] : -INFINITY;
+            mx4[x & 3] = fmaxf(mx4[x & 3], v[x]);
           }
         }
-        float mx = -INFINITY;
-#pragma unroll
-        for (int x = 0; x < BN; ++x) mx = fmaxf(mx, v[x]);
-        raw_max = fmaxf(raw_max, mx);
-        // lazy running max (log2 units)
+        const float mxh = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        const float mn = fminf(fminf(mn4[0], mn4[1]), fminf(mn4[2], mn4[3]));
+        bad |= (mxh == INFINITY) || (mn == -INFINITY);
+        raw_max = fmaxf(raw_max, mxh);
+        float mxo;
+        w = exchange(mxh, mxo) ? 1 : 0;
+        if (!__all_sync(0xffffffffu, w)) { failed = 1; break; }
+        const float mx = fmaxf(mxh, mxo);             // the full row's maximum
+        // lazy running max (log2 units); both halves decide identically
         float alpha = 1.f;
         bool rescale = false;
         if (mx != -INFINITY) {
@@ -302,17 +377,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             l *= alpha;
           }
         }
-        float sum = 0.f;
-        uint32_t pk[BN / 2];
+        uint32_t pk[32];
+        if (m_run == -INFINITY) {        // no valid key yet (a row past the sequence end)
 #pragma unroll
-        for (int x = 0; x < BN; x += 2) {
-          const float e0 = m_run == -INFINITY ? 0.f : ex2_approx(fmaf(v[x], c2, -m_run));
-          const float e1 = m_run == -INFINITY ? 0.f : ex2_approx(fmaf(v[x + 1], c2, -m_run));
-          sum += e0 + e1;
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
-          pk[x / 2] = *reinterpret_cast<uint32_t*>(&h2);
+          for (int x = 0; x < 32; ++x) pk[x] = 0u;
+        } else {
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int x = 0; x < 64; x += 2) {
+            const float e0 = ex2_approx(fmaf(v[x], c2, -m_run));
+            const float e1 = ex2_approx(fmaf(v[x + 1], c2, -m_run));
+            s4[(x >> 1) & 3] += e0 + e1;
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
+            pk[x / 2] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+          bad |= sum != sum;
+          l += sum;
         }
-        l += sum;
         // P buffer free and O updated once the previous block's P V is done
         if (lane == 0) w = mbar_wait(p_empty, (pc & 1) ^ 1, &abort_flag) ? 1 : 0;
         w = __shfl_sync(0xffffffffu, w, 0);
@@ -320,25 +402,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         if (__any_sync(0xffffffffu, rescale)) {
           const float a = rescale ? alpha : 1.f;
-          for (int c = 0; c < 2 * g.ncv; ++c) {
+          for (int c = 0; c < g.ncv; ++c) {
+            const uint32_t col = kOCol + hf * ocols + c * 32;
             uint32_t o[32];
-            tmem_ld_32x32b_x32_async(trow + kOCol + c * 32, o);
+            tmem_ld_32x32b_x32_async(trow + col, o);
             tmem_ld_wait();
             reg_fence32(o);
 #pragma unroll
             for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * a);
-            tmem_st_32x32b_x32(trow + kOCol + c * 32, o);
+            tmem_st_32x32b_x32(trow + col, o);
           }
           tmem_st_wait();
         }
-        // the previous item's O store must have read the staging buffer
+        // this warp's previous O store must have read its staging rows
         if (lane == 0) bulk_wait_read0();
         __syncwarp();
-        const int row = q * 32 + lane;
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
+        for (int u = 0; u < 8; ++u) {
           const uint4 val = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-          *reinterpret_cast<uint4*>(pbuf + (u >> 3) * CH + sw128(row, u & 7)) = val;
+          *reinterpret_cast<uint4*>(pbuf + hf * CH + sw128(row, u)) = val;
         }
         fence_async_smem();
         tc_fence_before();
@@ -349,27 +431,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       int w = failed ? 0 : 1;
       if (!failed && lane == 0) w = mbar_wait(o_full, li & 1, &abort_flag) ? 1 : 0;
       w = __shfl_sync(0xffffffffu, w, 0);
+      if (w) {
+        float lo;
+        w = exchange(l, lo) ? 1 : 0;               // the row sum is the two halves'
+        w = __all_sync(0xffffffffu, w);
+        l += lo;
+      }
       if (!w) { if (lane == 0) fail(); break; }
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      const int row = q * 32 + lane;
-      for (int c = 0; c < 2 * g.ncv; ++c) {
+      const int r32 = lane;                          // row within this warp's 32
+      for (int c = 0; c < g.ncv; ++c) {
         uint32_t o[32];
-        tmem_ld_32x32b_x32_async(trow + kOCol + c * 32, o);
+        tmem_ld_32x32b_x32_async(trow + kOCol + hf * ocols + c * 32, o);
         tmem_ld_wait();
         reg_fence32(o);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           uint32_t pk4[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(o[8 * u + 2 * e]) * inv,
-                                                      __uint_as_float(o[8 * u + 2 * e + 1]) * inv);
-            pk4[e] = *reinterpret_cast<uint32_t*>(&h2);
+          for (int x = 0; x < 4; ++x) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(o[8 * u + 2 * x]) * inv,
+                                                      __uint_as_float(o[8 * u + 2 * x + 1]) * inv);
+            pk4[x] = *reinterpret_cast<uint32_t*>(&h2);
           }
-          // 32 columns = four 16-byte units; chunk (c >> 1) holds 64 features
-          const int unit = ((c & 1) << 2) + u;
-          *reinterpret_cast<uint4*>(pbuf + (c >> 1) * CH + sw128(row, unit)) =
+          // 32 x 32 box, 64-byte rows, 64-byte swizzle; box c at 2 KB steps
+          *reinterpret_cast<uint4*>(mine + c * 2048 + r32 * 64 + ((u ^ ((r32 >> 1) & 3)) << 4)) =
               make_uint4(pk4[0], pk4[1], pk4[2], pk4[3]);
         }
       }
@@ -380,17 +467,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) {
         for (int c = 0; c < g.ncv; ++c)
-          tma_store_4d(&mp.o, pbuf + c * CH + q * 32 * 128, 64 * c, h, ib * BM + q * 32, b);
+          if (hf * ocols + 32 * c < p.d_v)
+            tma_store_4d(&mp.o, mine + c * 2048, hf * ocols + 32 * c, h, ib * BM + q * 32, b);
         bulk_commit();
       }
-      if (p.lse && i < p.S)
+      if (hf == 0 && p.lse && i < p.S)
         p.lse[((long long)b * p.H + h) * p.S + i] = l > 0.f ? (m_run + log2f(l)) * kLn2 : -INFINITY;
-      bad |= nanacc != 0.f;
       float wm = raw_max;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
       if (lane == 0 && wm > -INFINITY)
         atomicMax(reinterpret_cast<int32_t*>(p.smax) + h, float_to_ordered(wm * p.scale));
+      ++li;
     }
     if (lane == 0) bulk_wait0();
     if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(p.status, MC_STATUS_NONFINITE_LOGIT);
@@ -422,12 +510,13 @@ EncodeTiledFn get_encode() {
 }
 
 bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
-            const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+            const cuuint64_t* strides_bytes, const cuuint32_t* box,
+            CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = get_encode();
   if (!enc) return false;
   cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides_bytes,
-             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -436,8 +525,9 @@ bool geometry(const AttnFwdParams& p, Geo& g, size_t& smem, char* err, size_t er
   g.nch = p.d_shared > 0 ? g.nck + (p.d_shared + 63) / 64 : g.nck;
   g.ncv = (p.d_v + 63) / 64;
   g.nqb = (p.S + BM - 1) / BM;
-  g.items = (long long)p.B * p.H * g.nqb;
-  const size_t cap = 227 * 1024 - 1024 - 256;
+  g.nunit = p.causal ? (g.nqb + 1) / 2 : g.nqb;
+  g.units = (long long)p.B * p.H * g.nunit;
+  const size_t cap = 227 * 1024 - 1024 - 256 - 2 * 2 * BM * 4 - 64;   // static: red, abort flag
   const size_t fixed = (size_t)(g.nch + 2) * CH;      // Q, P
   g.kst = g.vst = 0;
   for (int ks = kMaxStages; ks >= 1 && !g.kst; --ks)
@@ -517,8 +607,8 @@ cudaError_t launch_attn_fwd(const AttnFwdParams& p, cudaStream_t s, char* err, s
   {
     cuuint64_t dims[4] = {(cuuint64_t)p.d_v, (cuuint64_t)p.H, (cuuint64_t)p.S, (cuuint64_t)p.B};
     cuuint64_t st[3] = {(cuuint64_t)p.os[2] * 2, (cuuint64_t)p.os[1] * 2, (cuuint64_t)p.os[0] * 2};
-    cuuint32_t box[4] = {64, 1, 32, 1};               // one warp's 32 rows
-    if (!encode(&mp.o, p.o, 4, dims, st, box)) { snprintf(err, errlen, "tensor map for o failed"); return cudaErrorInvalidValue; }
+    cuuint32_t box[4] = {32, 1, 32, 1};               // one warp's 32 rows x 32 features
+    if (!encode(&mp.o, p.o, 4, dims, st, box, CU_TENSOR_MAP_SWIZZLE_64B)) { snprintf(err, errlen, "tensor map for o failed"); return cudaErrorInvalidValue; }
   }
   const int hb = (p.H + 127) / 128;
   smax_init_kernel<<<hb, 128, 0, s>>>(p.smax, p.H, p.accumulate);
@@ -526,7 +616,7 @@ cudaError_t launch_attn_fwd(const AttnFwdParams& p, cudaStream_t s, char* err, s
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int grid = (int)(g.items < sm_count() ? g.items : sm_count());
+  const int grid = (int)(g.units < sm_count() ? g.units : sm_count());
   attn_fwd_kernel<<<grid, kThreads, smem, s>>>(p, mp, g);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
