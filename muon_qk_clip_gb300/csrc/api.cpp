@@ -295,8 +295,13 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
     const Group &a = P.groups[x], &b = P.groups[y];
     return (ph == kGram ? a.n : a.m) > (ph == kGram ? b.n : b.m);
   });
+  // split iterate: leading "fast" iterations take one bf16 product per
+  // k-step; the last three iterations always take the three-term product
+  const int fast = std::min(hp->ns_fast_steps, std::max(0, hp->ns_steps - 3));
+  const int terms = (P.xmode == kXSplit && it >= fast) ? 3 : 1;
+  const bool sym_out = P.xmode != kXF32 && (ph == kGram || ph == kPoly);
   int tileM = 64, tileN = 64, sym_step = 1;
-  if (P.xmode != kXF32) ns_tc_tile_shape(&tileM, &tileN, &sym_step);
+  if (P.xmode != kXF32) ns_tc_tile_shape(sym_out, terms, &tileM, &tileN, &sym_step);
   for (size_t g0 = 0; g0 < order.size(); g0 += kMaxGroups) {
     GemmParams gp;
     memset(&gp, 0, sizeof gp);
@@ -339,7 +344,7 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
       G.tiles_per_item = G.tiles_m * G.tiles_n;
       // Gram and polynomial outputs are symmetric: the tensor-core path
       // computes only the tiles touching the upper triangle
-      if (P.xmode != kXF32 && (ph == kGram || ph == kPoly)) {
+      if (sym_out) {
         G.symmetric = 1;
         G.tiles_per_item = 0;
         for (int tn = 0; tn < G.tiles_n; ++tn)
@@ -355,10 +360,7 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
     if (P.xmode != kXF32 && ns_dynamic_schedule() && launch < P.nsched)
       gp.sched = reinterpret_cast<int*>(wsp(ws, P.off_sched)) + launch;
     ++launch;
-    // split iterate: leading "fast" iterations take one bf16 product per
-    // k-step; the last three iterations always take the three-term product
-    const int fast = std::min(hp->ns_fast_steps, std::max(0, hp->ns_steps - 3));
-    gp.terms = (P.xmode == kXSplit && it >= fast) ? 3 : 1;
+    gp.terms = terms;
     // Three-term iterations fold a X into the polynomial: B' = c A^2 + b A + a I
     // and X' = B' X, so the last phase reads no C.  (B' holds ~16 significand
     // bits there; a one-plane bf16 B' would lose the small singular values, so

@@ -142,7 +142,10 @@ bool ns_dynamic_schedule();
 // Output tile of one tensor-core work unit (bm x bn) and, for symmetric
 // outputs, how many row tiles column tile tn holds per step (rows touching the
 // upper triangle: min(tiles_m, (tn + 1) * sym_rows_per_col_block)).
-void ns_tc_tile_shape(int* bm, int* bn, int* sym_rows_per_col_block);
+// Output tile of one work unit of the tensor-core GEMM for a launch of this
+// kind (symmetric output, products per k-step): bm x bn, and for symmetric
+// outputs the row units per 256-column block along the diagonal.
+void ns_tc_tile_shape(bool symmetric, int terms, int* bm, int* bn, int* sym_rows_per_col_block);
 // CUDA-core fp32 path.
 cudaError_t launch_ns_gemm_f32(const GemmParams& p, cudaStream_t s);
 

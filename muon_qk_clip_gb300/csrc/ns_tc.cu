@@ -18,7 +18,8 @@
 //   warp 0      TMA producer (one elected lane)
 //   warp 1      TMEM allocator + MMA issuer (one elected lane)
 //   warps 2..5  epilogue: TMEM -> registers -> fused polynomial -> global
-// Tiles are 128 x 256 with K advancing by 32 (64-byte swizzle rows); the
+// Tiles are 128 x 256 with K advancing by 32 (64-byte swizzle rows) in
+// three-product launches and by 64 (128-byte rows) in one-product ones; the
 // accumulator is double-buffered in TMEM (2 x 256 columns) so the epilogue of
 // tile t overlaps the MMAs of tile t+1.  The epilogue reads C straight into
 // registers and stages every 32 x 32 chunk of D (and, for symmetric outputs,
@@ -58,14 +59,22 @@ constexpr int kSmemCap = 227 * 1024;
 // 8-row atoms of 512 bytes.
 constexpr uint32_t kLayout = 4u;
 constexpr uint32_t kSbo = 8 * BKT * 2;
+// K-major operand layout for a k-step of BK: rows of BK bf16 with the 64-byte
+// (BK 32) or 128-byte (BK 64) swizzle, 8-row atoms.
+template <int BK>
+struct KLayout {
+  static_assert(BK == 32 || BK == 64, "k-step");
+  static constexpr uint32_t kType = BK == 64 ? 2u : 4u;
+  static constexpr uint32_t kSbo = 8 * BK * 2;
+};
 
 // TERMS: tensor-core products per k-step (1: hi*hi, 3: hi*hi + hi*lo + lo*hi).
 // LO: the iterate is stored as (hi, lo) planes (the epilogue reads and writes
 // both), independently of how many products the k-loop takes.
-template <int TERMS, int AROWS, int BROWS>
+template <int TERMS, int AROWS, int BROWS, int BK = BKT>
 struct Stages {
-  static constexpr int kABytes = AROWS * BKT * 2;
-  static constexpr int kBBytes = BROWS * BKT * 2;
+  static constexpr int kABytes = AROWS * BK * 2;
+  static constexpr int kBBytes = BROWS * BK * 2;
   static constexpr int kStageBytes = TERMS == 3 ? 2 * (kABytes + kBBytes) : (kABytes + kBBytes);
   static constexpr int kAvail = kSmemCap - kEpiBytes - 1024 - kBarBytes - 64;
   static constexpr int kStages = kAvail / kStageBytes > 8 ? 8 : kAvail / kStageBytes;
@@ -271,10 +280,11 @@ __device__ void epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
 // 256 B rows, so each CTA loads one 128-row half of B and multicasts it to
 // both (half the B traffic from L2).  A stage is refilled only when both
 // CTAs' MMAs have released it (each MMA thread's commit arrives on both).
-template <int TERMS, bool LO, int CL>
+template <int TERMS, bool LO, int CL, int BK>
 __global__ void __launch_bounds__(kThreads, 1)
     ns_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ TmaArgs tm) {
-  using C = Stages<TERMS, BM, BN>;
+  using C = Stages<TERMS, BM, BN, BK>;
+  using KL = KLayout<BK>;
   constexpr bool SPLIT = TERMS == 3;
   constexpr int TM_ROWS = BM * CL;
   const uint32_t crank = CL > 1 ? cluster_ctarank() : 0;
@@ -369,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t < 0) break;
         const TileCoord tc = tile_coord<TM_ROWS>(p, t);
         const GemmGroup& G = p.g[tc.g];
-        const int nk = (G.K + BKT - 1) / BKT;
+        const int nk = (G.K + BK - 1) / BK;
         const int m0 = tc.m0 + BM * (int)crank;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb, ++it) {
@@ -382,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* b_hi = st + (SPLIT ? 2 * C::kABytes : C::kABytes);
           uint8_t* b_lo = b_hi + C::kBBytes;
           mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-          const int k0 = kb * BKT;
+          const int k0 = kb * BK;
           tma_load_3d(a_hi, &tm.maps.a_hi[tc.g], &full[s], k0, m0, tc.b);
           if (SPLIT) tma_load_3d(a_lo, &tm.maps.a_lo[tc.g], &full[s], k0, m0, tc.b);
           if (CL == 1) {
@@ -392,25 +402,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
 #pragma unroll
               for (int qq = 0; qq < BN / 64; ++qq) {
-                tma_load_3d(b_hi + qq * (64 * BKT * 2), &tm.maps.b_hi[tc.g], &full[s], tc.n0 + 64 * qq, k0, tc.b);
+                tma_load_3d(b_hi + qq * (64 * BK * 2), &tm.maps.b_hi[tc.g], &full[s], tc.n0 + 64 * qq, k0, tc.b);
                 if (SPLIT)
-                  tma_load_3d(b_lo + qq * (64 * BKT * 2), &tm.maps.b_lo[tc.g], &full[s], tc.n0 + 64 * qq, k0, tc.b);
+                  tma_load_3d(b_lo + qq * (64 * BK * 2), &tm.maps.b_lo[tc.g], &full[s], tc.n0 + 64 * qq, k0, tc.b);
               }
             }
           } else {
             // this CTA's half of B (128 of the 256 rows), to both CTAs
             constexpr uint16_t kAll = (1u << CL) - 1;
             if (!G.b_mn_major) {
-              const int off = (int)crank * 128 * BKT * 2;     // 128 K-major rows of 64 bytes
+              const int off = (int)crank * 128 * BK * 2;     // 128 K-major rows of BK bf16
               tma_load_3d_mc(b_hi + off, &tm.maps.b_hi[tc.g], &full[s], k0, tc.n0 + 128 * (int)crank, tc.b, kAll);
               if (SPLIT)
                 tma_load_3d_mc(b_lo + off, &tm.maps.b_lo[tc.g], &full[s], k0, tc.n0 + 128 * (int)crank, tc.b, kAll);
             } else {
 #pragma unroll
               for (int qq = 2 * (int)crank; qq < 2 * (int)crank + 2; ++qq) {
-                tma_load_3d_mc(b_hi + qq * (64 * BKT * 2), &tm.maps.b_hi[tc.g], &full[s], tc.n0 + 64 * qq, k0, tc.b, kAll);
+                tma_load_3d_mc(b_hi + qq * (64 * BK * 2), &tm.maps.b_hi[tc.g], &full[s], tc.n0 + 64 * qq, k0, tc.b, kAll);
                 if (SPLIT)
-                  tma_load_3d_mc(b_lo + qq * (64 * BKT * 2), &tm.maps.b_lo[tc.g], &full[s], tc.n0 + 64 * qq, k0, tc.b, kAll);
+                  tma_load_3d_mc(b_lo + qq * (64 * BK * 2), &tm.maps.b_lo[tc.g], &full[s], tc.n0 + 64 * qq, k0, tc.b, kAll);
               }
             }
           }
@@ -436,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t < 0) break;
         const TileCoord tc = tile_coord<TM_ROWS>(p, t);
         const GemmGroup& G = p.g[tc.g];
-        const int nk = (G.K + BKT - 1) / BKT;
+        const int nk = (G.K + BK - 1) / BK;
         const int acc = tcount & 1;
         const uint32_t ause = tcount >> 1;
         if (!mbar_wait(&tempty[acc], (ause & 1) ^ 1, &abort_flag)) { fail(); break; }
@@ -453,23 +463,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a_hi = st, a_lo = st + C::kABytes;
           const uint32_t b_hi = st + (SPLIT ? 2 * C::kABytes : C::kABytes), b_lo = b_hi + C::kBBytes;
 #pragma unroll
-          for (int kk = 0; kk < BKT / 16; ++kk) {
+          for (int kk = 0; kk < BK / 16; ++kk) {
             // K-major: 16 elements = 32 bytes further along the swizzled row
-            const uint64_t dah = make_sdesc(a_hi + kk * 32, 16, kSbo, kLayout);
+            const uint64_t dah = make_sdesc(a_hi + kk * 32, 16, KL::kSbo, KL::kType);
             uint64_t dbh, dbl = 0, dal = 0;
             if (!G.b_mn_major) {
-              dbh = make_sdesc(b_hi + kk * 32, 16, kSbo, kLayout);
-              if (SPLIT) dbl = make_sdesc(b_lo + kk * 32, 16, kSbo, kLayout);
+              dbh = make_sdesc(b_hi + kk * 32, 16, KL::kSbo, KL::kType);
+              if (SPLIT) dbl = make_sdesc(b_lo + kk * 32, 16, KL::kSbo, KL::kType);
             } else {
               // MN-major (128-byte swizzle): 16 K-rows = two 1024-byte atoms;
-              // 64-wide N blocks are 64*BKT*2 bytes apart
-              dbh = make_sdesc(b_hi + kk * 2048, 64 * BKT * 2, 1024, 2);
-              if (SPLIT) dbl = make_sdesc(b_lo + kk * 2048, 64 * BKT * 2, 1024, 2);
+              // 64-wide N blocks are 64*BK*2 bytes apart
+              dbh = make_sdesc(b_hi + kk * 2048, 64 * BK * 2, 1024, 2);
+              if (SPLIT) dbl = make_sdesc(b_lo + kk * 2048, 64 * BK * 2, 1024, 2);
             }
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
             tc_mma(d_tmem, dah, dbh, idesc, accum);
             if (SPLIT) {
-              dal = make_sdesc(a_lo + kk * 32, 16, kSbo, kLayout);
+              dal = make_sdesc(a_lo + kk * 32, 16, KL::kSbo, KL::kType);
               tc_mma(d_tmem, dah, dbl, idesc, 1u);
               tc_mma(d_tmem, dal, dbh, idesc, 1u);
             }
@@ -765,18 +775,18 @@ bool encode_3d(CUtensorMap* m, const void* base, int cols, int rows, int batch, 
 // Operand maps (A rows of a_rows, B rows of b_rows per box) and the 32 x 32
 // epilogue store maps for D.
 bool encode_all(const GemmParams& p, TmaArgs& tm, bool split, bool lo, int a_rows, int b_rows,
-                char* err, size_t errlen) {
+                int bk, char* err, size_t errlen) {
   memset(&tm, 0, sizeof(tm));
   for (int g = 0; g < p.ngroups; ++g) {
     const GemmGroup& G = p.g[g];
-    if (!encode_3d(&tm.maps.a_hi[g], G.a_hi, G.K, G.M, G.batch, G.lda, G.a_bstride, BKT, a_rows, err, errlen)) return false;
-    if (split && !encode_3d(&tm.maps.a_lo[g], G.a_lo, G.K, G.M, G.batch, G.lda, G.a_bstride, BKT, a_rows, err, errlen)) return false;
+    if (!encode_3d(&tm.maps.a_hi[g], G.a_hi, G.K, G.M, G.batch, G.lda, G.a_bstride, bk, a_rows, err, errlen)) return false;
+    if (split && !encode_3d(&tm.maps.a_lo[g], G.a_lo, G.K, G.M, G.batch, G.lda, G.a_bstride, bk, a_rows, err, errlen)) return false;
     if (!G.b_mn_major) {   // B operand: rows of an [N, K] plane
-      if (!encode_3d(&tm.maps.b_hi[g], G.b_hi, G.K, G.N, G.batch, G.ldb, G.b_bstride, BKT, b_rows, err, errlen)) return false;
-      if (split && !encode_3d(&tm.maps.b_lo[g], G.b_lo, G.K, G.N, G.batch, G.ldb, G.b_bstride, BKT, b_rows, err, errlen)) return false;
-    } else {               // B operand: [K, N] plane, 64-wide N boxes of BKT rows
-      if (!encode_3d(&tm.maps.b_hi[g], G.b_hi, G.N, G.K, G.batch, G.ldb, G.b_bstride, 64, BKT, err, errlen)) return false;
-      if (split && !encode_3d(&tm.maps.b_lo[g], G.b_lo, G.N, G.K, G.batch, G.ldb, G.b_bstride, 64, BKT, err, errlen)) return false;
+      if (!encode_3d(&tm.maps.b_hi[g], G.b_hi, G.K, G.N, G.batch, G.ldb, G.b_bstride, bk, b_rows, err, errlen)) return false;
+      if (split && !encode_3d(&tm.maps.b_lo[g], G.b_lo, G.K, G.N, G.batch, G.ldb, G.b_bstride, bk, b_rows, err, errlen)) return false;
+    } else {               // B operand: [K, N] plane, 64-wide N boxes of bk rows
+      if (!encode_3d(&tm.maps.b_hi[g], G.b_hi, G.N, G.K, G.batch, G.ldb, G.b_bstride, 64, bk, err, errlen)) return false;
+      if (split && !encode_3d(&tm.maps.b_lo[g], G.b_lo, G.N, G.K, G.batch, G.ldb, G.b_bstride, 64, bk, err, errlen)) return false;
     }
     if (!encode_3d(&tm.maps.d_hi[g], G.d_hi, G.N, G.M, G.batch, G.ldd, G.d_bstride, 32, 32, err, errlen)) return false;
     if (lo && !encode_3d(&tm.maps.d_lo[g], G.d_lo, G.N, G.M, G.batch, G.ldd, G.d_bstride, 32, 32, err, errlen)) return false;
@@ -784,13 +794,13 @@ bool encode_all(const GemmParams& p, TmaArgs& tm, bool split, bool lo, int a_row
   return true;
 }
 
-template <int TERMS, bool LO, int CL>
+template <int TERMS, bool LO, int CL, int BK>
 cudaError_t launch_single(const GemmParams& p, cudaStream_t s, char* err, size_t errlen) {
   TmaArgs tm;
   // with clusters each CTA's B box is one 128-row half (multicast to both)
-  if (!encode_all(p, tm, TERMS == 3, LO, BM, CL > 1 ? 128 : BN, err, errlen)) return cudaErrorInvalidValue;
-  auto k = ns_gemm_tc_kernel<TERMS, LO, CL>;
-  const int smem = Stages<TERMS, BM, BN>::kSmem;
+  if (!encode_all(p, tm, TERMS == 3, LO, BM, CL > 1 ? 128 : BN, BK, err, errlen)) return cudaErrorInvalidValue;
+  auto k = ns_gemm_tc_kernel<TERMS, LO, CL, BK>;
+  const int smem = Stages<TERMS, BM, BN, BK>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (CL == 1) {
@@ -825,7 +835,7 @@ cudaError_t launch_single(const GemmParams& p, cudaStream_t s, char* err, size_t
 template <int TERMS, bool LO>
 cudaError_t launch_pair(const GemmParams& p, cudaStream_t s, char* err, size_t errlen) {
   TmaArgs tm;
-  if (!encode_all(p, tm, TERMS == 3, LO, 128, 128, err, errlen)) return cudaErrorInvalidValue;
+  if (!encode_all(p, tm, TERMS == 3, LO, 128, 128, BKT, err, errlen)) return cudaErrorInvalidValue;
   auto k = ns_gemm_pair_kernel<TERMS, LO>;
   const int smem = Stages<TERMS, 128, 128>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -866,7 +876,29 @@ int cta_mode() {
   }
   return v;
 }
-bool use_pairs() { return cta_mode() == 2; }
+// Cluster choice per launch (MC_NS_CTA=3, the default): the one-product
+// symmetric phases run on single CTAs (128-row tiles balance better and their
+// operands are small), everything else on B-multicast clusters of two.
+// k-step of the one-product launches: 64 (128-byte operand rows, 4 stages of
+// 48 KB) by default; MC_NS_BK_FAST=32 takes 64-byte rows and 8 stages.  With
+// one product per k-step, 64-byte rows leave the copy engine issuing more
+// rows per clock than it sustains (measured: the one-product launches take
+// 20-25 % less time with 128-byte rows); the three-product launches keep 32
+// for their 4 stages.
+int fast_bk() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("MC_NS_BK_FAST");
+    v = (e && atoi(e) == 32) ? 32 : 64;
+  }
+  return v;
+}
+
+int cta_mode_for(bool symmetric, int terms) {
+  const int m = cta_mode();
+  if (m == 3 && symmetric && terms == 1) return 1;
+  return m;
+}
 
 }  // namespace
 
@@ -883,20 +915,25 @@ cudaError_t launch_ns_gemm_tc(const GemmParams& p, cudaStream_t s, char* err, si
   if (p.total_tiles <= 0) return cudaSuccess;
   const bool lo = p.xmode == kXSplit;
   const bool three = lo && p.terms == 3;
-  if (use_pairs()) {
+  const int mode = cta_mode_for(p.g[0].symmetric != 0, p.terms);
+  if (mode == 2) {
     if (three) return launch_pair<3, true>(p, s, err, errlen);
     return lo ? launch_pair<1, true>(p, s, err, errlen) : launch_pair<1, false>(p, s, err, errlen);
   }
-  if (cta_mode() == 3) {
-    if (three) return launch_single<3, true, 2>(p, s, err, errlen);
-    return lo ? launch_single<1, true, 2>(p, s, err, errlen) : launch_single<1, false, 2>(p, s, err, errlen);
+  // one-product launches may take k-steps of 64 (128-byte rows)
+  const bool bk64 = !three && fast_bk() == 64;
+  if (mode == 3) {
+    if (three) return launch_single<3, true, 2, 32>(p, s, err, errlen);
+    if (bk64) return lo ? launch_single<1, true, 2, 64>(p, s, err, errlen) : launch_single<1, false, 2, 64>(p, s, err, errlen);
+    return lo ? launch_single<1, true, 2, 32>(p, s, err, errlen) : launch_single<1, false, 2, 32>(p, s, err, errlen);
   }
-  if (three) return launch_single<3, true, 1>(p, s, err, errlen);
-  return lo ? launch_single<1, true, 1>(p, s, err, errlen) : launch_single<1, false, 1>(p, s, err, errlen);
+  if (three) return launch_single<3, true, 1, 32>(p, s, err, errlen);
+  if (bk64) return lo ? launch_single<1, true, 1, 64>(p, s, err, errlen) : launch_single<1, false, 1, 64>(p, s, err, errlen);
+  return lo ? launch_single<1, true, 1, 32>(p, s, err, errlen) : launch_single<1, false, 1, 32>(p, s, err, errlen);
 }
 
-void ns_tc_tile_shape(int* bm, int* bn, int* sym_rows_per_col_block) {
-  if (cta_mode() != 1) { *bm = 256; *bn = 256; *sym_rows_per_col_block = 1; }
+void ns_tc_tile_shape(bool symmetric, int terms, int* bm, int* bn, int* sym_rows_per_col_block) {
+  if (cta_mode_for(symmetric, terms) != 1) { *bm = 256; *bn = 256; *sym_rows_per_col_block = 1; }
   else { *bm = 128; *bn = 256; *sym_rows_per_col_block = 2; }
 }
 
