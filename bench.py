@@ -322,12 +322,24 @@ def gpu_arm(args):
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
 
+    # the gradients come in on two copy streams while the features come in on
+    # the step's stream and the max logit runs on them; the copy streams first
+    # wait for the stream (the previous step has read G), and the step waits for them
+    copy_streams = [torch.cuda.Stream(device=dev) for _ in range(2)]
+
     def e2e_step():
-        for gd, gh in zip(Gl, Gh):
-            gd.copy_(gh, non_blocking=True)
+        for cs in copy_streams:
+            cs.wait_stream(stream)
+        for i, (gd, gh) in enumerate(zip(Gl, Gh)):
+            with torch.cuda.stream(copy_streams[i % 2]):
+                gd.copy_(gh, non_blocking=True)
         for td, th in zip(feats, fh):
             td.copy_(th, non_blocking=True)
-        step()
+        if att is not None:
+            mc.qk_max_logit(q, k, ks, smax=smax, status=status, stream=stream)
+        for cs in copy_streams:
+            stream.wait_stream(cs)
+        mc.muonclip_step(Wl, Gl, Ml, hp, layers=layers, workspace=ws, status=status, stream=stream)
         res[:H].copy_(smax)
         res[H:2 * H].copy_(gamma)
         res[2 * H:].copy_(ncl.float())
