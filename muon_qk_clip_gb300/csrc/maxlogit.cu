@@ -157,7 +157,8 @@ __global__ void __launch_bounds__(256) ml_simt_kernel(const __grid_constant__ Ma
 
 // ---------------------------------------------------------------- tensor cores
 // bf16 features, q.k length in 64-wide chunks.  One work item = (b, h, 128
-// query rows); its Q chunks are loaded once (double-buffered across items) and
+// query rows), in the paired (b, h)-major order of next_item; its Q chunks are
+// loaded once (double-buffered across items) and
 // 256-row key blocks stream through a ring of 64-feature chunk stages.  For
 // MLA the key chunks come first from the head's k^C, then from the shared k^R.
 // Each key block is one 128 x 256 x d product accumulated in TMEM (double
@@ -179,7 +180,8 @@ struct Geo {
   int nch, nck;        // chunks of q.k and of the head-specific key part
   int stages;
   int nqb;             // query blocks per (b, h)
-  long long items;
+  int nunit;           // work units per (b, h) (pairs of query blocks when causal)
+  long long units;
 };
 
 __device__ inline float max3(float a, float b, float c) {
@@ -188,13 +190,26 @@ __device__ inline float max3(float a, float b, float c) {
   return r;
 }
 
-__device__ inline void item_coords(const MaxLogitParams& p, const Geo& g, long long t, int& b,
-                                   int& h, int& ib) {
-  const long long bh = (long long)p.B * p.H;
-  ib = g.nqb - 1 - (int)(t / bh);        // heaviest query blocks first
-  const int r = (int)(t % bh);
-  h = r % p.H;
-  b = r / p.H;
+// Causal: a unit pairs query blocks ib and nqb - 1 - ib of one (b, h) (equal
+// work), numbered (b, h)-major so the CTAs in flight share a few heads' keys in
+// L2; without the mask a unit is one block.  Iteration n of a CTA is half
+// n & 1 of its (n >> 1)-th unit: 1 with coordinates, 0 for the missing half of
+// an unpaired middle block, -1 when the CTA has no units left.
+__device__ inline int next_item(const MaxLogitParams& p, const Geo& g, uint32_t n, int& b, int& h,
+                                int& ib) {
+  const long long u = blockIdx.x + (long long)(n >> 1) * gridDim.x;
+  if (u >= g.units) return -1;
+  const long long bh = u / g.nunit;
+  const int pu = (int)(u % g.nunit);
+  h = (int)(bh % p.H);
+  b = (int)(bh / p.H);
+  if (!p.causal) {
+    ib = pu;
+    return (n & 1) ? 0 : 1;
+  }
+  if ((n & 1) == 0) { ib = g.nqb - 1 - pu; return 1; }
+  ib = pu;
+  return pu < g.nqb - 1 - pu ? 1 : 0;
 }
 
 __device__ inline int kblocks(const MaxLogitParams& p, int ib) {
@@ -251,9 +266,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0, li = 0;
       bool used_q[2] = {false, false}, used_k[kMaxStages] = {};
       uint32_t par_q[2] = {0, 0}, par_k[kMaxStages] = {};
-      for (long long t = blockIdx.x; t < g.items && !abort_flag; t += gridDim.x, ++li) {
+      for (uint32_t n = 0; !abort_flag; ++n) {
         int b, h, ib;
-        item_coords(p, g, t, b, h, ib);
+        const int st = next_item(p, g, n, b, h, ib);
+        if (st < 0) break;
+        if (st == 0) continue;
         const int qb = li & 1;
         if (!mbar_wait(&q_empty[qb], ((li >> 1) & 1) ^ 1, &abort_flag)) { fail(); break; }
         mbar_arrive_expect_tx(&q_full[qb], g.nch * Q_CHUNK);
@@ -276,6 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
+        ++li;
       }
       for (int i = 0; i < 2; ++i) if (used_q[i]) mbar_wait(&q_full[i], par_q[i], nullptr);
       for (int s = 0; s < g.stages; ++s) if (used_k[s]) mbar_wait(&k_full[s], par_k[s], nullptr);
@@ -285,9 +303,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = make_idesc_bf16(BM, BN, 0, 0);
       uint32_t it = 0, li = 0, tcount = 0;
       bool issued = false;
-      for (long long t = blockIdx.x; t < g.items && !abort_flag; t += gridDim.x, ++li) {
+      for (uint32_t n = 0; !abort_flag; ++n) {
         int b, h, ib;
-        item_coords(p, g, t, b, h, ib);
+        const int st = next_item(p, g, n, b, h, ib);
+        if (st < 0) break;
+        if (st == 0) continue;
         const int qb = li & 1;
         if (!mbar_wait(&q_full[qb], (li >> 1) & 1, &abort_flag)) { fail(); break; }
         const int nkb = kblocks(p, ib);
@@ -314,6 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         tc_commit(&q_empty[qb]);
+        ++li;
       }
       if (issued) { tc_commit(drain); mbar_wait(drain, 0, nullptr); }
     }
@@ -323,9 +344,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;              // TMEM lane quadrant
     const int half = e >> 2;             // columns [half*128, half*128 + 128)
     uint32_t tcount = 0;
-    for (long long t = blockIdx.x; t < g.items; t += gridDim.x) {
+    for (uint32_t n = 0;; ++n) {
       int b, h, ib;
-      item_coords(p, g, t, b, h, ib);
+      const int st = next_item(p, g, n, b, h, ib);
+      if (st < 0) break;
+      if (st == 0) continue;
       const int nkb = kblocks(p, ib);
       const int i = ib * BM + q * 32 + lane;          // this thread's query row
       const int i_lo = ib * BM + q * 32;              // warp's first row
@@ -475,7 +498,8 @@ cudaError_t launch_ml_tc(const MaxLogitParams& p, cudaStream_t s, char* err, siz
   g.nck = (p.d_head + 63) / 64;
   g.nch = p.d_shared > 0 ? g.nck + (p.d_shared + 63) / 64 : g.nck;
   g.nqb = (p.S + BM - 1) / BM;
-  g.items = (long long)p.B * p.H * g.nqb;
+  g.nunit = p.causal ? (g.nqb + 1) / 2 : g.nqb;
+  g.units = (long long)p.B * p.H * g.nunit;
   const int smem_cap = 227 * 1024 - 2048;
   g.stages = (smem_cap - 2 * g.nch * Q_CHUNK) / K_CHUNK;
   if (g.stages > kMaxStages) g.stages = kMaxStages;
@@ -499,7 +523,7 @@ cudaError_t launch_ml_tc(const MaxLogitParams& p, cudaStream_t s, char* err, siz
     if (!encode(&mp.ks, p.ks, 3, dims, st, box)) { snprintf(err, errlen, "tensor map for k_shared failed"); return cudaErrorInvalidValue; }
   }
   const size_t smem = 1024 + 2 * g.nch * Q_CHUNK + g.stages * K_CHUNK + 256;
-  const int grid = (int)(g.items < sm_count() ? g.items : sm_count());
+  const int grid = (int)(g.units < sm_count() ? g.units : sm_count());
   cudaError_t e;
   if (p.argmax) {
     e = cudaFuncSetAttribute(ml_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
