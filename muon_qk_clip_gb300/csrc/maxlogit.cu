@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int i_lo = ib * BM + q * 32;              // warp's first row
       float best = -INFINITY;
       uint32_t bidx = 0xffffffffu;
-      float nanacc = 0.f;
+      float nan4[4] = {0.f, 0.f, 0.f, 0.f};
       int failed = 0;                    // warp-uniform
       for (int kb = 0; kb < nkb; ++kb, ++tcount) {
         if (failed) continue;            // every later wait would fail too
@@ -368,40 +368,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         // every element of this warp's 32 x 128 block valid?
         const bool interior = (j0 + 127 < p.S) && (i_lo + 31 < p.S) && (!p.causal || j0 + 127 <= i_lo);
         const bool empty = (j0 >= p.S) || (i_lo >= p.S) || (p.causal && j0 > i_lo + 31);
-        // all four 32-column loads in flight before one wait
-        uint32_t r[4][32];
-        const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + half * 128;
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) tmem_ld_32x32b_x32_async(tbase + ch * 32, r[ch]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) reg_fence32(r[ch]);
+        // two halves of two 32-column loads in flight before each wait (the
+        // warp's block is empty or not as a whole)
         if (!empty) {
+          const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + half * 128;
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            float* v = reinterpret_cast<float*>(r[ch]);
-            const int jc = j0 + ch * 32;
-            if (!interior) {
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t r[2][32];
 #pragma unroll
-              for (int x = 0; x < 32; ++x) {
-                const int j = jc + x;
-                const bool valid = j < p.S && i < p.S && (!p.causal || j <= i);
-                v[x] = valid ? v[x] : -3.402823466e38f;   // finite: keeps the NaN check exact
+            for (int c2 = 0; c2 < 2; ++c2) tmem_ld_32x32b_x32_async(tbase + (hh * 2 + c2) * 32, r[c2]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) reg_fence32(r[c2]);
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+              float* v = reinterpret_cast<float*>(r[c2]);
+              const int jc = j0 + (hh * 2 + c2) * 32;
+              if (!interior) {
+#pragma unroll
+                for (int x = 0; x < 32; ++x) {
+                  const int j = jc + x;
+                  const bool valid = j < p.S && i < p.S && (!p.causal || j <= i);
+                  v[x] = valid ? v[x] : -3.402823466e38f;   // finite: keeps the NaN check exact
+                }
               }
-            }
+              // four independent chains each for the NaN check and the max
+              float m4[4];
 #pragma unroll
-            for (int x = 0; x < 32; ++x) nanacc = fmaf(v[x], 0.f, nanacc);
-            float m = max3(v[0], v[1], v[2]);
+              for (int c = 0; c < 4; ++c) {
+                m4[c] = fmaxf(v[2 * c], v[2 * c + 1]);
+                nan4[c] = fmaf(v[2 * c], 0.f, nan4[c]);
+                nan4[c] = fmaf(v[2 * c + 1], 0.f, nan4[c]);
+              }
 #pragma unroll
-            for (int x = 3; x < 31; x += 2) m = max3(m, v[x], v[x + 1]);
-            m = fmaxf(m, v[31]);
-            if (m > best) {
-              best = m;
-              if (ARG) {
-                uint32_t jx = 31;
+              for (int x = 8; x < 32; x += 8)
 #pragma unroll
-                for (int x = 31; x >= 0; --x) jx = (v[x] == m) ? (uint32_t)x : jx;
-                bidx = (uint32_t)(((long long)b * p.S + i) * p.S + jc + (int)jx);
+                for (int c = 0; c < 4; ++c) {
+                  m4[c] = max3(m4[c], v[x + 2 * c], v[x + 2 * c + 1]);
+                  nan4[c] = fmaf(v[x + 2 * c], 0.f, nan4[c]);
+                  nan4[c] = fmaf(v[x + 2 * c + 1], 0.f, nan4[c]);
+                }
+              const float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+              if (m > best) {
+                best = m;
+                if (ARG) {
+                  uint32_t jx = 31;
+#pragma unroll
+                  for (int x = 31; x >= 0; --x) jx = (v[x] == m) ? (uint32_t)x : jx;
+                  bidx = (uint32_t)(((long long)b * p.S + i) * p.S + jc + (int)jx);
+                }
               }
             }
           }
@@ -410,7 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&t_empty[acc]);
       }
-      // nanacc became NaN iff some unmasked logit was NaN or infinite.
+      // nan4 became NaN iff some unmasked logit was NaN or infinite.
+      const float nanacc = (nan4[0] + nan4[1]) + (nan4[2] + nan4[3]);
       // Reduce (best, bidx) over the warp, then over the 8 epilogue warps.  All
       // 8 warps reach both named barriers for every item, failed or not, and
       // all leave after the same item.
