@@ -385,9 +385,11 @@ def gpu_arm(args):
     achieved = per_launch_flops / (t_gemm / n_gemm * 1e-3) / 1e12 if n_gemm else None
     launches = sum(v[0] for v in prof.values())
     cfg = {"workload": args.workload, **WORKLOAD_CONFIG[args.workload], "ns_steps": hp.ns_steps,
-           "ns_precision": ("split-bf16 (hi*hi+hi*lo+lo*hi) for the last 3 iterations, hi*hi for "
-                            "the first 2, fp32 accumulate" if wl.dtype == torch.bfloat16
-                            else "fp32 CUDA cores"),
+           "ns_precision": ((f"split-bf16 (hi*hi+hi*lo+lo*hi), fp32 accumulate, all {hp.ns_steps} iterations"
+                             if hp.ns_fast_steps == 0 else
+                             f"split-bf16 (hi*hi+hi*lo+lo*hi) for the last {hp.ns_steps - hp.ns_fast_steps} "
+                             f"iterations, hi*hi for the first {hp.ns_fast_steps}, fp32 accumulate")
+                            if wl.dtype == torch.bfloat16 else "fp32 CUDA cores"),
            "clipped_heads": len(att.scaled_heads) if att is not None else 0,
            "l2": "flushed (512 MB write) before each step",
            "parallelism": f"dp{world} (one layer per rank)"}

@@ -213,9 +213,9 @@ Plan make_plan(const mc_mat* mats, int count, int xmode) {
   P.off_partials = off; off += al((size_t)P.total_tiles * sizeof(double));
   P.off_inv = off; off += al((size_t)count * sizeof(float));
   P.off_inv_sq = off; off += al((size_t)count * sizeof(float));
-  // up to 32 iterations x 3 phases x (ceil(groups / kMaxGroups) + 1) launches
-  // (the groups may be split over two streams)
-  P.nsched = 3 * 32 * ((int)cdiv((long long)P.groups.size(), kMaxGroups) + 1);
+  // up to 32 iterations x 3 phases x (ceil(groups / kMaxGroups) + 3) launches
+  // (the groups may be split over two streams and by products per k-step)
+  P.nsched = 3 * 32 * ((int)cdiv((long long)P.groups.size(), kMaxGroups) + 3);
   P.off_sched = off; off += al((size_t)P.nsched * sizeof(int));
   P.bytes = off;
   return P;
@@ -285,6 +285,13 @@ mc_status run_norms(const Plan& P, void* ws, float eps, cudaStream_t s) {
 // One Newton-Schulz phase over every group (chunks of kMaxGroups).
 enum Phase { kGram = 1, kPoly = 2, kNext = 3 };
 
+// Smallest min(rows, cols) for which the one-product leading iterations keep
+// the Newton-Schulz output within 2e-2 of its RMS with margin: float64
+// emulation of the split arithmetic over adversarial spectra (a few dominant
+// directions over a near-null rest) gives at most 6e-3 from 1024 up, but
+// 1e-2 at 256-384 and up to 9e-2 at 64 and below.
+constexpr int kFastMinSide = 1024;
+
 mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams* hp,
                     int32_t* status, int& launch, const std::vector<int>& groups, cudaStream_t s) {
   const int cur = it & 1, nxt = cur ^ 1;
@@ -295,100 +302,110 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
     const Group &a = P.groups[x], &b = P.groups[y];
     return (ph == kGram ? a.n : a.m) > (ph == kGram ? b.n : b.m);
   });
-  // split iterate: leading "fast" iterations take one bf16 product per
-  // k-step; the last three iterations always take the three-term product
+  // split iterate: the leading ns_fast_steps iterations take one bf16
+  // product per k-step, for shape groups whose smaller side is at least
+  // kFastMinSide only; every other iteration takes the three-term product
   const int fast = std::min(hp->ns_fast_steps, std::max(0, hp->ns_steps - 3));
-  const int terms = (P.xmode == kXSplit && it >= fast) ? 3 : 1;
+  auto terms_of = [&](int g) {
+    if (P.xmode != kXSplit) return 1;
+    if (it >= fast) return 3;
+    return std::min(P.groups[g].m, P.groups[g].n) >= kFastMinSide ? 1 : 3;
+  };
   const bool sym_out = P.xmode != kXF32 && (ph == kGram || ph == kPoly);
-  int tileM = 64, tileN = 64, sym_step = 1;
-  if (P.xmode != kXF32) ns_tc_tile_shape(sym_out, terms, &tileM, &tileN, &sym_step);
-  for (size_t g0 = 0; g0 < order.size(); g0 += kMaxGroups) {
-    GemmParams gp;
-    memset(&gp, 0, sizeof gp);
-    gp.xmode = P.xmode;
-    gp.status = status;
-    int t = 0, ng = 0;
-    for (size_t q = g0; q < order.size() && ng < kMaxGroups; ++q, ++ng) {
-      const Group& g = P.groups[order[q]];
-      GemmGroup& G = gp.g[ng];
-      const long long xs = (long long)g.m * g.ldn, as = (long long)g.m * g.ldm;
-      auto X = [&](int i, int pl) { return (const void*)wsp(ws, g.x[i][pl]); };
-      G.batch = g.batch;
-      G.mat_base = g.mats[0];   // matrices of a group are contiguous in s[] order
+  for (int terms : {1, 3}) {
+    std::vector<int> sub;                    // the groups of this launch kind
+    for (int g : order)
+      if (terms_of(g) == terms) sub.push_back(g);
+    int tileM = 64, tileN = 64, sym_step = 1;
+    if (P.xmode != kXF32) ns_tc_tile_shape(sym_out, terms, &tileM, &tileN, &sym_step);
+    for (size_t g0 = 0; g0 < sub.size(); g0 += kMaxGroups) {
+      GemmParams gp;
+      memset(&gp, 0, sizeof gp);
+      gp.xmode = P.xmode;
+      gp.status = status;
+      int t = 0, ng = 0;
+      for (size_t q = g0; q < sub.size() && ng < kMaxGroups; ++q, ++ng) {
+        const Group& g = P.groups[sub[q]];
+        GemmGroup& G = gp.g[ng];
+        const long long xs = (long long)g.m * g.ldn, as = (long long)g.m * g.ldm;
+        auto X = [&](int i, int pl) { return (const void*)wsp(ws, g.x[i][pl]); };
+        G.batch = g.batch;
+        G.mat_base = g.mats[0];   // matrices of a group are contiguous in s[] order
+        switch (ph) {
+          case kGram:
+            G.M = g.m; G.N = g.m; G.K = g.n;
+            G.a_hi = X(cur, 0); G.a_lo = X(cur, 1); G.lda = g.ldn; G.a_bstride = xs;
+            G.b_hi = X(cur, 0); G.b_lo = X(cur, 1); G.ldb = g.ldn; G.b_bstride = xs;
+            G.d_hi = wsp(ws, g.a[0]); G.d_lo = wsp(ws, g.a[1]); G.ldd = g.ldm; G.d_bstride = as;
+            break;
+          case kPoly:
+            G.M = g.m; G.N = g.m; G.K = g.m;
+            G.a_hi = wsp(ws, g.a[0]); G.a_lo = wsp(ws, g.a[1]); G.lda = g.ldm; G.a_bstride = as;
+            G.b_hi = G.a_hi; G.b_lo = G.a_lo; G.ldb = g.ldm; G.b_bstride = as;
+            G.c_hi = G.a_hi; G.c_lo = G.a_lo; G.ldc = g.ldm; G.c_bstride = as;
+            G.d_hi = wsp(ws, g.b[0]); G.d_lo = wsp(ws, g.b[1]); G.ldd = g.ldm; G.d_bstride = as;
+            break;
+          case kNext:
+            G.M = g.m; G.N = g.n; G.K = g.m;
+            G.a_hi = wsp(ws, g.b[0]); G.a_lo = wsp(ws, g.b[1]); G.lda = g.ldm; G.a_bstride = as;
+            G.b_hi = X(cur, 0); G.b_lo = X(cur, 1); G.ldb = g.ldn; G.b_bstride = xs;
+            G.b_mn_major = 1;
+            G.c_hi = X(cur, 0); G.c_lo = X(cur, 1); G.ldc = g.ldn; G.c_bstride = xs;
+            G.d_hi = wsp(ws, g.x[nxt][0]); G.d_lo = wsp(ws, g.x[nxt][1]); G.ldd = g.ldn;
+            G.d_bstride = xs;
+            break;
+        }
+        G.tiles_m = (int)cdiv(G.M, tileM);
+        G.tiles_n = (int)cdiv(G.N, tileN);
+        G.tiles_per_item = G.tiles_m * G.tiles_n;
+        // Gram and polynomial outputs are symmetric: the tensor-core path
+        // computes only the tiles touching the upper triangle
+        if (sym_out) {
+          G.symmetric = 1;
+          G.tiles_per_item = 0;
+          for (int tn = 0; tn < G.tiles_n; ++tn)
+            G.tiles_per_item += std::min(G.tiles_m, (tn + 1) * sym_step);
+        }
+        G.tile_begin = t;
+        t += G.tiles_per_item * G.batch;
+        (void)es;
+      }
+      gp.ngroups = ng;
+      gp.total_tiles = t;
+      // tensor-core launches claim tiles from a zeroed counter of their own
+      if (P.xmode != kXF32 && ns_dynamic_schedule() && launch < P.nsched)
+        gp.sched = reinterpret_cast<int*>(wsp(ws, P.off_sched)) + launch;
+      ++launch;
+      gp.terms = terms;
+      // Three-term iterations fold a X into the polynomial: B' = c A^2 + b A + a I
+      // and X' = B' X, so the last phase reads no C.  (B' holds ~16 significand
+      // bits there; a one-plane bf16 B' would lose the small singular values, so
+      // the other iterations keep X' = B X + a X.)
+      const bool fold = P.xmode == kXSplit && gp.terms == 3;
       switch (ph) {
         case kGram:
-          G.M = g.m; G.N = g.m; G.K = g.n;
-          G.a_hi = X(cur, 0); G.a_lo = X(cur, 1); G.lda = g.ldn; G.a_bstride = xs;
-          G.b_hi = X(cur, 0); G.b_lo = X(cur, 1); G.ldb = g.ldn; G.b_bstride = xs;
-          G.d_hi = wsp(ws, g.a[0]); G.d_lo = wsp(ws, g.a[1]); G.ldd = g.ldm; G.d_bstride = as;
+          gp.alpha = 1.f; gp.beta = 0.f;
+          gp.s = it == 0 ? reinterpret_cast<const float*>(wsp(ws, P.off_inv_sq)) : nullptr;
           break;
         case kPoly:
-          G.M = g.m; G.N = g.m; G.K = g.m;
-          G.a_hi = wsp(ws, g.a[0]); G.a_lo = wsp(ws, g.a[1]); G.lda = g.ldm; G.a_bstride = as;
-          G.b_hi = G.a_hi; G.b_lo = G.a_lo; G.ldb = g.ldm; G.b_bstride = as;
-          G.c_hi = G.a_hi; G.c_lo = G.a_lo; G.ldc = g.ldm; G.c_bstride = as;
-          G.d_hi = wsp(ws, g.b[0]); G.d_lo = wsp(ws, g.b[1]); G.ldd = g.ldm; G.d_bstride = as;
+          gp.alpha = hp->ns_c; gp.beta = hp->ns_b; gp.s = nullptr;
+          gp.diag = fold ? hp->ns_a : 0.f;
           break;
         case kNext:
-          G.M = g.m; G.N = g.n; G.K = g.m;
-          G.a_hi = wsp(ws, g.b[0]); G.a_lo = wsp(ws, g.b[1]); G.lda = g.ldm; G.a_bstride = as;
-          G.b_hi = X(cur, 0); G.b_lo = X(cur, 1); G.ldb = g.ldn; G.b_bstride = xs;
-          G.b_mn_major = 1;
-          G.c_hi = X(cur, 0); G.c_lo = X(cur, 1); G.ldc = g.ldn; G.c_bstride = xs;
-          G.d_hi = wsp(ws, g.x[nxt][0]); G.d_lo = wsp(ws, g.x[nxt][1]); G.ldd = g.ldn;
-          G.d_bstride = xs;
+          gp.alpha = 1.f; gp.beta = fold ? 0.f : hp->ns_a;
+          gp.s = it == 0 ? reinterpret_cast<const float*>(wsp(ws, P.off_inv)) : nullptr;
           break;
       }
-      G.tiles_m = (int)cdiv(G.M, tileM);
-      G.tiles_n = (int)cdiv(G.N, tileN);
-      G.tiles_per_item = G.tiles_m * G.tiles_n;
-      // Gram and polynomial outputs are symmetric: the tensor-core path
-      // computes only the tiles touching the upper triangle
-      if (sym_out) {
-        G.symmetric = 1;
-        G.tiles_per_item = 0;
-        for (int tn = 0; tn < G.tiles_n; ++tn)
-          G.tiles_per_item += std::min(G.tiles_m, (tn + 1) * sym_step);
+      cudaError_t e;
+      if (P.xmode == kXF32) {
+        e = launch_ns_gemm_f32(gp, s);
+      } else {
+        char err[256] = {0};
+        e = launch_ns_gemm_tc(gp, s, err, sizeof err);
+        if (e != cudaSuccess && err[0]) return fail(MC_ERR_CUDA, "tensor-core GEMM: %s", err);
       }
-      G.tile_begin = t;
-      t += G.tiles_per_item * G.batch;
-      (void)es;
+      if (e != cudaSuccess) return cuda_fail(e, "Newton-Schulz GEMM launch");
     }
-    gp.ngroups = ng;
-    gp.total_tiles = t;
-    // tensor-core launches claim tiles from a zeroed counter of their own
-    if (P.xmode != kXF32 && ns_dynamic_schedule() && launch < P.nsched)
-      gp.sched = reinterpret_cast<int*>(wsp(ws, P.off_sched)) + launch;
-    ++launch;
-    gp.terms = terms;
-    // Three-term iterations fold a X into the polynomial: B' = c A^2 + b A + a I
-    // and X' = B' X, so the last phase reads no C.  (B' holds ~16 significand
-    // bits there; a one-plane bf16 B' would lose the small singular values, so
-    // the other iterations keep X' = B X + a X.)
-    const bool fold = P.xmode == kXSplit && gp.terms == 3;
-    switch (ph) {
-      case kGram:
-        gp.alpha = 1.f; gp.beta = 0.f;
-        gp.s = it == 0 ? reinterpret_cast<const float*>(wsp(ws, P.off_inv_sq)) : nullptr;
-        break;
-      case kPoly:
-        gp.alpha = hp->ns_c; gp.beta = hp->ns_b; gp.s = nullptr;
-        gp.diag = fold ? hp->ns_a : 0.f;
-        break;
-      case kNext:
-        gp.alpha = 1.f; gp.beta = fold ? 0.f : hp->ns_a;
-        gp.s = it == 0 ? reinterpret_cast<const float*>(wsp(ws, P.off_inv)) : nullptr;
-        break;
-    }
-    cudaError_t e;
-    if (P.xmode == kXF32) {
-      e = launch_ns_gemm_f32(gp, s);
-    } else {
-      char err[256] = {0};
-      e = launch_ns_gemm_tc(gp, s, err, sizeof err);
-      if (e != cudaSuccess && err[0]) return fail(MC_ERR_CUDA, "tensor-core GEMM: %s", err);
-    }
-    if (e != cudaSuccess) return cuda_fail(e, "Newton-Schulz GEMM launch");
   }
   return MC_OK;
 }
