@@ -322,16 +322,16 @@ def gpu_arm(args):
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
 
-    # the gradients come in on two copy streams while the features come in on
-    # the step's stream and the max logit runs on them; the copy streams first
-    # wait for the stream (the previous step has read G), and the step waits for them
-    copy_streams = [torch.cuda.Stream(device=dev) for _ in range(2)]
+    # the gradients come in on a copy stream while the features come in on the
+    # step's stream and the max logit runs on them; the copy stream first waits
+    # for the stream (the previous step has read G), and the step waits for it
+    copy_streams = [torch.cuda.Stream(device=dev)]
 
     def e2e_step():
         for cs in copy_streams:
             cs.wait_stream(stream)
-        for i, (gd, gh) in enumerate(zip(Gl, Gh)):
-            with torch.cuda.stream(copy_streams[i % 2]):
+        for gd, gh in zip(Gl, Gh):
+            with torch.cuda.stream(copy_streams[0]):
                 gd.copy_(gh, non_blocking=True)
         for td, th in zip(feats, fh):
             td.copy_(th, non_blocking=True)
