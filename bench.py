@@ -309,6 +309,32 @@ def gpu_arm(args):
                     "smax_equals_max_logit": bool(torch.allclose(smax_f, smax, rtol=1e-6, atol=0.0)),
                     "launches_per_call": pf[0] // args.steps}
 
+    # ---- HBM-streaming stress of the clip: every head over tau, on copies of the
+    # layer's Q/K weights (L2 flushed before each call)
+    clip_stress = None
+    if att is not None:
+        copies = {}
+        for sg in segs:
+            copies.setdefault(sg.w.data_ptr(), sg.w.clone())
+        ssegs = [mc.ClipSegment(copies[sg.w.data_ptr()], sg.offset, sg.stride, sg.rows, sg.exponent)
+                 for sg in segs]
+        s_all = torch.full((H,), 4.0 * hp.tau, dtype=torch.float32, device=dev)
+        stress_bytes = sum(2 * H * sg.rows * sg.w.shape[1] * sg.w.element_size() for sg in ssegs)
+        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        mc.qk_clip_apply(s_all, hp.tau, ssegs, stream=stream)
+        barrier()
+        for i in range(args.steps):
+            flush.zero_()
+            cev[i][0].record(stream)
+            mc.qk_clip_apply(s_all, hp.tau, ssegs, stream=stream)
+            cev[i][1].record(stream)
+        barrier()
+        cms = sum(a.elapsed_time(b) for a, b in cev) / args.steps
+        clip_stress = {"heads_clipped": H, "bytes": stress_bytes, "ms": round(cms, 4),
+                       "gbs": round(stress_bytes / (cms * 1e-3) / 1e9, 1)}
+        del copies, ssegs
+
     # ---- end to end through the public API: pinned host G (and Q, K) in, metrics out
     Gh = [g.to("cpu").pin_memory() for g in Gl]
     feats = [t for t in (q, ks) if t is not None]
@@ -380,6 +406,19 @@ def gpu_arm(args):
     ns_tflops = ns_flops * args.steps / (t_gemm * 1e-3) / 1e12 if t_gemm else None
     ml_tflops = ml_flops * args.steps / (t_ml * 1e-3) / 1e12 if t_ml else None
     clip_gbs = clip_bytes * args.steps / (t_clip * 1e-3) / 1e9 if t_clip and clip_bytes else None
+    # streaming kernels' algorithmic bytes: momentum/prep reads G and M, writes M
+    # and the oriented iterate; apply reads W and the iterate, writes W
+    elems = sum(m.rows * m.cols for m in wl.matrices)
+    g_b = Gl[0].element_size()
+    x_b = 4                                            # (hi, lo) bf16 planes, or one fp32 plane
+    w_b = Wl[0].element_size()
+    prep_bytes = elems * (g_b + 8 + x_b)
+    apply_bytes = elems * (2 * w_b + x_b)
+    hbm = pk.get("hbm_gbs") or 6764.0
+    n_prep, t_prep = prof.get("prep", (0, 0.0))
+    n_apply, t_apply = prof.get("apply", (0, 0.0))
+    prep_gbs = prep_bytes * args.steps / (t_prep * 1e-3) / 1e9 if t_prep else None
+    apply_gbs = apply_bytes * args.steps / (t_apply * 1e-3) / 1e9 if t_apply else None
     peak_t = pk["bf16_tflops"]
     per_launch_flops = ns_flops / (n_gemm / args.steps) if n_gemm else None
     achieved = per_launch_flops / (t_gemm / n_gemm * 1e-3) / 1e12 if n_gemm else None
@@ -425,6 +464,12 @@ def gpu_arm(args):
             "max_logit_tflops": round(ml_tflops, 2) if ml_tflops else None,
             "max_logit_frac_bf16_peak": round(ml_tflops / peak_t, 4) if ml_tflops else None,
             "clip_gbs": round(clip_gbs, 1) if clip_gbs else None,
+            "clip_stress_all_heads": dict(clip_stress, frac_hbm=round(clip_stress["gbs"] / hbm, 4))
+            if clip_stress else None,
+            "prep_gbs": round(prep_gbs, 1) if prep_gbs else None,
+            "prep_frac_hbm": round(prep_gbs / hbm, 4) if prep_gbs else None,
+            "apply_gbs": round(apply_gbs, 1) if apply_gbs else None,
+            "apply_frac_hbm": round(apply_gbs / hbm, 4) if apply_gbs else None,
             "kernel_ms_per_step": {k: round(v[1] / args.steps, 4) for k, v in prof.items()},
             "kernel_launches_per_step": {k: v[0] // args.steps for k, v in prof.items()},
             "step_ms_min": round(min(step_ms), 4), "step_ms_max": round(max(step_ms), 4),
