@@ -310,7 +310,7 @@ def gpu_arm(args):
                     "launches_per_call": pf[0] // args.steps}
 
     # ---- HBM-streaming stress of the clip: every head over tau, on copies of the
-    # layer's Q/K weights (L2 flushed before each call)
+    # layer's Q/K weights (L2 flushed before each call; one launch per call)
     clip_stress = None
     if att is not None:
         copies = {}
@@ -326,6 +326,9 @@ def gpu_arm(args):
         barrier()
         for i in range(args.steps):
             flush.zero_()
+            # a ~50 us device spin keeps the stream busy while the host builds
+            # the call, so the interval holds the launch and not the host
+            torch.cuda._sleep(100_000)
             cev[i][0].record(stream)
             mc.qk_clip_apply(s_all, hp.tau, ssegs, stream=stream)
             cev[i][1].record(stream)

@@ -587,7 +587,7 @@ mc_status run_clip(const float* smax, int H, float tau, int mode, const mc_clip_
     d.bf16 = segs[i].w.dtype == MC_BF16;
     d.exponent = segs[i].exponent;
   }
-  ProfScope ps(kClip, (gamma_out || nclipped || status) ? 2 : 1, s);
+  ProfScope ps(kClip, 1, s);
   cudaError_t e = launch_clip(cp, s);
   if (e != cudaSuccess) return cuda_fail(e, "clip launch");
   return MC_OK;

@@ -27,11 +27,6 @@ __device__ inline int find_job(const Job* jobs, int njobs, int t) {
   return lo;
 }
 
-__device__ inline float load_elem(const void* base, long long idx, int bf16) {
-  return bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[idx])
-              : reinterpret_cast<const float*>(base)[idx];
-}
-
 // Write one iterate element x at (r, c) of the oriented planes.
 template <int XM>
 __device__ inline void store_x(void* xh, void* xl, long long idx, float x) {
@@ -47,27 +42,7 @@ __device__ inline void store_x(void* xh, void* xl, long long idx, float x) {
   }
 }
 
-template <int XM>
-__device__ inline float load_x(const void* xh, const void* xl, long long idx) {
-  if (XM == kXSplit)
-    return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(xh)[idx]) +
-           __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(xl)[idx]);
-  if (XM == kXBf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(xh)[idx]);
-  return reinterpret_cast<const float*>(xh)[idx];
-}
-
 // Four consecutive elements (16-byte aligned fp32 or 8-byte aligned bf16).
-__device__ inline void load4(const void* base, long long idx, int bf16, float (&o)[4]) {
-  if (bf16) {
-    const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(base) + idx);
-    const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&u);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) o[e] = __bfloat162float(b[e]);
-  } else {
-    const float4 f = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + idx);
-    o[0] = f.x; o[1] = f.y; o[2] = f.z; o[3] = f.w;
-  }
-}
 __device__ inline void store4(void* base, long long idx, int bf16, const float (&v)[4]) {
   if (bf16) {
     uint2 u;
@@ -95,16 +70,54 @@ __device__ inline void store_x4(void* xh, void* xl, long long idx, const float (
     store4(xh, idx, 0, v);
   }
 }
-template <int XM>
-__device__ inline void load_x4(const void* xh, const void* xl, long long idx, float (&o)[4]) {
-  if (XM == kXSplit) {
-    float h[4], l[4];
-    load4(xh, idx, 1, h);
-    load4(xl, idx, 1, l);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) o[e] = h[e] + l[e];
+
+// Raw bits of up to four consecutive elements, unconverted, so that a tile's
+// loads can all be in flight before the first one is used: 16-bit elements
+// packed two per word in .x/.y, fp32 elements one per word; elements past
+// n (< 4 only at a matrix's right edge) are zero bits.
+__device__ inline uint4 raw_load4(const void* base, long long idx, int half, bool vec, int n) {
+  uint4 u = make_uint4(0u, 0u, 0u, 0u);
+  if (half) {
+    const uint16_t* b = reinterpret_cast<const uint16_t*>(base) + idx;
+    if (vec) {
+      const uint2 v = *reinterpret_cast<const uint2*>(b);
+      u.x = v.x; u.y = v.y;
+    } else {
+      uint32_t e[4] = {0u, 0u, 0u, 0u};
+      for (int i = 0; i < n && i < 4; ++i) e[i] = b[i];
+      u.x = e[0] | (e[1] << 16); u.y = e[2] | (e[3] << 16);
+    }
   } else {
-    load4(xh, idx, XM == kXBf16, o);
+    const uint32_t* f = reinterpret_cast<const uint32_t*>(base) + idx;
+    if (vec) {
+      u = *reinterpret_cast<const uint4*>(f);
+    } else {
+      uint32_t e[4] = {0u, 0u, 0u, 0u};
+      for (int i = 0; i < n && i < 4; ++i) e[i] = f[i];
+      u = make_uint4(e[0], e[1], e[2], e[3]);
+    }
+  }
+  return u;
+}
+// bf16 -> fp32 is exact: the 16 bits are the high half of the fp32 word.
+__device__ inline void raw_cvt4(const uint4& u, int half, float (&o)[4]) {
+  if (half) {
+    o[0] = __uint_as_float(u.x << 16); o[1] = __uint_as_float(u.x & 0xffff0000u);
+    o[2] = __uint_as_float(u.y << 16); o[3] = __uint_as_float(u.y & 0xffff0000u);
+  } else {
+    o[0] = __uint_as_float(u.x); o[1] = __uint_as_float(u.y);
+    o[2] = __uint_as_float(u.z); o[3] = __uint_as_float(u.w);
+  }
+}
+// The iterate's value from the raw words of its plane(s).
+template <int XM>
+__device__ inline void raw_cvt_x4(const uint4& a, const uint4& b, float (&o)[4]) {
+  raw_cvt4(a, XM != kXF32, o);
+  if (XM == kXSplit) {
+    float l[4];
+    raw_cvt4(b, 1, l);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] += l[e];
   }
 }
 
@@ -123,99 +136,116 @@ __device__ inline double block_sum(double v, double* red) {
 }
 
 // Thread layout inside a 64x64 tile: 16 threads x 4 columns per row,
-// 16 rows per pass, 4 passes.
+// 16 rows per pass, 4 passes.  Every load of a tile is issued before its
+// first store (the stores to M could alias the next rows' loads as far as
+// the compiler knows, which would leave one row's loads in flight at a
+// time).  partials[tile] is the fp64 sum of squares of the tile: a fixed
+// shuffle tree per warp, then the 8 warp sums in warp order (double-buffered
+// by tile parity, so one barrier per tile suffices).
 template <int XM>
 __global__ void __launch_bounds__(kThreads) prep_kernel(const __grid_constant__ PrepParams p) {
   __shared__ float tile[kTile][kTile + 1];
-  __shared__ double red[kThreads / 32];
+  __shared__ double red[2][kThreads / 32];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+  int parity = 0;
+  for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, parity ^= 1) {
     const PrepJob& jb = p.jobs[find_job(p.jobs, p.njobs, t)];
     const int lt = t - jb.tile_begin;
     const int r0 = (lt / jb.tiles_c) * kTile, c0 = (lt % jb.tiles_c) * kTile;
-    float ss = 0.f;
-    bool bad = false;
     const int cl0 = tx * 4, cbase = c0 + cl0;
     const bool vec = cbase + 3 < jb.cols;        // 4 in-range columns: one vector access
+    const int nc = jb.cols - cbase;               // valid columns of this thread (may be <= 0)
+    float m[4][4];
+    uint4 gr[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int r = r0 + ty + 16 * k;
+      gr[k] = make_uint4(0u, 0u, 0u, 0u);
+      const uint4 mr = r < jb.rows ? raw_load4(jb.M, (long long)r * jb.ldM + cbase, 0, vec, nc)
+                                   : make_uint4(0u, 0u, 0u, 0u);
+      m[k][0] = __uint_as_float(mr.x); m[k][1] = __uint_as_float(mr.y);
+      m[k][2] = __uint_as_float(mr.z); m[k][3] = __uint_as_float(mr.w);
+      if (p.do_momentum && r < jb.rows)
+        gr[k] = raw_load4(jb.G, (long long)r * jb.ldG + cbase, jb.g_bf16, vec, nc);
+    }
+    float ss = 0.f;
+    bool bad = false;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int rl = ty + 16 * k, r = r0 + rl;
-      float m[4] = {0.f, 0.f, 0.f, 0.f};
-      if (r < jb.rows) {
-        const long long im = (long long)r * jb.ldM + cbase;
-        if (vec) {
-          load4(jb.M, im, 0, m);
-          if (p.do_momentum) {
-            float g[4];
-            load4(jb.G, (long long)r * jb.ldG + cbase, jb.g_bf16, g);
+      if (p.do_momentum) {
+        float g[4];
+        raw_cvt4(gr[k], jb.g_bf16, g);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) m[e] = fmaf(p.mu, m[e], g[e]);
-            store4(jb.M, im, 0, m);
-          }
-        } else {
+        for (int e = 0; e < 4; ++e) m[k][e] = fmaf(p.mu, m[k][e], g[e]);
+        if (r < jb.rows) {
+          const long long im = (long long)r * jb.ldM + cbase;
+          if (vec) {
+            store4(jb.M, im, 0, m[k]);
+          } else {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (cbase + e >= jb.cols) continue;
-            m[e] = jb.M[im + e];
-            if (p.do_momentum) {
-              m[e] = fmaf(p.mu, m[e], load_elem(jb.G, (long long)r * jb.ldG + cbase + e, jb.g_bf16));
-              jb.M[im + e] = m[e];
-            }
+            for (int e = 0; e < 4; ++e)
+              if (cbase + e < jb.cols) jb.M[im + e] = m[k][e];
           }
         }
       }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        bad |= !finite_f(m[e]);
-        ss = fmaf(m[e], m[e], ss);
-        tile[rl][cl0 + e] = m[e];
+        bad |= !finite_f(m[k][e]);
+        ss = fmaf(m[k][e], m[k][e], ss);
+      }
+      if (!p.write_x || r >= jb.rows) continue;
+      if (jb.transpose) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) tile[rl][cl0 + e] = m[k][e];
+      } else {
+        const long long ix = (long long)r * jb.ldx + cbase;
+        if (vec) {
+          store_x4<XM>(jb.xh, jb.xl, ix, m[k]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (cbase + e < jb.cols) store_x<XM>(jb.xh, jb.xl, ix + e, m[k][e]);
+        }
       }
     }
     if (bad) set_status(p.status, MC_STATUS_NONFINITE_UPDATE);
-    if (p.write_x) {
-      if (!jb.transpose) {
+    if (p.write_x && jb.transpose) {
+      __syncthreads();
+      // oriented row = original column, oriented column = original row
+      // (rows of the tile past jb.rows were never written and are not read)
+      const int rbase = r0 + tx * 4;
+      const bool rvec = rbase + 3 < jb.rows;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int rl = ty + 16 * k, r = r0 + rl;
-          if (r >= jb.rows) continue;
-          const long long ix = (long long)r * jb.ldx + cbase;
-          if (vec) {
-            float v[4] = {tile[rl][cl0], tile[rl][cl0 + 1], tile[rl][cl0 + 2], tile[rl][cl0 + 3]};
-            store_x4<XM>(jb.xh, jb.xl, ix, v);
-          } else {
+      for (int k = 0; k < 4; ++k) {
+        const int cl = ty + 16 * k, c = c0 + cl;
+        if (c >= jb.cols) continue;
+        const long long ix = (long long)c * jb.ldx + rbase;
+        float v[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (cbase + e < jb.cols) store_x<XM>(jb.xh, jb.xl, ix + e, tile[rl][cl0 + e]);
-          }
-        }
-      } else {
-        __syncthreads();
-        // oriented row = original column, oriented column = original row
-        const int rbase = r0 + tx * 4;
-        const bool rvec = rbase + 3 < jb.rows;
+        for (int e = 0; e < 4; ++e) v[e] = tile[tx * 4 + e][cl];
+        if (rvec) {
+          store_x4<XM>(jb.xh, jb.xl, ix, v);
+        } else {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int cl = ty + 16 * k, c = c0 + cl;
-          if (c >= jb.cols) continue;
-          const long long ix = (long long)c * jb.ldx + rbase;
-          float v[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) v[e] = tile[tx * 4 + e][cl];
-          if (rvec) {
-            store_x4<XM>(jb.xh, jb.xl, ix, v);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (rbase + e < jb.rows) store_x<XM>(jb.xh, jb.xl, ix + e, v[e]);
-          }
+          for (int e = 0; e < 4; ++e)
+            if (rbase + e < jb.rows) store_x<XM>(jb.xh, jb.xl, ix + e, v[e]);
         }
       }
+      __syncthreads();
     }
     if (p.partials) {
-      const double s = block_sum((double)ss, red);
-      if (threadIdx.x == 0) p.partials[t] = s;
+      double v = ss;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+      if ((threadIdx.x & 31) == 0) red[parity][threadIdx.x >> 5] = v;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        double sum = 0.0;
+        for (int i = 0; i < kThreads / 32; ++i) sum += red[parity][i];
+        p.partials[t] = sum;
+      }
     }
-    __syncthreads();
   }
 }
 
@@ -223,9 +253,16 @@ __global__ void norms_kernel(const __grid_constant__ NormParams p) {
   __shared__ double red[kThreads / 32];
   const int j = blockIdx.x;
   if (j >= p.nmat) return;
-  double s = 0.0;
+  // eight independent accumulators per thread (their loads overlap), folded
+  // in a fixed order
+  double acc[8] = {0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0};
   const int b = p.begin[j], n = p.count[j];
-  for (int i = threadIdx.x; i < n; i += blockDim.x) s += p.partials[b + i];
+  for (int i0 = threadIdx.x; i0 < n; i0 += 8 * kThreads) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (i0 + u * kThreads < n) acc[u] += p.partials[b + i0 + u * kThreads];
+  }
+  double s = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
   s = block_sum(s, red);
   if (threadIdx.x == 0) {
     const double inv = 1.0 / (sqrt(s) + (double)p.eps);
@@ -234,6 +271,8 @@ __global__ void norms_kernel(const __grid_constant__ NormParams p) {
   }
 }
 
+// Same tile layout as prep_kernel; every load of a row pass is issued before
+// the first store of W.
 template <int XM>
 __global__ void __launch_bounds__(kThreads) apply_kernel(const __grid_constant__ ApplyParams p) {
   __shared__ float tile[kTile][kTile + 1];
@@ -248,59 +287,61 @@ __global__ void __launch_bounds__(kThreads) apply_kernel(const __grid_constant__
       // stage X^T tile: oriented rows c0.., oriented cols r0..
       const int rbase = r0 + tx * 4;
       const bool rvec = rbase + 3 < jb.rows;
+      const int nr = jb.rows - rbase;
+      uint4 xa[4], xb[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int cl = ty + 16 * k, c = c0 + cl;
-        float x[4] = {0.f, 0.f, 0.f, 0.f};
-        if (c < jb.cols) {
-          const long long ix = (long long)c * jb.ldx + rbase;
-          if (rvec) {
-            load_x4<XM>(jb.xh, jb.xl, ix, x);
-          } else {
+        const int c = c0 + ty + 16 * k;
+        xa[k] = xb[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (c >= jb.cols) continue;
+        const long long ix = (long long)c * jb.ldx + rbase;
+        xa[k] = raw_load4(jb.xh, ix, XM != kXF32, rvec, nr);
+        if (XM == kXSplit) xb[k] = raw_load4(jb.xl, ix, 1, rvec, nr);
+      }
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (rbase + e < jb.rows) x[e] = load_x<XM>(jb.xh, jb.xl, ix + e);
-          }
-        }
+      for (int k = 0; k < 4; ++k) {
+        float x[4];
+        raw_cvt_x4<XM>(xa[k], xb[k], x);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) tile[tx * 4 + e][cl] = x[e];
+        for (int e = 0; e < 4; ++e) tile[tx * 4 + e][ty + 16 * k] = x[e];
       }
       __syncthreads();
     }
-    bool bad = false;
     const bool vec = cbase + 3 < jb.cols;
+    const int nc = jb.cols - cbase;
+    uint4 xa[4], xb[4], wr[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int rl = ty + 16 * k, r = r0 + rl;
+      const int r = r0 + ty + 16 * k;
+      xa[k] = xb[k] = wr[k] = make_uint4(0u, 0u, 0u, 0u);
       if (r >= jb.rows) continue;
-      float x[4];
-      const long long ixo = (long long)r * jb.ldx + cbase;
+      if (!jb.transpose) {
+        const long long ixo = (long long)r * jb.ldx + cbase;
+        xa[k] = raw_load4(jb.xh, ixo, XM != kXF32, vec, nc);
+        if (XM == kXSplit) xb[k] = raw_load4(jb.xl, ixo, 1, vec, nc);
+      }
+      if (!p.write_o) wr[k] = raw_load4(jb.out, (long long)r * jb.ldo + cbase, jb.out_bf16, vec, nc);
+    }
+    bool bad = false;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int r = r0 + ty + 16 * k;
+      if (r >= jb.rows) continue;
+      float x[4], w[4], v[4];
       if (jb.transpose) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) x[e] = tile[rl][cl0 + e];
-      } else if (vec) {
-        load_x4<XM>(jb.xh, jb.xl, ixo, x);
+        for (int e = 0; e < 4; ++e) x[e] = tile[ty + 16 * k][cl0 + e];
       } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) x[e] = cbase + e < jb.cols ? load_x<XM>(jb.xh, jb.xl, ixo + e) : 0.f;
+        raw_cvt_x4<XM>(xa[k], xb[k], x);
       }
-      const long long io = (long long)r * jb.ldo + cbase;
-      float w[4] = {0.f, 0.f, 0.f, 0.f}, v[4];
-      if (!p.write_o) {
-        if (vec) {
-          load4(jb.out, io, jb.out_bf16, w);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (cbase + e < jb.cols) w[e] = load_elem(jb.out, io + e, jb.out_bf16);
-        }
-      }
+      raw_cvt4(wr[k], jb.out_bf16, w);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float o = s * x[e];
         v[e] = p.write_o ? o : fmaf(-p.lr, fmaf(p.wd, w[e], o), w[e]);   // w - lr (o + wd w)
         bad |= !finite_f(v[e]) && (cbase + e < jb.cols);
       }
+      const long long io = (long long)r * jb.ldo + cbase;
       if (vec) {
         store4(jb.out, io, jb.out_bf16, v);
       } else {
@@ -337,8 +378,8 @@ __device__ inline float total_smax(const ClipParams& p) {
   return nan ? NAN : mx;
 }
 
-__global__ void clip_stats_kernel(const __grid_constant__ ClipParams p) {
-  // one block: gamma_out, nclipped and the NaN flag
+// gamma_out, nclipped and the NaN flag, computed by one whole block
+__device__ void clip_stats(const ClipParams& p) {
   __shared__ float s_total;
   if (p.total) {
     if (threadIdx.x == 0) s_total = total_smax(p);
@@ -363,19 +404,57 @@ __global__ void clip_stats_kernel(const __grid_constant__ ClipParams p) {
   }
 }
 
-// grid.x over (segment, head) pairs, grid.y over row chunks of a head.
+// grid.x over (segment, head) pairs, grid.y over chunks of a head's rows.
+constexpr int kClipUnroll = 8;
 __global__ void __launch_bounds__(kThreads) clip_rows_kernel(const __grid_constant__ ClipParams p) {
+  if (blockIdx.x == 0 && blockIdx.y == 0 && (p.gamma_out || p.nclipped || p.status)) clip_stats(p);
   const int pair = blockIdx.x;
   const int seg = pair / p.H, h = pair % p.H;
   if (seg >= p.nsegs) return;
-  __shared__ float s_blk;
-  if (threadIdx.x == 0) s_blk = p.total ? total_smax(p) : p.smax[h];
-  __syncthreads();
-  const float s = s_blk;
+  float s;
+  if (p.total) {
+    __shared__ float s_blk;
+    if (threadIdx.x == 0) s_blk = total_smax(p);
+    __syncthreads();
+    s = s_blk;
+  } else {
+    s = p.smax[h];                                // one broadcast load, no barrier
+  }
   if (!(s > p.tau)) return;                       // untouched head (and NaN)
   const ClipSegDev& sg = p.segs[seg];
   const float f = clip_power(p.tau / s, sg.exponent);
   const long long row0 = sg.row_offset + (long long)h * sg.row_stride;
+  const int per_vec = sg.bf16 ? 8 : 4;
+  if (sg.ld == sg.cols && (sg.rows * (long long)sg.cols) % per_vec == 0) {
+    // the head's rows are one contiguous range: stride over its 16-byte
+    // vectors, kClipUnroll loads in flight per thread
+    const long long nvec = sg.rows * (long long)sg.cols / per_vec;
+    uint4* w = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(sg.w) +
+                                        row0 * sg.ld * (sg.bf16 ? 2 : 4));
+    const long long step = (long long)gridDim.y * blockDim.x;
+    for (long long v0 = (long long)blockIdx.y * blockDim.x + threadIdx.x; v0 < nvec;
+         v0 += kClipUnroll * step) {
+      uint4 raw[kClipUnroll];
+#pragma unroll
+      for (int u = 0; u < kClipUnroll; ++u)
+        if (v0 + u * step < nvec) raw[u] = w[v0 + u * step];
+#pragma unroll
+      for (int u = 0; u < kClipUnroll; ++u) {
+        if (v0 + u * step >= nvec) continue;
+        if (sg.bf16) {
+          __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(&raw[u]);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) e[i] = __float2bfloat16_rn(__bfloat162float(e[i]) * f);
+        } else {
+          float* e = reinterpret_cast<float*>(&raw[u]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) e[i] *= f;
+        }
+        w[v0 + u * step] = raw[u];
+      }
+    }
+    return;
+  }
   for (long long rr = blockIdx.y; rr < sg.rows; rr += gridDim.y) {
     const long long base = (row0 + rr) * sg.ld;
     if (sg.bf16) {
@@ -403,8 +482,19 @@ __global__ void __launch_bounds__(kThreads) clip_rows_kernel(const __grid_consta
   }
 }
 
-int grid_for(int tiles) {
-  const int cap = sm_count() * 8;
+// Grid of a tile-loop kernel: every block resident at once (blocks per SM
+// from the kernel's own occupancy), so the tiles split evenly over one wave.
+template <class Kernel>
+int grid_for(Kernel kernel, int tiles) {
+  static const int per_sm = [&] {
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kThreads, 0) != cudaSuccess) {
+      (void)cudaGetLastError();
+      nb = 0;
+    }
+    return nb > 0 ? nb : 4;
+  }();
+  const int cap = sm_count() * per_sm;
   return tiles < cap ? (tiles > 0 ? tiles : 1) : cap;
 }
 
@@ -423,11 +513,10 @@ int sm_count() {
 
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t s) {
   if (p.total_tiles <= 0) return cudaSuccess;
-  const int g = grid_for(p.total_tiles);
   switch (p.xmode) {
-    case kXSplit: prep_kernel<kXSplit><<<g, kThreads, 0, s>>>(p); break;
-    case kXBf16: prep_kernel<kXBf16><<<g, kThreads, 0, s>>>(p); break;
-    default: prep_kernel<kXF32><<<g, kThreads, 0, s>>>(p); break;
+    case kXSplit: prep_kernel<kXSplit><<<grid_for(prep_kernel<kXSplit>, p.total_tiles), kThreads, 0, s>>>(p); break;
+    case kXBf16: prep_kernel<kXBf16><<<grid_for(prep_kernel<kXBf16>, p.total_tiles), kThreads, 0, s>>>(p); break;
+    default: prep_kernel<kXF32><<<grid_for(prep_kernel<kXF32>, p.total_tiles), kThreads, 0, s>>>(p); break;
   }
   return cudaGetLastError();
 }
@@ -453,23 +542,31 @@ cudaError_t launch_norms(const double* partials, const int* tile_begin, const in
 
 cudaError_t launch_apply(const ApplyParams& p, cudaStream_t s) {
   if (p.total_tiles <= 0) return cudaSuccess;
-  const int g = grid_for(p.total_tiles);
   switch (p.xmode) {
-    case kXSplit: apply_kernel<kXSplit><<<g, kThreads, 0, s>>>(p); break;
-    case kXBf16: apply_kernel<kXBf16><<<g, kThreads, 0, s>>>(p); break;
-    default: apply_kernel<kXF32><<<g, kThreads, 0, s>>>(p); break;
+    case kXSplit: apply_kernel<kXSplit><<<grid_for(apply_kernel<kXSplit>, p.total_tiles), kThreads, 0, s>>>(p); break;
+    case kXBf16: apply_kernel<kXBf16><<<grid_for(apply_kernel<kXBf16>, p.total_tiles), kThreads, 0, s>>>(p); break;
+    default: apply_kernel<kXF32><<<grid_for(apply_kernel<kXF32>, p.total_tiles), kThreads, 0, s>>>(p); break;
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_clip(const ClipParams& p, cudaStream_t s) {
-  if (p.gamma_out || p.nclipped || p.status) clip_stats_kernel<<<1, 256, 0, s>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (p.nsegs <= 0 || p.H <= 0) return cudaSuccess;
-  long long max_rows = 1;
-  for (int i = 0; i < p.nsegs; ++i) max_rows = p.segs[i].rows > max_rows ? p.segs[i].rows : max_rows;
-  dim3 grid(p.nsegs * p.H, (unsigned)(max_rows < 64 ? max_rows : 64));
+  // one launch: block (0, 0) also writes the statistics
+  const bool stats = p.gamma_out || p.nclipped || p.status;
+  if (p.H <= 0 || (p.nsegs <= 0 && !stats)) return cudaSuccess;
+  // chunks per head: about kClipUnroll 16-byte vectors per thread for a
+  // contiguous head block, a row per chunk (up to 64) otherwise
+  long long chunks = 1;
+  for (int i = 0; i < p.nsegs; ++i) {
+    const ClipSegDev& sg = p.segs[i];
+    const int per_vec = sg.bf16 ? 8 : 4;
+    const long long want = sg.ld == sg.cols && (sg.rows * (long long)sg.cols) % per_vec == 0
+                               ? cdiv(sg.rows * (long long)sg.cols / per_vec, (long long)kThreads * kClipUnroll)
+                               : sg.rows;
+    chunks = want > chunks ? want : chunks;
+  }
+  const int pairs = p.nsegs > 0 ? p.nsegs * p.H : 1;
+  dim3 grid(pairs, (unsigned)(chunks < 64 ? chunks : 64));
   clip_rows_kernel<<<grid, kThreads, 0, s>>>(p);
   return cudaGetLastError();
 }

@@ -551,11 +551,13 @@ def test_zero1_single_rank_equals_direct_step():
 
 
 def test_step_with_many_shape_groups():
-    """Nine distinct shapes (more shape groups than one launch takes, split
+    """Eleven distinct shapes (more shape groups than one launch takes, split
     over two streams): tiny, one-row, ragged and tall matrices in one call,
-    each equal to its own oracle step."""
+    two with a column count that is not a multiple of 4 (the element-wise
+    edge of the streaming kernels, in both orientations), each equal to its
+    own oracle step."""
     shapes = [(8, 8), (1, 64), (24, 40), (129, 64), (64, 129 + 7), (200, 48), (48, 200), (513, 256),
-              (256, 513 + 7)]
+              (256, 513 + 7), (40, 130), (131, 37)]
     hp = mc.Hparams()
     W, G, M, want = [], [], [], []
     for i, (r, c) in enumerate(shapes):
