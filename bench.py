@@ -338,52 +338,77 @@ def gpu_arm(args):
                        "gbs": round(stress_bytes / (cms * 1e-3) / 1e9, 1)}
         del copies, ssegs
 
-    # ---- end to end through the public API: pinned host G (and Q, K) in, metrics out
+    # ---- end to end through the public API: pinned host G (and Q, K) in, metrics out.
+    # The inputs are double-buffered on the device: step i+1's host-to-device
+    # copies run on a copy stream while step i computes, and every copy, from
+    # the first step's to the last one's, lies inside the timed region (one
+    # region over the K steps: start event, then the first copy, ..., the last
+    # step's result read back).  Each step's inputs (G and Q/K) are larger than
+    # L2, so no flush runs in this region.
     Gh = [g.to("cpu").pin_memory() for g in Gl]
-    feats = [t for t in (q, ks) if t is not None]
-    if k is not None:
-        feats.append(k)
+    feats = [t for t in (q, k, ks) if t is not None]
     fh = [t.to("cpu").pin_memory() for t in feats]
     out_h = torch.empty(2 * H + 1, dtype=torch.float32).pin_memory()
     h2d = sum(g.numel() * g.element_size() for g in Gh) + sum(t.numel() * t.element_size() for t in fh)
     d2h = out_h.numel() * 4
     res = torch.empty(2 * H + 1, dtype=torch.float32, device=dev)
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
+    G_slots = [Gl, [torch.empty_like(g) for g in Gl]]
+    F_slots = [feats, [torch.empty_strided(t.size(), t.stride(), dtype=t.dtype, device=dev) for t in feats]]
+    copy_stream = torch.cuda.Stream(device=dev)
+    ready = [torch.cuda.Event(), torch.cuda.Event()]      # slot's inputs landed
+    consumed = [torch.cuda.Event(), torch.cuda.Event()]   # slot's inputs read by its step
+    used = [False, False]
 
-    # the gradients come in on a copy stream while the features come in on the
-    # step's stream and the max logit runs on them; the copy stream first waits
-    # for the stream (the previous step has read G), and the step waits for it
-    copy_streams = [torch.cuda.Stream(device=dev)]
-
-    def e2e_step():
-        for cs in copy_streams:
-            cs.wait_stream(stream)
-        for gd, gh in zip(Gl, Gh):
-            with torch.cuda.stream(copy_streams[0]):
+    def issue_copies(slot):
+        with torch.cuda.stream(copy_stream):
+            if used[slot]:
+                copy_stream.wait_event(consumed[slot])
+            for gd, gh in zip(G_slots[slot], Gh):
                 gd.copy_(gh, non_blocking=True)
-        for td, th in zip(feats, fh):
-            td.copy_(th, non_blocking=True)
+            for td, th in zip(F_slots[slot], fh):
+                td.copy_(th, non_blocking=True)
+            ready[slot].record(copy_stream)
+
+    # a step whose inputs fit in L2 flushes it inside the region (counted)
+    e2e_flush = h2d < 129 * 2 ** 20
+
+    def e2e_step(slot):
+        stream.wait_event(ready[slot])
+        if e2e_flush:
+            flush.zero_()
         if att is not None:
-            mc.qk_max_logit(q, k, ks, smax=smax, status=status, stream=stream)
-        for cs in copy_streams:
-            stream.wait_stream(cs)
-        mc.muonclip_step(Wl, Gl, Ml, hp, layers=layers, workspace=ws, status=status, stream=stream)
+            fq, fk = F_slots[slot][0], F_slots[slot][1]
+            fks = F_slots[slot][2] if ks is not None else None
+            mc.qk_max_logit(fq, fk, fks, smax=smax, status=status, stream=stream)
+        mc.muonclip_step(Wl, G_slots[slot], Ml, hp, layers=layers, workspace=ws, status=status,
+                         stream=stream)
+        consumed[slot].record(stream)
+        used[slot] = True
         res[:H].copy_(smax)
         res[H:2 * H].copy_(gamma)
         res[2 * H:].copy_(ncl.float())
         out_h.copy_(res, non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
+    def e2e_run(n):
+        copy_stream.wait_stream(stream)
+        issue_copies(0)
+        for i in range(n):
+            if i + 1 < n:
+                issue_copies((i + 1) % 2)
+            e2e_step(i % 2)
+
+    # warm-up: copies that overlap kernels run far below the link's rate for
+    # the first few hundred ms of such overlap in a process (measured 10-20 vs
+    # 208 GB/s), so the pipeline runs ~1.5 s of steps untimed first (a count
+    # from the max-over-ranks step time, the same on every rank)
+    e2e_run(max(args.warmup, int(math.ceil(1500.0 / max(ms_per_step, 1e-3)))))
     barrier()
-    for i in range(args.steps):
-        flush.zero_()
-        e2e_ev[i][0].record(stream)
-        e2e_step()
-        e2e_ev[i][1].record(stream)
+    e2e_t0, e2e_t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_t0.record(stream)
+    e2e_run(args.steps)
+    e2e_t1.record(stream)
     barrier()
-    e2e_local = sum(a.elapsed_time(b) for a, b in e2e_ev)
+    e2e_local = e2e_t0.elapsed_time(e2e_t1)
     if dist is not None:
         t = torch.tensor([e2e_local], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -433,7 +458,10 @@ def gpu_arm(args):
                              f"iterations, hi*hi for the first {hp.ns_fast_steps}, fp32 accumulate")
                             if wl.dtype == torch.bfloat16 else "fp32 CUDA cores"),
            "clipped_heads": len(att.scaled_heads) if att is not None else 0,
-           "l2": "flushed (512 MB write) before each step",
+           "l2": "flushed (512 MB write) before each step; e2e: " + (
+               "flushed inside the timed region before each step" if e2e_flush else
+               "not flushed, each step's host inputs (G, Q/K) are larger than L2"),
+           "e2e_pipeline": "inputs double-buffered: step i+1's host copies overlap step i",
            "parallelism": f"dp{world} (one layer per rank)"}
 
     if rank != 0:

@@ -55,10 +55,6 @@ constexpr int kBarBytes = 512;
 constexpr int kTS = 4;                 // tile-id ring (dynamic schedule)
 constexpr int kSmemCap = 227 * 1024;
 
-// K-major operand rows of 32 bf16 = 64 bytes: 64-byte swizzle (layout type 4),
-// 8-row atoms of 512 bytes.
-constexpr uint32_t kLayout = 4u;
-constexpr uint32_t kSbo = 8 * BKT * 2;
 // K-major operand layout for a k-step of BK: rows of BK bf16 with the 64-byte
 // (BK 32) or 128-byte (BK 64) swizzle, 8-row atoms.
 template <int BK>
@@ -280,10 +276,18 @@ __device__ void epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
 // 256 B rows, so each CTA loads one 128-row half of B and multicasts it to
 // both (half the B traffic from L2).  A stage is refilled only when both
 // CTAs' MMAs have released it (each MMA thread's commit arrives on both).
-template <int TERMS, bool LO, int CL, int BK>
+// PAIR (with CL 2): the two CTAs of a cluster form a tcgen05 .cta_group::2
+// pair.  Each CTA stages 128 rows of A and 128 rows (N values) of B, both
+// producers count their bytes on the first CTA's full barrier, the first CTA
+// issues M = 256 MMAs into both CTAs' TMEM and multicasts its commits, and the
+// epilogue warps of both CTAs release the first CTA's accumulator.  Per SM a
+// stage is two thirds of a multicast cluster's (B is not duplicated), so more
+// stages fit.
+template <int TERMS, bool LO, int CL, int BK, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     ns_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ TmaArgs tm) {
-  using C = Stages<TERMS, BM, BN, BK>;
+  static_assert(!PAIR || CL == 2, "pairs are clusters of 2");
+  using C = Stages<TERMS, BM, PAIR ? 128 : BN, BK>;
   using KL = KLayout<BK>;
   constexpr bool SPLIT = TERMS == 3;
   constexpr int TM_ROWS = BM * CL;
@@ -306,12 +310,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int s = 0; s < C::kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], CL); }
-    for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 4); }
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], PAIR ? 2 : 1);
+      mbar_init(&empty[s], PAIR ? 1 : CL);
+    }
+    for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], PAIR ? 8 : 4); }
     mbar_init(drain, 1);
     // readers of a ring slot: MMA + 4 epilogue warps of each CTA, and the
-    // second CTA's producer
-    for (int i = 0; i < kTS; ++i) { mbar_init(&sfull[i], 1); mbar_init(&sempty[i], CL > 1 ? 11 : 5); }
+    // second CTA's producer (pairs: only the first CTA's MMA warp)
+    for (int i = 0; i < kTS; ++i) {
+      mbar_init(&sfull[i], 1);
+      mbar_init(&sempty[i], CL > 1 ? (PAIR ? 10 : 11) : 5);
+    }
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -320,7 +330,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (SPLIT) { prefetch_tmap(&tm.maps.a_lo[g]); prefetch_tmap(&tm.maps.b_lo[g]); }
     }
   }
-  if (warp == 1) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
+  if (warp == 1) {
+    if (PAIR) { tmem_alloc_pair(tmem_slot, kTmemCols); tmem_relinquish_pair(); }
+    else { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
+  }
   tc_fence_before();
   if (CL > 1) { __syncwarp(); cluster_sync_all(); } else { __syncthreads(); }
   tc_fence_after();
@@ -391,8 +404,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* a_lo = st + C::kABytes;
           uint8_t* b_hi = st + (SPLIT ? 2 * C::kABytes : C::kABytes);
           uint8_t* b_lo = b_hi + C::kBBytes;
-          mbar_arrive_expect_tx(&full[s], C::kStageBytes);
           const int k0 = kb * BK;
+          if (PAIR) {
+            // this CTA's 128 rows of A and of B; bytes counted on the first CTA
+            const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
+            mbar_arrive_expect_tx_cluster(fb, C::kStageBytes);
+            const int nb = tc.n0 + 128 * (int)crank;
+            tma_load_3d_pair(a_hi, &tm.maps.a_hi[tc.g], fb, k0, m0, tc.b);
+            if (SPLIT) tma_load_3d_pair(a_lo, &tm.maps.a_lo[tc.g], fb, k0, m0, tc.b);
+            if (!G.b_mn_major) {
+              tma_load_3d_pair(b_hi, &tm.maps.b_hi[tc.g], fb, k0, nb, tc.b);
+              if (SPLIT) tma_load_3d_pair(b_lo, &tm.maps.b_lo[tc.g], fb, k0, nb, tc.b);
+            } else {
+#pragma unroll
+              for (int qq = 0; qq < 2; ++qq) {
+                tma_load_3d_pair(b_hi + qq * (64 * BK * 2), &tm.maps.b_hi[tc.g], fb, nb + 64 * qq, k0, tc.b);
+                if (SPLIT)
+                  tma_load_3d_pair(b_lo + qq * (64 * BK * 2), &tm.maps.b_lo[tc.g], fb, nb + 64 * qq, k0, tc.b);
+              }
+            }
+            used[s] = true;
+            last_par[s] = use & 1;
+            continue;
+          }
+          mbar_arrive_expect_tx(&full[s], C::kStageBytes);
           tma_load_3d(a_hi, &tm.maps.a_hi[tc.g], &full[s], k0, m0, tc.b);
           if (SPLIT) tma_load_3d(a_lo, &tm.maps.a_lo[tc.g], &full[s], k0, m0, tc.b);
           if (CL == 1) {
@@ -430,14 +465,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
       }
       // drain: every issued copy must have landed before the CTA may exit
-      for (int s = 0; s < C::kStages; ++s)
-        if (used[s]) mbar_wait(&full[s], last_par[s], nullptr);
+      // (pairs: the first CTA's barriers count both CTAs' copies, and the
+      // second CTA stays until the closing cluster barrier)
+      if (!PAIR || crank == 0)
+        for (int s = 0; s < C::kStages; ++s)
+          if (used[s]) mbar_wait(&full[s], last_par[s], nullptr);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_k = make_idesc_bf16(BM, BN, 0, 0);
-      constexpr uint32_t idesc_mn = make_idesc_bf16(BM, BN, 0, 1);
+    if (lane == 0 && (!PAIR || crank == 0)) {
+      constexpr uint32_t idesc_k = make_idesc_bf16(PAIR ? 2 * BM : BM, BN, 0, 0);
+      constexpr uint32_t idesc_mn = make_idesc_bf16(PAIR ? 2 * BM : BM, BN, 0, 1);
       uint32_t it = 0, tcount = 0;
       bool issued = false;
       for (uint32_t seq = 0; !abort_flag; ++seq, ++tcount) {
@@ -477,24 +515,37 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (SPLIT) dbl = make_sdesc(b_lo + kk * 2048, 64 * BK * 2, 1024, 2);
             }
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
-            tc_mma(d_tmem, dah, dbh, idesc, accum);
-            if (SPLIT) {
-              dal = make_sdesc(a_lo + kk * 32, 16, KL::kSbo, KL::kType);
-              tc_mma(d_tmem, dah, dbl, idesc, 1u);
-              tc_mma(d_tmem, dal, dbh, idesc, 1u);
+            if (SPLIT) dal = make_sdesc(a_lo + kk * 32, 16, KL::kSbo, KL::kType);
+            if (PAIR) {
+              tc_mma_pair(d_tmem, dah, dbh, idesc, accum);
+              if (SPLIT) {
+                tc_mma_pair(d_tmem, dah, dbl, idesc, 1u);
+                tc_mma_pair(d_tmem, dal, dbh, idesc, 1u);
+              }
+            } else {
+              tc_mma(d_tmem, dah, dbh, idesc, accum);
+              if (SPLIT) {
+                tc_mma(d_tmem, dah, dbl, idesc, 1u);
+                tc_mma(d_tmem, dal, dbh, idesc, 1u);
+              }
             }
           }
           issued = true;
           // stage free once these MMAs have read it (in both CTAs of a cluster:
-          // the peer multicasts into this stage too)
-          if (CL > 1) tc_commit_mc(&empty[s], (1u << CL) - 1);
+          // the peer multicasts into this stage too, or is the other half of
+          // the pair)
+          if (PAIR) tc_commit_pair_mc(&empty[s], 0x3);
+          else if (CL > 1) tc_commit_mc(&empty[s], (1u << CL) - 1);
           else tc_commit(&empty[s]);
         }
         if (!ok) break;
-        tc_commit(&tfull[acc]);          // accumulator ready for the epilogue
+        // accumulator ready for the epilogue (of both CTAs of a pair)
+        if (PAIR) tc_commit_pair_mc(&tfull[acc], 0x3);
+        else tc_commit(&tfull[acc]);
       }
       if (issued) {                      // all issued MMAs complete before teardown
-        tc_commit(drain);
+        if (PAIR) tc_commit_pair_mc(drain, 0x1);
+        else tc_commit(drain);
         mbar_wait(drain, 0, nullptr);
       }
     }
@@ -523,7 +574,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ek, bad);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (lane == 0) {
+        if (PAIR) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));   // the first CTA's MMA
+        else mbar_arrive(&tempty[acc]);
+      }
     }
     if (lane == 0) bulk_wait0();         // all TMA stores of this warp complete
     if (bad) set_status(p.status, MC_STATUS_NONFINITE_UPDATE);
@@ -533,199 +587,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (CL > 1) { __syncwarp(); cluster_sync_all(); } else { __syncthreads(); }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
-  }
-}
-
-// ---------------------------------------------------------------- CTA pairs
-// The same GEMM on CTA pairs (cluster of 2, tcgen05 .cta_group::2): one
-// 256 x 256 output tile per pair, each CTA holding 128 rows of A and 128 rows
-// (N values) of B, so each SM receives half the B operand of a 1-CTA 128 x 256
-// tile for the same MMA work.  The even CTA issues the MMAs; both CTAs' TMA
-// copies count on its full barrier; commits multicast to both CTAs.
-constexpr int PBM = 256, PBN = 256;
-
-template <int TERMS, bool LO>
-__global__ void __launch_bounds__(kThreads, 1)
-    ns_gemm_pair_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ TmaArgs tm) {
-  using C = Stages<TERMS, 128, 128>;
-  constexpr bool SPLIT = TERMS == 3;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* epi = smem + C::kStages * C::kStageBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(epi + kEpiBytes);
-  uint64_t* empty = full + 8;
-  uint64_t* tfull = empty + 8;             // [2]
-  uint64_t* tempty = tfull + 2;            // [2]
-  uint64_t* drain = tempty + 2;            // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  __shared__ volatile int abort_flag;
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const bool leader = rank == 0;
-  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-  if (threadIdx.x == 0) {
-    abort_flag = 0;
-    for (int s = 0; s < C::kStages; ++s) { mbar_init(&full[s], 2); mbar_init(&empty[s], 1); }
-    for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], 8); }
-    mbar_init(drain, 1);
-    fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    for (int g = 0; g < p.ngroups; ++g) {
-      prefetch_tmap(&tm.maps.a_hi[g]); prefetch_tmap(&tm.maps.b_hi[g]);
-      if (SPLIT) { prefetch_tmap(&tm.maps.a_lo[g]); prefetch_tmap(&tm.maps.b_lo[g]); }
-    }
-  }
-  if (warp == 1) { tmem_alloc_pair(tmem_slot, kTmemCols); tmem_relinquish_pair(); }
-  tc_fence_before();
-  __syncwarp();
-  cluster_sync_all();              // barriers and TMEM of both CTAs are ready
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-
-  auto fail = [&]() {
-    abort_flag = 1;
-    set_status(p.status, MC_STATUS_TIMEOUT);
-  };
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer (both CTAs)
-    if (lane == 0) {
-      uint32_t it = 0;
-      uint32_t last_par[8] = {};
-      bool used[8] = {};
-      for (int t = pair; t < p.total_tiles && !abort_flag; t += npairs) {
-        const TileCoord tc = tile_coord<PBM>(p, t);
-        const GemmGroup& G = p.g[tc.g];
-        const int nk = (G.K + BKT - 1) / BKT;
-        const int ma = tc.m0 + 128 * (int)rank, nb = tc.n0 + 128 * (int)rank;
-        bool ok = true;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int s = it % C::kStages;
-          const uint32_t use = it / C::kStages;
-          if (!mbar_wait(&empty[s], (use & 1) ^ 1, &abort_flag)) { fail(); ok = false; break; }
-          uint8_t* st = smem + s * C::kStageBytes;
-          uint8_t* a_hi = st;
-          uint8_t* a_lo = st + C::kABytes;
-          uint8_t* b_hi = st + (SPLIT ? 2 * C::kABytes : C::kABytes);
-          uint8_t* b_lo = b_hi + C::kBBytes;
-          const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);   // the even CTA's barrier
-          mbar_arrive_expect_tx_cluster(fb, C::kStageBytes);
-          const int k0 = kb * BKT;
-          tma_load_3d_pair(a_hi, &tm.maps.a_hi[tc.g], fb, k0, ma, tc.b);
-          if (SPLIT) tma_load_3d_pair(a_lo, &tm.maps.a_lo[tc.g], fb, k0, ma, tc.b);
-          if (!G.b_mn_major) {
-            tma_load_3d_pair(b_hi, &tm.maps.b_hi[tc.g], fb, k0, nb, tc.b);
-            if (SPLIT) tma_load_3d_pair(b_lo, &tm.maps.b_lo[tc.g], fb, k0, nb, tc.b);
-          } else {
-#pragma unroll
-            for (int qq = 0; qq < 2; ++qq) {
-              tma_load_3d_pair(b_hi + qq * (64 * BKT * 2), &tm.maps.b_hi[tc.g], fb, nb + 64 * qq, k0, tc.b);
-              if (SPLIT)
-                tma_load_3d_pair(b_lo + qq * (64 * BKT * 2), &tm.maps.b_lo[tc.g], fb, nb + 64 * qq, k0, tc.b);
-            }
-          }
-          used[s] = true;
-          last_par[s] = use & 1;
-        }
-        if (!ok) break;
-      }
-      // the even CTA's full barriers count both CTAs' copies: drain them there
-      if (leader)
-        for (int s = 0; s < C::kStages; ++s)
-          if (used[s]) mbar_wait(&full[s], last_par[s], nullptr);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (even CTA)
-    if (lane == 0 && leader) {
-      constexpr uint32_t idesc_k = make_idesc_bf16(PBM, PBN, 0, 0);
-      constexpr uint32_t idesc_mn = make_idesc_bf16(PBM, PBN, 0, 1);
-      uint32_t it = 0, tcount = 0;
-      bool issued = false;
-      for (int t = pair; t < p.total_tiles && !abort_flag; t += npairs, ++tcount) {
-        const TileCoord tc = tile_coord<PBM>(p, t);
-        const GemmGroup& G = p.g[tc.g];
-        const int nk = (G.K + BKT - 1) / BKT;
-        const int acc = tcount & 1;
-        const uint32_t ause = tcount >> 1;
-        if (!mbar_wait(&tempty[acc], (ause & 1) ^ 1, &abort_flag)) { fail(); break; }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * PBN;
-        const uint32_t idesc = G.b_mn_major ? idesc_mn : idesc_k;
-        bool ok = true;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int s = it % C::kStages;
-          const uint32_t use = it / C::kStages;
-          if (!mbar_wait(&full[s], use & 1, &abort_flag)) { fail(); ok = false; break; }
-          tc_fence_after();
-          const uint32_t st = smem_u32(smem + s * C::kStageBytes);
-          const uint32_t a_hi = st, a_lo = st + C::kABytes;
-          const uint32_t b_hi = st + (SPLIT ? 2 * C::kABytes : C::kABytes), b_lo = b_hi + C::kBBytes;
-#pragma unroll
-          for (int kk = 0; kk < BKT / 16; ++kk) {
-            const uint64_t dah = make_sdesc(a_hi + kk * 32, 16, kSbo, kLayout);
-            uint64_t dbh, dbl = 0, dal = 0;
-            if (!G.b_mn_major) {
-              dbh = make_sdesc(b_hi + kk * 32, 16, kSbo, kLayout);
-              if (SPLIT) dbl = make_sdesc(b_lo + kk * 32, 16, kSbo, kLayout);
-            } else {
-              dbh = make_sdesc(b_hi + kk * 2048, 64 * BKT * 2, 1024, 2);
-              if (SPLIT) dbl = make_sdesc(b_lo + kk * 2048, 64 * BKT * 2, 1024, 2);
-            }
-            const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
-            tc_mma_pair(d_tmem, dah, dbh, idesc, accum);
-            if (SPLIT) {
-              dal = make_sdesc(a_lo + kk * 32, 16, kSbo, kLayout);
-              tc_mma_pair(d_tmem, dah, dbl, idesc, 1u);
-              tc_mma_pair(d_tmem, dal, dbh, idesc, 1u);
-            }
-          }
-          issued = true;
-          tc_commit_pair_mc(&empty[s], 0x3);     // both CTAs' stage s is free
-        }
-        if (!ok) break;
-        tc_commit_pair_mc(&tfull[acc], 0x3);     // both CTAs' accumulators ready
-      }
-      if (issued) {
-        tc_commit_pair_mc(drain, 0x1);
-        mbar_wait(drain, 0, nullptr);
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ epilogue (both CTAs)
-    const int e = warp - 2;
-    const int q = warp & 3;
-    uint8_t* ebuf = epi + e * kEpiWarpBytes;
-    const uint32_t te_l[2] = {mapa_shared(smem_u32(&tempty[0]), 0), mapa_shared(smem_u32(&tempty[1]), 0)};
-    uint32_t ek = 0;
-    bool bad = false;
-    uint32_t tcount = 0;
-    for (int t = pair; t < p.total_tiles; t += npairs, ++tcount) {
-      const TileCoord tc = tile_coord<PBM>(p, t);
-      const int acc = tcount & 1;
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait(&tfull[acc], (tcount >> 1) & 1, &abort_flag) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) { if (lane == 0) fail(); break; }
-      tc_fence_after();
-      epilogue_rows<LO>(p, tm, tc, tc.m0 + 128 * (int)rank + q * 32, tmem_base + acc * PBN,
-                        q, lane, ebuf, ek, bad);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(te_l[acc]);   // the even CTA's MMA may reuse it
-    }
-    if (lane == 0) bulk_wait0();
-    if (bad) set_status(p.status, MC_STATUS_NONFINITE_UPDATE);
-  }
-
-  tc_fence_before();
-  __syncwarp();
-  cluster_sync_all();              // no MMA of the pair is still writing either TMEM
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc_pair(tmem_base, kTmemCols);
+    if (PAIR) tmem_dealloc_pair(tmem_base, kTmemCols);
+    else tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -794,13 +657,14 @@ bool encode_all(const GemmParams& p, TmaArgs& tm, bool split, bool lo, int a_row
   return true;
 }
 
-template <int TERMS, bool LO, int CL, int BK>
+template <int TERMS, bool LO, int CL, int BK, bool PAIR = false>
 cudaError_t launch_single(const GemmParams& p, cudaStream_t s, char* err, size_t errlen) {
   TmaArgs tm;
-  // with clusters each CTA's B box is one 128-row half (multicast to both)
+  // with clusters each CTA's B box is one 128-row half (multicast to both,
+  // or this CTA's half of a pair's B)
   if (!encode_all(p, tm, TERMS == 3, LO, BM, CL > 1 ? 128 : BN, BK, err, errlen)) return cudaErrorInvalidValue;
-  auto k = ns_gemm_tc_kernel<TERMS, LO, CL, BK>;
-  const int smem = Stages<TERMS, BM, BN, BK>::kSmem;
+  auto k = ns_gemm_tc_kernel<TERMS, LO, CL, BK, PAIR>;
+  const int smem = Stages<TERMS, BM, PAIR ? 128 : BN, BK>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (CL == 1) {
@@ -827,38 +691,6 @@ cudaError_t launch_single(const GemmParams& p, cudaStream_t s, char* err, size_t
   }
   const int units = p.total_tiles < max_clusters ? p.total_tiles : max_clusters;
   cfg.gridDim = dim3(CL * units);
-  e = cudaLaunchKernelEx(&cfg, k, p, tm);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
-}
-
-template <int TERMS, bool LO>
-cudaError_t launch_pair(const GemmParams& p, cudaStream_t s, char* err, size_t errlen) {
-  TmaArgs tm;
-  if (!encode_all(p, tm, TERMS == 3, LO, 128, 128, BKT, err, errlen)) return cudaErrorInvalidValue;
-  auto k = ns_gemm_pair_kernel<TERMS, LO>;
-  const int smem = Stages<TERMS, 128, 128>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  static int max_clusters = 0;
-  if (max_clusters == 0) {
-    cfg.gridDim = dim3(2 * (sm_count() / 2));
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, k, &cfg) != cudaSuccess || max_clusters <= 0)
-      max_clusters = sm_count() / 2;
-  }
-  const int pairs = p.total_tiles < max_clusters ? p.total_tiles : max_clusters;
-  cfg.gridDim = dim3(2 * pairs);
   e = cudaLaunchKernelEx(&cfg, k, p, tm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -894,10 +726,26 @@ int fast_bk() {
   return v;
 }
 
+// Launches that run on tcgen05 CTA pairs (MC_NS_PAIR): "none", "fast" (the
+// one-product launches) or "all".  MC_NS_CTA=2 puts every launch on pairs.
+int pair_policy() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("MC_NS_PAIR");
+    v = 0;
+    if (e && strcmp(e, "fast") == 0) v = 1;
+    if (e && strcmp(e, "all") == 0) v = 2;
+  }
+  return v;
+}
+
 int cta_mode_for(bool symmetric, int terms) {
   const int m = cta_mode();
-  if (m == 3 && symmetric && terms == 1) return 1;
-  return m;
+  if (m != 3) return m;
+  const int pp = pair_policy();
+  if (pp == 2 || (pp == 1 && terms == 1)) return 2;
+  if (symmetric && terms == 1) return 1;
+  return 3;
 }
 
 }  // namespace
@@ -916,12 +764,13 @@ cudaError_t launch_ns_gemm_tc(const GemmParams& p, cudaStream_t s, char* err, si
   const bool lo = p.xmode == kXSplit;
   const bool three = lo && p.terms == 3;
   const int mode = cta_mode_for(p.g[0].symmetric != 0, p.terms);
-  if (mode == 2) {
-    if (three) return launch_pair<3, true>(p, s, err, errlen);
-    return lo ? launch_pair<1, true>(p, s, err, errlen) : launch_pair<1, false>(p, s, err, errlen);
-  }
   // one-product launches may take k-steps of 64 (128-byte rows)
   const bool bk64 = !three && fast_bk() == 64;
+  if (mode == 2) {
+    if (three) return launch_single<3, true, 2, 32, true>(p, s, err, errlen);
+    if (bk64) return lo ? launch_single<1, true, 2, 64, true>(p, s, err, errlen) : launch_single<1, false, 2, 64, true>(p, s, err, errlen);
+    return lo ? launch_single<1, true, 2, 32, true>(p, s, err, errlen) : launch_single<1, false, 2, 32, true>(p, s, err, errlen);
+  }
   if (mode == 3) {
     if (three) return launch_single<3, true, 2, 32>(p, s, err, errlen);
     if (bk64) return lo ? launch_single<1, true, 2, 64>(p, s, err, errlen) : launch_single<1, false, 2, 64>(p, s, err, errlen);

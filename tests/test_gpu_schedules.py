@@ -1,9 +1,10 @@
 """The tensor-core Newton-Schulz result does not depend on how its tiles are
 scheduled: dynamic or round-robin tile order, one or two streams, single CTAs,
-B-multicast clusters or CTA pairs, 32- or 64-deep one-product k-steps give
-bit-identical outputs (every output tile is computed by the same sequence of
-MMAs whichever CTA or stream takes it).  The switches are read once per
-process, so each variant runs in a subprocess."""
+B-multicast clusters or CTA pairs (for every launch or the one-product ones),
+32- or 64-deep one-product k-steps give bit-identical outputs (every output
+tile is computed by the same sequence of MMAs whichever CTA or stream takes
+it).  The 1024 x 1152 matrix takes the one-product leading iterations.  The
+switches are read once per process, so each variant runs in a subprocess."""
 import os
 import subprocess
 import sys
@@ -19,7 +20,7 @@ CHILD = r'''
 import sys, numpy as np, torch
 sys.path.insert(0, sys.argv[1])
 from muon_qk_clip_gb300 import binding as mc, synth
-shapes = [(640, 384), (384, 640), (256, 256), (1000, 520), (520, 1000), (96, 136)]
+shapes = [(640, 384), (384, 640), (256, 256), (1000, 520), (520, 1000), (96, 136), (1024, 1152)]
 G = [synth.normal(s, 1e-3, f"sg{i}", 71).cuda() for i, s in enumerate(shapes)]
 O = [torch.empty(s, dtype=torch.bfloat16, device="cuda") for s in shapes]
 st = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -35,6 +36,9 @@ VARIANTS = {
     "one_stream": {"MC_NS_STREAMS": "1"},
     "single_cta": {"MC_NS_CTA": "1"},
     "cta_pairs": {"MC_NS_CTA": "2"},
+    "pairs_fast": {"MC_NS_PAIR": "fast"},
+    "pairs_all": {"MC_NS_PAIR": "all"},
+    "pairs_fast_bk32": {"MC_NS_PAIR": "fast", "MC_NS_BK_FAST": "32"},
     "bk32": {"MC_NS_BK_FAST": "32"},
 }
 
