@@ -174,6 +174,46 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# fp32 FMA peak of the part: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def ns_sym_entries(m, unit=256):
+    """Entries of an m x m symmetric Newton-Schulz output (the Gram A = X X^T
+    and the polynomial B) that the tensor-core kernel computes: every
+    256 x 256 unit on or above the diagonal, edge units over their real rows
+    and columns only."""
+    total = 0
+    for j in range(-(-m // unit)):
+        c = min(unit, m - j * unit)
+        total += c * min(unit * (j + 1), m)
+    return total
+
+
+def ns_flops_counted(rows, cols, steps, symmetric=True):
+    """Newton-Schulz flops credited to the kernel: per iteration 2 n E for the
+    Gram, 2 m E for the polynomial and 2 m^2 n for the update (m = min side,
+    n = max side), with E the computed entries of the symmetric outputs
+    (m^2 when the path does not exploit the symmetry).  Neither the skipped
+    lower triangles nor the extra products of the split arithmetic count."""
+    m, n = min(rows, cols), max(rows, cols)
+    e = ns_sym_entries(m) if symmetric else m * m
+    return steps * (2.0 * n * e + 2.0 * m * e + 2.0 * m * m * n)
+
+
+def ns_products(rows, cols, steps, fast_steps, split=True):
+    """Tensor-core products per k-step of each iteration under the default
+    plan: one (hi*hi) for the leading one-product iterations of matrices whose
+    smaller side is at least 1024 (two at most, three only from 2048 when
+    asked for), three (hi*hi + hi*lo + lo*hi) otherwise."""
+    if not split:
+        return [1] * steps
+    side = min(rows, cols)
+    f12 = min(fast_steps, 2, max(0, steps - 3))
+    nf = 3 if (side >= 2048 and f12 == 2 and fast_steps >= 3 and steps >= 5) else (f12 if side >= 1024 else 0)
+    return [1 if it < nf else 3 for it in range(steps)]
+
+
 def traffic_for(kernel_src, launches_per_call):
     """DRAM bytes per launch of the dominant kernel: the committed ncu total
     per Newton-Schulz call divided by this run's launches per call, or None
@@ -415,7 +455,13 @@ def gpu_arm(args):
         e2e_local = float(t.item())
 
     # ---- algorithmic work
-    ns_flops = sum(synth.flops_ns(m.rows, m.cols, hp.ns_steps) for m in wl.matrices)
+    tc_path = wl.dtype == torch.bfloat16
+    ns_flops_nominal = sum(synth.flops_ns(m.rows, m.cols, hp.ns_steps) for m in wl.matrices)
+    ns_flops = sum(ns_flops_counted(m.rows, m.cols, hp.ns_steps, symmetric=tc_path) for m in wl.matrices)
+    # what the tensor pipe executes: the counted flops times the products per k-step
+    ns_flops_products = sum(ns_flops_counted(m.rows, m.cols, 1, symmetric=tc_path) *
+                            sum(ns_products(m.rows, m.cols, hp.ns_steps, hp.ns_fast_steps, tc_path))
+                            for m in wl.matrices)
     ml_flops = 0.0
     clip_bytes = 0
     if att is not None:
@@ -454,9 +500,12 @@ def gpu_arm(args):
     cfg = {"workload": args.workload, **WORKLOAD_CONFIG[args.workload], "ns_steps": hp.ns_steps,
            "ns_precision": ((f"split-bf16 (hi*hi+hi*lo+lo*hi), fp32 accumulate, all {hp.ns_steps} iterations"
                              if hp.ns_fast_steps == 0 else
-                             f"split-bf16 (hi*hi+hi*lo+lo*hi) for the last {hp.ns_steps - hp.ns_fast_steps} "
-                             f"iterations, hi*hi for the first {hp.ns_fast_steps}, fp32 accumulate")
+                             f"split-bf16 (hi*hi+hi*lo+lo*hi), fp32 accumulate; hi*hi for the first "
+                             f"{hp.ns_fast_steps} iterations of matrices whose smaller side is >= 1024")
                             if wl.dtype == torch.bfloat16 else "fp32 CUDA cores"),
+           "ns_flops_counted": ("Gram and polynomial: the computed 256x256 units on or above the "
+                                "diagonal (symmetry exploited); update 2 m^2 n; split products not "
+                                "credited" if tc_path else "4 m^2 n + 2 m^3 per iteration"),
            "clipped_heads": len(att.scaled_heads) if att is not None else 0,
            "l2": "flushed (512 MB write) before each step; e2e: " + (
                "flushed inside the timed region before each step" if e2e_flush else
@@ -479,11 +528,14 @@ def gpu_arm(args):
         "e2e": {"value": round(e2e_local / args.steps / world, 4), "unit": "ms",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
-        "roofline": {"bound": "tensor", "kernel": "ns_gemm (tcgen05 split-bf16 Newton-Schulz phase)",
+        "roofline": {"bound": "tensor" if tc_path else "alu",
+                     "kernel": ("ns_gemm (tcgen05 split-bf16 Newton-Schulz phase)" if tc_path else
+                                "ns_gemm (fp32 CUDA-core Newton-Schulz phase)"),
                      "achieved": round(achieved, 2) if achieved else None,
-                     "peak": peak_t, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak_t, 4) if achieved else None,
-                     "peak_source": f"bf16_tflops {pk_src}",
+                     "peak": peak_t if tc_path else FP32_ALU_TFLOPS, "unit": "TFLOP/s",
+                     "frac": round(achieved / (peak_t if tc_path else FP32_ALU_TFLOPS), 4) if achieved else None,
+                     "peak_source": (f"bf16_tflops {pk_src}" if tc_path else
+                                     "152 SMs x 128 fp32 lanes x 2 flops (FMA) x 2.07 GHz"),
                      "traffic": traffic_for(os.path.join(ROOT, "muon_qk_clip_gb300", "csrc", "ns_tc.cu"),
                                             n_gemm // args.steps if n_gemm else 0)
                      if args.workload == WORKLOAD else None},
@@ -492,6 +544,12 @@ def gpu_arm(args):
             if attn_fwd and attn_fwd.get("tflops") else attn_fwd,
             "ns_algorithmic_tflops": round(ns_tflops, 2) if ns_tflops else None,
             "ns_frac_bf16_peak": round(ns_tflops / peak_t, 4) if ns_tflops else None,
+            "ns_nominal_tflops": round(ns_flops_nominal * args.steps / (t_gemm * 1e-3) / 1e12, 2)
+            if t_gemm else None,
+            "ns_tensor_pipe_tflops": round(ns_flops_products * args.steps / (t_gemm * 1e-3) / 1e12, 2)
+            if t_gemm and tc_path else None,
+            "ns_tensor_pipe_frac": round(ns_flops_products * args.steps / (t_gemm * 1e-3) / 1e12 / peak_t, 4)
+            if t_gemm and tc_path else None,
             "max_logit_tflops": round(ml_tflops, 2) if ml_tflops else None,
             "max_logit_frac_bf16_peak": round(ml_tflops / peak_t, 4) if ml_tflops else None,
             "clip_gbs": round(clip_gbs, 1) if clip_gbs else None,

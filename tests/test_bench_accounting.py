@@ -1,0 +1,56 @@
+"""The Newton-Schulz flop accounting bench.py reports its roofline with.
+
+The tensor-core kernel computes only the 256 x 256 units of the symmetric
+outputs (A = X X^T and the polynomial B) on or above the diagonal, so those
+phases are credited with the entries of those units, never with the full
+m x m output; the split products are not credited either."""
+import importlib.util
+import os
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+@pytest.mark.parametrize("m", [1, 100, 255, 256, 257, 300, 512, 1000, 2048, 2049])
+def test_sym_entries_brute_force(bench, m):
+    """Mark every entry (r, c) whose 256-unit block (r // 256, c // 256) lies on
+    or above the diagonal and count them."""
+    r = np.arange(m) // 256
+    mask = r[:, None] <= r[None, :]
+    assert bench.ns_sym_entries(m) == int(mask.sum())
+
+
+def test_sym_entries_closed_form(bench):
+    # m = 256 T: T (T + 1) / 2 full units
+    for t in (1, 2, 8, 28):
+        assert bench.ns_sym_entries(256 * t) == 256 * 256 * t * (t + 1) // 2
+
+
+def test_counted_flops(bench):
+    m, n, steps = 512, 1536, 5
+    e = 256 * 256 * 3                      # units (0,0), (0,1), (1,1)
+    want = steps * (2 * n * e + 2 * m * e + 2 * m * m * n)
+    assert bench.ns_flops_counted(m, n, steps) == want
+    assert bench.ns_flops_counted(n, m, steps) == want        # orientation
+    # without symmetry it is the nominal 4 m^2 n + 2 m^3
+    assert bench.ns_flops_counted(m, n, steps, symmetric=False) == steps * (4 * m * m * n + 2 * m ** 3)
+
+
+def test_products_per_iteration(bench):
+    assert bench.ns_products(512, 7168, 5, 2) == [3] * 5              # smaller side < 1024
+    assert bench.ns_products(1024, 1536, 5, 2) == [1, 1, 3, 3, 3]
+    assert bench.ns_products(1024, 1536, 5, 3) == [1, 1, 3, 3, 3]     # third only from 2048
+    assert bench.ns_products(2048, 5632, 5, 3) == [1, 1, 1, 3, 3]
+    assert bench.ns_products(2048, 5632, 4, 3) == [1, 3, 3, 3]        # three split ones kept
+    assert bench.ns_products(2048, 2048, 5, 0) == [3] * 5
+    assert bench.ns_products(2048, 2048, 5, 2, split=False) == [1] * 5
