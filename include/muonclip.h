@@ -301,6 +301,18 @@ typedef struct {
 void mc_profiler_enable(int32_t on);
 int32_t mc_profiler_read(mc_kernel_time* out, int32_t max, int32_t reset);
 
+/* Diagnostic: exercises the bounded device wait that every tcgen05 kernel of
+ * the library uses for its mbarrier phases.  One CTA waits on a phase that
+ * nothing completes, for at most budget_ns nanoseconds of %globaltimer
+ * (1 .. 1e9), or until a second warp of the CTA raises its abort flag after
+ * abort_after_ns (0: never; 0 .. 1e9).  Giving up ORs MC_STATUS_TIMEOUT into
+ * *status (device int32, required); *waited_ns (device uint64, nullable)
+ * receives how long the wait took.  Nothing else is touched and the context
+ * stays usable.  MC_ERR_INVALID_ARG (before any launch) for a budget outside
+ * its range or a null status.  Asynchronous on `stream`. */
+mc_status mc_selftest_bounded_wait(uint64_t budget_ns, uint64_t abort_after_ns, int32_t* status,
+                                   uint64_t* waited_ns, mc_stream_t stream);
+
 /* Thread-local description of the last non-OK return ("" if none). */
 const char* mc_last_error(void);
 

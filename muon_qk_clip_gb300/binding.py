@@ -249,6 +249,19 @@ def profiler_enable(on: bool = True):
     abi.load().mc_profiler_enable(1 if on else 0)
 
 
+def selftest_bounded_wait(budget_ns: int, abort_after_ns: int = 0, status=None, stream=None):
+    """Run the bounded-wait self-check; returns (status int32[1], waited_ns
+    int64[1]) device tensors, filled once the stream reaches the launch."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    waited = torch.zeros(1, dtype=torch.int64, device=dev)
+    check(abi.load().mc_selftest_bounded_wait(int(budget_ns), int(abort_after_ns), _ptr(status),
+                                              _ptr(waited), _stream(stream)),
+          "mc_selftest_bounded_wait")
+    return status, waited
+
+
 def profiler_read(reset: bool = True) -> dict:
     """{class: (launches, milliseconds)} accumulated since the last reset."""
     buf = (abi.McKernelTime * 16)()

@@ -689,6 +689,22 @@ int32_t mc_profiler_read(mc_kernel_time* out, int32_t max, int32_t reset) {
 
 const char* mc_version(void) { return "muonclip-gb300 0.1 (sm_103a)"; }
 
+mc_status mc_selftest_bounded_wait(uint64_t budget_ns, uint64_t abort_after_ns, int32_t* status,
+                                   uint64_t* waited_ns, mc_stream_t stream) {
+  if (budget_ns < 1 || budget_ns > 1000000000ull)
+    return fail(MC_ERR_INVALID_ARG, "mc_selftest_bounded_wait: budget_ns %llu outside [1, 1e9]",
+                (unsigned long long)budget_ns);
+  if (abort_after_ns > 1000000000ull)
+    return fail(MC_ERR_INVALID_ARG, "mc_selftest_bounded_wait: abort_after_ns %llu above 1e9",
+                (unsigned long long)abort_after_ns);
+  if (!status) return fail(MC_ERR_INVALID_ARG, "mc_selftest_bounded_wait: null status");
+  cudaError_t e = launch_wait_selftest(budget_ns, abort_after_ns, status,
+                                       reinterpret_cast<unsigned long long*>(waited_ns),
+                                       (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "bounded-wait self-test launch");
+  return MC_OK;
+}
+
 mc_status mc_workspace_size(const mc_mat* M, int32_t count, const mc_hparams* hp, size_t* bytes) {
   if (!bytes) return fail(MC_ERR_INVALID_ARG, "bytes: null");
   if (!M || count < 1) return fail(MC_ERR_INVALID_ARG, "need count >= 1 matrices");

@@ -73,17 +73,23 @@ __device__ inline bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait: returns false (and the caller must abort) when the phase did
-// not complete within kWaitBudgetNs, or when *abort was raised by a peer warp.
-__device__ inline bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+// not complete within budget_ns of %globaltimer, or when *abort was raised by
+// a peer warp.
+__device__ inline bool mbar_wait_budget(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                        unsigned long long budget_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   unsigned long long t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (abort_flag && *abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitBudgetNs) return false;
+      if (globaltimer_ns() - t0 > budget_ns) return false;
     }
   }
+}
+// The kernels' wait: kWaitBudgetNs.
+__device__ inline bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  return mbar_wait_budget(bar, parity, abort_flag, kWaitBudgetNs);
 }
 
 // ----------------------------------------------------------------------------

@@ -204,6 +204,10 @@ struct AttnFwdParams {
 cudaError_t launch_attn_fwd(const AttnFwdParams& p, cudaStream_t s, char* err, size_t errlen);
 bool attn_fwd_supported(const AttnFwdParams& p, char* err, size_t errlen);
 
+// Bounded-wait self-check (one CTA waits on a phase nothing completes).
+cudaError_t launch_wait_selftest(unsigned long long budget_ns, unsigned long long abort_after_ns,
+                                 int32_t* status, unsigned long long* waited_ns, cudaStream_t s);
+
 // Device/properties helpers.
 int sm_count();
 

@@ -258,3 +258,15 @@ def test_binding_raises_with_message(lib):
     with pytest.raises(abi.MuonClipError) as ei:
         abi.check(lib.muon_momentum(arr(m(4, 8, ptr=0)), arr(m(4, 8)), 1, 0.9, None, None), "muon_momentum")
     assert "null pointer" in str(ei.value)
+
+
+@pytest.mark.parametrize("budget,abort_after,status,needle", [
+    (0, 0, FAKE, "budget_ns"),
+    (2_000_000_000, 0, FAKE, "budget_ns"),
+    (1_000_000, 2_000_000_000, FAKE, "abort_after_ns"),
+    (1_000_000, 0, None, "null status"),
+])
+def test_bounded_wait_selftest_rejects(lib, budget, abort_after, status, needle):
+    st = None if status is None else ctypes.c_void_p(status)
+    assert lib.mc_selftest_bounded_wait(budget, abort_after, st, None, None) == abi.MC_ERR_INVALID_ARG
+    assert needle in lib.mc_last_error().decode()
