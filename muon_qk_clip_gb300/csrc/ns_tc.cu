@@ -218,10 +218,22 @@ __device__ void epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
       for (int e = 0; e < 32; ++e)
         if (col0 + e == row) v[e] += dg;
     }
+    // non-finite test: v * 0 is 0 for a finite v and NaN for Inf or NaN, so
+    // four chains of fma(v, 0, acc) end in NaN iff some value is not finite
+    // (the ragged edge tests its valid elements one by one)
+    if (row_ok && col0 + 31 < G.N) {
+      float z4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int e = 0; e < 32; ++e) z4[e & 3] = fmaf(v[e], 0.f, z4[e & 3]);
+      const float z = (z4[0] + z4[1]) + (z4[2] + z4[3]);
+      bad |= z != z;
+    } else if (row_ok) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) bad |= !finite_f(v[e]) && (col0 + e < G.N);
+    }
     __nv_bfloat16 hb[32], lb[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
-      bad |= !finite_f(v[e]) && (col0 + e < G.N) && row_ok;
       if (LO) split_bf16(v[e], hb[e], lb[e]);
       else hb[e] = __float2bfloat16_rn(v[e]);
     }
