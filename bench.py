@@ -378,6 +378,30 @@ def gpu_arm(args):
                        "gbs": round(stress_bytes / (cms * 1e-3) / 1e9, 1)}
         del copies, ssegs
 
+    # ---- the clip at a size where HBM bandwidth, not launch latency, decides:
+    # 64 heads of 8192 x 1024 bf16 rows (1 GiB), every head over tau
+    def clip_stress_large():
+        Hs, rows, cols = 64, 8192, 1024
+        Wbig = torch.ones(Hs * rows, cols, dtype=torch.bfloat16, device=dev)
+        segs_l = [mc.ClipSegment(Wbig, 0, rows, rows, 0.5)]
+        s_l = torch.full((Hs,), 4.0 * hp.tau, dtype=torch.float32, device=dev)
+        mc.qk_clip_apply(s_l, hp.tau, segs_l, stream=stream)
+        barrier()
+        ev_l = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(5)]
+        for a, b in ev_l:
+            torch.cuda._sleep(100_000)
+            a.record(stream)
+            mc.qk_clip_apply(s_l, hp.tau, segs_l, stream=stream)
+            b.record(stream)
+        barrier()
+        ms_l = sum(a.elapsed_time(b) for a, b in ev_l) / len(ev_l)
+        nbytes = 2 * Wbig.numel() * Wbig.element_size()          # read + write
+        del Wbig
+        return {"heads_clipped": Hs, "bytes": nbytes, "ms": round(ms_l, 4),
+                "gbs": round(nbytes / (ms_l * 1e-3) / 1e9, 1)}
+    clip_large = clip_stress_large()
+
     # ---- end to end through the public API: pinned host G (and Q, K) in, metrics out.
     # The inputs are double-buffered on the device: step i+1's host-to-device
     # copies run on a copy stream while step i computes, and every copy, from
@@ -553,6 +577,7 @@ def gpu_arm(args):
             "max_logit_tflops": round(ml_tflops, 2) if ml_tflops else None,
             "max_logit_frac_bf16_peak": round(ml_tflops / peak_t, 4) if ml_tflops else None,
             "clip_gbs": round(clip_gbs, 1) if clip_gbs else None,
+            "clip_stress_1gib": dict(clip_large, frac_hbm=round(clip_large["gbs"] / hbm, 4)),
             "clip_stress_all_heads": dict(clip_stress, frac_hbm=round(clip_stress["gbs"] / hbm, 4))
             if clip_stress else None,
             "prep_gbs": round(prep_gbs, 1) if prep_gbs else None,
