@@ -71,6 +71,25 @@ __device__ inline void store_x4(void* xh, void* xl, long long idx, const float (
   }
 }
 
+// Eight consecutive bf16 (16-byte aligned); elements past n (< 8 only at a
+// matrix's edge) read as zero / are not written.
+__device__ inline uint4 load8_bf16(const __nv_bfloat16* src, int n) {
+  if (n >= 8) return *reinterpret_cast<const uint4*>(src);
+  uint4 u = make_uint4(0u, 0u, 0u, 0u);
+  __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(&u);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (i < n) e[i] = src[i];
+  return u;
+}
+__device__ inline void store8_bf16(__nv_bfloat16* dst, const uint4& v, int n) {
+  if (n >= 8) { *reinterpret_cast<uint4*>(dst) = v; return; }
+  const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (i < n) dst[i] = e[i];
+}
+
 // Raw bits of up to four consecutive elements, unconverted, so that a tile's
 // loads can all be in flight before the first one is used: 16-bit elements
 // packed two per word in .x/.y, fp32 elements one per word; elements past
@@ -271,8 +290,9 @@ __global__ void norms_kernel(const __grid_constant__ NormParams p) {
   }
 }
 
-// Same tile layout as prep_kernel; every load of a row pass is issued before
-// the first store of W.
+// Same tile layout as prep_kernel (the step's split-bf16 / bf16-W case takes
+// 16-byte accesses instead); every load of a tile is issued before the first
+// store of W.
 template <int XM>
 __global__ void __launch_bounds__(kThreads) apply_kernel(const __grid_constant__ ApplyParams p) {
   __shared__ float tile[kTile][kTile + 1];
@@ -282,6 +302,75 @@ __global__ void __launch_bounds__(kThreads) apply_kernel(const __grid_constant__
     const int lt = t - jb.tile_begin;
     const int r0 = (lt / jb.tiles_c) * kTile, c0 = (lt % jb.tiles_c) * kTile;
     const float s = jb.scale * (p.mat_scale ? p.mat_scale[jb.mat] : 1.f);
+    if (XM == kXSplit && !p.write_o && jb.out_bf16) {
+      // the step's own case (split iterate, bf16 W): 16-byte accesses, 8
+      // threads x 8 columns per row, 32 rows per pass, two passes
+      const int tx8 = threadIdx.x & 7, ty8 = threadIdx.x >> 3;
+      const int cb = c0 + tx8 * 8, nc8 = jb.cols - cb;
+      uint4 wv[2], xh[2], xl[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int r = r0 + ty8 + 32 * k;
+        wv[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < jb.rows) wv[k] = load8_bf16(reinterpret_cast<const __nv_bfloat16*>(jb.out) + (long long)r * jb.ldo + cb, nc8);
+      }
+      if (jb.transpose) {
+        // X^T: oriented row c (a column of W) holds W rows rb .. rb + 7
+        const int rb = r0 + tx8 * 8, nr8 = jb.rows - rb;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int c = c0 + ty8 + 32 * k;
+          xh[k] = xl[k] = make_uint4(0u, 0u, 0u, 0u);
+          if (c >= jb.cols) continue;
+          const long long ix = (long long)c * jb.ldx + rb;
+          xh[k] = load8_bf16(reinterpret_cast<const __nv_bfloat16*>(jb.xh) + ix, nr8);
+          xl[k] = load8_bf16(reinterpret_cast<const __nv_bfloat16*>(jb.xl) + ix, nr8);
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const __nv_bfloat16* a = reinterpret_cast<const __nv_bfloat16*>(&xh[k]);
+          const __nv_bfloat16* b2 = reinterpret_cast<const __nv_bfloat16*>(&xl[k]);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            tile[tx8 * 8 + e][ty8 + 32 * k] = __bfloat162float(a[e]) + __bfloat162float(b2[e]);
+        }
+        __syncthreads();
+      } else {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int r = r0 + ty8 + 32 * k;
+          xh[k] = xl[k] = make_uint4(0u, 0u, 0u, 0u);
+          if (r >= jb.rows) continue;
+          const long long ix = (long long)r * jb.ldx + cb;
+          xh[k] = load8_bf16(reinterpret_cast<const __nv_bfloat16*>(jb.xh) + ix, nc8);
+          xl[k] = load8_bf16(reinterpret_cast<const __nv_bfloat16*>(jb.xl) + ix, nc8);
+        }
+      }
+      bool bad8 = false;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int rl = ty8 + 32 * k, r = r0 + rl;
+        if (r >= jb.rows) continue;
+        const __nv_bfloat16* a = reinterpret_cast<const __nv_bfloat16*>(&xh[k]);
+        const __nv_bfloat16* b2 = reinterpret_cast<const __nv_bfloat16*>(&xl[k]);
+        const __nv_bfloat16* w8 = reinterpret_cast<const __nv_bfloat16*>(&wv[k]);
+        uint4 outv;
+        __nv_bfloat16* o8 = reinterpret_cast<__nv_bfloat16*>(&outv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float x = jb.transpose ? tile[rl][tx8 * 8 + e]
+                                       : __bfloat162float(a[e]) + __bfloat162float(b2[e]);
+          const float w = __bfloat162float(w8[e]);
+          const float v = fmaf(-p.lr, fmaf(p.wd, w, s * x), w);   // w - lr (s x + wd w)
+          bad8 |= !finite_f(v) && (e < nc8);
+          o8[e] = __float2bfloat16_rn(v);
+        }
+        store8_bf16(reinterpret_cast<__nv_bfloat16*>(jb.out) + (long long)r * jb.ldo + cb, outv, nc8);
+      }
+      if (bad8) set_status(p.status, MC_STATUS_NONFINITE_UPDATE);
+      if (jb.transpose) __syncthreads();
+      continue;
+    }
     const int cl0 = tx * 4, cbase = c0 + cl0;
     if (jb.transpose) {
       // stage X^T tile: oriented rows c0.., oriented cols r0..
