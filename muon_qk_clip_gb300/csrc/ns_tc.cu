@@ -290,8 +290,8 @@ __device__ void epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
 // CTAs' MMAs have released it (each MMA thread's commit arrives on both).
 // PAIR (with CL 2): the two CTAs of a cluster form a tcgen05 .cta_group::2
 // pair.  Each CTA stages 128 rows of A and 128 rows (N values) of B, both
-// producers count their bytes on the first CTA's full barrier, the first CTA
-// issues M = 256 MMAs into both CTAs' TMEM and multicasts its commits, and the
+// CTAs' copies complete on the first CTA's full barrier (whose producer alone
+// arrives, expecting both CTAs' bytes), the first CTA issues M = 256 MMAs into both CTAs' TMEM and multicasts its commits, and the
 // epilogue warps of both CTAs release the first CTA's accumulator.  Per SM a
 // stage is two thirds of a multicast cluster's (B is not duplicated), so more
 // stages fit.
@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&full[s], PAIR ? 2 : 1);
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], PAIR ? 1 : CL);
     }
     for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], PAIR ? 8 : 4); }
@@ -418,9 +418,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* b_lo = b_hi + C::kBBytes;
           const int k0 = kb * BK;
           if (PAIR) {
-            // this CTA's 128 rows of A and of B; bytes counted on the first CTA
+            // this CTA's 128 rows of A and of B, counted on the first CTA's
+            // barrier; only the first CTA arrives (with both CTAs' bytes), so
+            // the second CTA's copies need no cross-CTA arrive per stage (its
+            // copies cannot complete the phase before that arrive)
             const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
-            mbar_arrive_expect_tx_cluster(fb, C::kStageBytes);
+            if (crank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::kStageBytes);
             const int nb = tc.n0 + 128 * (int)crank;
             tma_load_3d_pair(a_hi, &tm.maps.a_hi[tc.g], fb, k0, m0, tc.b);
             if (SPLIT) tma_load_3d_pair(a_lo, &tm.maps.a_lo[tc.g], fb, k0, m0, tc.b);
@@ -709,8 +712,8 @@ cudaError_t launch_single(const GemmParams& p, cudaStream_t s, char* err, size_t
 }
 
 // Work-unit layout of the tensor-core GEMM: MC_NS_CTA=1 single CTAs,
-// 2 = CTA pairs (cta_group::2), 3 = clusters of two CTAs sharing B by
-// multicast (default).
+// 2 = CTA pairs (cta_group::2), 3 = per-launch choice (default: see
+// cta_mode_for).
 int cta_mode() {
   static int v = -1;
   if (v < 0) {
@@ -720,9 +723,10 @@ int cta_mode() {
   }
   return v;
 }
-// Cluster choice per launch (MC_NS_CTA=3, the default): the one-product
-// symmetric phases run on single CTAs (128-row tiles balance better and their
-// operands are small), everything else on B-multicast clusters of two.
+// Per-launch choice (MC_NS_CTA=3, the default): every launch on tcgen05 CTA
+// pairs (MC_NS_PAIR=all, the default; measured fastest on every workload), or
+// with MC_NS_PAIR=none the one-product symmetric phases on single CTAs and
+// everything else on B-multicast clusters of two.
 // k-step of the one-product launches: 64 (128-byte operand rows, 4 stages of
 // 48 KB) by default; MC_NS_BK_FAST=32 takes 64-byte rows and 8 stages.  With
 // one product per k-step, 64-byte rows leave the copy engine issuing more
@@ -739,14 +743,15 @@ int fast_bk() {
 }
 
 // Launches that run on tcgen05 CTA pairs (MC_NS_PAIR): "none", "fast" (the
-// one-product launches) or "all".  MC_NS_CTA=2 puts every launch on pairs.
+// one-product launches) or "all" (default).  MC_NS_CTA=2 puts every launch on
+// pairs whatever MC_NS_PAIR says.
 int pair_policy() {
   static int v = -1;
   if (v < 0) {
     const char* e = getenv("MC_NS_PAIR");
-    v = 0;
+    v = 2;
+    if (e && strcmp(e, "none") == 0) v = 0;
     if (e && strcmp(e, "fast") == 0) v = 1;
-    if (e && strcmp(e, "all") == 0) v = 2;
   }
   return v;
 }

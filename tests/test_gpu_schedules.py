@@ -1,6 +1,7 @@
 """The tensor-core Newton-Schulz result does not depend on how its tiles are
 scheduled: dynamic or round-robin tile order, one or two streams, single CTAs,
-B-multicast clusters or CTA pairs (for every launch or the one-product ones),
+B-multicast clusters or CTA pairs (for every launch, the default, or the
+one-product ones),
 32- or 64-deep one-product k-steps give bit-identical outputs (every output
 tile is computed by the same sequence of MMAs whichever CTA or stream takes
 it).  The 1024 x 1152 matrix takes the one-product leading iterations.  The
@@ -36,9 +37,11 @@ VARIANTS = {
     "one_stream": {"MC_NS_STREAMS": "1"},
     "single_cta": {"MC_NS_CTA": "1"},
     "cta_pairs": {"MC_NS_CTA": "2"},
+    "clusters": {"MC_NS_PAIR": "none"},
     "pairs_fast": {"MC_NS_PAIR": "fast"},
     "pairs_all": {"MC_NS_PAIR": "all"},
     "pairs_fast_bk32": {"MC_NS_PAIR": "fast", "MC_NS_BK_FAST": "32"},
+    "clusters_bk32": {"MC_NS_PAIR": "none", "MC_NS_BK_FAST": "32"},
     "bk32": {"MC_NS_BK_FAST": "32"},
 }
 
