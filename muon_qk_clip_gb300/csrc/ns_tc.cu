@@ -47,10 +47,11 @@ namespace mc {
 namespace {
 
 constexpr int BM = 128, BN = 256, BKT = 32;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;           // two per TMEM lane quadrant (column halves)
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 512;    // two 128 x 256 fp32 accumulators
 constexpr int kEpiWarpBytes = 8192;    // per epilogue warp: two 32 x 32 hi+lo slots
-constexpr int kEpiBytes = 4 * kEpiWarpBytes;
+constexpr int kEpiBytes = kEpiWarps * kEpiWarpBytes;
 constexpr int kBarBytes = 512;
 constexpr int kTS = 4;                 // tile-id ring (dynamic schedule)
 constexpr int kSmemCap = 227 * 1024;
@@ -125,22 +126,42 @@ __device__ inline uint32_t swz64(int row, int b) {
 }
 
 // ------------------------------------------------------------ epilogue
-// One warp's 32 rows [r0, r0 + 32) of an output tile whose accumulator sits in
-// TMEM at `tacc` (lane quadrant q).  D = s_b * (alpha * acc + beta * C + diag I).
-// Symmetric outputs: 32-column chunks in blocks I < J are also stored
-// transposed (mirror); I > J are dropped.
+// One warp's 32 rows [r0, r0 + 32) and 32-column chunks [c_begin, c_end) of an
+// output tile whose accumulator sits in TMEM at `tacc` (lane quadrant q).
+// D = s_b * (alpha * acc + beta * C + diag I).  Symmetric outputs: chunks in
+// 128-column blocks I < J are also stored transposed (mirror); I > J are
+// dropped.
 //
 // The warp's 8 KB of shared memory is two 4 KB slots (a 32 x 32 chunk of hi
 // and lo planes each): D and its mirror for symmetric outputs, else a ring of
 // two D chunks, so a chunk waits only for the store group that last used its
 // slot.  `ek` counts this warp's store groups across tiles.  C is read by each
-// lane straight from global memory (its row's 64 contiguous bytes per plane),
-// one chunk ahead, and the next chunk's TMEM load is in flight while the
-// current one is converted.
+// lane straight from global memory (its row's 64 contiguous bytes per plane).
+// The next chunk's TMEM load and C loads are issued as soon as the current
+// chunk's values are converted, so they are in flight while it is stored; two
+// warps share each lane quadrant (one per column half), so one warp's waits
+// overlap the other's work.
+// The lane's C of a chunk: 4 x 8 columns per plane, zero past the edges.
+template <bool LO>
+__device__ inline void load_c_chunk(const GemmGroup& G, const TileCoord& tc, int row, int ch,
+                                    uint4 (&h)[4], uint4 (&l)[4]) {
+  const int col0 = tc.n0 + ch * 32;
+  const bool row_ok = row < G.M;
+  const long long o = (long long)tc.b * G.c_bstride + (long long)row * G.ldc + col0;
+  const __nv_bfloat16* c_hi = reinterpret_cast<const __nv_bfloat16*>(G.c_hi) + o;
+  const __nv_bfloat16* c_lo = reinterpret_cast<const __nv_bfloat16*>(G.c_lo) + o;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const bool ok = row_ok && col0 + 8 * j < G.N;
+    h[j] = ok ? __ldg(reinterpret_cast<const uint4*>(c_hi + 8 * j)) : make_uint4(0, 0, 0, 0);
+    if (LO) l[j] = ok ? __ldg(reinterpret_cast<const uint4*>(c_lo + 8 * j)) : make_uint4(0, 0, 0, 0);
+  }
+}
+
 template <bool LO>
 __device__ void epilogue_rows(const GemmParams& p, const TmaArgs& tm, const TileCoord& tc, int r0,
-                              uint32_t tacc, int q, int lane, uint8_t* ebuf, uint32_t& ek,
-                              bool& bad) {
+                              int c_begin, int c_end, uint32_t tacc, int q, int lane, uint8_t* ebuf,
+                              uint32_t& ek, bool& bad) {
   const GemmGroup& G = p.g[tc.g];
   if (r0 >= G.M) return;                            // no valid row in this warp
   const float sb = p.s ? p.s[G.mat_base + tc.b] : 1.f;
@@ -157,52 +178,33 @@ __device__ void epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
     return I < J ? 2 : (I == J ? 1 : 0);
   };
   auto next_live = [&](int ch) -> int {
-    for (int c = ch + 1; c < BN / 32; ++c)
+    for (int c = ch + 1; c < c_end; ++c)
       if (mode_of(c)) return c;
-    return BN / 32;
+    return c_end;
   };
   const int row = r0 + lane;
   const bool row_ok = row < G.M;
-  const __nv_bfloat16* c_hi = reinterpret_cast<const __nv_bfloat16*>(G.c_hi) +
-                              (long long)tc.b * G.c_bstride + (long long)row * G.ldc;
-  const __nv_bfloat16* c_lo = reinterpret_cast<const __nv_bfloat16*>(G.c_lo) +
-                              (long long)tc.b * G.c_bstride + (long long)row * G.ldc;
-  // C of one chunk for this lane: 4 x 8 columns per plane (zero past the edges)
-  auto load_c = [&](int ch, uint4 (&h)[4], uint4 (&l)[4]) {
-    const int col0 = tc.n0 + ch * 32;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const bool ok = row_ok && col0 + 8 * j < G.N;
-      h[j] = ok ? __ldg(reinterpret_cast<const uint4*>(c_hi + col0 + 8 * j)) : make_uint4(0, 0, 0, 0);
-      if (LO) l[j] = ok ? __ldg(reinterpret_cast<const uint4*>(c_lo + col0 + 8 * j)) : make_uint4(0, 0, 0, 0);
-    }
-  };
   const uint32_t trow = tacc + ((uint32_t)(q * 32) << 16);
-  int ch = next_live(-1);
-  if (ch >= BN / 32) return;
-  uint4 ch_h[4], ch_l[4], cn_h[4], cn_l[4];
-  if (use_c) load_c(ch, ch_h, ch_l);
-  // every async TMEM load is waited for within the iteration that issued it
+  int ch = next_live(c_begin - 1);
+  if (ch >= c_end) return;
+  uint4 c_h[4], c_l[4];
   uint32_t nr[32];
-  float v[32];
   tmem_ld_32x32b_x32_async(trow + ch * 32, nr);
-  tmem_ld_wait();
-  reg_fence32(nr);
-#pragma unroll
-  for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(nr[e]);
-  while (ch < BN / 32) {
+  if (use_c) load_c_chunk<LO>(G, tc, row, ch, c_h, c_l);
+  while (ch < c_end) {
     const int mode = mode_of(ch);
     const int col0 = tc.n0 + ch * 32;
     const int nx = next_live(ch);
-    if (nx < BN / 32) {
-      tmem_ld_32x32b_x32_async(trow + nx * 32, nr);
-      if (use_c) load_c(nx, cn_h, cn_l);
-    }
+    tmem_ld_wait();
+    reg_fence32(nr);
+    float v[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(nr[e]);
     if (use_c) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const __nv_bfloat16* hh = reinterpret_cast<const __nv_bfloat16*>(&ch_h[j]);
-        const __nv_bfloat16* ll = reinterpret_cast<const __nv_bfloat16*>(&ch_l[j]);
+        const __nv_bfloat16* hh = reinterpret_cast<const __nv_bfloat16*>(&c_h[j]);
+        const __nv_bfloat16* ll = reinterpret_cast<const __nv_bfloat16*>(&c_l[j]);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float cv = LO ? __bfloat162float(hh[e]) + __bfloat162float(ll[e]) : __bfloat162float(hh[e]);
@@ -237,6 +239,12 @@ __device__ void epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
       if (LO) split_bf16(v[e], hb[e], lb[e]);
       else hb[e] = __float2bfloat16_rn(v[e]);
     }
+    // this chunk's accumulator and C are consumed: start the next chunk's
+    // loads (warp-uniform: nx is the same in every lane)
+    if (nx < c_end) {
+      tmem_ld_32x32b_x32_async(trow + nx * 32, nr);
+      if (use_c) load_c_chunk<LO>(G, tc, row, nx, c_h, c_l);
+    }
     uint8_t* db = ebuf + (int)(ek % (uint32_t)depth) * per * 4096;
     uint8_t* mb = db + 4096;
     // the store group that last used these slots must have read them
@@ -268,16 +276,6 @@ __device__ void epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
       bulk_commit();
     }
     ++ek;
-    if (nx < BN / 32) {
-      tmem_ld_wait();
-      reg_fence32(nr);
-#pragma unroll
-      for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(nr[e]);
-      if (use_c) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) { ch_h[j] = cn_h[j]; ch_l[j] = cn_l[j]; }
-      }
-    }
     ch = nx;
   }
 }
@@ -326,13 +324,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], PAIR ? 1 : CL);
     }
-    for (int a = 0; a < 2; ++a) { mbar_init(&tfull[a], 1); mbar_init(&tempty[a], PAIR ? 8 : 4); }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], (PAIR ? 2 : 1) * kEpiWarps);
+    }
     mbar_init(drain, 1);
-    // readers of a ring slot: MMA + 4 epilogue warps of each CTA, and the
+    // readers of a ring slot: MMA + epilogue warps of each CTA, and the
     // second CTA's producer (pairs: only the first CTA's MMA warp)
     for (int i = 0; i < kTS; ++i) {
       mbar_init(&sfull[i], 1);
-      mbar_init(&sempty[i], CL > 1 ? (PAIR ? 10 : 11) : 5);
+      mbar_init(&sempty[i], CL > 1 ? (PAIR ? 2 * (1 + kEpiWarps) : 3 + 2 * kEpiWarps) : 1 + kEpiWarps);
     }
     fence_mbar_init();
   }
@@ -568,6 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int e = warp - 2;
     const int q = warp & 3;              // TMEM lane quadrant of this warp
+    const int hc = e >> 2;               // column half: chunks [4 hc, 4 hc + 4)
     uint8_t* ebuf = epi + e * kEpiWarpBytes;
     uint32_t ek = 0;
     bool bad = false;
@@ -580,13 +582,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t < 0) break;
       const TileCoord tc = tile_coord<TM_ROWS>(p, t);
       const int acc = tcount & 1;
+      const int r0 = tc.m0 + BM * (int)crank + q * 32;
+      const int c0 = hc * (BN / 64), c1 = (hc + 1) * (BN / 64);
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&tfull[acc], (tcount >> 1) & 1, &abort_flag) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) { if (lane == 0) fail(); break; }
       tc_fence_after();
-      epilogue_rows<LO>(p, tm, tc, tc.m0 + BM * (int)crank + q * 32, tmem_base + acc * BN, q, lane, ebuf,
-                        ek, bad);
+      epilogue_rows<LO>(p, tm, tc, r0, c0, c1, tmem_base + acc * BN, q, lane, ebuf, ek, bad);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
