@@ -730,12 +730,13 @@ int cta_mode() {
 // pairs (MC_NS_PAIR=all, the default; measured fastest on every workload), or
 // with MC_NS_PAIR=none the one-product symmetric phases on single CTAs and
 // everything else on B-multicast clusters of two.
-// k-step of the one-product launches: 64 (128-byte operand rows, 4 stages of
-// 48 KB) by default; MC_NS_BK_FAST=32 takes 64-byte rows and 8 stages.  With
-// one product per k-step, 64-byte rows leave the copy engine issuing more
-// rows per clock than it sustains (measured: the one-product launches take
-// 20-25 % less time with 128-byte rows); the three-product launches keep 32
-// for their 4 stages.
+// k-step of the one-product launches: 64 (128-byte operand rows) by default;
+// MC_NS_BK_FAST=32 takes 64-byte rows and twice the stages.  With one product
+// per k-step, 64-byte rows leave the copy engine issuing more rows per clock
+// than it sustains (measured: the one-product launches take 20-25 % less time
+// with 128-byte rows); the three-product launches keep 32.  The stage count
+// is whatever fits beside the epilogue's 64 KB (Stages): five of 32 KB per CTA
+// of a pair, three of 48 KB per CTA of a multicast cluster or single CTA.
 int fast_bk() {
   static int v = -1;
   if (v < 0) {
