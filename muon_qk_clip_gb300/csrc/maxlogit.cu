@@ -166,6 +166,8 @@ __global__ void __launch_bounds__(256) ml_simt_kernel(const __grid_constant__ Ma
 namespace tcml {
 
 constexpr int BM = 128, BN = 256;
+constexpr int kNBuf = 512 / BN;          // TMEM accumulators (512 columns)
+constexpr int kCols = BN / 2;            // columns per epilogue warp
 constexpr int kThreads = 320;            // producer, MMA, 8 epilogue warps
 constexpr int Q_CHUNK = BM * 64 * 2;     // 16 KB
 constexpr int K_CHUNK = BN * 64 * 2;     // 32 KB
@@ -228,10 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(kbuf + g.stages * K_CHUNK);
   uint64_t* q_full = bars;            // [2]
   uint64_t* q_empty = bars + 2;       // [2]
-  uint64_t* t_full = bars + 4;        // [2]
-  uint64_t* t_empty = bars + 6;       // [2]
-  uint64_t* drain = bars + 8;         // [1]
-  uint64_t* k_full = bars + 9;        // [stages]
+  uint64_t* t_full = bars + 4;        // [kNBuf]
+  uint64_t* t_empty = t_full + kNBuf; // [kNBuf]
+  uint64_t* drain = t_empty + kNBuf;  // [1]
+  uint64_t* k_full = drain + 1;       // [stages]
   uint64_t* k_empty = k_full + kMaxStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(k_empty + kMaxStages);
   __shared__ volatile int abort_flag;
@@ -242,10 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1);
-      mbar_init(&t_full[i], 1); mbar_init(&t_empty[i], 8);
-    }
+    for (int i = 0; i < 2; ++i) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
+    for (int i = 0; i < kNBuf; ++i) { mbar_init(&t_full[i], 1); mbar_init(&t_empty[i], 8); }
     mbar_init(drain, 1);
     for (int s = 0; s < g.stages; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
     fence_mbar_init();
@@ -313,8 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nkb = kblocks(p, ib);
         bool ok = true;
         for (int kb = 0; kb < nkb && ok; ++kb, ++tcount) {
-          const int acc = tcount & 1;
-          if (!mbar_wait(&t_empty[acc], ((tcount >> 1) & 1) ^ 1, &abort_flag)) { fail(); ok = false; break; }
+          const int acc = tcount % kNBuf;
+          if (!mbar_wait(&t_empty[acc], ((tcount / kNBuf) & 1) ^ 1, &abort_flag)) { fail(); ok = false; break; }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * BN;
           for (int c = 0; c < g.nch; ++c, ++it) {
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int e = warp - 2;              // 0..7
     const int q = warp & 3;              // TMEM lane quadrant
-    const int half = e >> 2;             // columns [half*128, half*128 + 128)
+    const int half = e >> 2;             // columns [half*kCols, half*kCols + kCols)
     uint32_t tcount = 0;
     for (uint32_t n = 0;; ++n) {
       int b, h, ib;
@@ -358,22 +358,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       int failed = 0;                    // warp-uniform
       for (int kb = 0; kb < nkb; ++kb, ++tcount) {
         if (failed) continue;            // every later wait would fail too
-        const int acc = tcount & 1;
+        const int acc = tcount % kNBuf;
         int w = 1;
-        if (lane == 0) w = mbar_wait(&t_full[acc], (tcount >> 1) & 1, &abort_flag) ? 1 : 0;
+        if (lane == 0) w = mbar_wait(&t_full[acc], (tcount / kNBuf) & 1, &abort_flag) ? 1 : 0;
         w = __shfl_sync(0xffffffffu, w, 0);
         if (!w) { failed = 1; if (lane == 0) fail(); continue; }
         tc_fence_after();
-        const int j0 = kb * BN + half * 128;
-        // every element of this warp's 32 x 128 block valid?
-        const bool interior = (j0 + 127 < p.S) && (i_lo + 31 < p.S) && (!p.causal || j0 + 127 <= i_lo);
+        const int j0 = kb * BN + half * kCols;
+        // every element of this warp's 32 x kCols block valid?
+        const bool interior = (j0 + kCols - 1 < p.S) && (i_lo + 31 < p.S) && (!p.causal || j0 + kCols - 1 <= i_lo);
         const bool empty = (j0 >= p.S) || (i_lo >= p.S) || (p.causal && j0 > i_lo + 31);
-        // two halves of two 32-column loads in flight before each wait (the
+        // rounds of two 32-column loads in flight before each wait (the
         // warp's block is empty or not as a whole)
         if (!empty) {
-          const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + half * 128;
+          const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + half * kCols;
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
+          for (int hh = 0; hh < kCols / 64; ++hh) {
             uint32_t r[2][32];
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) tmem_ld_32x32b_x32_async(tbase + (hh * 2 + c2) * 32, r[c2]);
@@ -538,7 +538,7 @@ cudaError_t launch_ml_tc(const MaxLogitParams& p, cudaStream_t s, char* err, siz
     cuuint32_t box[3] = {64, BN, 1};
     if (!encode(&mp.ks, p.ks, 3, dims, st, box)) { snprintf(err, errlen, "tensor map for k_shared failed"); return cudaErrorInvalidValue; }
   }
-  const size_t smem = 1024 + 2 * g.nch * Q_CHUNK + g.stages * K_CHUNK + 256;
+  const size_t smem = 1024 + 2 * g.nch * Q_CHUNK + g.stages * K_CHUNK + 512;
   const int grid = (int)(g.units < sm_count() ? g.units : sm_count());
   cudaError_t e;
   if (p.argmax) {
