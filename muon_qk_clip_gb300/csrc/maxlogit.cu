@@ -237,9 +237,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* k_empty = k_full + kMaxStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(k_empty + kMaxStages);
   __shared__ volatile int abort_flag;
-  __shared__ float red_v[8];
-  __shared__ uint32_t red_i[8];
-  __shared__ int red_bad[8];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -427,9 +424,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // nan4 became NaN iff some unmasked logit was NaN or infinite.
       const float nanacc = (nan4[0] + nan4[1]) + (nan4[2] + nan4[3]);
-      // Reduce (best, bidx) over the warp, then over the 8 epilogue warps.  All
-      // 8 warps reach both named barriers for every item, failed or not, and
-      // all leave after the same item.
+      // Reduce (best, bidx) over the warp; each warp publishes its own
+      // maximum (the packed atomic max is order-independent, and scaling by
+      // a positive factor commutes with max), so the eight epilogue warps
+      // never wait for one another between items.
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float ov = __shfl_down_sync(0xffffffffu, best, o);
@@ -437,18 +435,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ov > best || (ov == best && oi < bidx)) { best = ov; bidx = oi; }
       }
       const int badw = __any_sync(0xffffffffu, nanacc != 0.f);
-      if (lane == 0) { red_v[e] = best; red_i[e] = bidx; red_bad[e] = badw | (failed << 1); }
-      asm volatile("bar.sync 1, 256;" ::: "memory");
-      int any_fail = 0, bad = 0;
-      for (int x = 0; x < 8; ++x) { any_fail |= red_bad[x] >> 1; bad |= red_bad[x] & 1; }
-      if (e == 0 && lane == 0 && !any_fail) {
-        for (int x = 1; x < 8; ++x)
-          if (red_v[x] > best || (red_v[x] == best && red_i[x] < bidx)) { best = red_v[x]; bidx = red_i[x]; }
-        if (bad) set_status(p.status, MC_STATUS_NONFINITE_LOGIT);
+      if (lane == 0 && !failed) {
+        if (badw) set_status(p.status, MC_STATUS_NONFINITE_LOGIT);
         if (best > -INFINITY) publish(p, h, best * p.scale, bidx);
       }
-      asm volatile("bar.sync 1, 256;" ::: "memory");
-      if (any_fail) break;
+      if (failed) break;
     }
   }
 
