@@ -298,12 +298,8 @@ __device__ inline uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 __device__ inline void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// arrive (+ expect_tx) on an mbarrier given by a shared::cluster address
-__device__ inline void mbar_arrive_expect_tx_cluster(uint32_t cl_addr, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cl_addr),
-               "r"(bytes)
-               : "memory");
-}
+// arrive (release, cluster scope) on an mbarrier given by a shared::cluster
+// address (this CTA's or a peer's)
 __device__ inline void mbar_arrive_cluster(uint32_t cl_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr) : "memory");
 }
