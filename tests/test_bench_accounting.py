@@ -54,3 +54,22 @@ def test_products_per_iteration(bench):
     assert bench.ns_products(2048, 5632, 4, 3) == [1, 3, 3, 3]        # three split ones kept
     assert bench.ns_products(2048, 2048, 5, 0) == [3] * 5
     assert bench.ns_products(2048, 2048, 5, 2, split=False) == [1] * 5
+
+
+def test_traffic_is_taken_only_for_the_profiled_source(bench, tmp_path, monkeypatch):
+    """The roofline's DRAM traffic comes from the committed ncu total per
+    Newton-Schulz call, divided by this run's launches per call, and only while
+    the kernel source still has the hash the capture was taken with."""
+    import hashlib
+    import json
+    src = tmp_path / "kernel.cu"
+    src.write_text("// kernel source\n")
+    h = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    (tmp_path / "profiles").mkdir()
+    rec = {"ns_gemm": {"bytes_per_ns_call": 3000, "source_sha256_16": h}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_for(str(src), 30) == 100
+    assert bench.traffic_for(str(src), 0) is None
+    src.write_text("// kernel source, changed\n")
+    assert bench.traffic_for(str(src), 30) is None
