@@ -280,19 +280,21 @@ __device__ void epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
   }
 }
 
-// ------------------------------------------------------------ 1-CTA kernel
-// CL = 1: every CTA streams its own operands.  CL = 2: clusters of two CTAs
-// take the two 128-row halves of a 256 x 256 super-tile; they need the same
-// 256 B rows, so each CTA loads one 128-row half of B and multicasts it to
-// both (half the B traffic from L2).  A stage is refilled only when both
-// CTAs' MMAs have released it (each MMA thread's commit arrives on both).
-// PAIR (with CL 2): the two CTAs of a cluster form a tcgen05 .cta_group::2
-// pair.  Each CTA stages 128 rows of A and 128 rows (N values) of B, both
-// CTAs' copies complete on the first CTA's full barrier (whose producer alone
-// arrives, expecting both CTAs' bytes), the first CTA issues M = 256 MMAs into both CTAs' TMEM and multicasts its commits, and the
-// epilogue warps of both CTAs release the first CTA's accumulator.  Per SM a
-// stage is two thirds of a multicast cluster's (B is not duplicated), so more
-// stages fit.
+// ------------------------------------------------------------ the kernel
+// Roles: warp 0 produces (TMA), warp 1 issues the MMAs (one thread), warps
+// 2-9 are the epilogue.  CL = 1: every CTA streams its own operands.  CL = 2:
+// clusters of two CTAs take the two 128-row halves of a 256 x 256 super-tile;
+// they need the same 256 B rows, so each CTA loads one 128-row half of B and
+// multicasts it to both (half the B traffic from L2).  A stage is refilled
+// only when both CTAs' MMAs have released it (each MMA thread's commit
+// arrives on both).  PAIR (with CL 2, the default layout): the two CTAs of a
+// cluster form a tcgen05 .cta_group::2 pair.  Each CTA stages 128 rows of A
+// and 128 rows (N values) of B; both CTAs' copies complete on the first CTA's
+// full barrier, whose producer alone arrives (expecting both CTAs' bytes);
+// the first CTA issues M = 256 MMAs into both CTAs' TMEM and multicasts its
+// commits; the epilogue warps of both CTAs release the first CTA's
+// accumulator.  Per SM a stage is two thirds of a multicast cluster's (B is
+// not duplicated), so more stages fit: five of 32 KB beside the epilogue.
 template <int TERMS, bool LO, int CL, int BK, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     ns_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ TmaArgs tm) {
