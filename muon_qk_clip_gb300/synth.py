@@ -8,7 +8,7 @@ depend on which other tensors were drawn.  The stream differs between CPU and
 CUDA generators: tests that compare CPU and GPU results draw on the CPU and
 copy.
 
-Workloads (sizes and distributions of the K2 pages' model):
+Workloads (sizes and distributions of the Kimi K2 model that MuonClip trained):
   tiny_mha_fp32    d_model 256, 4 heads x 64, one 256x512 Muon matrix, fp32
   dense_block      d_model 2048, 16 heads x 128, FFN 2048->5632->2048, bf16
   k2_mla_layer     hidden 7168, 64 heads, q_lora 1536, kv_lora 512,

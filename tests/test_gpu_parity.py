@@ -1,10 +1,11 @@
 """GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
 same seeded inputs.
 
-Tolerances (floating point; see the design doc for their derivation):
+Tolerances (floating point; each derived from the arithmetic of its path):
   * momentum:                 within 1 fp32 rounding of the exact mu*M + G
   * Newton-Schulz, split bf16: |O - O_exact| <= 2e-2 * RMS(O_exact) before the
-                               output rounding (spec bound)
+                               output rounding (the bound stated for the
+                               bf16 tensor-core path)
   * Newton-Schulz, fp32:      1e-5 * RMS(O_exact)
   * Newton-Schulz, bf16:      2.5e-1 * RMS max, 2.5e-2 * RMS root-mean-square
   * updated weights:          |W - W_exact| <= tol * RMS(lr O) before the final
