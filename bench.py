@@ -202,16 +202,32 @@ def ns_flops_counted(rows, cols, steps, symmetric=True):
 
 
 def ns_products(rows, cols, steps, fast_steps, split=True):
-    """Tensor-core products per k-step of each iteration under the default
-    plan: one (hi*hi) for the leading one-product iterations of matrices whose
-    smaller side is at least 1024 (two at most, three only from 2048 when
-    asked for), three (hi*hi + hi*lo + lo*hi) otherwise."""
+    """Tensor-core products per k-step of each iteration's (Gram, polynomial,
+    update) under the default plan: one (hi*hi) for the leading one-product
+    iterations of matrices whose smaller side is at least 1024 (two at most,
+    three only from 2048 when asked for), three (hi*hi + hi*lo + lo*hi)
+    otherwise; from 2048, after two one-product iterations, the next
+    iteration's Gram takes one."""
     if not split:
-        return [1] * steps
+        return [(1, 1, 1)] * steps
     side = min(rows, cols)
     f12 = min(fast_steps, 2, max(0, steps - 3))
-    nf = 3 if (side >= 2048 and f12 == 2 and fast_steps >= 3 and steps >= 5) else (f12 if side >= 1024 else 0)
-    return [1 if it < nf else 3 for it in range(steps)]
+    fast3 = side >= 2048 and f12 == 2 and fast_steps >= 3 and steps >= 5
+    nf = 3 if fast3 else (f12 if side >= 1024 else 0)
+    out = [(1, 1, 1) if it < nf else (3, 3, 3) for it in range(steps)]
+    if nf == 2 and not fast3 and side >= 2048:
+        out[2] = (1, 3, 3)
+    return out
+
+
+def ns_flops_executed(rows, cols, steps, fast_steps, split=True, symmetric=True):
+    """What the tensor pipe executes: each phase's counted flops (Gram 2 n E,
+    polynomial 2 m E, update 2 m^2 n) times its products per k-step."""
+    m, n = min(rows, cols), max(rows, cols)
+    e = ns_sym_entries(m) if symmetric else m * m
+    ph = (2.0 * n * e, 2.0 * m * e, 2.0 * m * m * n)
+    return sum(sum(p * f for p, f in zip(prod, ph))
+               for prod in ns_products(rows, cols, steps, fast_steps, split))
 
 
 def traffic_for(kernel_src, launches_per_call):
@@ -483,9 +499,8 @@ def gpu_arm(args):
     ns_flops_nominal = sum(synth.flops_ns(m.rows, m.cols, hp.ns_steps) for m in wl.matrices)
     ns_flops = sum(ns_flops_counted(m.rows, m.cols, hp.ns_steps, symmetric=tc_path) for m in wl.matrices)
     # what the tensor pipe executes: the counted flops times the products per k-step
-    ns_flops_products = sum(ns_flops_counted(m.rows, m.cols, 1, symmetric=tc_path) *
-                            sum(ns_products(m.rows, m.cols, hp.ns_steps, hp.ns_fast_steps, tc_path))
-                            for m in wl.matrices)
+    ns_flops_products = sum(ns_flops_executed(m.rows, m.cols, hp.ns_steps, hp.ns_fast_steps, tc_path,
+                                              symmetric=tc_path) for m in wl.matrices)
     ml_flops = 0.0
     clip_bytes = 0
     if att is not None:
@@ -525,7 +540,8 @@ def gpu_arm(args):
            "ns_precision": ((f"split-bf16 (hi*hi+hi*lo+lo*hi), fp32 accumulate, all {hp.ns_steps} iterations"
                              if hp.ns_fast_steps == 0 else
                              f"split-bf16 (hi*hi+hi*lo+lo*hi), fp32 accumulate; hi*hi for the first "
-                             f"{hp.ns_fast_steps} iterations of matrices whose smaller side is >= 1024")
+                             f"{hp.ns_fast_steps} iterations of matrices whose smaller side is >= 1024, "
+                             f"and for the next iteration's Gram product from 2048")
                             if wl.dtype == torch.bfloat16 else "fp32 CUDA cores"),
            "ns_flops_counted": ("Gram and polynomial: the computed 256x256 units on or above the "
                                 "diagonal (symmetry exploited); update 2 m^2 n; split products not "

@@ -117,7 +117,12 @@ typedef struct {
                           product).  A value >= 3 adds a third for matrices
                           whose smaller side is at least 2048 when ns_steps
                           >= 5: 9-13 % faster steps, at most 1.6e-2 of RMS on
-                          adversarial spectra (3e-3 on Gaussian).  Default 2. */
+                          adversarial spectra (3e-3 on Gaussian).  With exactly
+                          two, matrices whose smaller side is at least 2048
+                          also take the third iteration's Gram product in one
+                          product (its polynomial and update stay three-term):
+                          at most 8.2e-3 of RMS on adversarial spectra at
+                          2048 x 2048 (1.6e-3 on Gaussian).  Default 2. */
   int32_t scale_mode;  /* mc_scale_mode: factor on NewtonSchulz(M)            */
 } mc_hparams;
 

@@ -296,6 +296,12 @@ constexpr int kFastMinSide = 1024;
 // 1.6e-2 of RMS (64 unit directions over a 1e-3 rest; 3e-3 on Gaussian
 // inputs), against 1.5e-2 on plain Gaussian inputs at 1024.
 constexpr int kFast3MinSide = 2048;
+// Smallest min(rows, cols) for which the first three-term iteration's Gram
+// product takes one bf16 product (its polynomial and update stay three-term):
+// float64 emulation at 2048 x 2048 gives at most 8.2e-3 of RMS (64 unit
+// directions over a 1e-3 rest; 1.6e-3 on Gaussian inputs), against 5.1e-3
+// with the Gram three-term; 1.1e-2 at 1024.
+constexpr int kGram1MinSide = 2048;
 
 mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams* hp,
                     int32_t* status, int& launch, const std::vector<int>& groups, cudaStream_t s) {
@@ -311,15 +317,19 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
   // product per k-step.  Up to two, followed by at least three three-term
   // iterations, for shape groups whose smaller side is at least
   // kFastMinSide; a third (ns_fast_steps >= 3, at least two three-term
-  // iterations after it) from kFast3MinSide.  Every other iteration takes the
-  // three-term product.
+  // iterations after it) from kFast3MinSide.  After exactly two, the next
+  // iteration's Gram takes one product from kGram1MinSide.  Every other
+  // launch takes the three-term product.
   const int fast12 = std::min({hp->ns_fast_steps, 2, std::max(0, hp->ns_steps - 3)});
   const bool fast3 = fast12 == 2 && hp->ns_fast_steps >= 3 && hp->ns_steps >= 5;
   auto terms_of = [&](int g) {
     if (P.xmode != kXSplit) return 1;
     const int side = std::min(P.groups[g].m, P.groups[g].n);
     const int n = side >= kFast3MinSide && fast3 ? 3 : side >= kFastMinSide ? fast12 : 0;
-    return it < n ? 1 : 3;
+    if (it < n) return 1;
+    // after two one-product iterations, the next iteration's Gram product
+    if (ph == kGram && it == n && n == 2 && !fast3 && side >= kGram1MinSide) return 1;
+    return 3;
   };
   const bool sym_out = P.xmode != kXF32 && (ph == kGram || ph == kPoly);
   for (int terms : {1, 3}) {

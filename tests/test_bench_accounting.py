@@ -47,13 +47,25 @@ def test_counted_flops(bench):
 
 
 def test_products_per_iteration(bench):
-    assert bench.ns_products(512, 7168, 5, 2) == [3] * 5              # smaller side < 1024
-    assert bench.ns_products(1024, 1536, 5, 2) == [1, 1, 3, 3, 3]
-    assert bench.ns_products(1024, 1536, 5, 3) == [1, 1, 3, 3, 3]     # third only from 2048
-    assert bench.ns_products(2048, 5632, 5, 3) == [1, 1, 1, 3, 3]
-    assert bench.ns_products(2048, 5632, 4, 3) == [1, 3, 3, 3]        # three split ones kept
-    assert bench.ns_products(2048, 2048, 5, 0) == [3] * 5
-    assert bench.ns_products(2048, 2048, 5, 2, split=False) == [1] * 5
+    F, S, G1 = (1, 1, 1), (3, 3, 3), (1, 3, 3)
+    assert bench.ns_products(512, 7168, 5, 2) == [S] * 5              # smaller side < 1024
+    assert bench.ns_products(1024, 1536, 5, 2) == [F, F, S, S, S]
+    assert bench.ns_products(1024, 1536, 5, 3) == [F, F, S, S, S]     # third only from 2048
+    assert bench.ns_products(2048, 5632, 5, 2) == [F, F, G1, S, S]    # one-product Gram from 2048
+    assert bench.ns_products(2048, 5632, 5, 3) == [F, F, F, S, S]
+    assert bench.ns_products(2048, 5632, 4, 3) == [F, S, S, S]        # three split ones kept
+    assert bench.ns_products(2048, 2048, 5, 0) == [S] * 5
+    assert bench.ns_products(2048, 2048, 5, 2, split=False) == [F] * 5
+
+
+def test_executed_flops_weight_each_phase_by_its_products(bench):
+    m, n = 2048, 5632
+    e = bench.ns_sym_entries(m)
+    g, p, u = 2.0 * n * e, 2.0 * m * e, 2.0 * m * m * n
+    # iterations: one-product x 2, one-product Gram + three-term rest, three-term x 2
+    want = 2 * (g + p + u) + (g + 3 * p + 3 * u) + 2 * 3 * (g + p + u)
+    assert bench.ns_flops_executed(m, n, 5, 2) == want
+    assert bench.ns_flops_executed(m, n, 5, 2, split=False) == bench.ns_flops_counted(m, n, 5)
 
 
 def test_traffic_is_taken_only_for_the_profiled_source(bench, tmp_path, monkeypatch):
