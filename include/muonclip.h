@@ -189,6 +189,17 @@ void mc_default_hparams(mc_hparams* hp);
  * `count` matrices (shapes and dtypes of M, or of W for muonclip_step). */
 mc_status mc_workspace_size(const mc_mat* M, int32_t count, const mc_hparams* hp, size_t* bytes);
 
+/* Products per k-step that the split-bf16 tensor-core Newton-Schulz takes for
+ * a rows x cols matrix under *hp ([K2-internals] Algorithm 1, orthogonalisation
+ * step; the arithmetic of the split iterate is this library's): for iteration
+ * i (0 .. ns_steps - 1), products[3 i + 0], [3 i + 1] and [3 i + 2] are those
+ * of the Gram product A = X X^T, the polynomial B = b A + c A^2 and the update,
+ * each 1 (hi*hi) or 3 (hi*hi + hi*lo + lo*hi).  products: host int32 array of
+ * 3 * ns_steps entries, owned by the caller.  Host-only; no GPU work.
+ * MC_ERR_INVALID_ARG for a null array, a shape outside 1 .. 2^30 or invalid
+ * hyper-parameters. */
+mc_status mc_ns_products(const mc_hparams* hp, int64_t rows, int64_t cols, int32_t* products);
+
 /* M_t = mu * M_{t-1} + G_t for each of `count` matrices, in place.
  * [K2-internals] Algorithm 1, momentum step (M_0 = 0: pass a zeroed M).
  * M: f32; G: f32 or bf16, same rows/cols as M.  A NaN/Inf in M_t sets

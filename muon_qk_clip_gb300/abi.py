@@ -73,6 +73,7 @@ class McKernelTime(ctypes.Structure):
 SIGNATURES = {
     "mc_default_hparams": (None, [POINTER(McHparams)]),
     "mc_workspace_size": (c_int32, [POINTER(McMat), c_int32, POINTER(McHparams), POINTER(c_size_t)]),
+    "mc_ns_products": (c_int32, [POINTER(McHparams), c_int64, c_int64, c_void_p]),
     "muon_momentum": (c_int32, [POINTER(McMat), POINTER(McMat), c_int32, c_float, c_void_p, c_void_p]),
     "muon_newton_schulz": (c_int32, [POINTER(McMat), POINTER(McMat), c_int32, POINTER(McHparams),
                                      c_void_p, c_size_t, c_void_p, c_void_p]),

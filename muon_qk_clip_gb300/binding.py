@@ -89,6 +89,16 @@ def workspace_size(shapes_or_tensors, hp: Hparams | None = None) -> int:
     return n.value
 
 
+def ns_products(rows: int, cols: int, hp: Hparams | None = None) -> list:
+    """Products per k-step of each Newton-Schulz iteration's (Gram, polynomial,
+    update) on the split-bf16 tensor-core path: a list of ns_steps triples."""
+    hp = hp or Hparams()
+    out = (ctypes.c_int32 * (3 * hp.ns_steps))()
+    hc = hp.c()
+    check(abi.load().mc_ns_products(ctypes.byref(hc), rows, cols, out), "mc_ns_products")
+    return [tuple(out[3 * i:3 * i + 3]) for i in range(hp.ns_steps)]
+
+
 def alloc_workspace(shapes_or_tensors, hp=None, device="cuda") -> torch.Tensor:
     n = workspace_size(shapes_or_tensors, hp)
     return torch.empty(max(n, 256), dtype=torch.uint8, device=device)

@@ -303,6 +303,22 @@ constexpr int kFast3MinSide = 2048;
 // with the Gram three-term; 1.1e-2 at 1024.
 constexpr int kGram1MinSide = 2048;
 
+// Products per k-step (1: hi*hi; 3: hi*hi + hi*lo + lo*hi) of phase `ph` of
+// iteration `it` on the split iterate, for a shape group whose smaller side
+// is `side`.  The leading ns_fast_steps iterations take one product: up to
+// two, followed by at least three three-term iterations, from kFastMinSide;
+// a third (ns_fast_steps >= 3, at least two three-term iterations after it)
+// from kFast3MinSide.  After exactly two, the next iteration's Gram takes one
+// product from kGram1MinSide.  Every other launch takes three.
+int ns_terms(const mc_hparams* hp, int side, int it, int ph) {
+  const int fast12 = std::min({hp->ns_fast_steps, 2, std::max(0, hp->ns_steps - 3)});
+  const bool fast3 = fast12 == 2 && hp->ns_fast_steps >= 3 && hp->ns_steps >= 5;
+  const int n = side >= kFast3MinSide && fast3 ? 3 : side >= kFastMinSide ? fast12 : 0;
+  if (it < n) return 1;
+  if (ph == kGram && it == n && n == 2 && !fast3 && side >= kGram1MinSide) return 1;
+  return 3;
+}
+
 mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams* hp,
                     int32_t* status, int& launch, const std::vector<int>& groups, cudaStream_t s) {
   const int cur = it & 1, nxt = cur ^ 1;
@@ -313,23 +329,10 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
     const Group &a = P.groups[x], &b = P.groups[y];
     return (ph == kGram ? a.n : a.m) > (ph == kGram ? b.n : b.m);
   });
-  // split iterate: the leading ns_fast_steps iterations take one bf16
-  // product per k-step.  Up to two, followed by at least three three-term
-  // iterations, for shape groups whose smaller side is at least
-  // kFastMinSide; a third (ns_fast_steps >= 3, at least two three-term
-  // iterations after it) from kFast3MinSide.  After exactly two, the next
-  // iteration's Gram takes one product from kGram1MinSide.  Every other
-  // launch takes the three-term product.
-  const int fast12 = std::min({hp->ns_fast_steps, 2, std::max(0, hp->ns_steps - 3)});
-  const bool fast3 = fast12 == 2 && hp->ns_fast_steps >= 3 && hp->ns_steps >= 5;
+  // products per k-step of this launch kind (ns_terms; 1 off the split iterate)
   auto terms_of = [&](int g) {
     if (P.xmode != kXSplit) return 1;
-    const int side = std::min(P.groups[g].m, P.groups[g].n);
-    const int n = side >= kFast3MinSide && fast3 ? 3 : side >= kFastMinSide ? fast12 : 0;
-    if (it < n) return 1;
-    // after two one-product iterations, the next iteration's Gram product
-    if (ph == kGram && it == n && n == 2 && !fast3 && side >= kGram1MinSide) return 1;
-    return 3;
+    return ns_terms(hp, std::min(P.groups[g].m, P.groups[g].n), it, ph);
   };
   const bool sym_out = P.xmode != kXF32 && (ph == kGram || ph == kPoly);
   for (int terms : {1, 3}) {
@@ -731,6 +734,18 @@ mc_status mc_workspace_size(const mc_mat* M, int32_t count, const mc_hparams* hp
   // largest variant (fp32 planes and split planes take the same bytes).
   const int xm = hp->ns_precision == MC_NS_BF16 ? kXBf16 : kXSplit;
   *bytes = make_plan(M, count, xm).bytes;
+  return ok();
+}
+
+mc_status mc_ns_products(const mc_hparams* hp, int64_t rows, int64_t cols, int32_t* products) {
+  if (!products) return fail(MC_ERR_INVALID_ARG, "products: null");
+  if (rows < 1 || cols < 1 || rows > (1 << 30) || cols > (1 << 30))
+    return fail(MC_ERR_INVALID_ARG, "bad shape %lld x %lld", (long long)rows, (long long)cols);
+  mc_status st = check_hparams(hp);
+  if (st != MC_OK) return st;
+  const int side = (int)std::min(rows, cols);
+  for (int it = 0; it < hp->ns_steps; ++it)
+    for (int ph = 1; ph <= 3; ++ph) products[3 * it + ph - 1] = ns_terms(hp, side, it, ph);
   return ok();
 }
 

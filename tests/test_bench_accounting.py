@@ -85,3 +85,31 @@ def test_traffic_is_taken_only_for_the_profiled_source(bench, tmp_path, monkeypa
     assert bench.traffic_for(str(src), 0) is None
     src.write_text("// kernel source, changed\n")
     assert bench.traffic_for(str(src), 30) is None
+
+
+@pytest.mark.parametrize("steps,fast", [(5, 2), (5, 3), (5, 0), (5, 1), (4, 3), (6, 2), (3, 2), (0, 2)])
+def test_products_mirror_the_library_plan(bench, steps, fast):
+    """bench.py's executed-flop accounting uses a copy of the library's plan of
+    products per k-step; the library reports its own through mc_ns_products."""
+    from muon_qk_clip_gb300 import abi, build
+    from muon_qk_clip_gb300 import binding as mc
+    build.build()
+    abi.load()
+    hp = mc.Hparams(ns_steps=steps, ns_fast_steps=fast)
+    for r, c in [(64, 64), (512, 7168), (1024, 1536), (1536, 1024), (2047, 4096), (2048, 2048),
+                 (2048, 5632), (7168, 2048), (8192, 7168)]:
+        assert mc.ns_products(r, c, hp) == bench.ns_products(r, c, steps, fast), (r, c)
+
+
+def test_products_call_rejects(bench):
+    from muon_qk_clip_gb300 import abi, build
+    from muon_qk_clip_gb300 import binding as mc
+    build.build()
+    lib = abi.load()
+    hc = mc.Hparams().c()
+    import ctypes
+    out = (ctypes.c_int32 * 15)()
+    assert lib.mc_ns_products(ctypes.byref(hc), 0, 5, out) == abi.MC_ERR_INVALID_ARG
+    assert lib.mc_ns_products(ctypes.byref(hc), 5, 5, None) == abi.MC_ERR_INVALID_ARG
+    bad = mc.Hparams(ns_fast_steps=-1).c()
+    assert lib.mc_ns_products(ctypes.byref(bad), 5, 5, out) == abi.MC_ERR_INVALID_ARG
