@@ -339,8 +339,9 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
     std::vector<int> sub;                    // the groups of this launch kind
     for (int g : order)
       if (terms_of(g) == terms) sub.push_back(g);
-    int tileM = 64, tileN = 64, sym_step = 1;
-    if (P.xmode != kXF32) ns_tc_tile_shape(sym_out, terms, &tileM, &tileN, &sym_step);
+    // output tiles: 256 x 256 per CTA pair (tensor cores), 64 x 64 (fp32)
+    const int tileM = P.xmode != kXF32 ? kTcTileM : 64, tileN = P.xmode != kXF32 ? kTcTileN : 64;
+    const int sym_step = 1;
     for (size_t g0 = 0; g0 < sub.size(); g0 += kMaxGroups) {
       GemmParams gp;
       memset(&gp, 0, sizeof gp);
@@ -396,8 +397,11 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
       gp.ngroups = ng;
       gp.total_tiles = t;
       // tensor-core launches claim tiles from a zeroed counter of their own
-      if (P.xmode != kXF32 && ns_dynamic_schedule() && launch < P.nsched)
+      if (P.xmode != kXF32) {
+        if (launch >= P.nsched)
+          return fail(MC_ERR_UNSUPPORTED, "Newton-Schulz plan needs more than %d tile counters", P.nsched);
         gp.sched = reinterpret_cast<int*>(wsp(ws, P.off_sched)) + launch;
+      }
       ++launch;
       gp.terms = terms;
       // Three-term iterations fold a X into the polynomial: B' = c A^2 + b A + a I
@@ -439,20 +443,11 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
 // A second stream for Newton-Schulz (one per host thread and device, created
 // on first use and kept): shape groups are independent chains of launches, so
 // running two sets of them side by side lets one set's launches fill the SMs
-// that the other's launch tails leave idle.  MC_NS_STREAMS=1 keeps one stream.
+// that the other's launch tails leave idle.
 struct AuxStream {
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
 };
-
-bool ns_two_streams() {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = getenv("MC_NS_STREAMS");
-    v = (e && atoi(e) == 1) ? 1 : 2;
-  }
-  return v == 2;
-}
 
 cudaError_t aux_stream(AuxStream*& out) {
   thread_local std::map<int, AuxStream> cache;
@@ -479,7 +474,7 @@ mc_status run_newton_schulz(Plan& P, void* ws, const mc_hparams* hp, int32_t* st
   // (largest first onto the lighter set)
   std::vector<int> set[2];
   const int ng = (int)P.groups.size();
-  if (ng >= 2 && P.xmode != kXF32 && ns_two_streams()) {
+  if (ng >= 2 && P.xmode != kXF32) {
     std::vector<int> idx(ng);
     for (int g = 0; g < ng; ++g) idx[g] = g;
     auto work = [&](int g) {
@@ -504,22 +499,27 @@ mc_status run_newton_schulz(Plan& P, void* ws, const mc_hparams* hp, int32_t* st
     if (e != cudaSuccess) return cuda_fail(e, "Newton-Schulz second stream");
   }
   // the profiler times the whole Newton-Schulz section (launches overlap)
-  ProfScope ps(kGemm, 0, s);
-  int launch = 0;
-  for (int it = 0; it < hp->ns_steps; ++it) {
-    for (Phase ph : {kGram, kPoly, kNext}) {
-      mc_status st;
-      if ((st = run_phase(P, ws, ph, it, hp, status, launch, set[0], s)) != MC_OK) return st;
-      if (aux && (st = run_phase(P, ws, ph, it, hp, status, launch, set[1], aux->s)) != MC_OK) return st;
+  mc_status st = MC_OK;
+  {
+    ProfScope ps(kGemm, 0, s);
+    int launch = 0;
+    for (int it = 0; it < hp->ns_steps && st == MC_OK; ++it) {
+      for (Phase ph : {kGram, kPoly, kNext}) {
+        if ((st = run_phase(P, ws, ph, it, hp, status, launch, set[0], s)) != MC_OK) break;
+        if (aux && (st = run_phase(P, ws, ph, it, hp, status, launch, set[1], aux->s)) != MC_OK) break;
+      }
+    }
+    ps.n = launch;
+    // join the second stream even after a failed launch, so that no work it
+    // already queued on the caller's workspace is left unordered against the
+    // caller's stream (and a stream capture is not left with an open fork)
+    if (aux) {
+      cudaError_t e = cudaEventRecord(aux->join, aux->s);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(s, aux->join, 0);
+      if (e != cudaSuccess && st == MC_OK) st = cuda_fail(e, "Newton-Schulz stream join");
     }
   }
-  ps.n = launch;
-  if (aux) {
-    cudaError_t e = cudaEventRecord(aux->join, aux->s);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, aux->join, 0);
-    if (e != cudaSuccess) return cuda_fail(e, "Newton-Schulz stream join");
-  }
-  return MC_OK;
+  return st;
 }
 
 mc_status run_apply(const Plan& P, void* ws, mc_mat* out, bool write_o, const mc_hparams* hp,

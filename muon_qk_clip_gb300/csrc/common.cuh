@@ -342,26 +342,6 @@ __device__ inline void tma_load_3d_pair(void* smem_dst, const CUtensorMap* map, 
       "l"(reinterpret_cast<uint64_t>(map)), "r"(cl_bar), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
-// TMA load multicast to every CTA in `mask`: the box lands at the same shared
-// offset in each of them and completes bytes on the mbarrier at the same
-// offset in each of them.
-__device__ inline void tma_load_3d_mc(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int32_t x,
-                                      int32_t y, int32_t z, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "h"(mask)
-      : "memory");
-}
-// 1-CTA tcgen05 commit whose mbarrier arrive goes to every CTA in `mask`.
-__device__ inline void tc_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
-
 __device__ inline void tmem_alloc_pair(uint32_t* smem_result, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                    smem_u32(smem_result)),

@@ -132,20 +132,13 @@ struct GemmParams {
   float diag;             // added on the diagonal of each output item
   const float* s;         // per-matrix scale, or null
   int32_t* status;
-  int* sched;             // zeroed tile counter (dynamic schedule), or null (static)
+  int* sched;             // zeroed tile counter of this launch (tensor-core path)
 };
 
 // Tensor-core path (split bf16 or bf16).  Encodes its own tensor maps.
 cudaError_t launch_ns_gemm_tc(const GemmParams& p, cudaStream_t s, char* err, size_t errlen);
-// false when MC_NS_SCHED=static: the tensor-core GEMM hands tiles out round robin
-bool ns_dynamic_schedule();
-// Output tile of one tensor-core work unit (bm x bn) and, for symmetric
-// outputs, how many row tiles column tile tn holds per step (rows touching the
-// upper triangle: min(tiles_m, (tn + 1) * sym_rows_per_col_block)).
-// Output tile of one work unit of the tensor-core GEMM for a launch of this
-// kind (symmetric output, products per k-step): bm x bn, and for symmetric
-// outputs the row units per 256-column block along the diagonal.
-void ns_tc_tile_shape(bool symmetric, int terms, int* bm, int* bn, int* sym_rows_per_col_block);
+// Output tiles of the tensor-core GEMM: 256 x 256 per CTA pair.
+constexpr int kTcTileM = 256, kTcTileN = 256;
 // CUDA-core fp32 path.
 cudaError_t launch_ns_gemm_f32(const GemmParams& p, cudaStream_t s);
 

@@ -14,18 +14,20 @@
 // ~16 significand bits; D is stored again as a (hi, lo) pair.  Plain mode:
 // one bf16 plane, one MMA per k-step.
 //
-// Kernel layout (one CTA per SM, persistent over output tiles):
+// Kernel layout (one CTA per SM, persistent over output tiles, CTAs paired
+// into tcgen05 .cta_group::2 clusters of two):
 //   warp 0      TMA producer (one elected lane)
-//   warp 1      TMEM allocator + MMA issuer (one elected lane)
-//   warps 2..5  epilogue: TMEM -> registers -> fused polynomial -> global
-// Tiles are 128 x 256 with K advancing by 32 (64-byte swizzle rows) in
-// three-product launches and by 64 (128-byte rows) in one-product ones; the
-// accumulator is double-buffered in TMEM (2 x 256 columns) so the epilogue of
-// tile t overlaps the MMAs of tile t+1.  The epilogue reads C straight into
-// registers and stages every 32 x 32 chunk of D (and, for symmetric outputs,
-// its transpose) through 8 KB of shared memory per warp, from where TMA bulk
-// stores write whole 64-byte rows; the small epilogue footprint leaves room
-// for 4 operand stages in split mode and 8 in one-product mode.
+//   warp 1      TMEM allocator + MMA issuer (one elected lane of the first
+//               CTA of the pair)
+//   warps 2..9  epilogue: TMEM -> registers -> fused polynomial -> global
+// A pair computes 256 x 256 output tiles (128 rows per CTA) with K advancing
+// by 32 (64-byte swizzle rows) in three-product launches and by 64 (128-byte
+// rows) in one-product ones; the accumulator is double-buffered in TMEM
+// (2 x 256 columns) so the epilogue of tile t overlaps the MMAs of tile t+1.
+// The epilogue reads C straight into registers and stages every 32 x 32
+// chunk of D (and, for symmetric outputs, its transpose) through 8 KB of
+// shared memory per warp, from where TMA bulk stores write whole 64-byte
+// rows.
 //
 // Symmetric outputs (phases 1 and 2) are computed only on tiles that touch
 // the upper triangle.  Per 128 x 128 block (I, J) of such a tile: I < J is
@@ -282,29 +284,25 @@ __device__ void epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
 
 // ------------------------------------------------------------ the kernel
 // Roles: warp 0 produces (TMA), warp 1 issues the MMAs (one thread), warps
-// 2-9 are the epilogue.  CL = 1: every CTA streams its own operands.  CL = 2:
-// clusters of two CTAs take the two 128-row halves of a 256 x 256 super-tile;
-// they need the same 256 B rows, so each CTA loads one 128-row half of B and
-// multicasts it to both (half the B traffic from L2).  A stage is refilled
-// only when both CTAs' MMAs have released it (each MMA thread's commit
-// arrives on both).  PAIR (with CL 2, the default layout): the two CTAs of a
-// cluster form a tcgen05 .cta_group::2 pair.  Each CTA stages 128 rows of A
-// and 128 rows (N values) of B; both CTAs' copies complete on the first CTA's
-// full barrier, whose producer alone arrives (expecting both CTAs' bytes);
-// the first CTA issues M = 256 MMAs into both CTAs' TMEM and multicasts its
-// commits; the epilogue warps of both CTAs release the first CTA's
-// accumulator.  Per SM a stage is two thirds of a multicast cluster's (B is
-// not duplicated), so more stages fit: five of 32 KB beside the epilogue.
-template <int TERMS, bool LO, int CL, int BK, bool PAIR>
+// 2-9 are the epilogue.  The CTAs run as tcgen05 .cta_group::2 pairs
+// (clusters of two): the pair owns a 256 x 256 output tile, each CTA stages
+// 128 rows of A and 128 rows (N values) of B per k-step, and both CTAs'
+// copies complete on the first CTA's full barrier, whose producer alone
+// arrives (expecting both CTAs' bytes).  The first CTA issues M = 256 MMAs
+// into both CTAs' TMEM and multicasts its commits (mbarrier arrivals) to
+// both; the epilogue warps of both CTAs release the first CTA's accumulator.
+// A stage is 32 KB per CTA, so five fit beside the epilogue's 64 KB.
+// Tiles are handed out dynamically: the first CTA's producer claims the next
+// tile id from a zeroed per-launch counter and publishes it to every role of
+// both CTAs through a kTS-deep shared-memory ring.
+template <int TERMS, bool LO, int BK>
 __global__ void __launch_bounds__(kThreads, 1)
     ns_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ TmaArgs tm) {
-  static_assert(!PAIR || CL == 2, "pairs are clusters of 2");
-  using C = Stages<TERMS, BM, PAIR ? 128 : BN, BK>;
+  using C = Stages<TERMS, BM, 128, BK>;
   using KL = KLayout<BK>;
   constexpr bool SPLIT = TERMS == 3;
-  constexpr int TM_ROWS = BM * CL;
-  const uint32_t crank = CL > 1 ? cluster_ctarank() : 0;
-  const int unit = blockIdx.x / CL, nunits = gridDim.x / CL;
+  constexpr int TM_ROWS = 2 * BM;
+  const uint32_t crank = cluster_ctarank();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* epi = smem + C::kStages * C::kStageBytes;
@@ -324,18 +322,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     abort_flag = 0;
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], PAIR ? 1 : CL);
+      mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], (PAIR ? 2 : 1) * kEpiWarps);
+      mbar_init(&tempty[a], 2 * kEpiWarps);
     }
     mbar_init(drain, 1);
-    // readers of a ring slot: MMA + epilogue warps of each CTA, and the
-    // second CTA's producer (pairs: only the first CTA's MMA warp)
+    // readers of a ring slot: the producer and the epilogue warps of each
+    // CTA (the first CTA's producer and MMA warp, the second's producer)
     for (int i = 0; i < kTS; ++i) {
       mbar_init(&sfull[i], 1);
-      mbar_init(&sempty[i], CL > 1 ? (PAIR ? 2 * (1 + kEpiWarps) : 3 + 2 * kEpiWarps) : 1 + kEpiWarps);
+      mbar_init(&sempty[i], 2 * (1 + kEpiWarps));
     }
     fence_mbar_init();
   }
@@ -345,12 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (SPLIT) { prefetch_tmap(&tm.maps.a_lo[g]); prefetch_tmap(&tm.maps.b_lo[g]); }
     }
   }
-  if (warp == 1) {
-    if (PAIR) { tmem_alloc_pair(tmem_slot, kTmemCols); tmem_relinquish_pair(); }
-    else { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
-  }
+  if (warp == 1) { tmem_alloc_pair(tmem_slot, kTmemCols); tmem_relinquish_pair(); }
   tc_fence_before();
-  if (CL > 1) { __syncwarp(); cluster_sync_all(); } else { __syncthreads(); }
+  __syncwarp();
+  cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -359,38 +355,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     set_status(p.status, MC_STATUS_TIMEOUT);
   };
 
-  // Tile schedule.  Static: unit u takes tiles u, u + nunits, ...  Dynamic
-  // (p.sched set): the first CTA's producer claims the next tile from a global
-  // counter and publishes its id in a kTS-deep ring (in both CTAs of a
-  // cluster); every role reads the seq-th id from the ring.  Tiles are
-  // numbered heaviest group first, so claiming in order approximates
+  // Tile schedule: the first CTA's producer claims the next tile from the
+  // launch's global counter and publishes its id in a kTS-deep ring (in both
+  // CTAs); every role reads the seq-th id from the ring.  Tiles are numbered
+  // heaviest group first, so claiming in order approximates
   // longest-processing-time-first scheduling.  -1 ends the sequence, -2 is a
   // wait timeout.
-  const bool dyn = p.sched != nullptr;
-  const uint32_t sempty_r0 = CL > 1 ? mapa_shared(smem_u32(&sempty[0]), 0) : smem_u32(&sempty[0]);
+  const uint32_t sempty_r0 = mapa_shared(smem_u32(&sempty[0]), 0);
   auto take = [&](uint32_t seq) -> int {
-    if (!dyn) {
-      const int t = unit + (int)seq * nunits;
-      return t < p.total_tiles ? t : -1;
-    }
     const int slot = (int)(seq % kTS);
     if (!mbar_wait_acq_cluster(&sfull[slot], (seq / kTS) & 1, &abort_flag)) return -2;
     const int t = reinterpret_cast<volatile int*>(sid)[slot];
-    if (CL > 1) mbar_arrive_cluster(sempty_r0 + slot * 8);
-    else mbar_arrive(&sempty[slot]);
+    mbar_arrive_cluster(sempty_r0 + slot * 8);
     return t;
   };
   auto claim = [&](uint32_t seq) -> int {      // first CTA's producer
-    if (!dyn) return take(seq);
     const int slot = (int)(seq % kTS);
     if (!mbar_wait_acq_cluster(&sempty[slot], ((seq / kTS) & 1) ^ 1, &abort_flag)) return -2;
     int t = atomicAdd(p.sched, 1);
     if (t >= p.total_tiles) t = -1;
     sid[slot] = t;
-    if (CL > 1) {
-      st_shared_cluster_u32(mapa_shared(smem_u32(&sid[slot]), 1), (uint32_t)t);
-      mbar_arrive_cluster(mapa_shared(smem_u32(&sfull[slot]), 1));
-    }
+    st_shared_cluster_u32(mapa_shared(smem_u32(&sid[slot]), 1), (uint32_t)t);
+    mbar_arrive_cluster(mapa_shared(smem_u32(&sfull[slot]), 1));
     mbar_arrive(&sfull[slot]);
     return t;
   };
@@ -420,61 +406,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* b_hi = st + (SPLIT ? 2 * C::kABytes : C::kABytes);
           uint8_t* b_lo = b_hi + C::kBBytes;
           const int k0 = kb * BK;
-          if (PAIR) {
-            // this CTA's 128 rows of A and of B, counted on the first CTA's
-            // barrier; only the first CTA arrives (with both CTAs' bytes), so
-            // the second CTA's copies need no cross-CTA arrive per stage (its
-            // copies cannot complete the phase before that arrive)
-            const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
-            if (crank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::kStageBytes);
-            const int nb = tc.n0 + 128 * (int)crank;
-            tma_load_3d_pair(a_hi, &tm.maps.a_hi[tc.g], fb, k0, m0, tc.b);
-            if (SPLIT) tma_load_3d_pair(a_lo, &tm.maps.a_lo[tc.g], fb, k0, m0, tc.b);
-            if (!G.b_mn_major) {
-              tma_load_3d_pair(b_hi, &tm.maps.b_hi[tc.g], fb, k0, nb, tc.b);
-              if (SPLIT) tma_load_3d_pair(b_lo, &tm.maps.b_lo[tc.g], fb, k0, nb, tc.b);
-            } else {
-#pragma unroll
-              for (int qq = 0; qq < 2; ++qq) {
-                tma_load_3d_pair(b_hi + qq * (64 * BK * 2), &tm.maps.b_hi[tc.g], fb, nb + 64 * qq, k0, tc.b);
-                if (SPLIT)
-                  tma_load_3d_pair(b_lo + qq * (64 * BK * 2), &tm.maps.b_lo[tc.g], fb, nb + 64 * qq, k0, tc.b);
-              }
-            }
-            used[s] = true;
-            last_par[s] = use & 1;
-            continue;
-          }
-          mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-          tma_load_3d(a_hi, &tm.maps.a_hi[tc.g], &full[s], k0, m0, tc.b);
-          if (SPLIT) tma_load_3d(a_lo, &tm.maps.a_lo[tc.g], &full[s], k0, m0, tc.b);
-          if (CL == 1) {
-            if (!G.b_mn_major) {
-              tma_load_3d(b_hi, &tm.maps.b_hi[tc.g], &full[s], k0, tc.n0, tc.b);
-              if (SPLIT) tma_load_3d(b_lo, &tm.maps.b_lo[tc.g], &full[s], k0, tc.n0, tc.b);
-            } else {
-#pragma unroll
-              for (int qq = 0; qq < BN / 64; ++qq) {
-                tma_load_3d(b_hi + qq * (64 * BK * 2), &tm.maps.b_hi[tc.g], &full[s], tc.n0 + 64 * qq, k0, tc.b);
-                if (SPLIT)
-                  tma_load_3d(b_lo + qq * (64 * BK * 2), &tm.maps.b_lo[tc.g], &full[s], tc.n0 + 64 * qq, k0, tc.b);
-              }
-            }
+          // this CTA's 128 rows of A and of B, counted on the first CTA's
+          // barrier; only the first CTA arrives (with both CTAs' bytes), so
+          // the second CTA's copies need no cross-CTA arrive per stage (its
+          // copies cannot complete the phase before that arrive)
+          const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
+          if (crank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::kStageBytes);
+          const int nb = tc.n0 + 128 * (int)crank;
+          tma_load_3d_pair(a_hi, &tm.maps.a_hi[tc.g], fb, k0, m0, tc.b);
+          if (SPLIT) tma_load_3d_pair(a_lo, &tm.maps.a_lo[tc.g], fb, k0, m0, tc.b);
+          if (!G.b_mn_major) {
+            tma_load_3d_pair(b_hi, &tm.maps.b_hi[tc.g], fb, k0, nb, tc.b);
+            if (SPLIT) tma_load_3d_pair(b_lo, &tm.maps.b_lo[tc.g], fb, k0, nb, tc.b);
           } else {
-            // this CTA's half of B (128 of the 256 rows), to both CTAs
-            constexpr uint16_t kAll = (1u << CL) - 1;
-            if (!G.b_mn_major) {
-              const int off = (int)crank * 128 * BK * 2;     // 128 K-major rows of BK bf16
-              tma_load_3d_mc(b_hi + off, &tm.maps.b_hi[tc.g], &full[s], k0, tc.n0 + 128 * (int)crank, tc.b, kAll);
-              if (SPLIT)
-                tma_load_3d_mc(b_lo + off, &tm.maps.b_lo[tc.g], &full[s], k0, tc.n0 + 128 * (int)crank, tc.b, kAll);
-            } else {
 #pragma unroll
-              for (int qq = 2 * (int)crank; qq < 2 * (int)crank + 2; ++qq) {
-                tma_load_3d_mc(b_hi + qq * (64 * BK * 2), &tm.maps.b_hi[tc.g], &full[s], tc.n0 + 64 * qq, k0, tc.b, kAll);
-                if (SPLIT)
-                  tma_load_3d_mc(b_lo + qq * (64 * BK * 2), &tm.maps.b_lo[tc.g], &full[s], tc.n0 + 64 * qq, k0, tc.b, kAll);
-              }
+            for (int qq = 0; qq < 2; ++qq) {
+              tma_load_3d_pair(b_hi + qq * (64 * BK * 2), &tm.maps.b_hi[tc.g], fb, nb + 64 * qq, k0, tc.b);
+              if (SPLIT)
+                tma_load_3d_pair(b_lo + qq * (64 * BK * 2), &tm.maps.b_lo[tc.g], fb, nb + 64 * qq, k0, tc.b);
             }
           }
           used[s] = true;
@@ -483,17 +432,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
       }
       // drain: every issued copy must have landed before the CTA may exit
-      // (pairs: the first CTA's barriers count both CTAs' copies, and the
-      // second CTA stays until the closing cluster barrier)
-      if (!PAIR || crank == 0)
+      // (the first CTA's barriers count both CTAs' copies, and the second
+      // CTA stays until the closing cluster barrier)
+      if (crank == 0)
         for (int s = 0; s < C::kStages; ++s)
           if (used[s]) mbar_wait(&full[s], last_par[s], nullptr);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && (!PAIR || crank == 0)) {
-      constexpr uint32_t idesc_k = make_idesc_bf16(PAIR ? 2 * BM : BM, BN, 0, 0);
-      constexpr uint32_t idesc_mn = make_idesc_bf16(PAIR ? 2 * BM : BM, BN, 0, 1);
+    if (lane == 0 && crank == 0) {
+      constexpr uint32_t idesc_k = make_idesc_bf16(2 * BM, BN, 0, 0);
+      constexpr uint32_t idesc_mn = make_idesc_bf16(2 * BM, BN, 0, 1);
       uint32_t it = 0, tcount = 0;
       bool issued = false;
       for (uint32_t seq = 0; !abort_flag; ++seq, ++tcount) {
@@ -534,36 +483,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
             if (SPLIT) dal = make_sdesc(a_lo + kk * 32, 16, KL::kSbo, KL::kType);
-            if (PAIR) {
-              tc_mma_pair(d_tmem, dah, dbh, idesc, accum);
-              if (SPLIT) {
-                tc_mma_pair(d_tmem, dah, dbl, idesc, 1u);
-                tc_mma_pair(d_tmem, dal, dbh, idesc, 1u);
-              }
-            } else {
-              tc_mma(d_tmem, dah, dbh, idesc, accum);
-              if (SPLIT) {
-                tc_mma(d_tmem, dah, dbl, idesc, 1u);
-                tc_mma(d_tmem, dal, dbh, idesc, 1u);
-              }
+            tc_mma_pair(d_tmem, dah, dbh, idesc, accum);
+            if (SPLIT) {
+              tc_mma_pair(d_tmem, dah, dbl, idesc, 1u);
+              tc_mma_pair(d_tmem, dal, dbh, idesc, 1u);
             }
           }
           issued = true;
-          // stage free once these MMAs have read it (in both CTAs of a cluster:
-          // the peer multicasts into this stage too, or is the other half of
-          // the pair)
-          if (PAIR) tc_commit_pair_mc(&empty[s], 0x3);
-          else if (CL > 1) tc_commit_mc(&empty[s], (1u << CL) - 1);
-          else tc_commit(&empty[s]);
+          // stage free (in both CTAs of the pair) once these MMAs have read it
+          tc_commit_pair_mc(&empty[s], 0x3);
         }
         if (!ok) break;
-        // accumulator ready for the epilogue (of both CTAs of a pair)
-        if (PAIR) tc_commit_pair_mc(&tfull[acc], 0x3);
-        else tc_commit(&tfull[acc]);
+        // accumulator ready for the epilogue of both CTAs
+        tc_commit_pair_mc(&tfull[acc], 0x3);
       }
       if (issued) {                      // all issued MMAs complete before teardown
-        if (PAIR) tc_commit_pair_mc(drain, 0x1);
-        else tc_commit(drain);
+        tc_commit_pair_mc(drain, 0x1);
         mbar_wait(drain, 0, nullptr);
       }
     }
@@ -595,8 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if (PAIR) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));   // the first CTA's MMA
-        else mbar_arrive(&tempty[acc]);
+        mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));   // the first CTA's MMA
       }
     }
     if (lane == 0) bulk_wait0();         // all TMA stores of this warp complete
@@ -604,11 +538,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc_fence_before();
-  if (CL > 1) { __syncwarp(); cluster_sync_all(); } else { __syncthreads(); }
+  __syncwarp();
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    if (PAIR) tmem_dealloc_pair(tmem_base, kTmemCols);
-    else tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
@@ -677,25 +611,19 @@ bool encode_all(const GemmParams& p, TmaArgs& tm, bool split, bool lo, int a_row
   return true;
 }
 
-template <int TERMS, bool LO, int CL, int BK, bool PAIR = false>
-cudaError_t launch_single(const GemmParams& p, cudaStream_t s, char* err, size_t errlen) {
+template <int TERMS, bool LO, int BK>
+cudaError_t launch_pairs(const GemmParams& p, cudaStream_t s, char* err, size_t errlen) {
   TmaArgs tm;
-  // with clusters each CTA's B box is one 128-row half (multicast to both,
-  // or this CTA's half of a pair's B)
-  if (!encode_all(p, tm, TERMS == 3, LO, BM, CL > 1 ? 128 : BN, BK, err, errlen)) return cudaErrorInvalidValue;
-  auto k = ns_gemm_tc_kernel<TERMS, LO, CL, BK, PAIR>;
-  const int smem = Stages<TERMS, BM, PAIR ? 128 : BN, BK>::kSmem;
+  // each CTA's B box is its 128-row half of the pair's 256 B rows
+  if (!encode_all(p, tm, TERMS == 3, LO, BM, 128, BK, err, errlen)) return cudaErrorInvalidValue;
+  auto k = ns_gemm_tc_kernel<TERMS, LO, BK>;
+  const int smem = Stages<TERMS, BM, 128, BK>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  if (CL == 1) {
-    const int grid = p.total_tiles < sm_count() ? p.total_tiles : sm_count();
-    k<<<grid, kThreads, smem, s>>>(p, tm);
-    return cudaGetLastError();
-  }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(kThreads);
@@ -705,108 +633,32 @@ cudaError_t launch_single(const GemmParams& p, cudaStream_t s, char* err, size_t
   cfg.numAttrs = 1;
   static int max_clusters = 0;
   if (max_clusters == 0) {
-    cfg.gridDim = dim3(CL * (sm_count() / CL));
+    cfg.gridDim = dim3(2 * (sm_count() / 2));
     if (cudaOccupancyMaxActiveClusters(&max_clusters, k, &cfg) != cudaSuccess || max_clusters <= 0)
-      max_clusters = sm_count() / CL;
+      max_clusters = sm_count() / 2;
   }
   const int units = p.total_tiles < max_clusters ? p.total_tiles : max_clusters;
-  cfg.gridDim = dim3(CL * units);
+  cfg.gridDim = dim3(2 * units);
   e = cudaLaunchKernelEx(&cfg, k, p, tm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-// Work-unit layout of the tensor-core GEMM: MC_NS_CTA=1 single CTAs,
-// 2 = CTA pairs (cta_group::2), 3 = per-launch choice (default: see
-// cta_mode_for).
-int cta_mode() {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = getenv("MC_NS_CTA");
-    v = e ? atoi(e) : 3;
-    if (v < 1 || v > 3) v = 3;
-  }
-  return v;
-}
-// Per-launch choice (MC_NS_CTA=3, the default): every launch on tcgen05 CTA
-// pairs (MC_NS_PAIR=all, the default; measured fastest on every workload), or
-// with MC_NS_PAIR=none the one-product symmetric phases on single CTAs and
-// everything else on B-multicast clusters of two.
-// k-step of the one-product launches: 64 (128-byte operand rows) by default;
-// MC_NS_BK_FAST=32 takes 64-byte rows and twice the stages.  With one product
-// per k-step, 64-byte rows leave the copy engine issuing more rows per clock
-// than it sustains (measured: the one-product launches take 20-25 % less time
-// with 128-byte rows); the three-product launches keep 32.  The stage count
-// is whatever fits beside the epilogue's 64 KB (Stages): five of 32 KB per CTA
-// of a pair, three of 48 KB per CTA of a multicast cluster or single CTA.
-int fast_bk() {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = getenv("MC_NS_BK_FAST");
-    v = (e && atoi(e) == 32) ? 32 : 64;
-  }
-  return v;
-}
-
-// Launches that run on tcgen05 CTA pairs (MC_NS_PAIR): "none", "fast" (the
-// one-product launches) or "all" (default).  MC_NS_CTA=2 puts every launch on
-// pairs whatever MC_NS_PAIR says.
-int pair_policy() {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = getenv("MC_NS_PAIR");
-    v = 2;
-    if (e && strcmp(e, "none") == 0) v = 0;
-    if (e && strcmp(e, "fast") == 0) v = 1;
-  }
-  return v;
-}
-
-int cta_mode_for(bool symmetric, int terms) {
-  const int m = cta_mode();
-  if (m != 3) return m;
-  const int pp = pair_policy();
-  if (pp == 2 || (pp == 1 && terms == 1)) return 2;
-  if (symmetric && terms == 1) return 1;
-  return 3;
-}
-
 }  // namespace
 
-bool ns_dynamic_schedule() {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = getenv("MC_NS_SCHED");
-    v = (e && strcmp(e, "static") == 0) ? 0 : 1;
-  }
-  return v == 1;
-}
-
+// One layout: CTA pairs.  Three-product launches take k-steps of 32 (64-byte
+// swizzled operand rows); one-product launches take 64 (128-byte rows): with
+// one product per k-step, 64-byte rows asked the copy engine for more rows
+// per clock than it sustains (measured: 20-38 % longer one-product launches).
 cudaError_t launch_ns_gemm_tc(const GemmParams& p, cudaStream_t s, char* err, size_t errlen) {
   if (p.total_tiles <= 0) return cudaSuccess;
+  if (!p.sched) {
+    snprintf(err, errlen, "tensor-core GEMM launched without a tile counter");
+    return cudaErrorInvalidValue;
+  }
   const bool lo = p.xmode == kXSplit;
-  const bool three = lo && p.terms == 3;
-  const int mode = cta_mode_for(p.g[0].symmetric != 0, p.terms);
-  // one-product launches may take k-steps of 64 (128-byte rows)
-  const bool bk64 = !three && fast_bk() == 64;
-  if (mode == 2) {
-    if (three) return launch_single<3, true, 2, 32, true>(p, s, err, errlen);
-    if (bk64) return lo ? launch_single<1, true, 2, 64, true>(p, s, err, errlen) : launch_single<1, false, 2, 64, true>(p, s, err, errlen);
-    return lo ? launch_single<1, true, 2, 32, true>(p, s, err, errlen) : launch_single<1, false, 2, 32, true>(p, s, err, errlen);
-  }
-  if (mode == 3) {
-    if (three) return launch_single<3, true, 2, 32>(p, s, err, errlen);
-    if (bk64) return lo ? launch_single<1, true, 2, 64>(p, s, err, errlen) : launch_single<1, false, 2, 64>(p, s, err, errlen);
-    return lo ? launch_single<1, true, 2, 32>(p, s, err, errlen) : launch_single<1, false, 2, 32>(p, s, err, errlen);
-  }
-  if (three) return launch_single<3, true, 1, 32>(p, s, err, errlen);
-  if (bk64) return lo ? launch_single<1, true, 1, 64>(p, s, err, errlen) : launch_single<1, false, 1, 64>(p, s, err, errlen);
-  return lo ? launch_single<1, true, 1, 32>(p, s, err, errlen) : launch_single<1, false, 1, 32>(p, s, err, errlen);
-}
-
-void ns_tc_tile_shape(bool symmetric, int terms, int* bm, int* bn, int* sym_rows_per_col_block) {
-  if (cta_mode_for(symmetric, terms) != 1) { *bm = 256; *bn = 256; *sym_rows_per_col_block = 1; }
-  else { *bm = 128; *bn = 256; *sym_rows_per_col_block = 2; }
+  if (lo && p.terms == 3) return launch_pairs<3, true, 32>(p, s, err, errlen);
+  return lo ? launch_pairs<1, true, 64>(p, s, err, errlen) : launch_pairs<1, false, 64>(p, s, err, errlen);
 }
 
 }  // namespace mc
