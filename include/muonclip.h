@@ -228,8 +228,10 @@ mc_status muon_newton_schulz(const mc_mat* M, mc_mat* O, int32_t count, const mc
  *   - Requests whose workspace (mc_workspace_size) exceeds that size return
  *     MC_ERR_WORKSPACE with a message; use muon_newton_schulz for them.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and keeps it; make
+ *     that first call before any stream capture.  The kept address is not
+ *     looked up again: after cudaDeviceReset in this process the array may
+ *     live elsewhere, so do not use this entry point after a device reset.
  *   - Every call shares the one array.  Nothing in it needs to start at zero
  *     (each value a kernel reads was written earlier in the same call), but
  *     calls that overlap on the GPU (different streams, or several host

@@ -34,7 +34,9 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
 
-// Device address of the scratch on the current device (set-up on first use).
+// Device address of the scratch on the current device (set-up on first use,
+// then kept: a cudaDeviceReset would invalidate it, which the header rules
+// out for callers of this entry point).
 mc_status scratch_address(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);

@@ -4,7 +4,10 @@ memory, a loop that cannot afford cudaFree's device-wide synchronisation, a
 plugin without an allocator).  Its scratch is a fixed array inside the
 library, so these tests check that two calls in a row, each reusing whatever
 the previous call left in that array, give the same results as the
-workspace entry point.  This file is collected last on purpose."""
+workspace entry point, bit for bit: both run the same kernels on the same
+plan, so any difference would be a stale read of the shared array.  The
+larger call goes first, so the second runs over its leftovers.  This file is
+collected last on purpose."""
 import ctypes
 
 import numpy as np
@@ -30,10 +33,6 @@ def noalloc(lib, M, O, hp, status=None):
     abi.check(rc, "muon_newton_schulz_noalloc")
 
 
-def rms(x):
-    return float(torch.sqrt(torch.mean(x.double() ** 2)))
-
-
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_entry_point_on_two_calls(lib):
     assert torch.cuda.is_available()
@@ -53,8 +52,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(lib):
         assert st.item() == 0
         for a, b in zip(O_na, O_ws):
             assert torch.isfinite(a).all()
-            # the tolerance the Newton-Schulz parity tests use (2e-2 of the RMS)
-            assert float((a.double() - b.double()).abs().max()) <= 2e-2 * rms(b)
+            assert torch.equal(a, b)
 
 
 def test_noalloc_rejects_oversize_before_any_launch(lib):
