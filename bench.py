@@ -1,13 +1,19 @@
 """Benchmark of one MuonClip step on GB300 (prints one JSON line on rank 0).
 
-Workload (dense_block): one dense transformer block, d_model 2048, 16 heads x
-128, FFN 2048 -> 5632 -> 2048; bf16 weights, fp32 momentum and gradients;
-attention features of a batch of 4 x 4096 tokens; 3 heads pre-scaled past
-tau = 100.  One step = qk_max_logit on the layer's Q/K (the S_max the forward
-records) + muonclip_step over all 7 matrices (momentum, Newton-Schulz x5,
-RMS-matched update with weight decay, per-head QK-Clip).
+Default workload (moe_experts): the Muon half of MuonClip over one MoE expert
+batch shaped like Kimi K2's experts, 64 matrices of 2048 x 7168 (up/gate) and
+64 of 7168 x 2048 (down), bf16 weights, fp32 momentum and gradients (gradient
+scale log-uniform in [0.1, 10] per expert).  One step = muonclip_step over
+all 128 matrices (momentum, Newton-Schulz x5, RMS-matched update with weight
+decay).  The expert batch has no attention, so the per-head max logit, the
+attention forward with S_max fused in and QK-Clip are measured on the K2 MLA
+layer at 32768 tokens (64 heads, q.k 128 + 64 with a shared rotary key,
+8 heads with a heavy-tailed max logit) and reported under `components`.
+Workloads with attention (--workload dense_block, k2_mla_layer, long_mla,
+tiny_mha_fp32) put qk_max_logit and the clip inside the step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                  [--workload NAME]
 
 --impl reference times the CPU oracle (fp64 numpy) on a bounded sample of the
 same workload on the host cores, scaled to the full step.
@@ -28,7 +34,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MuonClip step ms per layer; NS & max-logit TFLOP/s (% BF16 peak); clip GB/s"
-WORKLOAD = "dense_block"
+WORKLOAD = "moe_experts"
+ATTN_WORKLOAD = "long_mla"        # attention components for workloads without attention
 WORKLOAD_CONFIG = {
     "tiny_mha_fp32": {"matrices": "1x256x512 (fp32)", "attention": "B2 S128 H4 d64 causal (fp32)"},
     "dense_block": {"matrices": "4x2048x2048, 2x5632x2048, 1x2048x5632",
@@ -67,37 +74,62 @@ def cpu_cores():
 
 
 # ------------------------------------------------------------------ CPU oracle sample
-def oracle_sample(seed=0, heads=1):
-    """Time the oracle on a bounded sample of the dense_block step and scale
-    it to the full step: Newton-Schulz on one 2048x2048 and one 2048x5632
-    matrix (momentum, NS, update) and the max logit of `heads` head(s) over the
-    4 x 4096 batch.  Returns (ms per full step, description)."""
+# Per workload: the Muon matrices the oracle steps (momentum, Newton-Schulz,
+# update), and how many of the attention heads it takes the max logit of.
+# The time is scaled to the full step by Newton-Schulz flops and by heads.
+ORACLE_SAMPLE = {
+    "tiny_mha_fp32": {"mats": [(256, 512)], "heads": 4},
+    "dense_block": {"mats": [(2048, 2048), (5632, 2048)], "heads": 1},
+    "k2_mla_layer": {"mats": [(1536, 7168), (64, 7168)], "heads": 4},
+    "moe_experts": {"mats": [(2048, 7168), (7168, 2048)], "heads": 0},
+    "long_mla": {"mats": [(1536, 7168), (64, 7168)], "heads": 4},
+}
+
+
+def oracle_sample(workload, seed=0, small=False):
+    """Time the oracle on a bounded sample of `workload`'s step and scale it
+    to the full step.  small: one matrix (alternating with the seed) and one
+    head, for the reference arm's per-step samples.  Returns (ms per full
+    step, description)."""
     import numpy as np
 
     import oracle as O
     from muon_qk_clip_gb300 import synth
-    wl = synth.workload(WORKLOAD)
+    wl = synth.workload(workload)
+    plan = ORACLE_SAMPLE[workload]
+    mats = plan["mats"]
+    heads = plan["heads"]
+    if small:
+        mats = [mats[seed % len(mats)]]
+        heads = min(heads, 1)
     rng = np.random.default_rng(seed)
     hp = O.Hparams()
     t0 = time.perf_counter()
     sample_flops = 0.0
-    for (r, c) in ((2048, 2048), (5632, 2048)):
-        W = rng.standard_normal((r, c)) * 0.02
-        G = rng.standard_normal((r, c)) * 1e-3
+    for (r, c) in mats:
+        W = rng.standard_normal((r, c)) * wl.w_std
+        G = rng.standard_normal((r, c)) * wl.g_std
         O.muon_step(W, G, np.zeros((r, c)), hp)
         sample_flops += synth.flops_ns(r, c)
     t_ns = time.perf_counter() - t0
     full_ns = sum(synth.flops_ns(m.rows, m.cols) for m in wl.matrices)
+    ms = 1e3 * t_ns * full_ns / sample_flops
+    shapes = " + ".join(f"{r}x{c}" for r, c in mats)
+    desc = (f"extrapolated: oracle (fp64 numpy) Muon step of {shapes} ({t_ns:.1f} s), scaled by "
+            f"Newton-Schulz flops x{full_ns / sample_flops:.1f} to all {len(wl.matrices)} matrices")
     att = wl.attention
-    q = rng.standard_normal((att.B, att.S, heads, att.d_head))
-    k = rng.standard_normal((att.B, att.S, heads, att.d_head))
-    t1 = time.perf_counter()
-    O.max_logit(q, k)
-    t_ml = time.perf_counter() - t1
-    ms = 1e3 * (t_ns * full_ns / sample_flops + t_ml * att.H / heads)
-    desc = (f"oracle (fp64 numpy) on a sample: Muon step of one 2048x2048 and one 5632x2048 "
-            f"matrix ({t_ns:.1f} s, scaled by NS flops x{full_ns / sample_flops:.2f}) + max logit "
-            f"of {heads} of {att.H} heads over 4x4096 tokens ({t_ml:.1f} s, scaled x{att.H // heads})")
+    if att is not None and heads > 0:
+        dq = att.d_head if att.kind == "mha" else att.d_nope + att.d_rope
+        dk = att.d_head if att.kind == "mha" else att.d_nope
+        q = rng.standard_normal((att.B, att.S, heads, dq))
+        k = rng.standard_normal((att.B, att.S, heads, dk))
+        ks = rng.standard_normal((att.B, att.S, att.d_rope)) if att.kind == "mla" else None
+        t1 = time.perf_counter()
+        O.max_logit(q, k, ks)
+        t_ml = time.perf_counter() - t1
+        ms += 1e3 * t_ml * att.H / heads
+        desc += (f"; + max logit of {heads} of {att.H} heads over {att.B}x{att.S} tokens "
+                 f"({t_ml:.1f} s, scaled x{att.H / heads:g})")
     return ms, desc
 
 
@@ -105,21 +137,21 @@ def reference_arm(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    for _ in range(args.warmup):
-        oracle_sample(heads=1)
+    for i in range(args.warmup):
+        oracle_sample(args.workload, seed=i, small=True)
     vals = []
     desc = ""
-    for _ in range(args.steps):
-        v, desc = oracle_sample(heads=1)
+    for i in range(args.steps):
+        v, desc = oracle_sample(args.workload, seed=i, small=True)
         vals.append(v)
     value = statistics.mean(vals)
     cores = cpu_cores()
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "ms",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": value,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD},
+            "data": "synthetic", "config": {"workload": args.workload, **WORKLOAD_CONFIG[args.workload]},
             "cpu_baseline": {"value": value, "unit": "ms", "cores": cores, "kind": "oracle",
-                             "sample": desc},
+                             "sample": "each step: " + desc},
             "e2e": {"value": value, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -230,20 +262,180 @@ def ns_flops_executed(rows, cols, steps, fast_steps, split=True, symmetric=True)
                for prod in ns_products(rows, cols, steps, fast_steps, split))
 
 
-def traffic_for(kernel_src, launches_per_call):
+# Sources that decide the Newton-Schulz GEMM's DRAM traffic: the kernel and
+# the planner that picks each launch's products and shapes.
+TRAFFIC_SOURCES = ("muon_qk_clip_gb300/csrc/ns_tc.cu", "muon_qk_clip_gb300/csrc/common.cuh",
+                   "muon_qk_clip_gb300/csrc/api.cpp")
+
+
+def traffic_sources_hash():
+    h = hashlib.sha256()
+    for rel in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(workload, launches_per_call):
     """DRAM bytes per launch of the dominant kernel: the committed ncu total
-    per Newton-Schulz call divided by this run's launches per call, or None
-    when the kernel source changed since the capture."""
+    per Newton-Schulz call on this workload divided by this run's launches per
+    call, or None when no capture exists for the workload or a source that
+    decides the traffic changed since it was taken."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p) or not launches_per_call:
         return None
-    d = json.load(open(p)).get("ns_gemm")
-    if not d:
-        return None
-    h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
-    if d.get("source_sha256_16") != h:
+    d = json.load(open(p)).get("ns_gemm", {}).get(workload)
+    if not d or d.get("source_sha256_16") != traffic_sources_hash():
         return None
     return int(d["bytes_per_ns_call"] / launches_per_call)
+
+
+def attention_setup(wname, seed, dev, hp, mc, forward, synth, W=None):
+    """Q/K (and V) features of `wname`'s attention layer from its weights
+    (untimed setup forward), and the layer's clip segments on the weights in
+    W (the step's own weights) or on the setup weights."""
+    wl = synth.workload(wname)
+    att = wl.attention
+    X, Wa = synth.attention_inputs(wl, seed=seed, device=dev)
+    W = W if W is not None else Wa
+    if att.kind == "mha":
+        q, k = forward.project_mha(X, Wa["Wq"], Wa["Wk"], att.H)
+        q, k = q.contiguous(), k.contiguous()
+        Wv = W["Wv"] if "Wv" in W else Wa.get("Wv", Wa["Wq"])
+        v, _ = forward.project_mha(X, Wv, Wv, att.H)
+        v = v.contiguous()
+        Wq = W["Wq"] if "Wq" in W else Wa["Wq"]
+        Wk = W["Wk"] if "Wk" in W else Wa["Wk"]
+        segs = mc.mha_segments(Wq, Wk, att.H, hp.alpha)
+        ks = None
+    else:
+        q, kc, ks, v = forward.project_mla(X, Wa, att.H, att.d_nope, att.d_rope, att.d_v, with_v=True)
+        q, ks = q.contiguous(), ks.contiguous()
+        k = kc                                          # strided views of [k^C || v]
+        segs = mc.mla_segments(W["W_UQ"], W["W_UKV"], att.H, att.d_nope, att.d_rope, att.d_v)
+    del X
+    return {"wl": wl, "att": att, "q": q, "k": k, "ks": ks, "v": v, "segs": segs,
+            "weights": Wa}
+
+
+def attention_components(A, args, hp, mc, dev, stream, flush, barrier, peak_t, hbm):
+    """The attention-side figures on layer A: qk_max_logit, the attention
+    forward with S_max fused in, the clip of the layer's offending heads and
+    an all-heads clip stress (L2 flushed before each timed call)."""
+    import torch
+    att, q, k, ks, v, segs = A["att"], A["q"], A["k"], A["ks"], A["v"], A["segs"]
+    H = att.H
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    smax = torch.zeros(H, dtype=torch.float32, device=dev)
+    d_qk = q.shape[-1]
+    out = {"workload": A["wl"].name, "attention": WORKLOAD_CONFIG[A["wl"].name]["attention"]}
+
+    def timed(fn, n, spin=False):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in evs:
+            flush.zero_()
+            if spin:
+                # a ~50 us device spin keeps the stream busy while the host
+                # builds the call, so the interval holds the launch, not the host
+                torch.cuda._sleep(100_000)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        barrier()
+        return sorted(a.elapsed_time(b) for a, b in evs)
+
+    # max logit
+    ml = lambda: mc.qk_max_logit(q, k, ks, smax=smax, status=status, stream=stream)  # noqa: E731
+    for _ in range(2):
+        ml()
+    barrier()
+    t = timed(ml, args.steps)
+    ml_ms = statistics.median(t)
+    ml_flops = synth_flops_max_logit(att, d_qk)
+    out["max_logit"] = {"ms": round(ml_ms, 4), "tflops": round(ml_flops / (ml_ms * 1e-3) / 1e12, 2),
+                        "frac_bf16_peak": round(ml_flops / (ml_ms * 1e-3) / 1e12 / peak_t, 4),
+                        "algorithmic_flops": ml_flops}
+    # attention forward with S_max fused in
+    if q.dtype == torch.bfloat16:
+        o_buf = torch.empty(v.shape, dtype=v.dtype, device=dev)
+        smax_f = torch.empty(H, dtype=torch.float32, device=dev)
+        fw = lambda: mc.qk_attention_forward(q, k, v, ks, out=o_buf, smax=smax_f, status=status,  # noqa: E731
+                                             stream=stream)
+        for _ in range(2):
+            fw()
+        barrier()
+        t = timed(fw, args.steps)
+        fwd_ms = statistics.median(t)
+        fwd_flops = 2.0 * (d_qk + v.shape[-1]) * att.B * att.H * att.S * (att.S + 1) / 2
+        out["attn_fwd_fused_smax"] = {
+            "ms": round(fwd_ms, 4), "tflops": round(fwd_flops / (fwd_ms * 1e-3) / 1e12, 2),
+            "frac_bf16_peak": round(fwd_flops / (fwd_ms * 1e-3) / 1e12 / peak_t, 4),
+            "algorithmic_flops": fwd_flops,
+            "smax_equals_max_logit": bool(torch.equal(smax_f, smax))}
+        del o_buf
+    # the clip of this layer's offending heads with the measured S_max (on
+    # copies of the weights, restored before each call)
+    copies = {}
+    for sg in segs:
+        copies.setdefault(sg.w.data_ptr(), (sg.w, sg.w.clone()))
+    csegs = [mc.ClipSegment(copies[sg.w.data_ptr()][1], sg.offset, sg.stride, sg.rows, sg.exponent)
+             for sg in segs]
+    gamma = torch.zeros(H, dtype=torch.float32, device=dev)
+    ncl = torch.zeros(1, dtype=torch.int32, device=dev)
+    mc.qk_clip_apply(smax, hp.tau, csegs, gamma_out=gamma, nclipped=ncl, status=status, stream=stream)
+    barrier()
+    n_clipped = int(ncl.item())
+    t = timed(lambda: mc.qk_clip_apply(smax, hp.tau, csegs, stream=stream), args.steps, spin=True)
+    clip_ms = statistics.median(t)
+    esz = q.element_size()
+    per_head_rows = 2 * att.d_head if att.kind == "mha" else att.d_nope + att.d_rope + att.d_nope
+    row_len = max(sg.w.shape[1] for sg in segs)
+    clip_bytes = 2 * n_clipped * per_head_rows * row_len * esz          # read + write
+    out["clip_layer"] = {"heads_clipped": n_clipped, "bytes": clip_bytes, "us": round(clip_ms * 1e3, 2),
+                         "gbs": round(clip_bytes / (clip_ms * 1e-3) / 1e9, 1)}
+    # every head over tau
+    s_all = torch.full((H,), 4.0 * hp.tau, dtype=torch.float32, device=dev)
+    stress_bytes = sum(2 * H * sg.rows * sg.w.shape[1] * sg.w.element_size() for sg in csegs)
+    mc.qk_clip_apply(s_all, hp.tau, csegs, stream=stream)
+    barrier()
+    t = timed(lambda: mc.qk_clip_apply(s_all, hp.tau, csegs, stream=stream), args.steps, spin=True)
+    cms = statistics.median(t)
+    out["clip_stress_all_heads"] = {"heads_clipped": H, "bytes": stress_bytes, "ms": round(cms, 4),
+                                    "gbs": round(stress_bytes / (cms * 1e-3) / 1e9, 1),
+                                    "frac_hbm": round(stress_bytes / (cms * 1e-3) / 1e9 / hbm, 4)}
+    out["smax_head_max"] = round(float(smax.max().item()), 3)
+    out["device_status"] = int(status.item())
+    del copies, csegs
+    return out
+
+
+def synth_flops_max_logit(att, d_qk):
+    from muon_qk_clip_gb300 import synth
+    return synth.flops_max_logit(att.B, att.S, att.H, d_qk)
+
+
+def clip_stress_large(mc, hp, dev, stream, barrier, hbm):
+    """The clip where HBM bandwidth, not launch latency, decides: 64 heads of
+    8192 x 1024 bf16 rows (1 GiB), every head over tau."""
+    import torch
+    Hs, rows, cols = 64, 8192, 1024
+    Wbig = torch.ones(Hs * rows, cols, dtype=torch.bfloat16, device=dev)
+    segs_l = [mc.ClipSegment(Wbig, 0, rows, rows, 0.5)]
+    s_l = torch.full((Hs,), 4.0 * hp.tau, dtype=torch.float32, device=dev)
+    mc.qk_clip_apply(s_l, hp.tau, segs_l, stream=stream)
+    barrier()
+    ev_l = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(5)]
+    for a, b in ev_l:
+        torch.cuda._sleep(100_000)
+        a.record(stream)
+        mc.qk_clip_apply(s_l, hp.tau, segs_l, stream=stream)
+        b.record(stream)
+    barrier()
+    ms_l = statistics.median(a.elapsed_time(b) for a, b in ev_l)
+    nbytes = 2 * Wbig.numel() * Wbig.element_size()          # read + write
+    del Wbig
+    return {"heads_clipped": Hs, "bytes": nbytes, "ms": round(ms_l, 4),
+            "gbs": round(nbytes / (ms_l * 1e-3) / 1e9, 1), "frac_hbm": round(nbytes / (ms_l * 1e-3) / 1e9 / hbm, 4)}
 
 
 def gpu_arm(args):
@@ -268,26 +460,11 @@ def gpu_arm(args):
     names = [m.name for m in wl.matrices]
     Wl, Gl, Ml = [W[n] for n in names], [G[n] for n in names], [M[n] for n in names]
     hp = mc.Hparams()
-    q = k = ks = v = None
+    A = attention_setup(args.workload, seed, dev, hp, mc, forward, synth, W) if att is not None else None
+    q = k = ks = None
     segs = []
-    if att is not None:                                 # setup forward (untimed)
-        X, Wa = synth.attention_inputs(wl, seed=seed, device=dev)
-        if att.kind == "mha":
-            q, k = forward.project_mha(X, Wa["Wq"], Wa["Wk"], att.H)
-            q, k = q.contiguous(), k.contiguous()
-            Wv = W["Wv"] if "Wv" in W else Wa["Wv"]
-            v, _ = forward.project_mha(X, Wv, Wv, att.H)
-            v = v.contiguous()
-            Wq = W["Wq"] if "Wq" in W else Wa["Wq"]
-            Wk = W["Wk"] if "Wk" in W else Wa["Wk"]
-            segs = mc.mha_segments(Wq, Wk, att.H, hp.alpha)
-        else:
-            q, kc, ks, v = forward.project_mla(X, Wa, att.H, att.d_nope, att.d_rope, att.d_v,
-                                               with_v=True)
-            q, ks = q.contiguous(), ks.contiguous()
-            k = kc                                      # strided views of [k^C || v]
-            segs = mc.mla_segments(W["W_UQ"], W["W_UKV"], att.H, att.d_nope, att.d_rope, att.d_v)
-        del X
+    if A is not None:
+        q, k, ks, segs = A["q"], A["k"], A["ks"], A["segs"]
     ws = mc.alloc_workspace(Wl, hp, dev)
     H = att.H if att is not None else 1
     smax = torch.zeros(H, dtype=torch.float32, device=dev)
@@ -338,85 +515,7 @@ def gpu_arm(args):
         t_local = float(t.item())
     ms_per_step = t_local / args.steps
     stat = int(status.item())
-
-    # ---- the attention forward with S_max fused in (its production placement;
-    # timed apart from the step, L2 flushed before each launch)
-    attn_fwd = None
-    if att is not None and q.dtype == torch.bfloat16:
-        o_buf = torch.empty(v.shape, dtype=v.dtype, device=dev)
-        smax_f = torch.empty(H, dtype=torch.float32, device=dev)
-        for _ in range(2):
-            mc.qk_attention_forward(q, k, v, ks, out=o_buf, smax=smax_f, status=status, stream=stream)
-        barrier()
-        mc.profiler_enable(True)
-        mc.profiler_read(reset=True)
-        for _ in range(args.steps):
-            flush.zero_()
-            mc.qk_attention_forward(q, k, v, ks, out=o_buf, smax=smax_f, status=status, stream=stream)
-        barrier()
-        pf = mc.profiler_read(reset=True).get("attn_fwd", (0, 0.0))
-        mc.profiler_enable(False)
-        d_qk = q.shape[-1]
-        fwd_flops = 2.0 * (d_qk + v.shape[-1]) * att.B * att.H * att.S * (att.S + 1) / 2
-        fwd_ms = pf[1] / args.steps
-        attn_fwd = {"ms": round(fwd_ms, 4),
-                    "tflops": round(fwd_flops / (fwd_ms * 1e-3) / 1e12, 2) if fwd_ms else None,
-                    "algorithmic_flops": fwd_flops,
-                    "smax_equals_max_logit": bool(torch.allclose(smax_f, smax, rtol=1e-6, atol=0.0)),
-                    "launches_per_call": pf[0] // args.steps}
-
-    # ---- HBM-streaming stress of the clip: every head over tau, on copies of the
-    # layer's Q/K weights (L2 flushed before each call; one launch per call)
-    clip_stress = None
-    if att is not None:
-        copies = {}
-        for sg in segs:
-            copies.setdefault(sg.w.data_ptr(), sg.w.clone())
-        ssegs = [mc.ClipSegment(copies[sg.w.data_ptr()], sg.offset, sg.stride, sg.rows, sg.exponent)
-                 for sg in segs]
-        s_all = torch.full((H,), 4.0 * hp.tau, dtype=torch.float32, device=dev)
-        stress_bytes = sum(2 * H * sg.rows * sg.w.shape[1] * sg.w.element_size() for sg in ssegs)
-        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        mc.qk_clip_apply(s_all, hp.tau, ssegs, stream=stream)
-        barrier()
-        for i in range(args.steps):
-            flush.zero_()
-            # a ~50 us device spin keeps the stream busy while the host builds
-            # the call, so the interval holds the launch and not the host
-            torch.cuda._sleep(100_000)
-            cev[i][0].record(stream)
-            mc.qk_clip_apply(s_all, hp.tau, ssegs, stream=stream)
-            cev[i][1].record(stream)
-        barrier()
-        cms = sum(a.elapsed_time(b) for a, b in cev) / args.steps
-        clip_stress = {"heads_clipped": H, "bytes": stress_bytes, "ms": round(cms, 4),
-                       "gbs": round(stress_bytes / (cms * 1e-3) / 1e9, 1)}
-        del copies, ssegs
-
-    # ---- the clip at a size where HBM bandwidth, not launch latency, decides:
-    # 64 heads of 8192 x 1024 bf16 rows (1 GiB), every head over tau
-    def clip_stress_large():
-        Hs, rows, cols = 64, 8192, 1024
-        Wbig = torch.ones(Hs * rows, cols, dtype=torch.bfloat16, device=dev)
-        segs_l = [mc.ClipSegment(Wbig, 0, rows, rows, 0.5)]
-        s_l = torch.full((Hs,), 4.0 * hp.tau, dtype=torch.float32, device=dev)
-        mc.qk_clip_apply(s_l, hp.tau, segs_l, stream=stream)
-        barrier()
-        ev_l = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(5)]
-        for a, b in ev_l:
-            torch.cuda._sleep(100_000)
-            a.record(stream)
-            mc.qk_clip_apply(s_l, hp.tau, segs_l, stream=stream)
-            b.record(stream)
-        barrier()
-        ms_l = sum(a.elapsed_time(b) for a, b in ev_l) / len(ev_l)
-        nbytes = 2 * Wbig.numel() * Wbig.element_size()          # read + write
-        del Wbig
-        return {"heads_clipped": Hs, "bytes": nbytes, "ms": round(ms_l, 4),
-                "gbs": round(nbytes / (ms_l * 1e-3) / 1e9, 1)}
-    clip_large = clip_stress_large()
+    n_clipped_step = int(ncl.item()) if att is not None else 0
 
     # ---- end to end through the public API: pinned host G (and Q, K) in, metrics out.
     # The inputs are double-buffered on the device: step i+1's host-to-device
@@ -428,10 +527,10 @@ def gpu_arm(args):
     Gh = [g.to("cpu").pin_memory() for g in Gl]
     feats = [t for t in (q, k, ks) if t is not None]
     fh = [t.to("cpu").pin_memory() for t in feats]
-    out_h = torch.empty(2 * H + 1, dtype=torch.float32).pin_memory()
+    out_h = torch.empty(2 * H + 2, dtype=torch.float32).pin_memory()
     h2d = sum(g.numel() * g.element_size() for g in Gh) + sum(t.numel() * t.element_size() for t in fh)
     d2h = out_h.numel() * 4
-    res = torch.empty(2 * H + 1, dtype=torch.float32, device=dev)
+    res = torch.empty(2 * H + 2, dtype=torch.float32, device=dev)
     G_slots = [Gl, [torch.empty_like(g) for g in Gl]]
     F_slots = [feats, [torch.empty_strided(t.size(), t.stride(), dtype=t.dtype, device=dev) for t in feats]]
     copy_stream = torch.cuda.Stream(device=dev)
@@ -464,9 +563,11 @@ def gpu_arm(args):
                          stream=stream)
         consumed[slot].record(stream)
         used[slot] = True
+        # the step's result: S_max, gamma, heads clipped and the status word
         res[:H].copy_(smax)
         res[H:2 * H].copy_(gamma)
-        res[2 * H:].copy_(ncl.float())
+        res[2 * H:2 * H + 1].copy_(ncl.float())
+        res[2 * H + 1:].copy_(status.float())
         out_h.copy_(res, non_blocking=True)
 
     def e2e_run(n):
@@ -493,6 +594,24 @@ def gpu_arm(args):
         t = torch.tensor([e2e_local], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_local = float(t.item())
+    del Gh, fh, G_slots, F_slots
+
+    pk, pk_src = peaks()
+    peak_t = pk["bf16_tflops"]
+    hbm = pk.get("hbm_gbs") or 6764.0
+
+    # ---- attention-side components: this workload's layer, or for a
+    # workload without attention the 32768-token K2 MLA layer
+    comp_att = None
+    if rank == 0 and not args.no_components:
+        if A is None:
+            A2 = attention_setup(ATTN_WORKLOAD, seed, dev, hp, mc, forward, synth)
+            comp_att = attention_components(A2, args, hp, mc, dev, stream, flush, barrier, peak_t, hbm)
+            del A2
+        else:
+            comp_att = attention_components(A, args, hp, mc, dev, stream, flush, barrier, peak_t, hbm)
+        torch.cuda.empty_cache()
+    clip_large = clip_stress_large(mc, hp, dev, stream, barrier, hbm) if rank == 0 and not args.no_components else None
 
     # ---- algorithmic work
     tc_path = wl.dtype == torch.bfloat16
@@ -507,12 +626,10 @@ def gpu_arm(args):
         d_qk = att.d_head if att.kind == "mha" else att.d_nope + att.d_rope
         ml_flops = synth.flops_max_logit(att.B, att.S, att.H, d_qk)
         esz = 2 if wl.dtype == torch.bfloat16 else 4
-        clipped_heads = len(att.scaled_heads)
         per_head_rows = (2 * att.d_head if att.kind == "mha"
                          else att.d_nope + att.d_rope + att.d_nope)
         row_len = {s_.w.shape[1] for s_ in segs}
-        clip_bytes = 2 * clipped_heads * per_head_rows * max(row_len) * esz   # read + write
-    pk, pk_src = peaks()
+        clip_bytes = 2 * n_clipped_step * per_head_rows * max(row_len) * esz   # read + write
     n_gemm, t_gemm = prof.get("ns_gemm", (0, 0.0))
     n_ml, t_ml = prof.get("max_logit", (0, 0.0))
     n_clip, t_clip = prof.get("clip", (0, 0.0))
@@ -523,30 +640,23 @@ def gpu_arm(args):
     # and the oriented iterate; apply reads W and the iterate, writes W
     elems = sum(m.rows * m.cols for m in wl.matrices)
     g_b = Gl[0].element_size()
-    x_b = 4                                            # (hi, lo) bf16 planes, or one fp32 plane
+    x_b = 4                                            # (hi, lo) 16-bit planes, or one fp32 plane
     w_b = Wl[0].element_size()
     prep_bytes = elems * (g_b + 8 + x_b)
     apply_bytes = elems * (2 * w_b + x_b)
-    hbm = pk.get("hbm_gbs") or 6764.0
     n_prep, t_prep = prof.get("prep", (0, 0.0))
     n_apply, t_apply = prof.get("apply", (0, 0.0))
     prep_gbs = prep_bytes * args.steps / (t_prep * 1e-3) / 1e9 if t_prep else None
     apply_gbs = apply_bytes * args.steps / (t_apply * 1e-3) / 1e9 if t_apply else None
-    peak_t = pk["bf16_tflops"]
     per_launch_flops = ns_flops / (n_gemm / args.steps) if n_gemm else None
     achieved = per_launch_flops / (t_gemm / n_gemm * 1e-3) / 1e12 if n_gemm else None
     launches = sum(v[0] for v in prof.values())
     cfg = {"workload": args.workload, **WORKLOAD_CONFIG[args.workload], "ns_steps": hp.ns_steps,
-           "ns_precision": ((f"split-bf16 (hi*hi+hi*lo+lo*hi), fp32 accumulate, all {hp.ns_steps} iterations"
-                             if hp.ns_fast_steps == 0 else
-                             f"split-bf16 (hi*hi+hi*lo+lo*hi), fp32 accumulate; hi*hi for the first "
-                             f"{hp.ns_fast_steps} iterations of matrices whose smaller side is >= 1024, "
-                             f"and for the next iteration's Gram product from 2048")
-                            if wl.dtype == torch.bfloat16 else "fp32 CUDA cores"),
+           "ns_precision": ns_precision_text(hp) if tc_path else "fp32 CUDA cores",
            "ns_flops_counted": ("Gram and polynomial: the computed 256x256 units on or above the "
                                 "diagonal (symmetry exploited); update 2 m^2 n; split products not "
                                 "credited" if tc_path else "4 m^2 n + 2 m^3 per iteration"),
-           "clipped_heads": len(att.scaled_heads) if att is not None else 0,
+           "clipped_heads": n_clipped_step,
            "l2": "flushed (512 MB write) before each step; e2e: " + (
                "flushed inside the timed region before each step" if e2e_flush else
                "not flushed, each step's host inputs (G, Q/K) are larger than L2"),
@@ -569,19 +679,17 @@ def gpu_arm(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "roofline": {"bound": "tensor" if tc_path else "alu",
-                     "kernel": ("ns_gemm (tcgen05 split-bf16 Newton-Schulz phase)" if tc_path else
+                     "kernel": ("ns_gemm (tcgen05 Newton-Schulz phase GEMM)" if tc_path else
                                 "ns_gemm (fp32 CUDA-core Newton-Schulz phase)"),
                      "achieved": round(achieved, 2) if achieved else None,
                      "peak": peak_t if tc_path else FP32_ALU_TFLOPS, "unit": "TFLOP/s",
                      "frac": round(achieved / (peak_t if tc_path else FP32_ALU_TFLOPS), 4) if achieved else None,
-                     "peak_source": (f"bf16_tflops {pk_src}" if tc_path else
-                                     "152 SMs x 128 fp32 lanes x 2 flops (FMA) x 2.07 GHz"),
-                     "traffic": traffic_for(os.path.join(ROOT, "muon_qk_clip_gb300", "csrc", "ns_tc.cu"),
-                                            n_gemm // args.steps if n_gemm else 0)
-                     if args.workload == WORKLOAD else None},
+                     "peak_source": (f"bf16_tflops {pk_src} (16-bit dense; fp16 and bf16 share the rate)"
+                                     if tc_path else "152 SMs x 128 fp32 lanes x 2 flops (FMA) x 2.07 GHz"),
+                     "traffic": traffic_for(args.workload, n_gemm // args.steps if n_gemm else 0)},
         "components": {
-            "attn_fwd_fused_smax": dict(attn_fwd, frac_bf16_peak=round(attn_fwd["tflops"] / peak_t, 4))
-            if attn_fwd and attn_fwd.get("tflops") else attn_fwd,
+            "attention": comp_att,
+            "clip_stress_1gib": clip_large,
             "ns_algorithmic_tflops": round(ns_tflops, 2) if ns_tflops else None,
             "ns_frac_bf16_peak": round(ns_tflops / peak_t, 4) if ns_tflops else None,
             "ns_nominal_tflops": round(ns_flops_nominal * args.steps / (t_gemm * 1e-3) / 1e12, 2)
@@ -590,12 +698,9 @@ def gpu_arm(args):
             if t_gemm and tc_path else None,
             "ns_tensor_pipe_frac": round(ns_flops_products * args.steps / (t_gemm * 1e-3) / 1e12 / peak_t, 4)
             if t_gemm and tc_path else None,
-            "max_logit_tflops": round(ml_tflops, 2) if ml_tflops else None,
-            "max_logit_frac_bf16_peak": round(ml_tflops / peak_t, 4) if ml_tflops else None,
-            "clip_gbs": round(clip_gbs, 1) if clip_gbs else None,
-            "clip_stress_1gib": dict(clip_large, frac_hbm=round(clip_large["gbs"] / hbm, 4)),
-            "clip_stress_all_heads": dict(clip_stress, frac_hbm=round(clip_stress["gbs"] / hbm, 4))
-            if clip_stress else None,
+            "max_logit_tflops_in_step": round(ml_tflops, 2) if ml_tflops else None,
+            "max_logit_frac_bf16_peak_in_step": round(ml_tflops / peak_t, 4) if ml_tflops else None,
+            "clip_gbs_in_step": round(clip_gbs, 1) if clip_gbs else None,
             "prep_gbs": round(prep_gbs, 1) if prep_gbs else None,
             "prep_frac_hbm": round(prep_gbs / hbm, 4) if prep_gbs else None,
             "apply_gbs": round(apply_gbs, 1) if apply_gbs else None,
@@ -606,13 +711,21 @@ def gpu_arm(args):
             "wall_s_timed_loop": round(wall, 3), "device_status": stat,
         },
     }
-    if not args.no_cpu_baseline and args.workload == WORKLOAD:
-        v, desc = oracle_sample(heads=1)
+    if not args.no_cpu_baseline:
+        v, desc = oracle_sample(args.workload)
         line["cpu_baseline"] = {"value": round(v, 1), "unit": "ms", "cores": cpu_cores(),
                                 "kind": "oracle", "sample": desc}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def ns_precision_text(hp):
+    if hp.ns_fast_steps == 0:
+        return f"split-bf16 (hi*hi+hi*lo+lo*hi), fp32 accumulate, all {hp.ns_steps} iterations"
+    return (f"split-bf16 (hi*hi+hi*lo+lo*hi), fp32 accumulate; hi*hi for the first "
+            f"{hp.ns_fast_steps} iterations of matrices whose smaller side is >= 1024, "
+            f"and for the next iteration's Gram product from 2048")
 
 
 def main():
@@ -622,8 +735,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-components", action="store_true",
+                    help="skip the attention-side and clip-stress figures")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(WORKLOAD_CONFIG),
-                    help="dense_block is the reported workload; the others for exploration")
+                    help="moe_experts (the K2 expert batch) is the reported workload")
     args = ap.parse_args()
     if args.impl == "reference":
         reference_arm(args)

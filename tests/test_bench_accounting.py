@@ -70,21 +70,39 @@ def test_executed_flops_weight_each_phase_by_its_products(bench):
 
 def test_traffic_is_taken_only_for_the_profiled_source(bench, tmp_path, monkeypatch):
     """The roofline's DRAM traffic comes from the committed ncu total per
-    Newton-Schulz call, divided by this run's launches per call, and only while
-    the kernel source still has the hash the capture was taken with."""
-    import hashlib
+    Newton-Schulz call on the same workload, divided by this run's launches
+    per call, and only while every source that decides the traffic (the
+    kernel, its helpers and the planner) still hashes as when it was taken."""
     import json
-    src = tmp_path / "kernel.cu"
-    src.write_text("// kernel source\n")
-    h = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
-    (tmp_path / "profiles").mkdir()
-    rec = {"ns_gemm": {"bytes_per_ns_call": 3000, "source_sha256_16": h}}
-    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    for rel in bench.TRAFFIC_SOURCES:
+        f = tmp_path / rel
+        f.parent.mkdir(parents=True, exist_ok=True)
+        f.write_text(f"// {rel}\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.traffic_for(str(src), 30) == 100
-    assert bench.traffic_for(str(src), 0) is None
-    src.write_text("// kernel source, changed\n")
-    assert bench.traffic_for(str(src), 30) is None
+    h = bench.traffic_sources_hash()
+    (tmp_path / "profiles").mkdir()
+    rec = {"ns_gemm": {"moe_experts": {"bytes_per_ns_call": 3000, "source_sha256_16": h}}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    assert bench.traffic_for("moe_experts", 30) == 100
+    assert bench.traffic_for("moe_experts", 0) is None
+    assert bench.traffic_for("dense_block", 30) is None           # no capture for it
+    for rel in bench.TRAFFIC_SOURCES:                               # any source change voids it
+        f = tmp_path / rel
+        old = f.read_text()
+        f.write_text(old + "// changed\n")
+        assert bench.traffic_for("moe_experts", 30) is None, rel
+        f.write_text(old)
+    assert bench.traffic_for("moe_experts", 30) == 100
+
+
+def test_oracle_sample_covers_every_workload(bench):
+    from muon_qk_clip_gb300 import synth
+    for name in synth.WORKLOADS:
+        plan = bench.ORACLE_SAMPLE[name]
+        wl = synth.workload(name)
+        shapes = {(m.rows, m.cols) for m in wl.matrices}
+        assert all(s in shapes for s in plan["mats"]), name
+        assert (plan["heads"] > 0) == (wl.attention is not None), name
 
 
 @pytest.mark.parametrize("steps,fast", [(5, 2), (5, 3), (5, 0), (5, 1), (4, 3), (6, 2), (3, 2), (0, 2)])
