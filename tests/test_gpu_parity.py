@@ -459,6 +459,41 @@ def test_clip_total_mode_nan_clips_nothing():
     assert torch.equal(gamma.cpu(), torch.ones(H))
 
 
+@pytest.mark.parametrize("kind", ["mha", "mla"])
+def test_clip_tau30(kind):
+    """The threshold of the pages' small-model ablation, tau = 30: heads
+    between 30 and 100 clip (at tau = 100 they would not), a head at exactly
+    30 does not, and the factor is gamma = 30 / S_max."""
+    tau = 30.0
+    if kind == "mha":
+        H, d, D = 8, 16, 40
+        Wq = synth.normal((H * d, D), 1.0, "t30q", 17).to(BF16)
+        Wk = synth.normal((H * d, D), 1.0, "t30k", 17).to(BF16)
+        smax = torch.tensor([10.0, 30.0, 31.0, 45.0, 99.0, 150.0, 29.9, 1000.0])
+        w = {"Wq": Wq, "Wk": Wk}
+        dev = {n: t.cuda() for n, t in w.items()}
+        segs, osegs = mc.mha_segments(dev["Wq"], dev["Wk"], H, 0.5), O.mha_segments(H, d, 0.5)
+        want = [False, False, True, True, True, True, False, True]
+    else:
+        H, dn, dr, dv, ql, kl = 4, 16, 8, 16, 24, 16
+        W_UQ = synth.normal((H * (dn + dr), ql), 1.0, "t30uq", 17).to(BF16)
+        W_UKV = synth.normal((H * (dn + dv), kl), 1.0, "t30ukv", 17).to(BF16)
+        smax = torch.tensor([30.5, 29.0, 80.0, 300.0])
+        w = {"W_UQ": W_UQ, "W_UKV": W_UKV}
+        dev = {n: t.cuda() for n, t in w.items()}
+        segs, osegs = mc.mla_segments(dev["W_UQ"], dev["W_UKV"], H, dn, dr, dv), O.mla_segments(H, dn, dr, dv)
+        want = [True, False, True, True]
+    gamma = torch.empty(H, device="cuda")
+    ncl = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mc.qk_clip_apply(smax.cuda(), tau, segs, gamma_out=gamma, nclipped=ncl)
+    torch.cuda.synchronize()
+    out, g, mask = O.qk_clip({n: f64(t) for n, t in w.items()}, osegs, f64(smax), tau)
+    assert mask.tolist() == want and ncl.item() == sum(want)
+    np.testing.assert_allclose(f64(gamma), g, rtol=1e-6)
+    for n in w:
+        assert_rounded_within(dev[n], out[n], 1e-6 * np.abs(out[n]), f"tau 30 {kind} {n}")
+
+
 # ------------------------------------------------------------------ MuonClip step, tiny MHA
 def test_tiny_mha_fp32_full_step():
     """The tiny fp32 MHA workload end to end: S_max from the forward features,
@@ -488,6 +523,39 @@ def test_tiny_mha_fp32_full_step():
     s2, _ = mc.qk_max_logit(q2.cuda(), k2.cuda())
     torch.cuda.synchronize()
     np.testing.assert_allclose(f64(s2), np.minimum(ref_s, 100.0), rtol=1e-5)
+
+
+def test_tiny_mha_step_tau30():
+    """The tiny fp32 MHA workload with heads 1 and 3 scaled x12 (max logit
+    ~67) stepped with tau = 30: both heads clip, which tau = 100 would not,
+    and the re-measured max logit after the step's clip is min(S, 30)."""
+    wl = synth.scaled(synth.workload("tiny_mha_fp32", "literal"), scaled_heads={1: 12.0, 3: 12.0})
+    X, Wa = synth.attention_inputs(wl, seed=5)
+    Wm, Gm, Mm = synth.muon_inputs(wl, seed=5)
+    q, k = forward.project_mha(X, Wa["Wq"], Wa["Wk"], wl.attention.H)
+    hp = mc.Hparams(tau=30.0)
+    smax, _ = mc.qk_max_logit(q.cuda(), k.cuda())
+    ref_s, _ = O.max_logit(f64(q), f64(k))
+    np.testing.assert_allclose(f64(smax), ref_s, rtol=1e-5)
+    assert list(ref_s > 30.0) == [False, True, False, True]
+    assert np.all(ref_s < 100.0) and np.all(np.abs(ref_s - 30.0) > 5.0)
+    W, G, M = [Wm["W"].cuda()], [Gm["W"].cuda()], [Mm["W"].cuda()]
+    Wq, Wk = Wa["Wq"].cuda(), Wa["Wk"].cuda()
+    ncl = torch.zeros(1, dtype=torch.int32, device="cuda")
+    layer = mc.ClipLayer(smax, mc.mha_segments(Wq, Wk, wl.attention.H), nclipped=ncl)
+    mc.muonclip_step(W, G, M, hp, layers=[layer])
+    torch.cuda.synchronize()
+    assert ncl.item() == 2
+    (Wn, _, Od), _ = oracle_muon(Wm["W"], Gm["W"], Mm["W"], hp)
+    assert_rounded_within(W[0], Wn, 1e-5 * rms(fp32(hp.lr) * Od), "tiny W")
+    out, _, mask = O.qk_clip({"Wq": f64(Wa["Wq"]), "Wk": f64(Wa["Wk"])},
+                             O.mha_segments(4, 64), ref_s, 30.0)
+    assert_rounded_within(Wq, out["Wq"], 1e-6 * np.abs(out["Wq"]), "Wq")
+    assert_rounded_within(Wk, out["Wk"], 1e-6 * np.abs(out["Wk"]), "Wk")
+    q2, k2 = forward.project_mha(X, Wq.cpu(), Wk.cpu(), 4)
+    s2, _ = mc.qk_max_logit(q2.cuda(), k2.cuda())
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(f64(s2), np.minimum(ref_s, 30.0), rtol=1e-5)
 
 
 def test_dense_block_step_reduced_tokens():

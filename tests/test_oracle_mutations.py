@@ -92,6 +92,37 @@ def _attention_unnormalised(Q, K, V, K_shared=None, causal=True, scale=None, row
 
 
 _attn_real = OM.attention_forward
+_rope_real = OM.rope
+_rms_real = OM.rms_norm
+
+
+def _rope_clockwise(x, theta=10000.0):
+    # the rotation by -angle: apply the real one to the conjugate pair and conjugate back
+    xc = x.copy()
+    xc[..., 1::2] *= -1.0
+    yc = _rope_real(xc, theta)
+    yc[..., 1::2] *= -1.0
+    return yc
+
+
+def _rope_positions_from_one(x, theta=10000.0):
+    S = x.shape[1]
+    pad = np.concatenate([np.zeros_like(x[:, :1]), x], axis=1)
+    return _rope_real(pad, theta)[:, 1:S + 1]                            # angle (p + 1) at p
+
+
+def _rope_frequency_over_d_half(x, theta=10000.0):
+    return _rope_real(x, theta ** 0.5)                                   # theta^(-t/d) for pair t
+
+
+def _rms_norm_mean_abs(x, eps=1e-6):
+    x = np.asarray(x, np.float64)
+    return x / (np.mean(np.abs(x), axis=-1, keepdims=True) + eps)         # mean |x| for the RMS
+
+
+def _rms_norm_eps_outside(x, eps=1e-6):
+    x = np.asarray(x, np.float64)
+    return x / (np.sqrt(np.mean(x * x, axis=-1, keepdims=True)) + eps)
 
 MUTATIONS = [
     ("ns_iterate", _ns_dropped_quintic, [P.test_golden_newton_schulz_one_step]),
@@ -105,6 +136,11 @@ MUTATIONS = [
     ("attention_forward", _attention_scale_one_over_d, [P.test_attention_one_hot_key_closed_form]),
     ("attention_forward", _attention_values_of_query, [P.test_attention_one_hot_key_closed_form]),
     ("attention_forward", _attention_unnormalised, [P.test_attention_constant_values_pass_through]),
+    ("rope", _rope_clockwise, [P.test_rope_hand_worked_angles]),
+    ("rope", _rope_positions_from_one, [P.test_rope_position_zero_is_identity_and_pairs_keep_their_norm]),
+    ("rope", _rope_frequency_over_d_half, [P.test_rope_hand_worked_angles]),
+    ("rms_norm", _rms_norm_mean_abs, [P.test_rms_norm_unit_rms_scale_invariance_and_hand_value]),
+    ("rms_norm", _rms_norm_eps_outside, [P.test_rms_norm_unit_rms_scale_invariance_and_hand_value]),
 ]
 
 

@@ -523,3 +523,73 @@ def test_attention_smax_is_the_max_logit(mla):
     _, _, smax = O.attention_forward(Q, K, V, Ks, row_chunk=5)
     ref, _ = O.max_logit(Q, K, Ks)
     np.testing.assert_allclose(smax, ref, rtol=1e-15)
+
+
+# ------------------------------------------------------------------ setup projection: RoPE, RMSNorm
+# The MLA feature projection (the untimed setup forward) uses a rotary
+# embedding on interleaved pairs and a weightless RMSNorm.  Both are pinned
+# by properties that fix them up to nothing: the rotation of each pair by a
+# position-proportional angle, its frequencies, its direction and the norm.
+
+def test_rope_hand_worked_angles():
+    """d = 2: the one pair turns by p radians at position p (frequency
+    theta^0 = 1).  d = 4, theta = 100: the second pair's frequency is
+    100^(-2/4) = 0.1, so at position 3 it turns by 0.3 rad.  The direction is
+    counter-clockwise: (1, 0) -> (cos a, sin a), (0, 1) -> (-sin a, cos a)."""
+    x = np.zeros((1, 3, 2))
+    x[0, 1] = (1.0, 0.0)
+    x[0, 2] = (0.0, 1.0)
+    y = O.rope(x, theta=10000.0)
+    np.testing.assert_allclose(y[0, 1], [math.cos(1.0), math.sin(1.0)], atol=1e-15)
+    np.testing.assert_allclose(y[0, 2], [-math.sin(2.0), math.cos(2.0)], atol=1e-15)
+    x4 = np.zeros((1, 4, 4))
+    x4[0, 3] = (0.0, 0.0, 2.0, -1.0)
+    y4 = O.rope(x4, theta=100.0)
+    a = 0.3
+    want = (0.0, 0.0, 2.0 * math.cos(a) + math.sin(a), 2.0 * math.sin(a) - math.cos(a))
+    np.testing.assert_allclose(y4[0, 3], want, atol=1e-15)
+
+
+def test_rope_position_zero_is_identity_and_pairs_keep_their_norm():
+    rng = np.random.default_rng(40)
+    x = rng.standard_normal((2, 37, 3, 64))
+    y = O.rope(x)
+    np.testing.assert_array_equal(y[:, 0], x[:, 0])
+    n_in = x[..., 0::2] ** 2 + x[..., 1::2] ** 2
+    n_out = y[..., 0::2] ** 2 + y[..., 1::2] ** 2
+    np.testing.assert_allclose(n_out, n_in, rtol=1e-12)
+    # a pair stays in its own two coordinates
+    e = np.zeros((1, 9, 8))
+    e[0, :, 4] = 1.0
+    z = O.rope(e)
+    assert np.all(z[0, :, [0, 1, 2, 3, 6, 7]] == 0.0)
+
+
+def test_rope_logits_depend_only_on_relative_position():
+    """With the same query vector q at every position and the same key vector
+    k, rope(q)_i . rope(k)_j is a function of i - j alone (the property that
+    makes the embedding relative)."""
+    rng = np.random.default_rng(41)
+    d, S = 64, 50
+    q = np.broadcast_to(rng.standard_normal(d), (1, S, d)).copy()
+    k = np.broadcast_to(rng.standard_normal(d), (1, S, d)).copy()
+    rq, rk = O.rope(q)[0], O.rope(k)[0]
+    for delta in (0, 1, 7, 30):
+        vals = [rq[i] @ rk[i - delta] for i in range(delta, S)]
+        np.testing.assert_allclose(vals, vals[0], rtol=1e-10, atol=1e-10)
+    assert abs(rq[10] @ rk[3] - rq[3] @ rk[10]) > 1e-6      # and on its sign
+
+
+def test_rms_norm_unit_rms_scale_invariance_and_hand_value():
+    rng = np.random.default_rng(42)
+    x = rng.standard_normal((5, 7, 512)) * rng.uniform(0.1, 10.0, size=(5, 7, 1))
+    y = O.rms_norm(x, eps=0.0)
+    np.testing.assert_allclose(np.sqrt(np.mean(y ** 2, axis=-1)), 1.0, rtol=1e-12)
+    np.testing.assert_allclose(O.rms_norm(3.5 * x, eps=0.0), y, rtol=1e-12)
+    assert np.all(np.sign(y) == np.sign(x))
+    # [3, 4]: mean square 12.5, so y = [3, 4] / sqrt(12.5)
+    np.testing.assert_allclose(O.rms_norm(np.array([3.0, 4.0]), eps=0.0),
+                               [3.0 / math.sqrt(12.5), 4.0 / math.sqrt(12.5)], rtol=1e-15)
+    # eps enters under the root: [1e-3, 1e-3] with eps 1e-6 -> 1e-3 / sqrt(2e-6)
+    np.testing.assert_allclose(O.rms_norm(np.array([1e-3, 1e-3]), eps=1e-6),
+                               1e-3 / math.sqrt(2e-6), rtol=1e-12)
