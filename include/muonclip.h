@@ -61,10 +61,14 @@ typedef enum {
 typedef enum { MC_F32 = 0, MC_BF16 = 1 } mc_dtype;
 
 /* Arithmetic of the Newton-Schulz products.
- *   MC_NS_SPLIT_BF16: tcgen05 tensor cores; every operand is split into a
- *     bf16 pair (hi + lo) and each product is hi*hi + hi*lo + lo*hi with fp32
- *     accumulation; iterates are stored as (hi, lo) pairs (~16 significand
- *     bits).  Default for bf16 weights.
+ *   MC_NS_SPLIT_BF16: tcgen05 tensor cores on 16-bit (hi, lo) planes, fp32
+ *     accumulation.  The first iteration reads the momentum's bf16 (hi, lo)
+ *     copy (bf16 keeps fp32's exponent range, whatever the scale of M); its
+ *     update normalises by 1/||M|| and every later iterate, Gram and
+ *     polynomial matrix is stored as an fp16 (hi, lo) pair (~22 significand
+ *     bits; entries stay bounded after the normalisation).  A product takes
+ *     one term (hi*hi) or three (hi*hi + hi*lo + lo*hi) per k-step, as
+ *     ns_fast_steps below says.  Default for bf16 weights.
  *   MC_NS_BF16: tcgen05, one bf16 product, bf16 iterates (fastest, ~1e-1
  *     max-abs / 1e-2 RMS deviation from exact arithmetic).
  *   MC_NS_FP32: CUDA-core fp32 products and fp32 iterates.  Default for fp32
@@ -108,21 +112,20 @@ typedef struct {
   float alpha;         /* MHA split: W_q by gamma^alpha, W_k by gamma^(1-alpha) */
   int32_t ns_precision;/* mc_ns_precision                                    */
   int32_t ns_fast_steps;/* MC_NS_SPLIT_BF16 only: this many leading iterations
-                          use one bf16 product (hi operands only) on the split
-                          iterate.  Up to two, each followed by at least three
-                          three-term iterations, for matrices whose smaller
-                          side is at least 1024 (there they stay within 6e-3 of
-                          RMS even for adversarial spectra; smaller matrices
-                          would reach 9e-2, so they always take the three-term
-                          product).  A value >= 3 adds a third for matrices
-                          whose smaller side is at least 2048 when ns_steps
-                          >= 5: 9-13 % faster steps, at most 1.6e-2 of RMS on
-                          adversarial spectra (3e-3 on Gaussian).  With exactly
-                          two, matrices whose smaller side is at least 2048
-                          also take the third iteration's Gram product in one
-                          product (its polynomial and update stay three-term):
-                          at most 8.2e-3 of RMS on adversarial spectra at
-                          2048 x 2048 (1.6e-3 on Gaussian).  Default 2. */
+                          take one product (hi*hi) per k-step, for matrices
+                          whose smaller side is at least 256: up to three,
+                          each run keeping at least two iterations after it,
+                          whose Gram products take one product and whose
+                          polynomial and update take three.  Float64
+                          emulation of this arithmetic gives at most 8.2e-3
+                          of RMS (512 x 16384 Gaussian; 2048 x 7168: 3.9e-3;
+                          adversarial spectra, a few dominant directions over
+                          a 1e-3 rest: at most 6.6e-3).  A value >= 4 allows
+                          four (keeping one) for matrices whose smaller side
+                          is at least 1024: fewer products, at most 1.0e-2 of
+                          RMS (1024 x 1536 Gaussian).  Matrices whose smaller
+                          side is under 256 take three products everywhere
+                          (1.4e-2 at 64 otherwise).  Default 3. */
   int32_t scale_mode;  /* mc_scale_mode: factor on NewtonSchulz(M)            */
 } mc_hparams;
 
@@ -182,14 +185,14 @@ typedef struct {
 
 /* Fill *hp with the defaults named above (mu 0.95, lr 2e-4, weight_decay 0.1,
  * rms_scale 0.2, 5 steps of the quintic (3.4445, -4.7750, 2.0315),
- * ns_eps 1e-7, tau 100, alpha 0.5, MC_NS_AUTO, ns_fast_steps 2, MC_SCALE_RMS). */
+ * ns_eps 1e-7, tau 100, alpha 0.5, MC_NS_AUTO, ns_fast_steps 3, MC_SCALE_RMS). */
 void mc_default_hparams(mc_hparams* hp);
 
 /* Bytes of workspace that muon_newton_schulz / muonclip_step need for these
  * `count` matrices (shapes and dtypes of M, or of W for muonclip_step). */
 mc_status mc_workspace_size(const mc_mat* M, int32_t count, const mc_hparams* hp, size_t* bytes);
 
-/* Products per k-step that the split-bf16 tensor-core Newton-Schulz takes for
+/* Products per k-step that the split tensor-core Newton-Schulz takes for
  * a rows x cols matrix under *hp ([K2-internals] Algorithm 1, orthogonalisation
  * step; the arithmetic of the split iterate is this library's): for iteration
  * i (0 .. ns_steps - 1), products[3 i + 0], [3 i + 1] and [3 i + 2] are those

@@ -59,7 +59,7 @@ class Hparams:
     tau: float = 100.0
     alpha: float = 0.5
     ns_precision: int = abi.MC_NS_AUTO
-    ns_fast_steps: int = 2
+    ns_fast_steps: int = 3
     scale_mode: int = abi.MC_SCALE_RMS
 
     def c(self) -> McHparams:

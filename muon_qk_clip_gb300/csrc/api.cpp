@@ -285,38 +285,54 @@ mc_status run_norms(const Plan& P, void* ws, float eps, cudaStream_t s) {
 // One Newton-Schulz phase over every group (chunks of kMaxGroups).
 enum Phase { kGram = 1, kPoly = 2, kNext = 3 };
 
-// Smallest min(rows, cols) for which the one-product leading iterations keep
-// the Newton-Schulz output within 2e-2 of its RMS with margin: float64
-// emulation of the split arithmetic over adversarial spectra (a few dominant
-// directions over a near-null rest) gives at most 6e-3 from 1024 up, but
-// 1e-2 at 256-384 and up to 9e-2 at 64 and below.
-constexpr int kFastMinSide = 1024;
-// Smallest min(rows, cols) for a third one-product iteration (only when
-// ns_fast_steps asks for it): float64 emulation at 2048 x 2048 gives at most
-// 1.6e-2 of RMS (64 unit directions over a 1e-3 rest; 3e-3 on Gaussian
-// inputs), against 1.5e-2 on plain Gaussian inputs at 1024.
-constexpr int kFast3MinSide = 2048;
-// Smallest min(rows, cols) for which the first three-term iteration's Gram
-// product takes one bf16 product (its polynomial and update stay three-term):
-// float64 emulation at 2048 x 2048 gives at most 8.2e-3 of RMS (64 unit
-// directions over a 1e-3 rest; 1.6e-3 on Gaussian inputs), against 5.1e-3
-// with the Gram three-term; 1.1e-2 at 1024.
-constexpr int kGram1MinSide = 2048;
+// The split Newton-Schulz plan.  Iteration 0 reads the iterate prep wrote
+// from the raw momentum, whose scale is arbitrary, so it works on bf16 planes
+// (fp32's exponent range); its update multiplies by 1/||M|| and stores X1 as
+// fp16 (hi, lo) planes, and every later iteration works on fp16 planes:
+// entries are then bounded (singular values stay below ~1.2) and fp16's 11
+// significand bits make a one-product (hi*hi) step 8x more accurate than
+// bf16's.  The leading iterations take one product per k-step, the trailing
+// ones three (hi*hi + hi*lo + lo*hi) in the polynomial and the update; the
+// trailing Gram products take one.
+//
+// Float64 emulation of this arithmetic (max error / RMS of the exact result;
+// the bound is 2e-2) over Gaussian inputs and adversarial spectra (64 or 4
+// unit directions over a 1e-3 rest), sides 64 to 2048 x 7168:
+//   - three leading one-product iterations (ns_fast_steps = 3): at most
+//     8.2e-3 from a smaller side of 256 (512 x 16384 Gaussian; 2048 x 7168:
+//     3.9e-3, about what every product split gives there); 1.4e-2 at 64;
+//   - four (ns_fast_steps >= 4): at most 1.0e-2 from 1024 (1024 x 1536
+//     Gaussian; 2048 x 7168: 9.5e-3), 9.8e-3 at 256 and 3.7e-2 at 512 x 16384;
+// so the one-product iterations run from a smaller side of kFastMinSide
+// (three) and kFast4MinSide (four); smaller matrices take three products in
+// every phase (2.8e-3 at 64).
+constexpr int kFastMinSide = 256;
+constexpr int kFast4MinSide = 1024;
+
+// Leading one-product iterations of a shape group whose smaller side is
+// `side`: up to three with at least two three-term iterations after them,
+// or four (ns_fast_steps >= 4, side >= kFast4MinSide) with at least one.
+int ns_fast_iterations(const mc_hparams* hp, int side) {
+  if (side < kFastMinSide) return 0;
+  if (hp->ns_fast_steps >= 4 && side >= kFast4MinSide)
+    return std::min(hp->ns_fast_steps, std::max(0, hp->ns_steps - 1));
+  return std::min({hp->ns_fast_steps, 3, std::max(0, hp->ns_steps - 2)});
+}
 
 // Products per k-step (1: hi*hi; 3: hi*hi + hi*lo + lo*hi) of phase `ph` of
-// iteration `it` on the split iterate, for a shape group whose smaller side
-// is `side`.  The leading ns_fast_steps iterations take one product: up to
-// two, followed by at least three three-term iterations, from kFastMinSide;
-// a third (ns_fast_steps >= 3, at least two three-term iterations after it)
-// from kFast3MinSide.  After exactly two, the next iteration's Gram takes one
-// product from kGram1MinSide.  Every other launch takes three.
+// iteration `it` on the split iterate.
 int ns_terms(const mc_hparams* hp, int side, int it, int ph) {
-  const int fast12 = std::min({hp->ns_fast_steps, 2, std::max(0, hp->ns_steps - 3)});
-  const bool fast3 = fast12 == 2 && hp->ns_fast_steps >= 3 && hp->ns_steps >= 5;
-  const int n = side >= kFast3MinSide && fast3 ? 3 : side >= kFastMinSide ? fast12 : 0;
-  if (it < n) return 1;
-  if (ph == kGram && it == n && n == 2 && !fast3 && side >= kGram1MinSide) return 1;
+  if (it < ns_fast_iterations(hp, side)) return 1;
+  if (ph == kGram && side >= kFastMinSide) return 1;
   return 3;
+}
+
+// 16-bit formats of phase `ph` of iteration `it`: bf16 in iteration 0 (its
+// update stores X1 as fp16), fp16 after it; plain bf16 planes throughout.
+int ns_fmt(int xmode, int it, int ph) {
+  if (xmode != kXSplit) return kFmtBf16;
+  if (it == 0) return ph == kNext ? kFmtBf16ToF16 : kFmtBf16;
+  return kFmtF16;
 }
 
 mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams* hp,
@@ -404,6 +420,7 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
       }
       ++launch;
       gp.terms = terms;
+      gp.fmt = ns_fmt(P.xmode, it, ph);
       // Three-term iterations fold a X into the polynomial: B' = c A^2 + b A + a I
       // and X' = B' X, so the last phase reads no C.  (B' holds ~16 significand
       // bits there; a one-plane bf16 B' would lose the small singular values, so
@@ -532,6 +549,8 @@ mc_status run_apply(const Plan& P, void* ws, mc_mat* out, bool write_o, const mc
     ap.njobs = nj;
     ap.xmode = P.xmode;
     ap.write_o = write_o;
+    // the split iterate is fp16 once an iteration has run (ns_fmt)
+    ap.x_f16 = P.xmode == kXSplit && hp->ns_steps >= 1;
     ap.lr = hp->lr;
     ap.wd = hp->weight_decay;
     ap.status = status;
@@ -676,7 +695,7 @@ void mc_default_hparams(mc_hparams* hp) {
   hp->tau = 100.f;
   hp->alpha = 0.5f;
   hp->ns_precision = MC_NS_AUTO;
-  hp->ns_fast_steps = 2;
+  hp->ns_fast_steps = 3;
   hp->scale_mode = MC_SCALE_RMS;
 }
 

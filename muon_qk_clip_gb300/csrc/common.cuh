@@ -6,6 +6,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -38,6 +39,26 @@ __device__ inline bool finite_f(float x) { return fabsf(x) <= 3.402823466e38f; }
 __device__ inline void split_bf16(float x, __nv_bfloat16& hi, __nv_bfloat16& lo) {
   hi = __float2bfloat16_rn(x);
   lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+}
+
+// 16-bit storage formats of the Newton-Schulz planes: bf16 (8 significand
+// bits, fp32's exponent range) or fp16 (11 significand bits, normal range
+// 6.1e-5 .. 65504, subnormals down to 6e-8), as raw bits.
+template <bool F16>
+__device__ inline float from16(uint16_t u) {
+  if (F16) return __half2float(__ushort_as_half(u));
+  return __bfloat162float(__ushort_as_bfloat16(u));
+}
+template <bool F16>
+__device__ inline uint16_t to16(float v) {
+  if (F16) return __half_as_ushort(__float2half_rn(v));
+  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+// (hi, lo) split in either format: hi = rn(x), lo = rn(x - hi)
+template <bool F16>
+__device__ inline void split16(float x, uint16_t& hi, uint16_t& lo) {
+  hi = to16<F16>(x);
+  lo = to16<F16>(x - from16<F16>(hi));
 }
 
 __device__ inline uint32_t smem_u32(const void* p) {
@@ -110,6 +131,10 @@ __device__ inline void tma_load_4d(void* smem_dst, const CUtensorMap* map, uint6
       " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
       : "memory");
+}
+// Bring the line holding `p` into L2 (no registers, no completion to wait for).
+__device__ inline void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 __device__ inline void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -223,17 +248,22 @@ __device__ inline void reg_fence32(uint32_t (&r)[32]) {
                  "+r"(r[30]), "+r"(r[31]));
 }
 
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, M x N tile.
-// a_mn / b_mn select MN-major (1) instead of K-major (0) operand layouts.
+// Instruction descriptor, kind::f16: D fp32, A and B both bf16 (f16 = 0) or
+// both fp16 (f16 = 1), M x N tile.  a_mn / b_mn select MN-major (1) instead
+// of K-major (0) operand layouts.
+__host__ __device__ constexpr uint32_t make_idesc_16(uint32_t M, uint32_t N, uint32_t a_mn,
+                                                     uint32_t b_mn, uint32_t f16) {
+  return (1u << 4)                  // D format: f32
+         | ((f16 ? 0u : 1u) << 7)   // A format: f16 (0) or bf16 (1)
+         | ((f16 ? 0u : 1u) << 10)  // B format: the same as A
+         | (a_mn << 15)             // A major
+         | (b_mn << 16)             // B major
+         | ((N >> 3) << 17)         // N / 8
+         | ((M >> 4) << 24);        // M / 16
+}
 __host__ __device__ constexpr uint32_t make_idesc_bf16(uint32_t M, uint32_t N, uint32_t a_mn,
                                                        uint32_t b_mn) {
-  return (1u << 4)            // D format: f32
-         | (1u << 7)          // A format: bf16
-         | (1u << 10)         // B format: bf16
-         | (a_mn << 15)       // A major
-         | (b_mn << 16)       // B major
-         | ((N >> 3) << 17)   // N / 8
-         | ((M >> 4) << 24);  // M / 16
+  return make_idesc_16(M, N, a_mn, b_mn, 0);
 }
 
 // Shared-memory matrix descriptor (descriptor version 1); lbo/sbo in bytes;

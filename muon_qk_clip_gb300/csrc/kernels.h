@@ -12,6 +12,14 @@ namespace mc {
 inline constexpr int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline constexpr int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 
+// 16-bit formats of a tensor-core Newton-Schulz launch: operands (A, B, C)
+// and stored output D.
+enum GemmFmt : int {
+  kFmtBf16 = 0,       // bf16 in, bf16 out
+  kFmtBf16ToF16 = 1,  // bf16 in, fp16 out
+  kFmtF16 = 2         // fp16 in, fp16 out
+};
+
 // Storage of a Newton-Schulz iterate (and of its Gram / polynomial matrices).
 enum XMode : int {
   kXSplit = 0,  // two bf16 planes, value = hi + lo
@@ -73,6 +81,7 @@ struct ApplyParams {
   int total_tiles;
   int xmode;
   int write_o;         // 1: out = scale * X; 0: W -= lr (scale X + wd W)
+  int x_f16;           // split iterate planes hold fp16 (else bf16)
   float lr, wd;
   const float* mat_scale;  // per-matrix extra factor on X, or null
   int32_t* status;
@@ -120,6 +129,7 @@ struct GemmGroup {
 struct GemmTmaps {
   CUtensorMap a_hi[kMaxGroups], a_lo[kMaxGroups], b_hi[kMaxGroups], b_lo[kMaxGroups];
   CUtensorMap d_hi[kMaxGroups], d_lo[kMaxGroups];
+  CUtensorMap c_hi[kMaxGroups], c_lo[kMaxGroups];   // C of non-symmetric outputs (32 x 32 boxes)
 };
 
 struct GemmParams {
@@ -127,7 +137,9 @@ struct GemmParams {
   int ngroups;
   int total_tiles;
   int xmode;
-  int terms;              // tensor-core products per k-step: 1 (hi*hi) or 3 (split)
+  int terms;              // tensor-core products per k-step: 1 (hi*hi), 2 (hi*hi + hi*lo_B)
+                          // or 3 (hi*hi + hi*lo + lo*hi)
+  int fmt;                // tensor-core planes: kFmtBf16, kFmtBf16ToF16 or kFmtF16
   float alpha, beta;
   float diag;             // added on the diagonal of each output item
   const float* s;         // per-matrix scale, or null

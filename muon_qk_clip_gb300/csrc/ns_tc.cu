@@ -67,7 +67,7 @@ struct KLayout {
   static constexpr uint32_t kSbo = 8 * BK * 2;
 };
 
-// TERMS: tensor-core products per k-step (1: hi*hi, 3: hi*hi + hi*lo + lo*hi).
+// TERMS: tensor-core products per k-step (1: hi*hi; 3: hi*hi + hi*lo + lo*hi).
 // LO: the iterate is stored as (hi, lo) planes (the epilogue reads and writes
 // both), independently of how many products the k-loop takes.
 template <int TERMS, int AROWS, int BROWS, int BK = BKT>
@@ -137,8 +137,10 @@ __device__ inline uint32_t swz64(int row, int b) {
 // The warp's 8 KB of shared memory is two 4 KB slots (a 32 x 32 chunk of hi
 // and lo planes each): D and its mirror for symmetric outputs, else a ring of
 // two D chunks, so a chunk waits only for the store group that last used its
-// slot.  `ek` counts this warp's store groups across tiles.  C is read by each
-// lane straight from global memory (its row's 64 contiguous bytes per plane).
+// slot.  `ek` counts this warp's store groups across tiles.  C of a
+// symmetric output (the polynomial's b A term) is read by each lane straight
+// from global memory (its row's 64 contiguous bytes per plane); C of a
+// non-symmetric output (the update's a X term) arrives by TMA (CSlots below).
 // The next chunk's TMEM load and C loads are issued as soon as the current
 // chunk's values are converted, so they are in flight while it is stored; two
 // warps share each lane quadrant (one per column half), so one warp's waits
@@ -160,15 +162,81 @@ __device__ inline void load_c_chunk(const GemmGroup& G, const TileCoord& tc, int
   }
 }
 
+// Before a tile's accumulator is ready: pull the C rows this warp will read
+// (its 32 rows, chunks [c_begin, c_end), both planes) into L2, so the
+// epilogue's loads, issued one chunk ahead, wait for L2 rather than DRAM.
 template <bool LO>
-__device__ void epilogue_rows(const GemmParams& p, const TmaArgs& tm, const TileCoord& tc, int r0,
-                              int c_begin, int c_end, uint32_t tacc, int q, int lane, uint8_t* ebuf,
-                              uint32_t& ek, bool& bad) {
+__device__ inline void prefetch_c_rows(const GemmParams& p, const TileCoord& tc, int r0, int c_begin,
+                                       int c_end, int lane) {
   const GemmGroup& G = p.g[tc.g];
-  if (r0 >= G.M) return;                            // no valid row in this warp
+  const int row = r0 + lane;
+  if (p.beta == 0.f || row >= G.M) return;
+  const long long o = (long long)tc.b * G.c_bstride + (long long)row * G.ldc;
+  const uint16_t* c_hi = reinterpret_cast<const uint16_t*>(G.c_hi) + o;
+  const uint16_t* c_lo = reinterpret_cast<const uint16_t*>(G.c_lo) + o;
+  for (int ch = c_begin; ch < c_end; ++ch) {
+    const int col0 = tc.n0 + ch * 32;
+    if (col0 >= G.N) break;
+    prefetch_l2(c_hi + col0);
+    if (LO) prefetch_l2(c_lo + col0);
+  }
+}
+
+// C through TMA (non-symmetric outputs with a C term): the warp's two 4 KB
+// slots take the C chunks as 32 x 32 boxes (hi and lo planes), loaded two
+// chunks ahead and, for a tile's first two chunks, before its accumulator is
+// ready; each chunk's D is then written over its C in the same slot and
+// leaves by TMA.  Chunk i of the warp's sequence uses slot ek & 1.
+struct CSlots {
+  uint64_t* bar;       // [2] completion of the C box loads of each slot
+  uint32_t par;        // bit s: parity of the next wait on bar[s]
+  uint32_t pending;    // bit s: a load into slot s has not been waited for
+};
+
+__device__ inline bool c_by_tma(const GemmParams& p, const GemmGroup& G) {
+  return p.beta != 0.f && !G.symmetric;
+}
+
+// Lane 0: load C chunk `ch` of rows [r0, r0 + 32) into slot `slot`, once the
+// store that last read the slot has finished reading it.
+template <bool LO>
+__device__ inline void c_load(const TmaArgs& tm, const TileCoord& tc, int r0, int ch, uint8_t* ebuf,
+                              int slot, CSlots& cs) {
+  bulk_wait_read_upto(0);
+  uint8_t* sb = ebuf + slot * 4096;
+  mbar_arrive_expect_tx(&cs.bar[slot], LO ? 4096 : 2048);
+  const int col0 = tc.n0 + ch * 32;
+  tma_load_3d(sb, &tm.maps.c_hi[tc.g], &cs.bar[slot], col0, r0, tc.b);
+  if (LO) tma_load_3d(sb + 2048, &tm.maps.c_lo[tc.g], &cs.bar[slot], col0, r0, tc.b);
+  cs.pending |= 1u << slot;
+}
+
+// The first two live chunks of this warp's share of a tile (issued before
+// the accumulator is ready).
+template <bool LO>
+__device__ inline void c_prologue(const GemmParams& p, const TmaArgs& tm, const TileCoord& tc, int r0,
+                                  int c_begin, int c_end, int lane, uint8_t* ebuf, uint32_t ek,
+                                  CSlots& cs) {
+  const GemmGroup& G = p.g[tc.g];
+  if (!c_by_tma(p, G) || r0 >= G.M || lane != 0) return;
+  int k = 0;
+  for (int ch = c_begin; ch < c_end && k < 2; ++ch) {
+    if (tc.n0 + ch * 32 >= G.N) break;
+    c_load<LO>(tm, tc, r0, ch, ebuf, (int)((ek + k) & 1), cs);
+    ++k;
+  }
+}
+
+template <bool LO, bool IN16, bool OUT16>
+__device__ bool epilogue_rows(const GemmParams& p, const TmaArgs& tm, const TileCoord& tc, int r0,
+                              int c_begin, int c_end, uint32_t tacc, int q, int lane, uint8_t* ebuf,
+                              uint32_t& ek, bool& bad, CSlots& cs, volatile int* abort_flag) {
+  const GemmGroup& G = p.g[tc.g];
+  if (r0 >= G.M) return true;                       // no valid row in this warp
   const float sb = p.s ? p.s[G.mat_base + tc.b] : 1.f;
   const float al = p.alpha * sb, be = p.beta * sb, dg = p.diag * sb;
   const bool use_c = p.beta != 0.f;
+  const bool tmac = c_by_tma(p, G);                 // C arrives by TMA in the slots
   const int per = G.symmetric ? 2 : 1;              // slots per store group
   const int depth = 2 / per;                        // store groups in flight
   const int I = r0 / 128;
@@ -188,15 +256,36 @@ __device__ void epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
   const bool row_ok = row < G.M;
   const uint32_t trow = tacc + ((uint32_t)(q * 32) << 16);
   int ch = next_live(c_begin - 1);
-  if (ch >= c_end) return;
+  if (ch >= c_end) return true;
   uint4 c_h[4], c_l[4];
   uint32_t nr[32];
   tmem_ld_32x32b_x32_async(trow + ch * 32, nr);
-  if (use_c) load_c_chunk<LO>(G, tc, row, ch, c_h, c_l);
+  if (use_c && !tmac) load_c_chunk<LO>(G, tc, row, ch, c_h, c_l);
   while (ch < c_end) {
     const int mode = mode_of(ch);
     const int col0 = tc.n0 + ch * 32;
     const int nx = next_live(ch);
+    uint8_t* db = ebuf + (int)(ek % (uint32_t)depth) * per * 4096;
+    if (tmac) {
+      // this chunk's C box: wait for it, then read the lane's row from the slot
+      const int slot = (int)(ek & 1);
+      int ok = 1;
+      if (lane == 0) {
+        ok = mbar_wait(&cs.bar[slot], (cs.par >> slot) & 1u, abort_flag) ? 1 : 0;
+        if (ok) cs.pending &= ~(1u << slot);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        tmem_ld_wait();                 // the chunk's TMEM load lands before giving up
+        return false;
+      }
+      cs.par ^= 1u << slot;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        c_h[j] = *reinterpret_cast<const uint4*>(db + swz64(lane, j * 16));
+        if (LO) c_l[j] = *reinterpret_cast<const uint4*>(db + 2048 + swz64(lane, j * 16));
+      }
+    }
     tmem_ld_wait();
     reg_fence32(nr);
     float v[32];
@@ -205,11 +294,11 @@ __device__ void epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
     if (use_c) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const __nv_bfloat16* hh = reinterpret_cast<const __nv_bfloat16*>(&c_h[j]);
-        const __nv_bfloat16* ll = reinterpret_cast<const __nv_bfloat16*>(&c_l[j]);
+        const uint16_t* hh = reinterpret_cast<const uint16_t*>(&c_h[j]);
+        const uint16_t* ll = reinterpret_cast<const uint16_t*>(&c_l[j]);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float cv = LO ? __bfloat162float(hh[e]) + __bfloat162float(ll[e]) : __bfloat162float(hh[e]);
+          const float cv = LO ? from16<IN16>(hh[e]) + from16<IN16>(ll[e]) : from16<IN16>(hh[e]);
           v[j * 8 + e] = fmaf(al, v[j * 8 + e], be * cv);
         }
       }
@@ -235,22 +324,22 @@ __device__ void epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
 #pragma unroll
       for (int e = 0; e < 32; ++e) bad |= !finite_f(v[e]) && (col0 + e < G.N);
     }
-    __nv_bfloat16 hb[32], lb[32];
+    uint16_t hb[32], lb[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
-      if (LO) split_bf16(v[e], hb[e], lb[e]);
-      else hb[e] = __float2bfloat16_rn(v[e]);
+      if (LO) split16<OUT16>(v[e], hb[e], lb[e]);
+      else hb[e] = to16<OUT16>(v[e]);
     }
     // this chunk's accumulator and C are consumed: start the next chunk's
     // loads (warp-uniform: nx is the same in every lane)
     if (nx < c_end) {
       tmem_ld_32x32b_x32_async(trow + nx * 32, nr);
-      if (use_c) load_c_chunk<LO>(G, tc, row, nx, c_h, c_l);
+      if (use_c && !tmac) load_c_chunk<LO>(G, tc, row, nx, c_h, c_l);
     }
-    uint8_t* db = ebuf + (int)(ek % (uint32_t)depth) * per * 4096;
     uint8_t* mb = db + 4096;
-    // the store group that last used these slots must have read them
-    if (lane == 0) bulk_wait_read_upto(depth - 1);
+    // the store group that last used these slots must have read them (with C
+    // by TMA the slot was last read by this chunk's own C box, already used)
+    if (lane == 0 && !tmac) bulk_wait_read_upto(depth - 1);
     __syncwarp();
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -262,8 +351,8 @@ __device__ void epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
       // mirror tile: row c holds column c of this chunk, i.e. lane (row) r -> byte 2r
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        *reinterpret_cast<__nv_bfloat16*>(mb + swz64(c, 2 * lane)) = hb[c];
-        if (LO) *reinterpret_cast<__nv_bfloat16*>(mb + 2048 + swz64(c, 2 * lane)) = lb[c];
+        *reinterpret_cast<uint16_t*>(mb + swz64(c, 2 * lane)) = hb[c];
+        if (LO) *reinterpret_cast<uint16_t*>(mb + 2048 + swz64(c, 2 * lane)) = lb[c];
       }
     }
     fence_async_smem();
@@ -276,10 +365,16 @@ __device__ void epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
         if (LO) tma_store_3d(&tm.maps.d_lo[tc.g], mb + 2048, r0, col0, tc.b);
       }
       bulk_commit();
+      // two chunks on, C goes into this slot again once the store has read it
+      if (tmac) {
+        const int n2 = nx < c_end ? next_live(nx) : c_end;
+        if (n2 < c_end) c_load<LO>(tm, tc, r0, n2, ebuf, (int)(ek & 1), cs);
+      }
     }
     ++ek;
     ch = nx;
   }
+  return true;
 }
 
 // ------------------------------------------------------------ the kernel
@@ -295,12 +390,15 @@ __device__ void epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
 // Tiles are handed out dynamically: the first CTA's producer claims the next
 // tile id from a zeroed per-launch counter and publishes it to every role of
 // both CTAs through a kTS-deep shared-memory ring.
-template <int TERMS, bool LO, int BK>
+template <int TERMS, bool LO, int BK, int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
     ns_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ TmaArgs tm) {
   using C = Stages<TERMS, BM, 128, BK>;
   using KL = KLayout<BK>;
-  constexpr bool SPLIT = TERMS == 3;
+  constexpr bool SPLIT = TERMS == 3;     // the A operand's lo plane is staged
+  constexpr bool BLO = TERMS == 3;       // the B operand's lo plane is staged
+  constexpr bool IN16 = FMT == kFmtF16;  // fp16 operands (else bf16)
+  constexpr bool OUT16 = FMT != kFmtBf16;
   constexpr int TM_ROWS = 2 * BM;
   const uint32_t crank = cluster_ctarank();
   extern __shared__ uint8_t smem_raw[];
@@ -313,7 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = tempty + 2;            // [1]
   uint64_t* sfull = drain + 1;             // [kTS] tile id published
   uint64_t* sempty = sfull + kTS;          // [kTS] tile id read by every role
-  int* sid = reinterpret_cast<int*>(sempty + kTS);   // [kTS]
+  uint64_t* cbar = sempty + kTS;           // [2 kEpiWarps] C box loads per epilogue slot
+  int* sid = reinterpret_cast<int*>(cbar + 2 * kEpiWarps);   // [kTS]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sid + kTS);
   __shared__ volatile int abort_flag;
 
@@ -335,12 +434,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sfull[i], 1);
       mbar_init(&sempty[i], 2 * (1 + kEpiWarps));
     }
+    for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(&cbar[i], 1);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     for (int g = 0; g < p.ngroups; ++g) {
       prefetch_tmap(&tm.maps.a_hi[g]); prefetch_tmap(&tm.maps.b_hi[g]);
-      if (SPLIT) { prefetch_tmap(&tm.maps.a_lo[g]); prefetch_tmap(&tm.maps.b_lo[g]); }
+      if (SPLIT) prefetch_tmap(&tm.maps.a_lo[g]);
+      if (BLO) prefetch_tmap(&tm.maps.b_lo[g]);
     }
   }
   if (warp == 1) { tmem_alloc_pair(tmem_slot, kTmemCols); tmem_relinquish_pair(); }
@@ -417,12 +518,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (SPLIT) tma_load_3d_pair(a_lo, &tm.maps.a_lo[tc.g], fb, k0, m0, tc.b);
           if (!G.b_mn_major) {
             tma_load_3d_pair(b_hi, &tm.maps.b_hi[tc.g], fb, k0, nb, tc.b);
-            if (SPLIT) tma_load_3d_pair(b_lo, &tm.maps.b_lo[tc.g], fb, k0, nb, tc.b);
+            if (BLO) tma_load_3d_pair(b_lo, &tm.maps.b_lo[tc.g], fb, k0, nb, tc.b);
           } else {
 #pragma unroll
             for (int qq = 0; qq < 2; ++qq) {
               tma_load_3d_pair(b_hi + qq * (64 * BK * 2), &tm.maps.b_hi[tc.g], fb, nb + 64 * qq, k0, tc.b);
-              if (SPLIT)
+              if (BLO)
                 tma_load_3d_pair(b_lo + qq * (64 * BK * 2), &tm.maps.b_lo[tc.g], fb, nb + 64 * qq, k0, tc.b);
             }
           }
@@ -441,8 +542,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && crank == 0) {
-      constexpr uint32_t idesc_k = make_idesc_bf16(2 * BM, BN, 0, 0);
-      constexpr uint32_t idesc_mn = make_idesc_bf16(2 * BM, BN, 0, 1);
+      constexpr uint32_t idesc_k = make_idesc_16(2 * BM, BN, 0, 0, IN16 ? 1u : 0u);
+      constexpr uint32_t idesc_mn = make_idesc_16(2 * BM, BN, 0, 1, IN16 ? 1u : 0u);
       uint32_t it = 0, tcount = 0;
       bool issued = false;
       for (uint32_t seq = 0; !abort_flag; ++seq, ++tcount) {
@@ -474,20 +575,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint64_t dbh, dbl = 0, dal = 0;
             if (!G.b_mn_major) {
               dbh = make_sdesc(b_hi + kk * 32, 16, KL::kSbo, KL::kType);
-              if (SPLIT) dbl = make_sdesc(b_lo + kk * 32, 16, KL::kSbo, KL::kType);
+              if (BLO) dbl = make_sdesc(b_lo + kk * 32, 16, KL::kSbo, KL::kType);
             } else {
               // MN-major (128-byte swizzle): 16 K-rows = two 1024-byte atoms;
               // 64-wide N blocks are 64*BK*2 bytes apart
               dbh = make_sdesc(b_hi + kk * 2048, 64 * BK * 2, 1024, 2);
-              if (SPLIT) dbl = make_sdesc(b_lo + kk * 2048, 64 * BK * 2, 1024, 2);
+              if (BLO) dbl = make_sdesc(b_lo + kk * 2048, 64 * BK * 2, 1024, 2);
             }
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
             if (SPLIT) dal = make_sdesc(a_lo + kk * 32, 16, KL::kSbo, KL::kType);
             tc_mma_pair(d_tmem, dah, dbh, idesc, accum);
-            if (SPLIT) {
-              tc_mma_pair(d_tmem, dah, dbl, idesc, 1u);
-              tc_mma_pair(d_tmem, dal, dbh, idesc, 1u);
-            }
+            if (BLO) tc_mma_pair(d_tmem, dah, dbl, idesc, 1u);
+            if (SPLIT) tc_mma_pair(d_tmem, dal, dbh, idesc, 1u);
           }
           issued = true;
           // stage free (in both CTAs of the pair) once these MMAs have read it
@@ -511,6 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ek = 0;
     bool bad = false;
     uint32_t tcount = 0;
+    CSlots cs{cbar + 2 * e, 0u, 0u};
     for (uint32_t seq = 0;; ++seq, ++tcount) {
       int t = 0;
       if (lane == 0) t = take(seq);
@@ -521,18 +621,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int acc = tcount & 1;
       const int r0 = tc.m0 + BM * (int)crank + q * 32;
       const int c0 = hc * (BN / 64), c1 = (hc + 1) * (BN / 64);
+      // C of this tile: the first two chunks' boxes now (TMA), every row into
+      // L2, while the MMAs still run
+      c_prologue<LO>(p, tm, tc, r0, c0, c1, lane, ebuf, ek, cs);
+      prefetch_c_rows<LO>(p, tc, r0, c0, c1, lane);
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&tfull[acc], (tcount >> 1) & 1, &abort_flag) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) { if (lane == 0) fail(); break; }
       tc_fence_after();
-      epilogue_rows<LO>(p, tm, tc, r0, c0, c1, tmem_base + acc * BN, q, lane, ebuf, ek, bad);
+      if (!epilogue_rows<LO, IN16, OUT16>(p, tm, tc, r0, c0, c1, tmem_base + acc * BN, q, lane, ebuf, ek,
+                                          bad, cs, &abort_flag)) {
+        if (lane == 0) fail();
+        break;
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));   // the first CTA's MMA
       }
     }
+    // C boxes still in flight (only after a failed wait) land before exit
+    if (lane == 0)
+      for (int sl = 0; sl < 2; ++sl)
+        if (cs.pending & (1u << sl)) mbar_wait(&cs.bar[sl], (cs.par >> sl) & 1u, nullptr);
     if (lane == 0) bulk_wait0();         // all TMA stores of this warp complete
     if (bad) set_status(p.status, MC_STATUS_NONFINITE_UPDATE);
   }
@@ -570,7 +682,7 @@ EncodeTiledFn get_encode() {
 // swizzle 128 B (box_cols 64) or 64 B (box_cols 32), zero fill (loads) and
 // clipping (stores) outside [cols, rows, batch].
 bool encode_3d(CUtensorMap* m, const void* base, int cols, int rows, int batch, long long ld,
-               long long bstride, int box_cols, int box_rows, char* err, size_t errlen) {
+               long long bstride, int box_cols, int box_rows, bool f16, char* err, size_t errlen) {
   EncodeTiledFn enc = get_encode();
   if (!enc) { snprintf(err, errlen, "cuTensorMapEncodeTiled unavailable"); return false; }
   cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)batch};
@@ -578,7 +690,8 @@ bool encode_3d(CUtensorMap* m, const void* base, int cols, int rows, int batch, 
   cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   const CUtensorMapSwizzle sw = box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+  CUresult r = enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                   const_cast<void*>(base), dims, strides,
                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -590,33 +703,43 @@ bool encode_3d(CUtensorMap* m, const void* base, int cols, int rows, int batch, 
 }
 
 // Operand maps (A rows of a_rows, B rows of b_rows per box) and the 32 x 32
-// epilogue store maps for D.
-bool encode_all(const GemmParams& p, TmaArgs& tm, bool split, bool lo, int a_rows, int b_rows,
-                int bk, char* err, size_t errlen) {
+// epilogue store maps for D.  a_lo: the A operand's lo plane is read; b_lo:
+// the B operand's; lo: D is stored as (hi, lo); in16 / out16: operand and
+// output planes hold fp16 (else bf16).
+bool encode_all(const GemmParams& p, TmaArgs& tm, bool a_lo, bool b_lo, bool lo, bool in16, bool out16,
+                int a_rows, int b_rows, int bk, char* err, size_t errlen) {
   memset(&tm, 0, sizeof(tm));
   for (int g = 0; g < p.ngroups; ++g) {
     const GemmGroup& G = p.g[g];
-    if (!encode_3d(&tm.maps.a_hi[g], G.a_hi, G.K, G.M, G.batch, G.lda, G.a_bstride, bk, a_rows, err, errlen)) return false;
-    if (split && !encode_3d(&tm.maps.a_lo[g], G.a_lo, G.K, G.M, G.batch, G.lda, G.a_bstride, bk, a_rows, err, errlen)) return false;
+    if (!encode_3d(&tm.maps.a_hi[g], G.a_hi, G.K, G.M, G.batch, G.lda, G.a_bstride, bk, a_rows, in16, err, errlen)) return false;
+    if (a_lo && !encode_3d(&tm.maps.a_lo[g], G.a_lo, G.K, G.M, G.batch, G.lda, G.a_bstride, bk, a_rows, in16, err, errlen)) return false;
     if (!G.b_mn_major) {   // B operand: rows of an [N, K] plane
-      if (!encode_3d(&tm.maps.b_hi[g], G.b_hi, G.K, G.N, G.batch, G.ldb, G.b_bstride, bk, b_rows, err, errlen)) return false;
-      if (split && !encode_3d(&tm.maps.b_lo[g], G.b_lo, G.K, G.N, G.batch, G.ldb, G.b_bstride, bk, b_rows, err, errlen)) return false;
+      if (!encode_3d(&tm.maps.b_hi[g], G.b_hi, G.K, G.N, G.batch, G.ldb, G.b_bstride, bk, b_rows, in16, err, errlen)) return false;
+      if (b_lo && !encode_3d(&tm.maps.b_lo[g], G.b_lo, G.K, G.N, G.batch, G.ldb, G.b_bstride, bk, b_rows, in16, err, errlen)) return false;
     } else {               // B operand: [K, N] plane, 64-wide N boxes of bk rows
-      if (!encode_3d(&tm.maps.b_hi[g], G.b_hi, G.N, G.K, G.batch, G.ldb, G.b_bstride, 64, bk, err, errlen)) return false;
-      if (split && !encode_3d(&tm.maps.b_lo[g], G.b_lo, G.N, G.K, G.batch, G.ldb, G.b_bstride, 64, bk, err, errlen)) return false;
+      if (!encode_3d(&tm.maps.b_hi[g], G.b_hi, G.N, G.K, G.batch, G.ldb, G.b_bstride, 64, bk, in16, err, errlen)) return false;
+      if (b_lo && !encode_3d(&tm.maps.b_lo[g], G.b_lo, G.N, G.K, G.batch, G.ldb, G.b_bstride, 64, bk, in16, err, errlen)) return false;
     }
-    if (!encode_3d(&tm.maps.d_hi[g], G.d_hi, G.N, G.M, G.batch, G.ldd, G.d_bstride, 32, 32, err, errlen)) return false;
-    if (lo && !encode_3d(&tm.maps.d_lo[g], G.d_lo, G.N, G.M, G.batch, G.ldd, G.d_bstride, 32, 32, err, errlen)) return false;
+    if (!encode_3d(&tm.maps.d_hi[g], G.d_hi, G.N, G.M, G.batch, G.ldd, G.d_bstride, 32, 32, out16, err, errlen)) return false;
+    if (lo && !encode_3d(&tm.maps.d_lo[g], G.d_lo, G.N, G.M, G.batch, G.ldd, G.d_bstride, 32, 32, out16, err, errlen)) return false;
+    // C of a non-symmetric output is read by the epilogue through TMA, in the
+    // operands' format
+    if (p.beta != 0.f && !G.symmetric) {
+      if (!encode_3d(&tm.maps.c_hi[g], G.c_hi, G.N, G.M, G.batch, G.ldc, G.c_bstride, 32, 32, in16, err, errlen)) return false;
+      if (lo && !encode_3d(&tm.maps.c_lo[g], G.c_lo, G.N, G.M, G.batch, G.ldc, G.c_bstride, 32, 32, in16, err, errlen)) return false;
+    }
   }
   return true;
 }
 
-template <int TERMS, bool LO, int BK>
+template <int TERMS, bool LO, int BK, int FMT>
 cudaError_t launch_pairs(const GemmParams& p, cudaStream_t s, char* err, size_t errlen) {
   TmaArgs tm;
   // each CTA's B box is its 128-row half of the pair's 256 B rows
-  if (!encode_all(p, tm, TERMS == 3, LO, BM, 128, BK, err, errlen)) return cudaErrorInvalidValue;
-  auto k = ns_gemm_tc_kernel<TERMS, LO, BK>;
+  if (!encode_all(p, tm, TERMS == 3, TERMS == 3, LO, FMT == kFmtF16, FMT != kFmtBf16, BM, 128, BK, err,
+                  errlen))
+    return cudaErrorInvalidValue;
+  auto k = ns_gemm_tc_kernel<TERMS, LO, BK, FMT>;
   const int smem = Stages<TERMS, BM, 128, BK>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -644,21 +767,36 @@ cudaError_t launch_pairs(const GemmParams& p, cudaStream_t s, char* err, size_t 
   return cudaGetLastError();
 }
 
-}  // namespace
-
 // One layout: CTA pairs.  Three-product launches take k-steps of 32 (64-byte
 // swizzled operand rows); one-product launches take 64 (128-byte rows): with
 // one product per k-step, 64-byte rows asked the copy engine for more rows
 // per clock than it sustains (measured: 20-38 % longer one-product launches).
+template <int FMT>
+cudaError_t launch_fmt(const GemmParams& p, cudaStream_t s, char* err, size_t errlen) {
+  if (p.terms == 3) return launch_pairs<3, true, 32, FMT>(p, s, err, errlen);
+  return launch_pairs<1, true, 64, FMT>(p, s, err, errlen);
+}
+
+}  // namespace
+
 cudaError_t launch_ns_gemm_tc(const GemmParams& p, cudaStream_t s, char* err, size_t errlen) {
   if (p.total_tiles <= 0) return cudaSuccess;
   if (!p.sched) {
     snprintf(err, errlen, "tensor-core GEMM launched without a tile counter");
     return cudaErrorInvalidValue;
   }
-  const bool lo = p.xmode == kXSplit;
-  if (lo && p.terms == 3) return launch_pairs<3, true, 32>(p, s, err, errlen);
-  return lo ? launch_pairs<1, true, 64>(p, s, err, errlen) : launch_pairs<1, false, 64>(p, s, err, errlen);
+  if (p.xmode != kXSplit) {            // one bf16 plane, one product
+    if (p.terms != 1 || p.fmt != kFmtBf16) {
+      snprintf(err, errlen, "plain bf16 planes take one bf16 product");
+      return cudaErrorInvalidValue;
+    }
+    return launch_pairs<1, false, 64, kFmtBf16>(p, s, err, errlen);
+  }
+  switch (p.fmt) {
+    case kFmtBf16: return launch_fmt<kFmtBf16>(p, s, err, errlen);
+    case kFmtBf16ToF16: return launch_fmt<kFmtBf16ToF16>(p, s, err, errlen);
+    default: return launch_fmt<kFmtF16>(p, s, err, errlen);
+  }
 }
 
 }  // namespace mc

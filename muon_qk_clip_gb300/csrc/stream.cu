@@ -128,13 +128,21 @@ __device__ inline void raw_cvt4(const uint4& u, int half, float (&o)[4]) {
     o[2] = __uint_as_float(u.z); o[3] = __uint_as_float(u.w);
   }
 }
-// The iterate's value from the raw words of its plane(s).
-template <int XM>
+// Four fp16 values packed two per word in .x/.y.
+__device__ inline void raw_cvt4_f16(const uint4& u, float (&o)[4]) {
+  o[0] = from16<true>((uint16_t)(u.x & 0xffffu)); o[1] = from16<true>((uint16_t)(u.x >> 16));
+  o[2] = from16<true>((uint16_t)(u.y & 0xffffu)); o[3] = from16<true>((uint16_t)(u.y >> 16));
+}
+// The iterate's value from the raw words of its plane(s); XF16: the split
+// planes hold fp16 (else bf16).
+template <int XM, bool XF16>
 __device__ inline void raw_cvt_x4(const uint4& a, const uint4& b, float (&o)[4]) {
-  raw_cvt4(a, XM != kXF32, o);
+  if (XM == kXSplit && XF16) raw_cvt4_f16(a, o);
+  else raw_cvt4(a, XM != kXF32, o);
   if (XM == kXSplit) {
     float l[4];
-    raw_cvt4(b, 1, l);
+    if (XF16) raw_cvt4_f16(b, l);
+    else raw_cvt4(b, 1, l);
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[e] += l[e];
   }
@@ -290,10 +298,11 @@ __global__ void norms_kernel(const __grid_constant__ NormParams p) {
   }
 }
 
-// Same tile layout as prep_kernel (the step's split-bf16 / bf16-W case takes
-// 16-byte accesses instead); every load of a tile is issued before the first
-// store of W.
-template <int XM>
+// Same tile layout as prep_kernel (the step's split-iterate / bf16-W case
+// takes 16-byte accesses instead); every load of a tile is issued before the
+// first store of W.  XF16: the split iterate's planes hold fp16 (after at
+// least one Newton-Schulz iteration), else bf16.
+template <int XM, bool XF16>
 __global__ void __launch_bounds__(kThreads) apply_kernel(const __grid_constant__ ApplyParams p) {
   __shared__ float tile[kTile][kTile + 1];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -328,11 +337,11 @@ __global__ void __launch_bounds__(kThreads) apply_kernel(const __grid_constant__
         }
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-          const __nv_bfloat16* a = reinterpret_cast<const __nv_bfloat16*>(&xh[k]);
-          const __nv_bfloat16* b2 = reinterpret_cast<const __nv_bfloat16*>(&xl[k]);
+          const uint16_t* a = reinterpret_cast<const uint16_t*>(&xh[k]);
+          const uint16_t* b2 = reinterpret_cast<const uint16_t*>(&xl[k]);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
-            tile[tx8 * 8 + e][ty8 + 32 * k] = __bfloat162float(a[e]) + __bfloat162float(b2[e]);
+            tile[tx8 * 8 + e][ty8 + 32 * k] = from16<XF16>(a[e]) + from16<XF16>(b2[e]);
         }
         __syncthreads();
       } else {
@@ -351,15 +360,15 @@ __global__ void __launch_bounds__(kThreads) apply_kernel(const __grid_constant__
       for (int k = 0; k < 2; ++k) {
         const int rl = ty8 + 32 * k, r = r0 + rl;
         if (r >= jb.rows) continue;
-        const __nv_bfloat16* a = reinterpret_cast<const __nv_bfloat16*>(&xh[k]);
-        const __nv_bfloat16* b2 = reinterpret_cast<const __nv_bfloat16*>(&xl[k]);
+        const uint16_t* a = reinterpret_cast<const uint16_t*>(&xh[k]);
+        const uint16_t* b2 = reinterpret_cast<const uint16_t*>(&xl[k]);
         const __nv_bfloat16* w8 = reinterpret_cast<const __nv_bfloat16*>(&wv[k]);
         uint4 outv;
         __nv_bfloat16* o8 = reinterpret_cast<__nv_bfloat16*>(&outv);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float x = jb.transpose ? tile[rl][tx8 * 8 + e]
-                                       : __bfloat162float(a[e]) + __bfloat162float(b2[e]);
+                                       : from16<XF16>(a[e]) + from16<XF16>(b2[e]);
           const float w = __bfloat162float(w8[e]);
           const float v = fmaf(-p.lr, fmaf(p.wd, w, s * x), w);   // w - lr (s x + wd w)
           bad8 |= !finite_f(v) && (e < nc8);
@@ -390,7 +399,7 @@ __global__ void __launch_bounds__(kThreads) apply_kernel(const __grid_constant__
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         float x[4];
-        raw_cvt_x4<XM>(xa[k], xb[k], x);
+        raw_cvt_x4<XM, XF16>(xa[k], xb[k], x);
 #pragma unroll
         for (int e = 0; e < 4; ++e) tile[tx * 4 + e][ty + 16 * k] = x[e];
       }
@@ -421,7 +430,7 @@ __global__ void __launch_bounds__(kThreads) apply_kernel(const __grid_constant__
 #pragma unroll
         for (int e = 0; e < 4; ++e) x[e] = tile[ty + 16 * k][cl0 + e];
       } else {
-        raw_cvt_x4<XM>(xa[k], xb[k], x);
+        raw_cvt_x4<XM, XF16>(xa[k], xb[k], x);
       }
       raw_cvt4(wr[k], jb.out_bf16, w);
 #pragma unroll
@@ -632,9 +641,14 @@ cudaError_t launch_norms(const double* partials, const int* tile_begin, const in
 cudaError_t launch_apply(const ApplyParams& p, cudaStream_t s) {
   if (p.total_tiles <= 0) return cudaSuccess;
   switch (p.xmode) {
-    case kXSplit: apply_kernel<kXSplit><<<grid_for(apply_kernel<kXSplit>, p.total_tiles), kThreads, 0, s>>>(p); break;
-    case kXBf16: apply_kernel<kXBf16><<<grid_for(apply_kernel<kXBf16>, p.total_tiles), kThreads, 0, s>>>(p); break;
-    default: apply_kernel<kXF32><<<grid_for(apply_kernel<kXF32>, p.total_tiles), kThreads, 0, s>>>(p); break;
+    case kXSplit:
+      if (p.x_f16)
+        apply_kernel<kXSplit, true><<<grid_for(apply_kernel<kXSplit, true>, p.total_tiles), kThreads, 0, s>>>(p);
+      else
+        apply_kernel<kXSplit, false><<<grid_for(apply_kernel<kXSplit, false>, p.total_tiles), kThreads, 0, s>>>(p);
+      break;
+    case kXBf16: apply_kernel<kXBf16, false><<<grid_for(apply_kernel<kXBf16, false>, p.total_tiles), kThreads, 0, s>>>(p); break;
+    default: apply_kernel<kXF32, false><<<grid_for(apply_kernel<kXF32, false>, p.total_tiles), kThreads, 0, s>>>(p); break;
   }
   return cudaGetLastError();
 }

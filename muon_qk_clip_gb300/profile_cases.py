@@ -1,5 +1,5 @@
 """One-shot cases for profilers (ncu): run a single call of the library on
-the dense_block shapes and exit.
+one workload's shapes (dense_block unless --workload says otherwise) and exit.
 
   python -m muon_qk_clip_gb300.profile_cases step        # one full MuonClip step
   python -m muon_qk_clip_gb300.profile_cases ns          # Newton-Schulz of the 7 matrices
@@ -25,15 +25,27 @@ def main():
     ap.add_argument("case", choices=["step", "ns", "max_logit", "attn_fwd", "momentum"])
     ap.add_argument("--repeat", type=int, default=1)
     ap.add_argument("--precision", type=int, default=0, help="mc_ns_precision")
+    ap.add_argument("--fast-steps", type=int, default=None, help="ns_fast_steps (library default if unset)")
+    ap.add_argument("--workload", default="dense_block", choices=list(synth.WORKLOADS))
+    ap.add_argument("--experts", type=int, default=0,
+                    help="moe_experts only: keep this many matrices of each shape (0: all 64)")
     args = ap.parse_args()
     build.build()
     dev = torch.device("cuda", 0)
-    wl = synth.workload("dense_block")
+    wl = synth.workload(args.workload)
     att = wl.attention
-    W, G, M = synth.muon_inputs(wl, device=dev)
+    if args.case in ("step", "max_logit", "attn_fwd") and (att is None or att.kind != "mha"):
+        raise SystemExit(f"case {args.case} runs on an MHA layer; {args.workload} has none")
+    if args.experts and args.workload != "moe_experts":
+        raise SystemExit("--experts applies to moe_experts")
     names = [m.name for m in wl.matrices]
+    if args.experts:
+        names = [n for n in names if int(n[1:n.index("_")]) < args.experts]
+    W, G, M = synth.muon_inputs(wl, device=dev, only=names)
     Wl, Gl, Ml = [W[n] for n in names], [G[n] for n in names], [M[n] for n in names]
     hp = mc.Hparams(ns_precision=args.precision)
+    if args.fast_steps is not None:
+        hp.ns_fast_steps = args.fast_steps
     if args.case in ("step", "max_logit", "attn_fwd"):
         X = synth.normal((att.B, att.S, att.d_model), 1.0, "X", 0, torch.bfloat16, dev)
         q, k = forward.project_mha(X, W["Wq"], W["Wk"], att.H)

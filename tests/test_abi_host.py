@@ -76,7 +76,7 @@ def test_default_hparams(lib):
     assert (h.mu, h.weight_decay, h.rms_scale, h.ns_steps, h.tau, h.alpha) == pytest.approx(
         (0.95, 0.1, 0.2, 5, 100.0, 0.5))
     assert (h.ns_a, h.ns_b, h.ns_c) == pytest.approx((3.4445, -4.7750, 2.0315))
-    assert h.ns_fast_steps == 2
+    assert h.ns_fast_steps == 3
     assert lib.mc_version().decode().startswith("muonclip")
 
 

@@ -48,24 +48,26 @@ def test_counted_flops(bench):
 
 def test_products_per_iteration(bench):
     F, S, G1 = (1, 1, 1), (3, 3, 3), (1, 3, 3)
-    assert bench.ns_products(512, 7168, 5, 2) == [S] * 5              # smaller side < 1024
-    assert bench.ns_products(1024, 1536, 5, 2) == [F, F, S, S, S]
-    assert bench.ns_products(1024, 1536, 5, 3) == [F, F, S, S, S]     # third only from 2048
-    assert bench.ns_products(2048, 5632, 5, 2) == [F, F, G1, S, S]    # one-product Gram from 2048
-    assert bench.ns_products(2048, 5632, 5, 3) == [F, F, F, S, S]
-    assert bench.ns_products(2048, 5632, 4, 3) == [F, S, S, S]        # three split ones kept
-    assert bench.ns_products(2048, 2048, 5, 0) == [S] * 5
-    assert bench.ns_products(2048, 2048, 5, 2, split=False) == [F] * 5
+    assert bench.ns_products(128, 7168, 5, 3) == [S] * 5              # smaller side < 256
+    assert bench.ns_products(256, 7168, 5, 3) == [F, F, F, G1, G1]
+    assert bench.ns_products(1024, 1536, 5, 3) == [F, F, F, G1, G1]
+    assert bench.ns_products(1024, 1536, 5, 4) == [F, F, F, F, G1]   # a fourth from 1024
+    assert bench.ns_products(512, 1536, 5, 4) == [F, F, F, G1, G1]   # not below it
+    assert bench.ns_products(2048, 5632, 5, 2) == [F, F, G1, G1, G1]
+    assert bench.ns_products(2048, 5632, 4, 3) == [F, F, G1, G1]     # two three-term kept
+    assert bench.ns_products(2048, 5632, 4, 4) == [F, F, F, G1]      # one kept
+    assert bench.ns_products(2048, 2048, 5, 0) == [G1] * 5
+    assert bench.ns_products(2048, 2048, 5, 3, split=False) == [F] * 5
 
 
 def test_executed_flops_weight_each_phase_by_its_products(bench):
     m, n = 2048, 5632
     e = bench.ns_sym_entries(m)
     g, p, u = 2.0 * n * e, 2.0 * m * e, 2.0 * m * m * n
-    # iterations: one-product x 2, one-product Gram + three-term rest, three-term x 2
-    want = 2 * (g + p + u) + (g + 3 * p + 3 * u) + 2 * 3 * (g + p + u)
-    assert bench.ns_flops_executed(m, n, 5, 2) == want
-    assert bench.ns_flops_executed(m, n, 5, 2, split=False) == bench.ns_flops_counted(m, n, 5)
+    # iterations: one-product x 3, then one-product Gram + three-term rest x 2
+    want = 3 * (g + p + u) + 2 * (g + 3 * p + 3 * u)
+    assert bench.ns_flops_executed(m, n, 5, 3) == want
+    assert bench.ns_flops_executed(m, n, 5, 3, split=False) == bench.ns_flops_counted(m, n, 5)
 
 
 def test_traffic_is_taken_only_for_the_profiled_source(bench, tmp_path, monkeypatch):
@@ -105,7 +107,8 @@ def test_oracle_sample_covers_every_workload(bench):
         assert (plan["heads"] > 0) == (wl.attention is not None), name
 
 
-@pytest.mark.parametrize("steps,fast", [(5, 2), (5, 3), (5, 0), (5, 1), (4, 3), (6, 2), (3, 2), (0, 2)])
+@pytest.mark.parametrize("steps,fast", [(5, 2), (5, 3), (5, 4), (5, 0), (5, 1), (4, 3), (4, 4), (6, 5),
+                                        (3, 2), (2, 4), (0, 2)])
 def test_products_mirror_the_library_plan(bench, steps, fast):
     """bench.py's executed-flop accounting uses a copy of the library's plan of
     products per k-step; the library reports its own through mc_ns_products."""
@@ -114,8 +117,8 @@ def test_products_mirror_the_library_plan(bench, steps, fast):
     build.build()
     abi.load()
     hp = mc.Hparams(ns_steps=steps, ns_fast_steps=fast)
-    for r, c in [(64, 64), (512, 7168), (1024, 1536), (1536, 1024), (2047, 4096), (2048, 2048),
-                 (2048, 5632), (7168, 2048), (8192, 7168)]:
+    for r, c in [(64, 64), (255, 300), (256, 256), (512, 7168), (1023, 1536), (1024, 1536),
+                 (1536, 1024), (2047, 4096), (2048, 2048), (2048, 5632), (7168, 2048), (8192, 7168)]:
         assert mc.ns_products(r, c, hp) == bench.ns_products(r, c, steps, fast), (r, c)
 
 
