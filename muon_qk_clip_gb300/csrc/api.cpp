@@ -421,6 +421,9 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
       ++launch;
       gp.terms = terms;
       gp.fmt = ns_fmt(P.xmode, it, ph);
+      // a one-product iteration's update reads only the polynomial's hi
+      // plane (its a X term comes from X), so that lo plane is not stored
+      gp.d_hi_only = P.xmode == kXSplit && ph == kPoly && terms == 1;
       // Three-term iterations fold a X into the polynomial: B' = c A^2 + b A + a I
       // and X' = B' X, so the last phase reads no C.  (B' holds ~16 significand
       // bits there; a one-plane bf16 B' would lose the small singular values, so

@@ -140,6 +140,7 @@ struct GemmParams {
   int terms;              // tensor-core products per k-step: 1 (hi*hi), 2 (hi*hi + hi*lo_B)
                           // or 3 (hi*hi + hi*lo + lo*hi)
   int fmt;                // tensor-core planes: kFmtBf16, kFmtBf16ToF16 or kFmtF16
+  int d_hi_only;          // split planes: store only D's hi plane (no consumer reads lo)
   float alpha, beta;
   float diag;             // added on the diagonal of each output item
   const float* s;         // per-matrix scale, or null

@@ -341,10 +341,11 @@ __device__ bool epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
     // by TMA the slot was last read by this chunk's own C box, already used)
     if (lane == 0 && !tmac) bulk_wait_read_upto(depth - 1);
     __syncwarp();
+    const bool st_lo = LO && !p.d_hi_only;          // warp-uniform
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       *reinterpret_cast<uint4*>(db + swz64(lane, j * 16)) = *reinterpret_cast<const uint4*>(hb + j * 8);
-      if (LO)
+      if (st_lo)
         *reinterpret_cast<uint4*>(db + 2048 + swz64(lane, j * 16)) = *reinterpret_cast<const uint4*>(lb + j * 8);
     }
     if (mode == 2) {
@@ -352,17 +353,17 @@ __device__ bool epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         *reinterpret_cast<uint16_t*>(mb + swz64(c, 2 * lane)) = hb[c];
-        if (LO) *reinterpret_cast<uint16_t*>(mb + 2048 + swz64(c, 2 * lane)) = lb[c];
+        if (st_lo) *reinterpret_cast<uint16_t*>(mb + 2048 + swz64(c, 2 * lane)) = lb[c];
       }
     }
     fence_async_smem();
     __syncwarp();
     if (lane == 0) {
       tma_store_3d(&tm.maps.d_hi[tc.g], db, col0, r0, tc.b);
-      if (LO) tma_store_3d(&tm.maps.d_lo[tc.g], db + 2048, col0, r0, tc.b);
+      if (st_lo) tma_store_3d(&tm.maps.d_lo[tc.g], db + 2048, col0, r0, tc.b);
       if (mode == 2) {
         tma_store_3d(&tm.maps.d_hi[tc.g], mb, r0, col0, tc.b);
-        if (LO) tma_store_3d(&tm.maps.d_lo[tc.g], mb + 2048, r0, col0, tc.b);
+        if (st_lo) tma_store_3d(&tm.maps.d_lo[tc.g], mb + 2048, r0, col0, tc.b);
       }
       bulk_commit();
       // two chunks on, C goes into this slot again once the store has read it
