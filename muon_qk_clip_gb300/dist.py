@@ -12,7 +12,9 @@ max over X in B), so the per-rank S_max vectors are combined with one
 all-reduce(MAX) of H floats per layer before the step; every rank then makes
 the same clip decision.
 
-The collectives run through torch.distributed (NCCL on GPUs, gloo on CPU).
+The collectives run through torch.distributed: NCCL on device tensors, or
+gloo, which takes host tensors (device tensors then go through host copies,
+so ranks sharing one GPU can run the library with gloo collectives).
 """
 from __future__ import annotations
 
@@ -38,10 +40,34 @@ def partition_matrices(shapes, world: int, steps: int = 5):
     return owner
 
 
+def _host_staged(t: torch.Tensor, group) -> bool:
+    """gloo collectives take host tensors: a device tensor is staged."""
+    return t.device.type != "cpu" and dist.get_backend(group) == "gloo"
+
+
+def _all_reduce(t: torch.Tensor, op, group=None):
+    if _host_staged(t, group):
+        h = t.cpu()
+        dist.all_reduce(h, op=op, group=group)
+        t.copy_(h)
+    else:
+        dist.all_reduce(t, op=op, group=group)
+
+
+def _all_gather(bufs, t: torch.Tensor, group=None):
+    if _host_staged(t, group):
+        hb = [torch.empty(b.shape, dtype=b.dtype) for b in bufs]
+        dist.all_gather(hb, t.cpu(), group=group)
+        for b, h in zip(bufs, hb):
+            b.copy_(h)
+    else:
+        dist.all_gather(bufs, t, group=group)
+
+
 def allreduce_smax(smax: torch.Tensor, group=None) -> torch.Tensor:
     """In place: S_max^h = max over every rank's micro-batches."""
     if dist.is_available() and dist.is_initialized():
-        dist.all_reduce(smax, op=dist.ReduceOp.MAX, group=group)
+        _all_reduce(smax, dist.ReduceOp.MAX, group)
     return smax
 
 
@@ -68,7 +94,12 @@ def sharded_step(W, G, M, layers, step_fn, hp=None, group=None, owner=None):
     if world > 1:
         for i, w in enumerate(W):
             src = owner[i] if group is None else dist.get_global_rank(group, owner[i])
-            dist.broadcast(w, src=src, group=group)
+            if _host_staged(w, group):
+                h = w.cpu()
+                dist.broadcast(h, src=src, group=group)
+                w.copy_(h)
+            else:
+                dist.broadcast(w, src=src, group=group)
     return owner
 
 
@@ -161,7 +192,7 @@ def _reduce_scatter_mean(flat, layout: Zero1Layout, rank, group):
     if dist.get_backend(group) == "nccl":
         dist.reduce_scatter_tensor(out, flat, op=dist.ReduceOp.SUM, group=group)
     else:                          # gloo has no reduce-scatter: all-reduce, keep the slice
-        dist.all_reduce(flat, op=dist.ReduceOp.SUM, group=group)
+        _all_reduce(flat, dist.ReduceOp.SUM, group)
         lo, hi = layout.slice(rank)
         out.copy_(flat[lo:hi])
     return out.div_(world)
@@ -183,7 +214,7 @@ def _gather_boundary(M_shard, layout: Zero1Layout, rank, group):
         pack[pos:pos + hi - lo].copy_(M_shard[a:a + hi - lo])
         pos += hi - lo
     bufs = [torch.empty_like(pack) for _ in range(world)]
-    dist.all_gather(bufs, pack, group=group)
+    _all_gather(bufs, pack, group)
     where = {}                                   # (matrix, rank) -> (buffer, position)
     for r in range(world):
         pos = 0
@@ -250,7 +281,7 @@ def zero1_step(W, G, M_shard, layout: Zero1Layout, layers, ops, hp, group=None):
         wflat = _flat(W, layout, W[0].dtype)
         lo, hi = layout.slice(rank)
         parts = [torch.empty(layout.shard, dtype=wflat.dtype, device=wflat.device) for _ in range(world)]
-        dist.all_gather(parts, wflat[lo:hi].contiguous(), group=group)
+        _all_gather(parts, wflat[lo:hi].contiguous(), group)
         wfull = torch.cat(parts)
         for i, w in enumerate(W):
             a = layout.offsets[i]
