@@ -535,26 +535,40 @@ def gpu_arm(args):
     res = torch.empty(2 * H + 2, dtype=torch.float32, device=dev)
     G_slots = [Gl, [torch.empty_like(g) for g in Gl]]
     F_slots = [feats, [torch.empty_strided(t.size(), t.stride(), dtype=t.dtype, device=dev) for t in feats]]
-    copy_stream = torch.cuda.Stream(device=dev)
-    ready = [torch.cuda.Event(), torch.cuda.Event()]      # slot's inputs landed
+    # the copies are spread over several streams (one copy engine each) in
+    # about equal byte shares, so the host link is not left to one engine
+    n_copy = args.copy_streams
+    copy_streams = [torch.cuda.Stream(device=dev) for _ in range(n_copy)]
+    pairs_of = [[] for _ in range(2)]
+    for slot in range(2):
+        items = list(zip(G_slots[slot], Gh)) + list(zip(F_slots[slot], fh))
+        items.sort(key=lambda x: -x[1].numel() * x[1].element_size())
+        loads = [0] * n_copy
+        share = [[] for _ in range(n_copy)]
+        for d, h in items:
+            k = loads.index(min(loads))
+            share[k].append((d, h))
+            loads[k] += h.numel() * h.element_size()
+        pairs_of[slot] = share
+    ready = [[torch.cuda.Event() for _ in range(n_copy)] for _ in range(2)]   # slot's inputs landed
     consumed = [torch.cuda.Event(), torch.cuda.Event()]   # slot's inputs read by its step
     used = [False, False]
 
     def issue_copies(slot):
-        with torch.cuda.stream(copy_stream):
-            if used[slot]:
-                copy_stream.wait_event(consumed[slot])
-            for gd, gh in zip(G_slots[slot], Gh):
-                gd.copy_(gh, non_blocking=True)
-            for td, th in zip(F_slots[slot], fh):
-                td.copy_(th, non_blocking=True)
-            ready[slot].record(copy_stream)
+        for k, cs in enumerate(copy_streams):
+            with torch.cuda.stream(cs):
+                if used[slot]:
+                    cs.wait_event(consumed[slot])
+                for d, h in pairs_of[slot][k]:
+                    d.copy_(h, non_blocking=True)
+                ready[slot][k].record(cs)
 
     # a step whose inputs fit in L2 flushes it inside the region (counted)
     e2e_flush = h2d < 129 * 2 ** 20
 
     def e2e_step(slot):
-        stream.wait_event(ready[slot])
+        for ev_k in ready[slot]:
+            stream.wait_event(ev_k)
         if e2e_flush:
             flush.zero_()
         if att is not None:
@@ -573,7 +587,8 @@ def gpu_arm(args):
         out_h.copy_(res, non_blocking=True)
 
     def e2e_run(n):
-        copy_stream.wait_stream(stream)
+        for cs in copy_streams:
+            cs.wait_stream(stream)
         issue_copies(0)
         for i in range(n):
             if i + 1 < n:
@@ -666,7 +681,8 @@ def gpu_arm(args):
            "l2": "flushed (512 MB write) before each step; e2e: " + (
                "flushed inside the timed region before each step" if e2e_flush else
                "not flushed, each step's host inputs (G, Q/K) are larger than L2"),
-           "e2e_pipeline": "inputs double-buffered: step i+1's host copies overlap step i",
+           "e2e_pipeline": (f"inputs double-buffered: step i+1's host copies overlap step i, spread "
+                            f"over {args.copy_streams} copy streams"),
            "parallelism": f"dp{world} (one layer per rank)"}
 
     if rank != 0:
@@ -743,6 +759,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--copy-streams", type=int, default=1,
+                    help="streams the end-to-end run spreads its host-to-device copies over")
     ap.add_argument("--no-components", action="store_true",
                     help="skip the attention-side and clip-stress figures")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(WORKLOAD_CONFIG),
