@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <memory>
 #include <string>
 #include <vector>
 
@@ -336,7 +337,8 @@ int ns_fmt(int xmode, int it, int ph) {
 }
 
 mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams* hp,
-                    int32_t* status, int& launch, const std::vector<int>& groups, cudaStream_t s) {
+                    int32_t* status, int& launch, const std::vector<int>& groups, cudaStream_t s,
+                    const FusedApply* fa) {
   const int cur = it & 1, nxt = cur ^ 1;
   const size_t es = P.xmode == kXF32 ? 4 : 2;
   // heavier K first for a better tail
@@ -448,7 +450,9 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
         e = launch_ns_gemm_f32(gp, s);
       } else {
         char err[256] = {0};
-        e = launch_ns_gemm_tc(gp, s, err, sizeof err);
+        // the last update applies the step itself when the caller's W allow it
+        const bool apply_here = fa && ph == kNext && it == hp->ns_steps - 1;
+        e = launch_ns_gemm_tc(gp, apply_here ? fa : nullptr, s, err, sizeof err);
         if (e != cudaSuccess && err[0]) return fail(MC_ERR_CUDA, "tensor-core GEMM: %s", err);
       }
       if (e != cudaSuccess) return cuda_fail(e, "Newton-Schulz GEMM launch");
@@ -485,7 +489,7 @@ cudaError_t aux_stream(AuxStream*& out) {
 }
 
 mc_status run_newton_schulz(Plan& P, void* ws, const mc_hparams* hp, int32_t* status,
-                            cudaStream_t s) {
+                            cudaStream_t s, const FusedApply* fa = nullptr) {
   if (P.nsched > 0 && hp->ns_steps > 0) {
     cudaError_t e = cudaMemsetAsync(wsp(ws, P.off_sched), 0, (size_t)P.nsched * sizeof(int), s);
     if (e != cudaSuccess) return cuda_fail(e, "tile counters");
@@ -525,8 +529,8 @@ mc_status run_newton_schulz(Plan& P, void* ws, const mc_hparams* hp, int32_t* st
     int launch = 0;
     for (int it = 0; it < hp->ns_steps && st == MC_OK; ++it) {
       for (Phase ph : {kGram, kPoly, kNext}) {
-        if ((st = run_phase(P, ws, ph, it, hp, status, launch, set[0], s)) != MC_OK) break;
-        if (aux && (st = run_phase(P, ws, ph, it, hp, status, launch, set[1], aux->s)) != MC_OK) break;
+        if ((st = run_phase(P, ws, ph, it, hp, status, launch, set[0], s, fa)) != MC_OK) break;
+        if (aux && (st = run_phase(P, ws, ph, it, hp, status, launch, set[1], aux->s, fa)) != MC_OK) break;
       }
     }
     ps.n = launch;
@@ -540,6 +544,37 @@ mc_status run_newton_schulz(Plan& P, void* ws, const mc_hparams* hp, int32_t* st
     }
   }
   return st;
+}
+
+// Update factor on NewtonSchulz(M) for a [rows, cols] weight (update-RMS or
+// spectral, mc_scale_mode).
+float update_factor(const mc_hparams* hp, int rows, int cols) {
+  return hp->scale_mode == MC_SCALE_SPECTRAL
+             ? (float)std::sqrt(std::max(1.0, (double)rows / (double)cols))
+             : (float)((double)hp->rms_scale * std::sqrt((double)std::max(rows, cols)));
+}
+
+// The last update can apply the step when the iterate is split, every W is
+// bf16, the table holds every matrix and that update takes three products.
+bool can_fuse_apply(const Plan& P, const mc_mat* W, const mc_hparams* hp) {
+  if (P.xmode != kXSplit || hp->ns_steps < 1 || P.count > kMaxFusedApply) return false;
+  for (int j = 0; j < P.count; ++j)
+    if (W[j].dtype != MC_BF16) return false;
+  for (const Group& g : P.groups)
+    if (ns_terms(hp, std::min(g.m, g.n), hp->ns_steps - 1, kNext) != 3) return false;
+  return true;
+}
+
+void fill_fused_apply(const Plan& P, const mc_mat* W, const mc_hparams* hp, FusedApply& fa) {
+  fa.lr = hp->lr;
+  fa.wd = hp->weight_decay;
+  for (int j = 0; j < P.count; ++j) {
+    FusedApplyJob& jb = fa.job[j];
+    jb.w = W[j].ptr;
+    jb.ld = W[j].ld;
+    jb.transpose = P.transpose[j];
+    jb.scale = update_factor(hp, (int)W[j].rows, (int)W[j].cols);
+  }
 }
 
 mc_status run_apply(const Plan& P, void* ws, mc_mat* out, bool write_o, const mc_hparams* hp,
@@ -574,9 +609,7 @@ mc_status run_apply(const Plan& P, void* ws, mc_mat* out, bool write_o, const mc
       jb.tile_begin = t;
       jb.tiles_c = (int)cdiv(jb.cols, 64);
       jb.mat = j;
-      jb.scale = hp->scale_mode == MC_SCALE_SPECTRAL
-                     ? (float)std::sqrt(std::max(1.0, (double)jb.rows / (double)jb.cols))
-                     : (float)((double)hp->rms_scale * std::sqrt((double)std::max(jb.rows, jb.cols)));
+      jb.scale = update_factor(hp, jb.rows, jb.cols);
       t += (int)(cdiv(jb.rows, 64) * jb.tiles_c);
     }
     ap.total_tiles = t;
@@ -952,11 +985,18 @@ mc_status muonclip_step(mc_mat* W, const mc_mat* G, mc_mat* M, int32_t count,
   Plan P = make_plan(Wo.data(), count, resolve_xmode(hp->ns_precision, any_f32));
   if ((st = check_ws(workspace, workspace_bytes, P.bytes)) != MC_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  // Algorithm 1, part 1: Muon on every matrix
+  // Algorithm 1, part 1: Muon on every matrix.  With bf16 weights on the split
+  // path the last Newton-Schulz update applies the step in its epilogue (no
+  // separate pass over the iterate); otherwise apply_kernel does.
+  std::unique_ptr<FusedApply> fa;
+  if (can_fuse_apply(P, Wo.data(), hp)) {
+    fa.reset(new FusedApply());
+    fill_fused_apply(P, Wo.data(), hp, *fa);
+  }
   if ((st = run_prep(P, workspace, Mo.data(), Go.data(), true, true, hp->mu, status, s)) != MC_OK) return st;
   if ((st = run_norms(P, workspace, hp->ns_eps, s)) != MC_OK) return st;
-  if ((st = run_newton_schulz(P, workspace, hp, status, s)) != MC_OK) return st;
-  if ((st = run_apply(P, workspace, Wo.data(), false, hp, status, s)) != MC_OK) return st;
+  if ((st = run_newton_schulz(P, workspace, hp, status, s, fa.get())) != MC_OK) return st;
+  if (!fa && (st = run_apply(P, workspace, Wo.data(), false, hp, status, s)) != MC_OK) return st;
   // Algorithm 1, part 2: per-head QK-Clip on the updated weights
   for (int l = 0; l < nlayers; ++l) {
     const mc_clip_layer& L = layers[l];

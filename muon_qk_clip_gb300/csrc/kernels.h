@@ -148,8 +148,28 @@ struct GemmParams {
   int* sched;             // zeroed tile counter of this launch (tensor-core path)
 };
 
-// Tensor-core path (split bf16 or bf16).  Encodes its own tensor maps.
-cudaError_t launch_ns_gemm_tc(const GemmParams& p, cudaStream_t s, char* err, size_t errlen);
+// The last Newton-Schulz update can apply the step itself: instead of storing
+// the final iterate it writes W <- W - lr (scale_j D + wd W) for each matrix j
+// (bf16 W in the caller's layout; the matrix is the transpose of its oriented
+// iterate when rows > cols).  Indexed by the matrix order of the plan.
+constexpr int kMaxFusedApply = 192;
+struct FusedApplyJob {
+  void* w;             // bf16 W [rows, cols], updated in place
+  long long ld;        // row pitch in elements (16-byte multiple)
+  int transpose;       // W = X^T (rows > cols)
+  float scale;         // factor on the Newton-Schulz output (update-RMS or spectral)
+};
+struct FusedApply {
+  static constexpr bool kOn = true;
+  FusedApplyJob job[kMaxFusedApply];
+  float lr, wd;
+};
+
+// Tensor-core path (split bf16 or bf16).  Encodes its own tensor maps.  With
+// `fa` (the last update of a step whose W the launch updates) the epilogue
+// applies the step instead of storing D.
+cudaError_t launch_ns_gemm_tc(const GemmParams& p, const FusedApply* fa, cudaStream_t s, char* err,
+                              size_t errlen);
 // Output tiles of the tensor-core GEMM: 256 x 256 per CTA pair.
 constexpr int kTcTileM = 256, kTcTileN = 256;
 // CUDA-core fp32 path.

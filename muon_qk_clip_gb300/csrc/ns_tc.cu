@@ -378,6 +378,170 @@ __device__ bool epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
   return true;
 }
 
+// ------------------------------------------------------------ fused apply
+// The last update of a step, applied in its epilogue: for chunk values v (the
+// oriented iterate X5 = D / alpha), W <- rn_bf16(W - lr (scale v + wd W)).
+// The W segment of a chunk is 32 rows of 64 contiguous bytes: rows r0 .. r0 +
+// 31 of W at columns col0 .. col0 + 31 (W oriented like X), or, when W is the
+// transpose of X, rows col0 .. col0 + 31 at columns r0 .. r0 + 31.  Full
+// segments move by 1-D bulk copies, one per row (slot row k holds the k-th
+// row, 80 bytes apart so that lanes reading their own rows spread over the
+// banks), loaded two chunks ahead and stored back from the slot; segments cut
+// by the matrix's edge are read and written by plain loads and stores.
+constexpr int kWRow = 80;
+
+struct NoApply {
+  static constexpr bool kOn = false;
+};
+
+__device__ inline const FusedApplyJob& fa_job(const FusedApply& fa, const GemmGroup& G, const TileCoord& tc) {
+  return fa.job[G.mat_base + tc.b];
+}
+// chunk ch of the warp's rows [r0, r0 + 32): are all 32 W rows full 64-byte
+// segments (no column cut by the edge)?
+__device__ inline bool w_full(const FusedApplyJob& J, const GemmGroup& G, int r0, int col0) {
+  return J.transpose ? (r0 + 32 <= G.M) : (col0 + 32 <= G.N);
+}
+__device__ inline int w_rows(const FusedApplyJob& J, const GemmGroup& G, int r0, int col0) {
+  return J.transpose ? min(32, G.N - col0) : min(32, G.M - r0);
+}
+__device__ inline __nv_bfloat16* w_row(const FusedApplyJob& J, int r0, int col0, int k) {
+  __nv_bfloat16* w = reinterpret_cast<__nv_bfloat16*>(J.w);
+  return J.transpose ? w + (long long)(col0 + k) * J.ld + r0 : w + (long long)(r0 + k) * J.ld + col0;
+}
+
+// All lanes: bring chunk ch's W segment into slot `slot` (full segments only),
+// once this lane's earlier stores from the slot have read it.
+__device__ inline void w_load(const FusedApply& fa, const GemmParams& p, const TileCoord& tc, int r0, int ch,
+                              uint8_t* ebuf, int slot, CSlots& cs, int lane) {
+  const GemmGroup& G = p.g[tc.g];
+  const FusedApplyJob& J = fa_job(fa, G, tc);
+  const int col0 = tc.n0 + ch * 32;
+  if (!w_full(J, G, r0, col0)) return;
+  const int nr = w_rows(J, G, r0, col0);
+  bulk_wait_read0();
+  __syncwarp();
+  if (lane == 0) {
+    mbar_arrive_expect_tx(&cs.bar[slot], 64u * (uint32_t)nr);
+    cs.pending |= 1u << slot;
+  }
+  __syncwarp();
+  if (lane < nr) bulk_load_1d(ebuf + slot * 4096 + lane * kWRow, w_row(J, r0, col0, lane), 64, &cs.bar[slot]);
+}
+
+__device__ inline void w_prologue(const FusedApply& fa, const GemmParams& p, const TileCoord& tc, int r0,
+                                  int c_begin, int c_end, int lane, uint8_t* ebuf, uint32_t ek, CSlots& cs) {
+  const GemmGroup& G = p.g[tc.g];
+  if (r0 >= G.M) return;
+  int k = 0;
+  for (int ch = c_begin; ch < c_end && k < 2; ++ch) {
+    if (tc.n0 + ch * 32 >= G.N) break;
+    w_load(fa, p, tc, r0, ch, ebuf, (int)((ek + k) & 1), cs, lane);
+    ++k;
+  }
+}
+
+__device__ bool epilogue_apply(const GemmParams& p, const FusedApply& fa, const TileCoord& tc, int r0,
+                               int c_begin, int c_end, uint32_t tacc, int q, int lane, uint8_t* ebuf,
+                               uint32_t& ek, bool& bad, CSlots& cs, volatile int* abort_flag) {
+  const GemmGroup& G = p.g[tc.g];
+  if (r0 >= G.M) return true;
+  const FusedApplyJob& J = fa_job(fa, G, tc);
+  const float sb = p.s ? p.s[G.mat_base + tc.b] : 1.f;
+  const float al = p.alpha * sb * J.scale;           // O = scale * X
+  const float lr = fa.lr, wd = fa.wd;
+  const int row = r0 + lane;
+  const bool row_ok = row < G.M;
+  const uint32_t trow = tacc + ((uint32_t)(q * 32) << 16);
+  auto live = [&](int ch) { return tc.n0 + ch * 32 < G.N; };
+  int ch = c_begin;
+  if (!live(ch)) return true;
+  uint32_t nr[32];
+  tmem_ld_32x32b_x32_async(trow + ch * 32, nr);
+  while (ch < c_end && live(ch)) {
+    const int col0 = tc.n0 + ch * 32;
+    const int nx = ch + 1 < c_end && live(ch + 1) ? ch + 1 : c_end;
+    const int slot = (int)(ek & 1);
+    uint8_t* sb8 = ebuf + slot * 4096;
+    const bool full = w_full(J, G, r0, col0);
+    const int nrows = w_rows(J, G, r0, col0);
+    if (full) {
+      int ok = mbar_wait(&cs.bar[slot], (cs.par >> slot) & 1u, abort_flag) ? 1 : 0;
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        tmem_ld_wait();
+        return false;
+      }
+      if (lane == 0) cs.pending &= ~(1u << slot);
+      cs.par ^= 1u << slot;
+    }
+    tmem_ld_wait();
+    reg_fence32(nr);
+    float v[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = al * __uint_as_float(nr[e]);
+    if (nx < c_end) tmem_ld_32x32b_x32_async(trow + nx * 32, nr);
+    if (full && !J.transpose) {
+      // the lane's own row: W[row][col0 .. col0 + 31]
+      uint8_t* rp = sb8 + lane * kWRow;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint4 u = *reinterpret_cast<const uint4*>(rp + 16 * j);
+        __nv_bfloat16* w8 = reinterpret_cast<__nv_bfloat16*>(&u);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float w = __bfloat162float(w8[e]);
+          const float nw = fmaf(-lr, fmaf(wd, w, v[8 * j + e]), w);
+          bad |= row_ok && !finite_f(nw);
+          w8[e] = __float2bfloat16_rn(nw);
+        }
+        *reinterpret_cast<uint4*>(rp + 16 * j) = u;
+      }
+    } else if (full) {
+      // W = X^T: slot row e holds W[col0 + e][r0 .. r0 + 31]; the lane's
+      // values sit in column `lane` of every row
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        __nv_bfloat16* wp = reinterpret_cast<__nv_bfloat16*>(sb8 + e * kWRow + 2 * lane);
+        const float w = __bfloat162float(*wp);
+        const float nw = fmaf(-lr, fmaf(wd, w, v[e]), w);
+        bad |= e < nrows && !finite_f(nw);
+        *wp = __float2bfloat16_rn(nw);
+      }
+    } else {
+      // a segment cut by the matrix's edge: element by element
+      __nv_bfloat16* w = reinterpret_cast<__nv_bfloat16*>(J.w);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int c = col0 + e;
+        if (!row_ok || c >= G.N) continue;
+        __nv_bfloat16* wp = J.transpose ? w + (long long)c * J.ld + row : w + (long long)row * J.ld + c;
+        const float wv = __bfloat162float(*wp);
+        const float nw = fmaf(-lr, fmaf(wd, wv, v[e]), wv);
+        bad |= !finite_f(nw);
+        *wp = __float2bfloat16_rn(nw);
+      }
+    }
+    if (full) {
+      fence_async_smem();
+      __syncwarp();
+      if (lane < nrows) {
+        bulk_store_1d(w_row(J, r0, col0, lane), sb8 + lane * kWRow, 64);
+        bulk_commit();
+      }
+      // the chunk two on takes its W into this slot once these stores have read it
+      const int n2 = nx < c_end && nx + 1 < c_end && live(nx + 1) ? nx + 1 : c_end;
+      if (n2 < c_end) w_load(fa, p, tc, r0, n2, ebuf, slot, cs, lane);
+    } else {
+      const int n2 = nx < c_end && nx + 1 < c_end && live(nx + 1) ? nx + 1 : c_end;
+      if (n2 < c_end) w_load(fa, p, tc, r0, n2, ebuf, slot, cs, lane);
+    }
+    ++ek;
+    ch = nx;
+  }
+  return true;
+}
+
 // ------------------------------------------------------------ the kernel
 // Roles: warp 0 produces (TMA), warp 1 issues the MMAs (one thread), warps
 // 2-9 are the epilogue.  The CTAs run as tcgen05 .cta_group::2 pairs
@@ -391,9 +555,10 @@ __device__ bool epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
 // Tiles are handed out dynamically: the first CTA's producer claims the next
 // tile id from a zeroed per-launch counter and publishes it to every role of
 // both CTAs through a kTS-deep shared-memory ring.
-template <int TERMS, bool LO, int BK, int FMT>
+template <int TERMS, bool LO, int BK, int FMT, class AP>
 __global__ void __launch_bounds__(kThreads, 1)
-    ns_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ TmaArgs tm) {
+    ns_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ TmaArgs tm,
+                      const __grid_constant__ AP ap) {
   using C = Stages<TERMS, BM, 128, BK>;
   using KL = KLayout<BK>;
   constexpr bool SPLIT = TERMS == 3;     // the A operand's lo plane is staged
@@ -622,17 +787,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int acc = tcount & 1;
       const int r0 = tc.m0 + BM * (int)crank + q * 32;
       const int c0 = hc * (BN / 64), c1 = (hc + 1) * (BN / 64);
-      // C of this tile: the first two chunks' boxes now (TMA), every row into
-      // L2, while the MMAs still run
-      c_prologue<LO>(p, tm, tc, r0, c0, c1, lane, ebuf, ek, cs);
-      prefetch_c_rows<LO>(p, tc, r0, c0, c1, lane);
+      // C (or W) of this tile: the first two chunks' boxes now, every C row
+      // into L2, while the MMAs still run
+      if constexpr (AP::kOn) {
+        w_prologue(ap, p, tc, r0, c0, c1, lane, ebuf, ek, cs);
+      } else {
+        c_prologue<LO>(p, tm, tc, r0, c0, c1, lane, ebuf, ek, cs);
+        prefetch_c_rows<LO>(p, tc, r0, c0, c1, lane);
+      }
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&tfull[acc], (tcount >> 1) & 1, &abort_flag) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) { if (lane == 0) fail(); break; }
       tc_fence_after();
-      if (!epilogue_rows<LO, IN16, OUT16>(p, tm, tc, r0, c0, c1, tmem_base + acc * BN, q, lane, ebuf, ek,
-                                          bad, cs, &abort_flag)) {
+      bool eok;
+      if constexpr (AP::kOn)
+        eok = epilogue_apply(p, ap, tc, r0, c0, c1, tmem_base + acc * BN, q, lane, ebuf, ek, bad, cs, &abort_flag);
+      else
+        eok = epilogue_rows<LO, IN16, OUT16>(p, tm, tc, r0, c0, c1, tmem_base + acc * BN, q, lane, ebuf, ek,
+                                             bad, cs, &abort_flag);
+      if (!eok) {
         if (lane == 0) fail();
         break;
       }
@@ -646,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0)
       for (int sl = 0; sl < 2; ++sl)
         if (cs.pending & (1u << sl)) mbar_wait(&cs.bar[sl], (cs.par >> sl) & 1u, nullptr);
-    if (lane == 0) bulk_wait0();         // all TMA stores of this warp complete
+    bulk_wait0();                        // every store of this warp (fused apply: every lane's) completes
     if (bad) set_status(p.status, MC_STATUS_NONFINITE_UPDATE);
   }
 
@@ -733,14 +907,14 @@ bool encode_all(const GemmParams& p, TmaArgs& tm, bool a_lo, bool b_lo, bool lo,
   return true;
 }
 
-template <int TERMS, bool LO, int BK, int FMT>
-cudaError_t launch_pairs(const GemmParams& p, cudaStream_t s, char* err, size_t errlen) {
+template <int TERMS, bool LO, int BK, int FMT, class AP = NoApply>
+cudaError_t launch_pairs(const GemmParams& p, const AP& ap, cudaStream_t s, char* err, size_t errlen) {
   TmaArgs tm;
   // each CTA's B box is its 128-row half of the pair's 256 B rows
   if (!encode_all(p, tm, TERMS == 3, TERMS == 3, LO, FMT == kFmtF16, FMT != kFmtBf16, BM, 128, BK, err,
                   errlen))
     return cudaErrorInvalidValue;
-  auto k = ns_gemm_tc_kernel<TERMS, LO, BK, FMT>;
+  auto k = ns_gemm_tc_kernel<TERMS, LO, BK, FMT, AP>;
   const int smem = Stages<TERMS, BM, 128, BK>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -763,7 +937,7 @@ cudaError_t launch_pairs(const GemmParams& p, cudaStream_t s, char* err, size_t 
   }
   const int units = p.total_tiles < max_clusters ? p.total_tiles : max_clusters;
   cfg.gridDim = dim3(2 * units);
-  e = cudaLaunchKernelEx(&cfg, k, p, tm);
+  e = cudaLaunchKernelEx(&cfg, k, p, tm, ap);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -773,15 +947,24 @@ cudaError_t launch_pairs(const GemmParams& p, cudaStream_t s, char* err, size_t 
 // one product per k-step, 64-byte rows asked the copy engine for more rows
 // per clock than it sustains (measured: 20-38 % longer one-product launches).
 template <int FMT>
-cudaError_t launch_fmt(const GemmParams& p, cudaStream_t s, char* err, size_t errlen) {
-  if (p.terms == 3) return launch_pairs<3, true, 32, FMT>(p, s, err, errlen);
-  return launch_pairs<1, true, 64, FMT>(p, s, err, errlen);
+cudaError_t launch_fmt(const GemmParams& p, const FusedApply* fa, cudaStream_t s, char* err, size_t errlen) {
+  if (p.terms == 3) {
+    if constexpr (FMT != kFmtBf16)
+      if (fa) return launch_pairs<3, true, 32, FMT, FusedApply>(p, *fa, s, err, errlen);
+    return launch_pairs<3, true, 32, FMT>(p, NoApply{}, s, err, errlen);
+  }
+  return launch_pairs<1, true, 64, FMT>(p, NoApply{}, s, err, errlen);
 }
 
 }  // namespace
 
-cudaError_t launch_ns_gemm_tc(const GemmParams& p, cudaStream_t s, char* err, size_t errlen) {
+cudaError_t launch_ns_gemm_tc(const GemmParams& p, const FusedApply* fa, cudaStream_t s, char* err,
+                              size_t errlen) {
   if (p.total_tiles <= 0) return cudaSuccess;
+  if (fa && (p.xmode != kXSplit || p.terms != 3 || p.fmt == kFmtBf16 || p.beta != 0.f || p.g[0].symmetric)) {
+    snprintf(err, errlen, "the fused apply runs in a three-product, fp16-output update launch");
+    return cudaErrorInvalidValue;
+  }
   if (!p.sched) {
     snprintf(err, errlen, "tensor-core GEMM launched without a tile counter");
     return cudaErrorInvalidValue;
@@ -791,12 +974,12 @@ cudaError_t launch_ns_gemm_tc(const GemmParams& p, cudaStream_t s, char* err, si
       snprintf(err, errlen, "plain bf16 planes take one bf16 product");
       return cudaErrorInvalidValue;
     }
-    return launch_pairs<1, false, 64, kFmtBf16>(p, s, err, errlen);
+    return launch_pairs<1, false, 64, kFmtBf16>(p, NoApply{}, s, err, errlen);
   }
   switch (p.fmt) {
-    case kFmtBf16: return launch_fmt<kFmtBf16>(p, s, err, errlen);
-    case kFmtBf16ToF16: return launch_fmt<kFmtBf16ToF16>(p, s, err, errlen);
-    default: return launch_fmt<kFmtF16>(p, s, err, errlen);
+    case kFmtBf16: return launch_fmt<kFmtBf16>(p, nullptr, s, err, errlen);
+    case kFmtBf16ToF16: return launch_fmt<kFmtBf16ToF16>(p, fa, s, err, errlen);
+    default: return launch_fmt<kFmtF16>(p, fa, s, err, errlen);
   }
 }
 
