@@ -593,6 +593,26 @@ def test_dense_block_step_reduced_tokens():
         assert np.all((g >= lo) & (g <= hi)), n
 
 
+def test_step_beyond_the_fused_apply_table():
+    """More matrices than the last Newton-Schulz launch can apply in its
+    epilogue (192): the step falls back to the separate apply pass; a sample
+    of the 200 matrices, both orientations, against the oracle."""
+    hp = mc.Hparams()
+    shapes = [(64, 96) if i % 2 == 0 else (96, 64) for i in range(200)]
+    W0 = [synth.normal(s, 0.02, f"bw{i}", 19).to(BF16) for i, s in enumerate(shapes)]
+    G0 = [synth.normal(s, 1.0, f"bg{i}", 19) for i, s in enumerate(shapes)]
+    W = [w.cuda() for w in W0]
+    G = [g.cuda() for g in G0]
+    M = [torch.zeros(s, device="cuda") for s in shapes]
+    st = new_status()
+    mc.muonclip_step(W, G, M, hp, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    for i in (0, 1, 117, 199):
+        (Wn, _, Od), _ = oracle_muon(W0[i], G0[i], torch.zeros(shapes[i]), hp)
+        assert_rounded_within(W[i], Wn, 2e-2 * rms(fp32(hp.lr) * Od), f"W {i}")
+
+
 # ------------------------------------------------------------------ ZeRO-1 ranks on the library
 def test_zero1_single_rank_equals_direct_step():
     """A ZeRO-1 step on one rank (momentum on the flat slice, then
