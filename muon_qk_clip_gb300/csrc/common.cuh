@@ -216,6 +216,17 @@ __device__ inline void tmem_ld_32x32b_x32_async(uint32_t taddr, uint32_t (&r)[32
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
+// 32 lanes x 16 columns (thread t: row lane base + t, columns [col, col + 16)),
+// issue only, like tmem_ld_32x32b_x32_async
+__device__ inline void tmem_ld_32x32b_x16_async(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
 __device__ inline void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 // 32 lanes x 32 columns of 32-bit values from registers into TMEM (the
 // inverse of tmem_ld_32x32b_x32); tmem_st_wait() orders them before later use
@@ -232,6 +243,12 @@ __device__ inline void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 __device__ inline void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ inline void reg_fence16(uint32_t (&r)[16]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
+}
 // 2^x by the hardware's approximate base-2 exponential (PTX ex2.approx)
 __device__ inline float ex2_approx(float x) {
   float r;

@@ -128,8 +128,9 @@ struct GemmGroup {
 
 struct GemmTmaps {
   CUtensorMap a_hi[kMaxGroups], a_lo[kMaxGroups], b_hi[kMaxGroups], b_lo[kMaxGroups];
-  CUtensorMap d_hi[kMaxGroups], d_lo[kMaxGroups];
-  CUtensorMap c_hi[kMaxGroups], c_lo[kMaxGroups];   // C of non-symmetric outputs (32 x 32 boxes)
+  CUtensorMap d_hi[kMaxGroups], d_lo[kMaxGroups];     // D chunks (16 columns x 32 rows)
+  CUtensorMap dm_hi[kMaxGroups], dm_lo[kMaxGroups];   // mirrored D chunks (32 columns x 16 rows)
+  CUtensorMap c_hi[kMaxGroups], c_lo[kMaxGroups];     // C of non-symmetric outputs (16 x 32 boxes)
 };
 
 struct GemmParams {

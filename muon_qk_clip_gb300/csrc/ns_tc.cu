@@ -52,7 +52,7 @@ constexpr int BM = 128, BN = 256, BKT = 32;
 constexpr int kEpiWarps = 8;           // two per TMEM lane quadrant (column halves)
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 512;    // two 128 x 256 fp32 accumulators
-constexpr int kEpiWarpBytes = 8192;    // per epilogue warp: two 32 x 32 hi+lo slots
+constexpr int kEpiWarpBytes = 4096;    // per epilogue warp: two 32 x 16 hi+lo slots
 constexpr int kEpiBytes = kEpiWarps * kEpiWarpBytes;
 constexpr int kBarBytes = 512;
 constexpr int kTS = 4;                 // tile-id ring (dynamic schedule)
@@ -62,9 +62,11 @@ constexpr int kSmemCap = 227 * 1024;
 // (BK 32) or 128-byte (BK 64) swizzle, 8-row atoms.
 template <int BK>
 struct KLayout {
-  static_assert(BK == 32 || BK == 64, "k-step");
-  static constexpr uint32_t kType = BK == 64 ? 2u : 4u;
-  static constexpr uint32_t kSbo = 8 * BK * 2;
+  static_assert(BK == 32 || BK == 64 || BK == 128, "k-step");
+  static constexpr int kBX = BK < 64 ? BK : 64;           // K elements per TMA box (<= 128 bytes)
+  static constexpr int kSub = BK / kBX;                   // boxes along K per operand per stage
+  static constexpr uint32_t kType = kBX == 64 ? 2u : 4u;
+  static constexpr uint32_t kSbo = 8 * kBX * 2;
 };
 
 // TERMS: tensor-core products per k-step (1: hi*hi; 3: hi*hi + hi*lo + lo*hi).
@@ -121,41 +123,51 @@ __device__ inline TileCoord tile_coord(const GemmParams& p, int t) {
   return c;
 }
 
-// Byte offset of (row, byte b) in a 32 x 64-byte plane with the 64-byte TMA
-// swizzle: 16-byte unit index XOR ((row >> 1) & 3).
+// Byte offsets in the TMA swizzle patterns (the 16-byte unit index of a row is
+// XOR-ed with address bits 7 and up): 32-byte rows (32-byte swizzle, one bit)
+// and 64-byte rows (64-byte swizzle, two bits).
+__device__ inline uint32_t swz32(int row, int b) {
+  return (uint32_t)(row * 32 + ((((b >> 4) ^ ((row >> 2) & 1)) & 1) << 4) + (b & 15));
+}
 __device__ inline uint32_t swz64(int row, int b) {
   return (uint32_t)(row * 64 + ((((b >> 4) ^ ((row >> 1) & 3)) & 3) << 4) + (b & 15));
 }
 
 // ------------------------------------------------------------ epilogue
-// One warp's 32 rows [r0, r0 + 32) and 32-column chunks [c_begin, c_end) of an
+// One warp's 32 rows [r0, r0 + 32) and 16-column chunks [c_begin, c_end) of an
 // output tile whose accumulator sits in TMEM at `tacc` (lane quadrant q).
 // D = s_b * (alpha * acc + beta * C + diag I).  Symmetric outputs: chunks in
 // 128-column blocks I < J are also stored transposed (mirror); I > J are
 // dropped.
 //
-// The warp's 8 KB of shared memory is two 4 KB slots (a 32 x 32 chunk of hi
-// and lo planes each): D and its mirror for symmetric outputs, else a ring of
-// two D chunks, so a chunk waits only for the store group that last used its
-// slot.  `ek` counts this warp's store groups across tiles.  C of a
+// The warp's 4 KB of shared memory is two 2 KB slots, each a 32 x 16 chunk of
+// hi and lo planes (32-byte rows, 32-byte swizzle): a chunk of D and its
+// mirror (16 rows of 64 bytes, 64-byte swizzle) for symmetric outputs, else a
+// ring of two D chunks, so a chunk waits only for the store group that last
+// used its slot.  The small footprint leaves room for three 64 KB operand
+// stages.  `ek` counts this warp's store groups across tiles.  C of a
 // symmetric output (the polynomial's b A term) is read by each lane straight
-// from global memory (its row's 64 contiguous bytes per plane); C of a
+// from global memory (its row's 32 contiguous bytes per plane); C of a
 // non-symmetric output (the update's a X term) arrives by TMA (CSlots below).
 // The next chunk's TMEM load and C loads are issued as soon as the current
 // chunk's values are converted, so they are in flight while it is stored; two
 // warps share each lane quadrant (one per column half), so one warp's waits
 // overlap the other's work.
-// The lane's C of a chunk: 4 x 8 columns per plane, zero past the edges.
+constexpr int kCW = 16;                         // chunk width (columns)
+constexpr int kPlane = 32 * kCW * 2;            // 1 KB: one plane of a chunk
+constexpr int kSlot = 2 * kPlane;               // hi + lo
+
+// The lane's C of a chunk: 2 x 8 columns per plane, zero past the edges.
 template <bool LO>
 __device__ inline void load_c_chunk(const GemmGroup& G, const TileCoord& tc, int row, int ch,
-                                    uint4 (&h)[4], uint4 (&l)[4]) {
-  const int col0 = tc.n0 + ch * 32;
+                                    uint4 (&h)[2], uint4 (&l)[2]) {
+  const int col0 = tc.n0 + ch * kCW;
   const bool row_ok = row < G.M;
   const long long o = (long long)tc.b * G.c_bstride + (long long)row * G.ldc + col0;
-  const __nv_bfloat16* c_hi = reinterpret_cast<const __nv_bfloat16*>(G.c_hi) + o;
-  const __nv_bfloat16* c_lo = reinterpret_cast<const __nv_bfloat16*>(G.c_lo) + o;
+  const uint16_t* c_hi = reinterpret_cast<const uint16_t*>(G.c_hi) + o;
+  const uint16_t* c_lo = reinterpret_cast<const uint16_t*>(G.c_lo) + o;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < 2; ++j) {
     const bool ok = row_ok && col0 + 8 * j < G.N;
     h[j] = ok ? __ldg(reinterpret_cast<const uint4*>(c_hi + 8 * j)) : make_uint4(0, 0, 0, 0);
     if (LO) l[j] = ok ? __ldg(reinterpret_cast<const uint4*>(c_lo + 8 * j)) : make_uint4(0, 0, 0, 0);
@@ -174,19 +186,19 @@ __device__ inline void prefetch_c_rows(const GemmParams& p, const TileCoord& tc,
   const long long o = (long long)tc.b * G.c_bstride + (long long)row * G.ldc;
   const uint16_t* c_hi = reinterpret_cast<const uint16_t*>(G.c_hi) + o;
   const uint16_t* c_lo = reinterpret_cast<const uint16_t*>(G.c_lo) + o;
-  for (int ch = c_begin; ch < c_end; ++ch) {
-    const int col0 = tc.n0 + ch * 32;
+  for (int ch = c_begin; ch < c_end; ch += 4) {      // one 128-byte line per four chunks
+    const int col0 = tc.n0 + ch * kCW;
     if (col0 >= G.N) break;
     prefetch_l2(c_hi + col0);
     if (LO) prefetch_l2(c_lo + col0);
   }
 }
 
-// C through TMA (non-symmetric outputs with a C term): the warp's two 4 KB
-// slots take the C chunks as 32 x 32 boxes (hi and lo planes), loaded two
-// chunks ahead and, for a tile's first two chunks, before its accumulator is
-// ready; each chunk's D is then written over its C in the same slot and
-// leaves by TMA.  Chunk i of the warp's sequence uses slot ek & 1.
+// C through TMA (non-symmetric outputs with a C term): the warp's two slots
+// take the C chunks as 16 x 32 boxes (hi and lo planes), loaded two chunks
+// ahead and, for a tile's first two chunks, before its accumulator is ready;
+// each chunk's D is then written over its C in the same slot and leaves by
+// TMA.  Chunk i of the warp's sequence uses slot ek & 1.
 struct CSlots {
   uint64_t* bar;       // [2] completion of the C box loads of each slot
   uint32_t par;        // bit s: parity of the next wait on bar[s]
@@ -203,11 +215,11 @@ template <bool LO>
 __device__ inline void c_load(const TmaArgs& tm, const TileCoord& tc, int r0, int ch, uint8_t* ebuf,
                               int slot, CSlots& cs) {
   bulk_wait_read_upto(0);
-  uint8_t* sb = ebuf + slot * 4096;
-  mbar_arrive_expect_tx(&cs.bar[slot], LO ? 4096 : 2048);
-  const int col0 = tc.n0 + ch * 32;
+  uint8_t* sb = ebuf + slot * kSlot;
+  mbar_arrive_expect_tx(&cs.bar[slot], LO ? 2 * kPlane : kPlane);
+  const int col0 = tc.n0 + ch * kCW;
   tma_load_3d(sb, &tm.maps.c_hi[tc.g], &cs.bar[slot], col0, r0, tc.b);
-  if (LO) tma_load_3d(sb + 2048, &tm.maps.c_lo[tc.g], &cs.bar[slot], col0, r0, tc.b);
+  if (LO) tma_load_3d(sb + kPlane, &tm.maps.c_lo[tc.g], &cs.bar[slot], col0, r0, tc.b);
   cs.pending |= 1u << slot;
 }
 
@@ -221,7 +233,7 @@ __device__ inline void c_prologue(const GemmParams& p, const TmaArgs& tm, const 
   if (!c_by_tma(p, G) || r0 >= G.M || lane != 0) return;
   int k = 0;
   for (int ch = c_begin; ch < c_end && k < 2; ++ch) {
-    if (tc.n0 + ch * 32 >= G.N) break;
+    if (tc.n0 + ch * kCW >= G.N) break;
     c_load<LO>(tm, tc, r0, ch, ebuf, (int)((ek + k) & 1), cs);
     ++k;
   }
@@ -241,7 +253,7 @@ __device__ bool epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
   const int depth = 2 / per;                        // store groups in flight
   const int I = r0 / 128;
   auto mode_of = [&](int ch) -> int {             // 0 skip, 1 store, 2 store + mirror
-    const int col0 = tc.n0 + ch * 32;
+    const int col0 = tc.n0 + ch * kCW;
     if (col0 >= G.N) return 0;
     if (!G.symmetric) return 1;
     const int J = col0 / 128;
@@ -257,15 +269,15 @@ __device__ bool epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
   const uint32_t trow = tacc + ((uint32_t)(q * 32) << 16);
   int ch = next_live(c_begin - 1);
   if (ch >= c_end) return true;
-  uint4 c_h[4], c_l[4];
-  uint32_t nr[32];
-  tmem_ld_32x32b_x32_async(trow + ch * 32, nr);
+  uint4 c_h[2], c_l[2];
+  uint32_t nr[16];
+  tmem_ld_32x32b_x16_async(trow + ch * kCW, nr);
   if (use_c && !tmac) load_c_chunk<LO>(G, tc, row, ch, c_h, c_l);
   while (ch < c_end) {
     const int mode = mode_of(ch);
-    const int col0 = tc.n0 + ch * 32;
+    const int col0 = tc.n0 + ch * kCW;
     const int nx = next_live(ch);
-    uint8_t* db = ebuf + (int)(ek % (uint32_t)depth) * per * 4096;
+    uint8_t* db = ebuf + (int)(ek % (uint32_t)depth) * per * kSlot;
     if (tmac) {
       // this chunk's C box: wait for it, then read the lane's row from the slot
       const int slot = (int)(ek & 1);
@@ -281,19 +293,19 @@ __device__ bool epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
       }
       cs.par ^= 1u << slot;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        c_h[j] = *reinterpret_cast<const uint4*>(db + swz64(lane, j * 16));
-        if (LO) c_l[j] = *reinterpret_cast<const uint4*>(db + 2048 + swz64(lane, j * 16));
+      for (int j = 0; j < 2; ++j) {
+        c_h[j] = *reinterpret_cast<const uint4*>(db + swz32(lane, j * 16));
+        if (LO) c_l[j] = *reinterpret_cast<const uint4*>(db + kPlane + swz32(lane, j * 16));
       }
     }
     tmem_ld_wait();
-    reg_fence32(nr);
-    float v[32];
+    reg_fence16(nr);
+    float v[16];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(nr[e]);
+    for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(nr[e]);
     if (use_c) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 2; ++j) {
         const uint16_t* hh = reinterpret_cast<const uint16_t*>(&c_h[j]);
         const uint16_t* ll = reinterpret_cast<const uint16_t*>(&c_l[j]);
 #pragma unroll
@@ -304,69 +316,70 @@ __device__ bool epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
       }
     } else {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) v[e] *= al;
+      for (int e = 0; e < 16; ++e) v[e] *= al;
     }
-    if (dg != 0.f && row >= col0 && row < col0 + 32) {
+    if (dg != 0.f && row >= col0 && row < col0 + kCW) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e)
+      for (int e = 0; e < 16; ++e)
         if (col0 + e == row) v[e] += dg;
     }
     // non-finite test: v * 0 is 0 for a finite v and NaN for Inf or NaN, so
     // four chains of fma(v, 0, acc) end in NaN iff some value is not finite
     // (the ragged edge tests its valid elements one by one)
-    if (row_ok && col0 + 31 < G.N) {
+    if (row_ok && col0 + kCW - 1 < G.N) {
       float z4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int e = 0; e < 32; ++e) z4[e & 3] = fmaf(v[e], 0.f, z4[e & 3]);
+      for (int e = 0; e < 16; ++e) z4[e & 3] = fmaf(v[e], 0.f, z4[e & 3]);
       const float z = (z4[0] + z4[1]) + (z4[2] + z4[3]);
       bad |= z != z;
     } else if (row_ok) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) bad |= !finite_f(v[e]) && (col0 + e < G.N);
+      for (int e = 0; e < 16; ++e) bad |= !finite_f(v[e]) && (col0 + e < G.N);
     }
-    uint16_t hb[32], lb[32];
+    uint16_t hb[16], lb[16];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
+    for (int e = 0; e < 16; ++e) {
       if (LO) split16<OUT16>(v[e], hb[e], lb[e]);
       else hb[e] = to16<OUT16>(v[e]);
     }
     // this chunk's accumulator and C are consumed: start the next chunk's
     // loads (warp-uniform: nx is the same in every lane)
     if (nx < c_end) {
-      tmem_ld_32x32b_x32_async(trow + nx * 32, nr);
+      tmem_ld_32x32b_x16_async(trow + nx * kCW, nr);
       if (use_c && !tmac) load_c_chunk<LO>(G, tc, row, nx, c_h, c_l);
     }
-    uint8_t* mb = db + 4096;
+    uint8_t* mb = db + kSlot;
     // the store group that last used these slots must have read them (with C
     // by TMA the slot was last read by this chunk's own C box, already used)
     if (lane == 0 && !tmac) bulk_wait_read_upto(depth - 1);
     __syncwarp();
     const bool st_lo = LO && !p.d_hi_only;          // warp-uniform
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      *reinterpret_cast<uint4*>(db + swz64(lane, j * 16)) = *reinterpret_cast<const uint4*>(hb + j * 8);
+    for (int j = 0; j < 2; ++j) {
+      *reinterpret_cast<uint4*>(db + swz32(lane, j * 16)) = *reinterpret_cast<const uint4*>(hb + j * 8);
       if (st_lo)
-        *reinterpret_cast<uint4*>(db + 2048 + swz64(lane, j * 16)) = *reinterpret_cast<const uint4*>(lb + j * 8);
+        *reinterpret_cast<uint4*>(db + kPlane + swz32(lane, j * 16)) = *reinterpret_cast<const uint4*>(lb + j * 8);
     }
     if (mode == 2) {
-      // mirror tile: row c holds column c of this chunk, i.e. lane (row) r -> byte 2r
+      // mirror: row c of a 16 x 32 plane holds column c of this chunk, i.e.
+      // lane (row) r -> byte 2r
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
+      for (int c = 0; c < 16; ++c) {
         *reinterpret_cast<uint16_t*>(mb + swz64(c, 2 * lane)) = hb[c];
-        if (st_lo) *reinterpret_cast<uint16_t*>(mb + 2048 + swz64(c, 2 * lane)) = lb[c];
+        if (st_lo) *reinterpret_cast<uint16_t*>(mb + kPlane + swz64(c, 2 * lane)) = lb[c];
       }
     }
     fence_async_smem();
     __syncwarp();
     if (lane == 0) {
       tma_store_3d(&tm.maps.d_hi[tc.g], db, col0, r0, tc.b);
-      if (st_lo) tma_store_3d(&tm.maps.d_lo[tc.g], db + 2048, col0, r0, tc.b);
+      if (st_lo) tma_store_3d(&tm.maps.d_lo[tc.g], db + kPlane, col0, r0, tc.b);
       if (mode == 2) {
-        tma_store_3d(&tm.maps.d_hi[tc.g], mb, r0, col0, tc.b);
-        if (st_lo) tma_store_3d(&tm.maps.d_lo[tc.g], mb + 2048, r0, col0, tc.b);
+        tma_store_3d(&tm.maps.dm_hi[tc.g], mb, r0, col0, tc.b);
+        if (st_lo) tma_store_3d(&tm.maps.dm_lo[tc.g], mb + kPlane, r0, col0, tc.b);
       }
       bulk_commit();
-      // two chunks on, C goes into this slot again once the store has read it
+      // the chunk two on takes its C into this slot once the store has read it
       if (tmac) {
         const int n2 = nx < c_end ? next_live(nx) : c_end;
         if (n2 < c_end) c_load<LO>(tm, tc, r0, n2, ebuf, (int)(ek & 1), cs);
@@ -381,15 +394,14 @@ __device__ bool epilogue_rows(const GemmParams& p, const TmaArgs& tm, const Tile
 // ------------------------------------------------------------ fused apply
 // The last update of a step, applied in its epilogue: for chunk values v (the
 // oriented iterate X5 = D / alpha), W <- rn_bf16(W - lr (scale v + wd W)).
-// The W segment of a chunk is 32 rows of 64 contiguous bytes: rows r0 .. r0 +
-// 31 of W at columns col0 .. col0 + 31 (W oriented like X), or, when W is the
-// transpose of X, rows col0 .. col0 + 31 at columns r0 .. r0 + 31.  Full
-// segments move by 1-D bulk copies, one per row (slot row k holds the k-th
-// row, 80 bytes apart so that lanes reading their own rows spread over the
-// banks), loaded two chunks ahead and stored back from the slot; segments cut
-// by the matrix's edge are read and written by plain loads and stores.
-constexpr int kWRow = 80;
-
+// A chunk covers X rows r0 .. r0 + 31 and columns col0 .. col0 + 15.  When W
+// is oriented like X its segment is 32 rows of 32 contiguous bytes (W rows
+// r0 + k at columns col0 ..); when W is the transpose of X it is 16 rows of 64
+// bytes (W rows col0 + e at columns r0 ..).  Full segments move by 1-D bulk
+// copies, one per row (slot rows 48 or 80 bytes apart, which spreads the
+// lanes' accesses over the banks), loaded two chunks ahead and stored back
+// from the slot; segments cut by the matrix's edge are read and written by
+// plain loads and stores.
 struct NoApply {
   static constexpr bool kOn = false;
 };
@@ -397,14 +409,15 @@ struct NoApply {
 __device__ inline const FusedApplyJob& fa_job(const FusedApply& fa, const GemmGroup& G, const TileCoord& tc) {
   return fa.job[G.mat_base + tc.b];
 }
-// chunk ch of the warp's rows [r0, r0 + 32): are all 32 W rows full 64-byte
-// segments (no column cut by the edge)?
 __device__ inline bool w_full(const FusedApplyJob& J, const GemmGroup& G, int r0, int col0) {
-  return J.transpose ? (r0 + 32 <= G.M) : (col0 + 32 <= G.N);
+  return J.transpose ? (r0 + 32 <= G.M) : (col0 + kCW <= G.N);
 }
+// slot rows of the segment, their bytes and their pitch in the slot
 __device__ inline int w_rows(const FusedApplyJob& J, const GemmGroup& G, int r0, int col0) {
-  return J.transpose ? min(32, G.N - col0) : min(32, G.M - r0);
+  return J.transpose ? min(kCW, G.N - col0) : min(32, G.M - r0);
 }
+__device__ inline int w_row_bytes(const FusedApplyJob& J) { return J.transpose ? 64 : 2 * kCW; }
+__device__ inline int w_pitch(const FusedApplyJob& J) { return J.transpose ? 80 : 48; }
 __device__ inline __nv_bfloat16* w_row(const FusedApplyJob& J, int r0, int col0, int k) {
   __nv_bfloat16* w = reinterpret_cast<__nv_bfloat16*>(J.w);
   return J.transpose ? w + (long long)(col0 + k) * J.ld + r0 : w + (long long)(r0 + k) * J.ld + col0;
@@ -416,17 +429,18 @@ __device__ inline void w_load(const FusedApply& fa, const GemmParams& p, const T
                               uint8_t* ebuf, int slot, CSlots& cs, int lane) {
   const GemmGroup& G = p.g[tc.g];
   const FusedApplyJob& J = fa_job(fa, G, tc);
-  const int col0 = tc.n0 + ch * 32;
+  const int col0 = tc.n0 + ch * kCW;
   if (!w_full(J, G, r0, col0)) return;
-  const int nr = w_rows(J, G, r0, col0);
+  const int nr = w_rows(J, G, r0, col0), rb = w_row_bytes(J);
   bulk_wait_read0();
   __syncwarp();
   if (lane == 0) {
-    mbar_arrive_expect_tx(&cs.bar[slot], 64u * (uint32_t)nr);
+    mbar_arrive_expect_tx(&cs.bar[slot], (uint32_t)(rb * nr));
     cs.pending |= 1u << slot;
   }
   __syncwarp();
-  if (lane < nr) bulk_load_1d(ebuf + slot * 4096 + lane * kWRow, w_row(J, r0, col0, lane), 64, &cs.bar[slot]);
+  if (lane < nr)
+    bulk_load_1d(ebuf + slot * kSlot + lane * w_pitch(J), w_row(J, r0, col0, lane), (uint32_t)rb, &cs.bar[slot]);
 }
 
 __device__ inline void w_prologue(const FusedApply& fa, const GemmParams& p, const TileCoord& tc, int r0,
@@ -435,7 +449,7 @@ __device__ inline void w_prologue(const FusedApply& fa, const GemmParams& p, con
   if (r0 >= G.M) return;
   int k = 0;
   for (int ch = c_begin; ch < c_end && k < 2; ++ch) {
-    if (tc.n0 + ch * 32 >= G.N) break;
+    if (tc.n0 + ch * kCW >= G.N) break;
     w_load(fa, p, tc, r0, ch, ebuf, (int)((ek + k) & 1), cs, lane);
     ++k;
   }
@@ -453,16 +467,16 @@ __device__ bool epilogue_apply(const GemmParams& p, const FusedApply& fa, const 
   const int row = r0 + lane;
   const bool row_ok = row < G.M;
   const uint32_t trow = tacc + ((uint32_t)(q * 32) << 16);
-  auto live = [&](int ch) { return tc.n0 + ch * 32 < G.N; };
+  auto live = [&](int ch) { return tc.n0 + ch * kCW < G.N; };
   int ch = c_begin;
   if (!live(ch)) return true;
-  uint32_t nr[32];
-  tmem_ld_32x32b_x32_async(trow + ch * 32, nr);
+  uint32_t nr[16];
+  tmem_ld_32x32b_x16_async(trow + ch * kCW, nr);
   while (ch < c_end && live(ch)) {
-    const int col0 = tc.n0 + ch * 32;
+    const int col0 = tc.n0 + ch * kCW;
     const int nx = ch + 1 < c_end && live(ch + 1) ? ch + 1 : c_end;
     const int slot = (int)(ek & 1);
-    uint8_t* sb8 = ebuf + slot * 4096;
+    uint8_t* sb8 = ebuf + slot * kSlot;
     const bool full = w_full(J, G, r0, col0);
     const int nrows = w_rows(J, G, r0, col0);
     if (full) {
@@ -476,16 +490,16 @@ __device__ bool epilogue_apply(const GemmParams& p, const FusedApply& fa, const 
       cs.par ^= 1u << slot;
     }
     tmem_ld_wait();
-    reg_fence32(nr);
-    float v[32];
+    reg_fence16(nr);
+    float v[16];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) v[e] = al * __uint_as_float(nr[e]);
-    if (nx < c_end) tmem_ld_32x32b_x32_async(trow + nx * 32, nr);
+    for (int e = 0; e < 16; ++e) v[e] = al * __uint_as_float(nr[e]);
+    if (nx < c_end) tmem_ld_32x32b_x16_async(trow + nx * kCW, nr);
     if (full && !J.transpose) {
-      // the lane's own row: W[row][col0 .. col0 + 31]
-      uint8_t* rp = sb8 + lane * kWRow;
+      // the lane's own row: W[row][col0 .. col0 + 15]
+      uint8_t* rp = sb8 + lane * 48;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 2; ++j) {
         uint4 u = *reinterpret_cast<const uint4*>(rp + 16 * j);
         __nv_bfloat16* w8 = reinterpret_cast<__nv_bfloat16*>(&u);
 #pragma unroll
@@ -501,8 +515,8 @@ __device__ bool epilogue_apply(const GemmParams& p, const FusedApply& fa, const 
       // W = X^T: slot row e holds W[col0 + e][r0 .. r0 + 31]; the lane's
       // values sit in column `lane` of every row
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        __nv_bfloat16* wp = reinterpret_cast<__nv_bfloat16*>(sb8 + e * kWRow + 2 * lane);
+      for (int e = 0; e < 16; ++e) {
+        __nv_bfloat16* wp = reinterpret_cast<__nv_bfloat16*>(sb8 + e * 80 + 2 * lane);
         const float w = __bfloat162float(*wp);
         const float nw = fmaf(-lr, fmaf(wd, w, v[e]), w);
         bad |= e < nrows && !finite_f(nw);
@@ -512,7 +526,7 @@ __device__ bool epilogue_apply(const GemmParams& p, const FusedApply& fa, const 
       // a segment cut by the matrix's edge: element by element
       __nv_bfloat16* w = reinterpret_cast<__nv_bfloat16*>(J.w);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
+      for (int e = 0; e < 16; ++e) {
         const int c = col0 + e;
         if (!row_ok || c >= G.N) continue;
         __nv_bfloat16* wp = J.transpose ? w + (long long)c * J.ld + row : w + (long long)row * J.ld + c;
@@ -526,16 +540,13 @@ __device__ bool epilogue_apply(const GemmParams& p, const FusedApply& fa, const 
       fence_async_smem();
       __syncwarp();
       if (lane < nrows) {
-        bulk_store_1d(w_row(J, r0, col0, lane), sb8 + lane * kWRow, 64);
+        bulk_store_1d(w_row(J, r0, col0, lane), sb8 + lane * w_pitch(J), (uint32_t)w_row_bytes(J));
         bulk_commit();
       }
-      // the chunk two on takes its W into this slot once these stores have read it
-      const int n2 = nx < c_end && nx + 1 < c_end && live(nx + 1) ? nx + 1 : c_end;
-      if (n2 < c_end) w_load(fa, p, tc, r0, n2, ebuf, slot, cs, lane);
-    } else {
-      const int n2 = nx < c_end && nx + 1 < c_end && live(nx + 1) ? nx + 1 : c_end;
-      if (n2 < c_end) w_load(fa, p, tc, r0, n2, ebuf, slot, cs, lane);
     }
+    // the chunk two on takes its W into this slot once these stores have read it
+    const int n2 = nx < c_end && nx + 1 < c_end && live(nx + 1) ? nx + 1 : c_end;
+    if (n2 < c_end) w_load(fa, p, tc, r0, n2, ebuf, slot, cs, lane);
     ++ek;
     ch = nx;
   }
@@ -680,11 +691,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
           if (crank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::kStageBytes);
           const int nb = tc.n0 + 128 * (int)crank;
-          tma_load_3d_pair(a_hi, &tm.maps.a_hi[tc.g], fb, k0, m0, tc.b);
-          if (SPLIT) tma_load_3d_pair(a_lo, &tm.maps.a_lo[tc.g], fb, k0, m0, tc.b);
+#pragma unroll
+          for (int sub = 0; sub < KL::kSub; ++sub) {
+            const int ks = k0 + sub * KL::kBX, so = sub * 128 * KL::kBX * 2;
+            tma_load_3d_pair(a_hi + so, &tm.maps.a_hi[tc.g], fb, ks, m0, tc.b);
+            if (SPLIT) tma_load_3d_pair(a_lo + so, &tm.maps.a_lo[tc.g], fb, ks, m0, tc.b);
+          }
           if (!G.b_mn_major) {
-            tma_load_3d_pair(b_hi, &tm.maps.b_hi[tc.g], fb, k0, nb, tc.b);
-            if (BLO) tma_load_3d_pair(b_lo, &tm.maps.b_lo[tc.g], fb, k0, nb, tc.b);
+#pragma unroll
+            for (int sub = 0; sub < KL::kSub; ++sub) {
+              const int ks = k0 + sub * KL::kBX, so = sub * 128 * KL::kBX * 2;
+              tma_load_3d_pair(b_hi + so, &tm.maps.b_hi[tc.g], fb, ks, nb, tc.b);
+              if (BLO) tma_load_3d_pair(b_lo + so, &tm.maps.b_lo[tc.g], fb, ks, nb, tc.b);
+            }
           } else {
 #pragma unroll
             for (int qq = 0; qq < 2; ++qq) {
@@ -736,12 +755,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b_hi = st + (SPLIT ? 2 * C::kABytes : C::kABytes), b_lo = b_hi + C::kBBytes;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            // K-major: 16 elements = 32 bytes further along the swizzled row
-            const uint64_t dah = make_sdesc(a_hi + kk * 32, 16, KL::kSbo, KL::kType);
+            // K-major: 16 elements = 32 bytes further along the swizzled row,
+            // in sub-tile kk / (kBX / 16) of the stage
+            const uint32_t ko = (uint32_t)((kk / (KL::kBX / 16)) * 128 * KL::kBX * 2 + (kk % (KL::kBX / 16)) * 32);
+            const uint64_t dah = make_sdesc(a_hi + ko, 16, KL::kSbo, KL::kType);
             uint64_t dbh, dbl = 0, dal = 0;
             if (!G.b_mn_major) {
-              dbh = make_sdesc(b_hi + kk * 32, 16, KL::kSbo, KL::kType);
-              if (BLO) dbl = make_sdesc(b_lo + kk * 32, 16, KL::kSbo, KL::kType);
+              dbh = make_sdesc(b_hi + ko, 16, KL::kSbo, KL::kType);
+              if (BLO) dbl = make_sdesc(b_lo + ko, 16, KL::kSbo, KL::kType);
             } else {
               // MN-major (128-byte swizzle): 16 K-rows = two 1024-byte atoms;
               // 64-wide N blocks are 64*BK*2 bytes apart
@@ -749,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (BLO) dbl = make_sdesc(b_lo + kk * 2048, 64 * BK * 2, 1024, 2);
             }
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
-            if (SPLIT) dal = make_sdesc(a_lo + kk * 32, 16, KL::kSbo, KL::kType);
+            if (SPLIT) dal = make_sdesc(a_lo + ko, 16, KL::kSbo, KL::kType);
             tc_mma_pair(d_tmem, dah, dbh, idesc, accum);
             if (BLO) tc_mma_pair(d_tmem, dah, dbl, idesc, 1u);
             if (SPLIT) tc_mma_pair(d_tmem, dal, dbh, idesc, 1u);
@@ -786,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileCoord tc = tile_coord<TM_ROWS>(p, t);
       const int acc = tcount & 1;
       const int r0 = tc.m0 + BM * (int)crank + q * 32;
-      const int c0 = hc * (BN / 64), c1 = (hc + 1) * (BN / 64);
+      const int c0 = hc * (BN / 2 / kCW), c1 = (hc + 1) * (BN / 2 / kCW);
       // C (or W) of this tile: the first two chunks' boxes now, every C row
       // into L2, while the MMAs still run
       if constexpr (AP::kOn) {
@@ -864,7 +885,9 @@ bool encode_3d(CUtensorMap* m, const void* base, int cols, int rows, int batch, 
   cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)bstride * 2};
   cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
-  const CUtensorMapSwizzle sw = box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const CUtensorMapSwizzle sw = box_cols == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                 : CU_TENSOR_MAP_SWIZZLE_32B;
   CUresult r = enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                    const_cast<void*>(base), dims, strides,
                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -882,26 +905,31 @@ bool encode_3d(CUtensorMap* m, const void* base, int cols, int rows, int batch, 
 // the B operand's; lo: D is stored as (hi, lo); in16 / out16: operand and
 // output planes hold fp16 (else bf16).
 bool encode_all(const GemmParams& p, TmaArgs& tm, bool a_lo, bool b_lo, bool lo, bool in16, bool out16,
-                int a_rows, int b_rows, int bk, char* err, size_t errlen) {
+                int a_rows, int b_rows, int bk, int bx, char* err, size_t errlen) {
   memset(&tm, 0, sizeof(tm));
   for (int g = 0; g < p.ngroups; ++g) {
     const GemmGroup& G = p.g[g];
-    if (!encode_3d(&tm.maps.a_hi[g], G.a_hi, G.K, G.M, G.batch, G.lda, G.a_bstride, bk, a_rows, in16, err, errlen)) return false;
-    if (a_lo && !encode_3d(&tm.maps.a_lo[g], G.a_lo, G.K, G.M, G.batch, G.lda, G.a_bstride, bk, a_rows, in16, err, errlen)) return false;
-    if (!G.b_mn_major) {   // B operand: rows of an [N, K] plane
-      if (!encode_3d(&tm.maps.b_hi[g], G.b_hi, G.K, G.N, G.batch, G.ldb, G.b_bstride, bk, b_rows, in16, err, errlen)) return false;
-      if (b_lo && !encode_3d(&tm.maps.b_lo[g], G.b_lo, G.K, G.N, G.batch, G.ldb, G.b_bstride, bk, b_rows, in16, err, errlen)) return false;
+    if (!encode_3d(&tm.maps.a_hi[g], G.a_hi, G.K, G.M, G.batch, G.lda, G.a_bstride, bx, a_rows, in16, err, errlen)) return false;
+    if (a_lo && !encode_3d(&tm.maps.a_lo[g], G.a_lo, G.K, G.M, G.batch, G.lda, G.a_bstride, bx, a_rows, in16, err, errlen)) return false;
+    if (!G.b_mn_major) {   // B operand: rows of an [N, K] plane, boxes bx wide
+      if (!encode_3d(&tm.maps.b_hi[g], G.b_hi, G.K, G.N, G.batch, G.ldb, G.b_bstride, bx, b_rows, in16, err, errlen)) return false;
+      if (b_lo && !encode_3d(&tm.maps.b_lo[g], G.b_lo, G.K, G.N, G.batch, G.ldb, G.b_bstride, bx, b_rows, in16, err, errlen)) return false;
     } else {               // B operand: [K, N] plane, 64-wide N boxes of bk rows
       if (!encode_3d(&tm.maps.b_hi[g], G.b_hi, G.N, G.K, G.batch, G.ldb, G.b_bstride, 64, bk, in16, err, errlen)) return false;
       if (b_lo && !encode_3d(&tm.maps.b_lo[g], G.b_lo, G.N, G.K, G.batch, G.ldb, G.b_bstride, 64, bk, in16, err, errlen)) return false;
     }
-    if (!encode_3d(&tm.maps.d_hi[g], G.d_hi, G.N, G.M, G.batch, G.ldd, G.d_bstride, 32, 32, out16, err, errlen)) return false;
-    if (lo && !encode_3d(&tm.maps.d_lo[g], G.d_lo, G.N, G.M, G.batch, G.ldd, G.d_bstride, 32, 32, out16, err, errlen)) return false;
+    // D chunks of 16 columns x 32 rows; their mirrors 32 columns x 16 rows
+    if (!encode_3d(&tm.maps.d_hi[g], G.d_hi, G.N, G.M, G.batch, G.ldd, G.d_bstride, 16, 32, out16, err, errlen)) return false;
+    if (lo && !encode_3d(&tm.maps.d_lo[g], G.d_lo, G.N, G.M, G.batch, G.ldd, G.d_bstride, 16, 32, out16, err, errlen)) return false;
+    if (G.symmetric) {
+      if (!encode_3d(&tm.maps.dm_hi[g], G.d_hi, G.N, G.M, G.batch, G.ldd, G.d_bstride, 32, 16, out16, err, errlen)) return false;
+      if (lo && !encode_3d(&tm.maps.dm_lo[g], G.d_lo, G.N, G.M, G.batch, G.ldd, G.d_bstride, 32, 16, out16, err, errlen)) return false;
+    }
     // C of a non-symmetric output is read by the epilogue through TMA, in the
     // operands' format
     if (p.beta != 0.f && !G.symmetric) {
-      if (!encode_3d(&tm.maps.c_hi[g], G.c_hi, G.N, G.M, G.batch, G.ldc, G.c_bstride, 32, 32, in16, err, errlen)) return false;
-      if (lo && !encode_3d(&tm.maps.c_lo[g], G.c_lo, G.N, G.M, G.batch, G.ldc, G.c_bstride, 32, 32, in16, err, errlen)) return false;
+      if (!encode_3d(&tm.maps.c_hi[g], G.c_hi, G.N, G.M, G.batch, G.ldc, G.c_bstride, 16, 32, in16, err, errlen)) return false;
+      if (lo && !encode_3d(&tm.maps.c_lo[g], G.c_lo, G.N, G.M, G.batch, G.ldc, G.c_bstride, 16, 32, in16, err, errlen)) return false;
     }
   }
   return true;
@@ -911,8 +939,8 @@ template <int TERMS, bool LO, int BK, int FMT, class AP = NoApply>
 cudaError_t launch_pairs(const GemmParams& p, const AP& ap, cudaStream_t s, char* err, size_t errlen) {
   TmaArgs tm;
   // each CTA's B box is its 128-row half of the pair's 256 B rows
-  if (!encode_all(p, tm, TERMS == 3, TERMS == 3, LO, FMT == kFmtF16, FMT != kFmtBf16, BM, 128, BK, err,
-                  errlen))
+  if (!encode_all(p, tm, TERMS == 3, TERMS == 3, LO, FMT == kFmtF16, FMT != kFmtBf16, BM, 128, BK,
+                  KLayout<BK>::kBX, err, errlen))
     return cudaErrorInvalidValue;
   auto k = ns_gemm_tc_kernel<TERMS, LO, BK, FMT, AP>;
   const int smem = Stages<TERMS, BM, 128, BK>::kSmem;
@@ -953,7 +981,7 @@ cudaError_t launch_fmt(const GemmParams& p, const FusedApply* fa, cudaStream_t s
       if (fa) return launch_pairs<3, true, 32, FMT, FusedApply>(p, *fa, s, err, errlen);
     return launch_pairs<3, true, 32, FMT>(p, NoApply{}, s, err, errlen);
   }
-  return launch_pairs<1, true, 64, FMT>(p, NoApply{}, s, err, errlen);
+  return launch_pairs<1, true, 128, FMT>(p, NoApply{}, s, err, errlen);
 }
 
 }  // namespace
@@ -974,7 +1002,7 @@ cudaError_t launch_ns_gemm_tc(const GemmParams& p, const FusedApply* fa, cudaStr
       snprintf(err, errlen, "plain bf16 planes take one bf16 product");
       return cudaErrorInvalidValue;
     }
-    return launch_pairs<1, false, 64, kFmtBf16>(p, NoApply{}, s, err, errlen);
+    return launch_pairs<1, false, 128, kFmtBf16>(p, NoApply{}, s, err, errlen);
   }
   switch (p.fmt) {
     case kFmtBf16: return launch_fmt<kFmtBf16>(p, nullptr, s, err, errlen);
