@@ -21,13 +21,12 @@
 //               CTA of the pair)
 //   warps 2..9  epilogue: TMEM -> registers -> fused polynomial -> global
 // A pair computes 256 x 256 output tiles (128 rows per CTA) with K advancing
-// by 32 (64-byte swizzle rows) in three-product launches and by 64 (128-byte
-// rows) in one-product ones; the accumulator is double-buffered in TMEM
-// (2 x 256 columns) so the epilogue of tile t overlaps the MMAs of tile t+1.
-// The epilogue reads C straight into registers and stages every 32 x 32
-// chunk of D (and, for symmetric outputs, its transpose) through 8 KB of
-// shared memory per warp, from where TMA bulk stores write whole 64-byte
-// rows.
+// by 64 in three-product launches and by 128 in one-product ones (operand
+// rows in 128-byte swizzled boxes of 64 elements, three 64 KB stages); the
+// accumulator is double-buffered in TMEM (2 x 256 columns) so the epilogue of
+// tile t overlaps the MMAs of tile t+1.  The epilogue stages every 32 x 16
+// chunk of D (and, for symmetric outputs, its transpose) through 4 KB of
+// shared memory per warp, from where TMA bulk stores write it.
 //
 // Symmetric outputs (phases 1 and 2) are computed only on tiles that touch
 // the upper triangle.  Per 128 x 128 block (I, J) of such a tile: I < J is
@@ -970,16 +969,19 @@ cudaError_t launch_pairs(const GemmParams& p, const AP& ap, cudaStream_t s, char
   return cudaGetLastError();
 }
 
-// One layout: CTA pairs.  Three-product launches take k-steps of 32 (64-byte
-// swizzled operand rows); one-product launches take 64 (128-byte rows): with
-// one product per k-step, 64-byte rows asked the copy engine for more rows
-// per clock than it sustains (measured: 20-38 % longer one-product launches).
+// One layout: CTA pairs.  Operand rows are 128-byte swizzled boxes of 64
+// K-elements; three-product launches take 64-deep k-steps (three 64 KB stages,
+// twelve MMAs per stage), one-product launches 128-deep ones (two boxes per
+// operand per stage, eight MMAs, three 64 KB stages): the single issuing
+// thread's per-stage cost is then spread over more MMAs (measured: 32-deep
+// one-product stages took 48 % longer than 64-deep, 128-deep ones 4-9 % less;
+// 64-deep three-product stages 5-9 % less than 32-deep).
 template <int FMT>
 cudaError_t launch_fmt(const GemmParams& p, const FusedApply* fa, cudaStream_t s, char* err, size_t errlen) {
   if (p.terms == 3) {
     if constexpr (FMT != kFmtBf16)
-      if (fa) return launch_pairs<3, true, 32, FMT, FusedApply>(p, *fa, s, err, errlen);
-    return launch_pairs<3, true, 32, FMT>(p, NoApply{}, s, err, errlen);
+      if (fa) return launch_pairs<3, true, 64, FMT, FusedApply>(p, *fa, s, err, errlen);
+    return launch_pairs<3, true, 64, FMT>(p, NoApply{}, s, err, errlen);
   }
   return launch_pairs<1, true, 128, FMT>(p, NoApply{}, s, err, errlen);
 }
