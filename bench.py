@@ -351,7 +351,7 @@ def attention_components(A, args, hp, mc, dev, stream, flush, barrier, peak_t, h
     for _ in range(2):
         ml()
     barrier()
-    t = timed(ml, args.steps)
+    t = timed(ml, args.steps, spin=True)
     ml_ms = statistics.median(t)
     ml_flops = synth_flops_max_logit(att, d_qk)
     out["max_logit"] = {"ms": round(ml_ms, 4), "tflops": round(ml_flops / (ml_ms * 1e-3) / 1e12, 2),
@@ -366,7 +366,7 @@ def attention_components(A, args, hp, mc, dev, stream, flush, barrier, peak_t, h
         for _ in range(2):
             fw()
         barrier()
-        t = timed(fw, args.steps)
+        t = timed(fw, args.steps, spin=True)
         fwd_ms = statistics.median(t)
         fwd_flops = 2.0 * (d_qk + v.shape[-1]) * att.B * att.H * att.S * (att.S + 1) / 2
         out["attn_fwd_fused_smax"] = {

@@ -34,6 +34,7 @@
 #include <string.h>
 
 #include "common.cuh"
+#include "fastdiv.cuh"
 #include "kernels.h"
 
 namespace mc {
@@ -59,7 +60,8 @@ struct Geo {
   int kst, vst;        // K and V stages
   int nqb;             // query blocks per (b, h)
   int nunit;           // units per (b, h) (pairs of query blocks when causal)
-  long long units;
+  uint32_t units;      // below 2^30 (checked on the host)
+  FastDiv div_nunit, div_h;
 };
 
 // Work order.  Causal: a unit is a pair of query blocks (ib, nqb - 1 - ib) of
@@ -72,12 +74,13 @@ struct Geo {
 // -1 when the CTA has no units left.
 __device__ inline int next_item(const AttnFwdParams& p, const Geo& g, uint32_t n, int& b, int& h,
                                 int& ib) {
-  const long long u = blockIdx.x + (long long)(n >> 1) * gridDim.x;
+  // divisions by run-time values as multiply-shifts (fastdiv.cuh)
+  const uint32_t u = blockIdx.x + (n >> 1) * gridDim.x;
   if (u >= g.units) return -1;
-  const long long bh = u / g.nunit;
-  const int pu = (int)(u % g.nunit);
-  h = (int)(bh % p.H);
-  b = (int)(bh / p.H);
+  const uint32_t bh = fastdiv(u, g.div_nunit);
+  const int pu = (int)(u - bh * (uint32_t)g.nunit);
+  b = (int)fastdiv(bh, g.div_h);
+  h = (int)(bh - (uint32_t)b * (uint32_t)p.H);
   if (!p.causal) {
     ib = pu;
     return (n & 1) ? 0 : 1;
@@ -109,13 +112,12 @@ __device__ inline float min3f(float a, float b, float c) {
   return r;
 }
 
-__global__ void smax_init_kernel(float* smax, int H, int accumulate) {
+// S_max stays a float throughout: a non-negative value (sign bit clear) is
+// max-combined as a signed int, a negative one min-combined as an unsigned
+// int, which orders all non-NaN floats as float max does (-0 below +0).
+__global__ void smax_init_kernel(float* smax, int H) {
   const int h = blockIdx.x * blockDim.x + threadIdx.x;
-  if (h < H) reinterpret_cast<int32_t*>(smax)[h] = float_to_ordered(accumulate ? smax[h] : -INFINITY);
-}
-__global__ void smax_final_kernel(float* smax, int H) {
-  const int h = blockIdx.x * blockDim.x + threadIdx.x;
-  if (h < H) smax[h] = ordered_to_float(reinterpret_cast<int32_t*>(smax)[h]);
+  if (h < H) smax[h] = -INFINITY;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -173,7 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t ik = 0, iv = 0, li = 0;
+      // K and V stage rings: next stage and its use parity (counters, no division)
+      uint32_t ks = 0, kph = 0, vs = 0, vph = 0, li = 0;
       bool used_q = false, used_k[kMaxStages] = {}, used_v[kMaxStages] = {};
       uint32_t par_q = 0, par_k[kMaxStages] = {}, par_v[kMaxStages] = {};
       for (uint32_t n = 0; !abort_flag; ++n) {
@@ -189,23 +192,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int j = 0; j < nkb && ok; ++j) {
           {
-            const int s = ik % g.kst;
-            if (!mbar_wait(&k_empty[s], ((ik / g.kst) & 1) ^ 1, &abort_flag)) { fail(); ok = false; break; }
+            const int s = (int)ks;
+            if (!mbar_wait(&k_empty[s], kph ^ 1, &abort_flag)) { fail(); ok = false; break; }
             mbar_arrive_expect_tx(&k_full[s], g.nch * CH);
             uint8_t* dst = kbuf + s * g.nch * CH;
             for (int c = 0; c < g.nch; ++c) {
               if (c < g.nck) tma_load_4d(dst + c * CH, &mp.k, &k_full[s], 64 * c, h, j * BN, b);
               else tma_load_3d(dst + c * CH, &mp.ks, &k_full[s], 64 * (c - g.nck), j * BN, b);
             }
-            used_k[s] = true; par_k[s] = (ik / g.kst) & 1; ++ik;
+            used_k[s] = true; par_k[s] = kph;
+            if (++ks == (uint32_t)g.kst) { ks = 0; kph ^= 1; }
           }
           {
-            const int s = iv % g.vst;
-            if (!mbar_wait(&v_empty[s], ((iv / g.vst) & 1) ^ 1, &abort_flag)) { fail(); ok = false; break; }
+            const int s = (int)vs;
+            if (!mbar_wait(&v_empty[s], vph ^ 1, &abort_flag)) { fail(); ok = false; break; }
             mbar_arrive_expect_tx(&v_full[s], g.ncv * CH);
             uint8_t* dst = vbuf + s * g.ncv * CH;
             for (int c = 0; c < g.ncv; ++c) tma_load_4d(dst + c * CH, &mp.v, &v_full[s], 64 * c, h, j * BN, b);
-            used_v[s] = true; par_v[s] = (iv / g.vst) & 1; ++iv;
+            used_v[s] = true; par_v[s] = vph;
+            if (++vs == (uint32_t)g.vst) { vs = 0; vph ^= 1; }
           }
         }
         if (!ok) break;
@@ -221,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc_bf16(BM, BN, 0, 0);   // Q (K-major) x K (K-major)
       const uint32_t idesc_o = make_idesc_bf16(BM, 64 * g.ncv, 0, 1);  // P (K-major) x V (MN-major)
-      uint32_t ik = 0, iv = 0, sc = 0, pc = 0, li = 0;
+      uint32_t ks = 0, kph = 0, vs = 0, vph = 0, sc = 0, pc = 0, li = 0;   // rings as in the producer
       bool issued = false;
       for (uint32_t n = 0; !abort_flag; ++n) {
         int b, h, ib;
@@ -235,8 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j < nkb) {                 // S_j = Q K_j^T
             const int buf = sc & 1;
             if (!mbar_wait(&s_empty[buf], ((sc >> 1) & 1) ^ 1, &abort_flag)) { fail(); ok = false; break; }
-            const int s = ik % g.kst;
-            if (!mbar_wait(&k_full[s], (ik / g.kst) & 1, &abort_flag)) { fail(); ok = false; break; }
+            const int s = (int)ks;
+            if (!mbar_wait(&k_full[s], kph, &abort_flag)) { fail(); ok = false; break; }
             tc_fence_after();
             const uint32_t qa = smem_u32(qbuf), ka = smem_u32(kbuf + s * g.nch * CH);
             for (int c = 0; c < g.nch; ++c)
@@ -249,13 +254,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(&k_empty[s]);
             tc_commit(&s_full[buf]);
             if (j == nkb - 1) tc_commit(q_empty);
-            ++ik; ++sc;
+            if (++ks == (uint32_t)g.kst) { ks = 0; kph ^= 1; }
+            ++sc;
           }
           if (j >= 1) {                  // O += P_{j-1} V_{j-1}
             if (j == 1 && !mbar_wait(o_empty, (li & 1) ^ 1, &abort_flag)) { fail(); ok = false; break; }
             if (!mbar_wait(p_full, pc & 1, &abort_flag)) { fail(); ok = false; break; }
-            const int s = iv % g.vst;
-            if (!mbar_wait(&v_full[s], (iv / g.vst) & 1, &abort_flag)) { fail(); ok = false; break; }
+            const int s = (int)vs;
+            if (!mbar_wait(&v_full[s], vph, &abort_flag)) { fail(); ok = false; break; }
             tc_fence_after();
             const uint32_t pa = smem_u32(pbuf), va = smem_u32(vbuf + s * g.ncv * CH);
 #pragma unroll
@@ -267,7 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                      make_sdesc(va + kk * 2048, CH, 1024, 2), idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
             tc_commit(&v_empty[s]);
             tc_commit(p_empty);
-            ++iv; ++pc;
+            if (++vs == (uint32_t)g.vst) { vs = 0; vph ^= 1; }
+            ++pc;
           }
         }
         if (!ok) break;
@@ -476,8 +483,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       float wm = raw_max;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
-      if (lane == 0 && wm > -INFINITY)
-        atomicMax(reinterpret_cast<int32_t*>(p.smax) + h, float_to_ordered(wm * p.scale));
+      if (lane == 0 && wm > -INFINITY) {
+        const float v = wm * p.scale;
+        if (__float_as_int(v) >= 0) atomicMax(reinterpret_cast<int*>(p.smax) + h, __float_as_int(v));
+        else atomicMin(reinterpret_cast<unsigned int*>(p.smax) + h, __float_as_uint(v));
+      }
       ++li;
     }
     if (lane == 0) bulk_wait0();
@@ -526,7 +536,11 @@ bool geometry(const AttnFwdParams& p, Geo& g, size_t& smem, char* err, size_t er
   g.ncv = (p.d_v + 63) / 64;
   g.nqb = (p.S + BM - 1) / BM;
   g.nunit = p.causal ? (g.nqb + 1) / 2 : g.nqb;
-  g.units = (long long)p.B * p.H * g.nunit;
+  const long long units = (long long)p.B * p.H * g.nunit;
+  if (units >= (1ll << 30)) { snprintf(err, errlen, "%lld work units exceed the kernel's 2^30", units); return false; }
+  g.units = (uint32_t)units;
+  g.div_nunit = make_fastdiv((uint32_t)g.nunit);
+  g.div_h = make_fastdiv((uint32_t)p.H);
   const size_t cap = 227 * 1024 - 1024 - 256 - 2 * 2 * BM * 4 - 64;   // static: red, abort flag
   const size_t fixed = (size_t)(g.nch + 2) * CH;      // Q, P
   g.kst = g.vst = 0;
@@ -611,16 +625,16 @@ cudaError_t launch_attn_fwd(const AttnFwdParams& p, cudaStream_t s, char* err, s
     if (!encode(&mp.o, p.o, 4, dims, st, box, CU_TENSOR_MAP_SWIZZLE_64B)) { snprintf(err, errlen, "tensor map for o failed"); return cudaErrorInvalidValue; }
   }
   const int hb = (p.H + 127) / 128;
-  smax_init_kernel<<<hb, 128, 0, s>>>(p.smax, p.H, p.accumulate);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (!p.accumulate) {
+    smax_init_kernel<<<hb, 128, 0, s>>>(p.smax, p.H);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   e = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int grid = (int)(g.units < sm_count() ? g.units : sm_count());
+  const int grid = (int)(g.units < (uint32_t)sm_count() ? g.units : (uint32_t)sm_count());
   attn_fwd_kernel<<<grid, kThreads, smem, s>>>(p, mp, g);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  smax_final_kernel<<<hb, 128, 0, s>>>(p.smax, p.H);
   return cudaGetLastError();
 }
 

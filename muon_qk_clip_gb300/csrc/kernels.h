@@ -207,7 +207,7 @@ struct MaxLogitParams {
   float scale;
   const void* q; const void* k; const void* ks;
   long long qs[3], kst[3], kss[2];
-  float* smax;             // ordered-int scratch view when argmax is null
+  float* smax;             // [H] float maxima (with argmax: written at the end)
   long long* argmax;       // packed (ordered value << 32 | ~index) scratch view
   int accumulate;
   int32_t* status;
@@ -222,7 +222,7 @@ struct AttnFwdParams {
   const void* q; const void* k; const void* ks; const void* v; void* o;
   long long qs[3], kst[3], kss[2], vs[3], os[3];   // element strides (batch, seq, head)
   float* lse;              // [B, H, S] or null
-  float* smax;             // [H]; ordered-int view during the launch
+  float* smax;             // [H] float maxima, max-combined in place
   int accumulate;
   int32_t* status;
 };

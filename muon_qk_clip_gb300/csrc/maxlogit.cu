@@ -4,8 +4,11 @@
 // running maxima in registers and publishes one packed atomicMax per head.
 //
 // Results travel through the caller's output buffers:
-//   argmax == null : smax[h] holds an order-preserving int32 image of the
-//                    scaled max during the launch (init -> atomicMax -> decode)
+//   argmax == null : smax[h] holds the float maximum throughout: a
+//                    non-negative value (sign bit clear) is max-combined as a
+//                    signed int, a negative one min-combined as an unsigned
+//                    int, which orders all non-NaN floats as float max does
+//                    (-0 below +0); initialised to -inf unless accumulating
 //   argmax != null : argmax[h] holds a packed 64-bit key
 //                    (ordered value << 32 | (0xffffffff - flat index)) so one
 //                    atomicMax keeps the largest value and, among equal
@@ -14,6 +17,7 @@
 #include <string.h>
 
 #include "common.cuh"
+#include "fastdiv.cuh"
 #include "kernels.h"
 
 namespace mc {
@@ -27,33 +31,28 @@ __device__ inline unsigned long long pack_key(float v, uint32_t idx) {
 __global__ void ml_init_kernel(MaxLogitParams p) {
   const int h = blockIdx.x * blockDim.x + threadIdx.x;
   if (h >= p.H) return;
-  if (p.argmax) {
+  if (p.argmax)
     reinterpret_cast<unsigned long long*>(p.argmax)[h] = 0ull;
-  } else {
-    int32_t* si = reinterpret_cast<int32_t*>(p.smax);
-    si[h] = float_to_ordered(p.accumulate ? p.smax[h] : -INFINITY);
-  }
+  else if (!p.accumulate)
+    p.smax[h] = -INFINITY;
 }
 
 __global__ void ml_final_kernel(MaxLogitParams p) {
   const int h = blockIdx.x * blockDim.x + threadIdx.x;
   if (h >= p.H) return;
-  if (p.argmax) {
-    const unsigned long long key = reinterpret_cast<unsigned long long*>(p.argmax)[h];
-    const int32_t ord = (int32_t)((uint32_t)(key >> 32) ^ 0x80000000u);
-    p.smax[h] = ordered_to_float(ord);
-    p.argmax[h] = (long long)(0xffffffffu - (uint32_t)(key & 0xffffffffull));
-  } else {
-    const int32_t ord = reinterpret_cast<int32_t*>(p.smax)[h];
-    p.smax[h] = ordered_to_float(ord);
-  }
+  const unsigned long long key = reinterpret_cast<unsigned long long*>(p.argmax)[h];
+  const int32_t ord = (int32_t)((uint32_t)(key >> 32) ^ 0x80000000u);
+  p.smax[h] = ordered_to_float(ord);
+  p.argmax[h] = (long long)(0xffffffffu - (uint32_t)(key & 0xffffffffull));
 }
 
 __device__ inline void publish(const MaxLogitParams& p, int h, float v, uint32_t idx) {
   if (p.argmax)
     atomicMax(reinterpret_cast<unsigned long long*>(p.argmax) + h, pack_key(v, idx));
+  else if (__float_as_int(v) >= 0)
+    atomicMax(reinterpret_cast<int*>(p.smax) + h, __float_as_int(v));
   else
-    atomicMax(reinterpret_cast<int32_t*>(p.smax) + h, float_to_ordered(v));
+    atomicMin(reinterpret_cast<unsigned int*>(p.smax) + h, __float_as_uint(v));
 }
 
 // ---------------------------------------------------------------- CUDA cores
@@ -157,12 +156,15 @@ __global__ void __launch_bounds__(256) ml_simt_kernel(const __grid_constant__ Ma
 
 // ---------------------------------------------------------------- tensor cores
 // bf16 features, q.k length in 64-wide chunks.  One work item = (b, h, 128
-// query rows), in the paired (b, h)-major order of next_item; its Q chunks are
-// loaded once (double-buffered across items) and
-// 256-row key blocks stream through a ring of 64-feature chunk stages.  For
-// MLA the key chunks come first from the head's k^C, then from the shared k^R.
-// Each key block is one 128 x 256 x d product accumulated in TMEM (double
-// buffered); 8 epilogue warps take running row maxima straight out of TMEM.
+// query rows), in the order of next_item; its Q chunks are loaded once
+// (double-buffered across items) and 256-row key blocks stream through a ring
+// of 64-feature chunk stages.  For MLA the key chunks come first from the
+// head's k^C, then from the shared k^R.  Each key block is one 128 x 256 x d
+// product accumulated in TMEM (double buffered); 8 epilogue warps take running
+// row maxima straight out of TMEM.
+// With a few 128 x 256 x 16 MMAs per stage the single issuing thread is on the
+// critical path, so its loop does no division (ring counters, multiply-shift
+// item decoding) and builds each stage's two descriptors once.
 namespace tcml {
 
 constexpr int BM = 128, BN = 256;
@@ -183,9 +185,19 @@ struct Geo {
   int stages;
   int nqb;             // query blocks per (b, h)
   int nunit;           // work units per (b, h) (pairs of query blocks when causal)
-  long long units;
+  uint32_t units;       // below 2^30 (checked on the host)
+  FastDiv div_nunit, div_h, div_bh;   // by nunit, H and B H
+  int snake;           // 1: items heaviest first, dealt to the CTAs in snake order
+  uint32_t items;      // B H nqb (snake order)
 };
 
+
+// 3-input minimum that returns NaN when any input is NaN
+__device__ inline float min3_nan(float a, float b, float c) {
+  float r;
+  asm("min.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 __device__ inline float max3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
@@ -199,12 +211,28 @@ __device__ inline float max3(float a, float b, float c) {
 // an unpaired middle block, -1 when the CTA has no units left.
 __device__ inline int next_item(const MaxLogitParams& p, const Geo& g, uint32_t n, int& b, int& h,
                                 int& ib) {
-  const long long u = blockIdx.x + (long long)(n >> 1) * gridDim.x;
+  if (g.snake) {
+    // item k = (b h, query block): blocks in decreasing order of work (the
+    // query block from the last down), every head within a block; round n
+    // deals G consecutive items to the G CTAs, alternately forward and back,
+    // so every CTA's total stays within one item of the others'
+    const uint32_t G = gridDim.x;
+    const uint32_t k = n * G + ((n & 1) ? G - 1 - blockIdx.x : blockIdx.x);
+    if (k >= g.items) return -1;
+    const uint32_t q = fastdiv(k, g.div_bh);
+    const uint32_t bh = k - q * (uint32_t)(p.B * p.H);
+    ib = g.nqb - 1 - (int)q;
+    b = (int)fastdiv(bh, g.div_h);
+    h = (int)(bh - (uint32_t)b * (uint32_t)p.H);
+    return 1;
+  }
+  // divisions by run-time values as multiply-shifts (fastdiv.cuh)
+  const uint32_t u = blockIdx.x + (n >> 1) * gridDim.x;
   if (u >= g.units) return -1;
-  const long long bh = u / g.nunit;
-  const int pu = (int)(u % g.nunit);
-  h = (int)(bh % p.H);
-  b = (int)(bh / p.H);
+  const uint32_t bh = fastdiv(u, g.div_nunit);
+  const int pu = (int)(u - bh * (uint32_t)g.nunit);
+  b = (int)fastdiv(bh, g.div_h);
+  h = (int)(bh - (uint32_t)b * (uint32_t)p.H);
   if (!p.causal) {
     ib = pu;
     return (n & 1) ? 0 : 1;
@@ -260,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      uint32_t it = 0, li = 0;
+      uint32_t ks = 0, kph = 0, li = 0;     // next key stage and its use parity
       bool used_q[2] = {false, false}, used_k[kMaxStages] = {};
       uint32_t par_q[2] = {0, 0}, par_k[kMaxStages] = {};
       for (uint32_t n = 0; !abort_flag; ++n) {
@@ -277,16 +305,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nkb = kblocks(p, ib);
         bool ok = true;
         for (int kb = 0; kb < nkb && ok; ++kb) {
-          for (int c = 0; c < g.nch; ++c, ++it) {
-            const int s = it % g.stages;
-            const uint32_t use = it / g.stages;
-            if (!mbar_wait(&k_empty[s], (use & 1) ^ 1, &abort_flag)) { fail(); ok = false; break; }
+          for (int c = 0; c < g.nch; ++c) {
+            const int s = (int)ks;
+            if (!mbar_wait(&k_empty[s], kph ^ 1, &abort_flag)) { fail(); ok = false; break; }
             mbar_arrive_expect_tx(&k_full[s], K_CHUNK);
             if (c < g.nck)
               tma_load_4d(kbuf + s * K_CHUNK, &mp.k, &k_full[s], 64 * c, h, kb * BN, b);
             else
               tma_load_3d(kbuf + s * K_CHUNK, &mp.ks, &k_full[s], 64 * (c - g.nck), kb * BN, b);
-            used_k[s] = true; par_k[s] = use & 1;
+            used_k[s] = true; par_k[s] = kph;
+            if (++ks == (uint32_t)g.stages) { ks = 0; kph ^= 1; }
           }
         }
         if (!ok) break;
@@ -298,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = make_idesc_bf16(BM, BN, 0, 0);
-      uint32_t it = 0, li = 0, tcount = 0;
+      uint32_t ks = 0, kph = 0, li = 0, tcount = 0;   // key stage ring as in the producer
       bool issued = false;
       for (uint32_t n = 0; !abort_flag; ++n) {
         int b, h, ib;
@@ -314,18 +342,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&t_empty[acc], ((tcount / kNBuf) & 1) ^ 1, &abort_flag)) { fail(); ok = false; break; }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * BN;
-          for (int c = 0; c < g.nch; ++c, ++it) {
-            const int s = it % g.stages;
-            if (!mbar_wait(&k_full[s], (it / g.stages) & 1, &abort_flag)) { fail(); ok = false; break; }
+          for (int c = 0; c < g.nch; ++c) {
+            const int s = (int)ks;
+            if (!mbar_wait(&k_full[s], kph, &abort_flag)) { fail(); ok = false; break; }
             tc_fence_after();
-            const uint32_t qa = smem_u32(qbuf + (qb * g.nch + c) * Q_CHUNK);
-            const uint32_t ka = smem_u32(kbuf + s * K_CHUNK);
+            const uint64_t qd = make_sdesc_sw128(smem_u32(qbuf + (qb * g.nch + c) * Q_CHUNK), 16, 1024);
+            const uint64_t kd = make_sdesc_sw128(smem_u32(kbuf + s * K_CHUNK), 16, 1024);
+            tc_mma(d_tmem, qd, kd, idesc, c > 0 ? 1u : 0u);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc_mma(d_tmem, make_sdesc_sw128(qa + kk * 32, 16, 1024),
-                     make_sdesc_sw128(ka + kk * 32, 16, 1024), idesc, (c > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 1; kk < 4; ++kk) tc_mma(d_tmem, qd + 2 * kk, kd + 2 * kk, idesc, 1u);
             issued = true;
             tc_commit(&k_empty[s]);
+            if (++ks == (uint32_t)g.stages) { ks = 0; kph ^= 1; }
           }
           if (ok) tc_commit(&t_full[acc]);
         }
@@ -351,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int i_lo = ib * BM + q * 32;              // warp's first row
       float best = -INFINITY;
       uint32_t bidx = 0xffffffffu;
-      float nan4[4] = {0.f, 0.f, 0.f, 0.f};
+      float lo4[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
       int failed = 0;                    // warp-uniform
       for (int kb = 0; kb < nkb; ++kb, ++tcount) {
         if (failed) continue;            // every later wait would fail too
@@ -386,24 +414,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int x = 0; x < 32; ++x) {
                   const int j = jc + x;
                   const bool valid = j < p.S && i < p.S && (!p.causal || j <= i);
-                  v[x] = valid ? v[x] : -3.402823466e38f;   // finite: keeps the NaN check exact
+                  v[x] = valid ? v[x] : -3.402823466e38f;   // finite: invisible to the non-finite check
                 }
               }
-              // four independent chains each for the NaN check and the max
+              // four independent chains each for the maximum and for the
+              // NaN-propagating minimum (the non-finite check): one 3-input
+              // min or max per two logits
               float m4[4];
 #pragma unroll
               for (int c = 0; c < 4; ++c) {
                 m4[c] = fmaxf(v[2 * c], v[2 * c + 1]);
-                nan4[c] = fmaf(v[2 * c], 0.f, nan4[c]);
-                nan4[c] = fmaf(v[2 * c + 1], 0.f, nan4[c]);
+                lo4[c] = min3_nan(lo4[c], v[2 * c], v[2 * c + 1]);
               }
 #pragma unroll
               for (int x = 8; x < 32; x += 8)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                   m4[c] = max3(m4[c], v[x + 2 * c], v[x + 2 * c + 1]);
-                  nan4[c] = fmaf(v[x + 2 * c], 0.f, nan4[c]);
-                  nan4[c] = fmaf(v[x + 2 * c + 1], 0.f, nan4[c]);
+                  lo4[c] = min3_nan(lo4[c], v[x + 2 * c], v[x + 2 * c + 1]);
                 }
               const float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
               if (m > best) {
@@ -422,8 +450,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&t_empty[acc]);
       }
-      // nan4 became NaN iff some unmasked logit was NaN or infinite.
-      const float nanacc = (nan4[0] + nan4[1]) + (nan4[2] + nan4[3]);
+      // some unmasked logit was NaN or -inf iff the NaN-propagating minimum is
+      // NaN or -inf; +inf iff the running maximum is
+      const float lo = min3_nan(lo4[0], lo4[1], min3_nan(lo4[2], lo4[3], lo4[3]));
+      const bool nonfinite = !(lo > -INFINITY) || best == INFINITY;
       // Reduce (best, bidx) over the warp; each warp publishes its own
       // maximum (the packed atomic max is order-independent, and scaling by
       // a positive factor commutes with max), so the eight epilogue warps
@@ -434,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t oi = __shfl_down_sync(0xffffffffu, bidx, o);
         if (ov > best || (ov == best && oi < bidx)) { best = ov; bidx = oi; }
       }
-      const int badw = __any_sync(0xffffffffu, nanacc != 0.f);
+      const int badw = __any_sync(0xffffffffu, nonfinite);
       if (lane == 0 && !failed) {
         if (badw) set_status(p.status, MC_STATUS_NONFINITE_LOGIT);
         if (best > -INFINITY) publish(p, h, best * p.scale, bidx);
@@ -506,7 +536,22 @@ cudaError_t launch_ml_tc(const MaxLogitParams& p, cudaStream_t s, char* err, siz
   g.nch = p.d_shared > 0 ? g.nck + (p.d_shared + 63) / 64 : g.nck;
   g.nqb = (p.S + BM - 1) / BM;
   g.nunit = p.causal ? (g.nqb + 1) / 2 : g.nqb;
-  g.units = (long long)p.B * p.H * g.nunit;
+  const long long units = (long long)p.B * p.H * g.nunit;
+  if (units >= (1ll << 30)) { snprintf(err, errlen, "%lld work units exceed the kernel's 2^30", units); return cudaErrorInvalidValue; }
+  g.units = (uint32_t)units;
+  g.div_nunit = make_fastdiv((uint32_t)g.nunit);
+  g.div_h = make_fastdiv((uint32_t)p.H);
+  g.div_bh = make_fastdiv((uint32_t)(p.B * p.H));
+  {
+    // Heaviest-first snake order balances the CTAs' work to within one item,
+    // but interleaves every head, so it is taken only while all the keys
+    // stay resident in L2 (at most 96 MB); beyond that the paired
+    // (b, h)-major order keeps the heads in flight few.
+    const long long kbytes = (long long)p.B * p.S * ((long long)p.H * p.d_head + p.d_shared) * 2;
+    const long long items = (long long)p.B * p.H * g.nqb;
+    g.snake = (p.causal && kbytes <= (96ll << 20) && items < (1ll << 30)) ? 1 : 0;
+    g.items = g.snake ? (uint32_t)items : 0u;
+  }
   const int smem_cap = 227 * 1024 - 2048;
   g.stages = (smem_cap - 2 * g.nch * Q_CHUNK) / K_CHUNK;
   if (g.stages > kMaxStages) g.stages = kMaxStages;
@@ -530,7 +575,7 @@ cudaError_t launch_ml_tc(const MaxLogitParams& p, cudaStream_t s, char* err, siz
     if (!encode(&mp.ks, p.ks, 3, dims, st, box)) { snprintf(err, errlen, "tensor map for k_shared failed"); return cudaErrorInvalidValue; }
   }
   const size_t smem = 1024 + 2 * g.nch * Q_CHUNK + g.stages * K_CHUNK + 512;
-  const int grid = (int)(g.units < sm_count() ? g.units : sm_count());
+  const int grid = (int)(g.units < (uint32_t)sm_count() ? g.units : (uint32_t)sm_count());
   cudaError_t e;
   if (p.argmax) {
     e = cudaFuncSetAttribute(ml_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -548,13 +593,18 @@ cudaError_t launch_ml_tc(const MaxLogitParams& p, cudaStream_t s, char* err, siz
 
 cudaError_t launch_max_logit(const MaxLogitParams& p, cudaStream_t s, char* err, size_t errlen) {
   const int hb = (p.H + 127) / 128;
-  ml_init_kernel<<<hb, 128, 0, s>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  // an accumulating S_max needs neither the initial nor the decoding pass;
+  // a plain one only the initial -inf; the argmax keys both
+  if (p.argmax || !p.accumulate) {
+    ml_init_kernel<<<hb, 128, 0, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   if (tc_eligible(p)) {
     e = launch_ml_tc(p, s, err, errlen);
     if (e != cudaSuccess) return e;
-    ml_final_kernel<<<hb, 128, 0, s>>>(p);
+    if (p.argmax) ml_final_kernel<<<hb, 128, 0, s>>>(p);
     return cudaGetLastError();
   }
   const int D = p.d_head + p.d_shared;
@@ -573,7 +623,7 @@ cudaError_t launch_max_logit(const MaxLogitParams& p, cudaStream_t s, char* err,
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  ml_final_kernel<<<hb, 128, 0, s>>>(p);
+  if (p.argmax) ml_final_kernel<<<hb, 128, 0, s>>>(p);
   (void)err; (void)errlen;
   return cudaGetLastError();
 }

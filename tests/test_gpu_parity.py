@@ -324,6 +324,29 @@ def test_max_logit_flags_nonfinite():
     assert st.item() & abi.MC_STATUS_NONFINITE_LOGIT
 
 
+@pytest.mark.parametrize("kind", ["+inf", "-inf", "nan"])
+def test_max_logit_flags_each_nonfinite_kind(kind):
+    """One query row whose logits are all +inf, all -inf or all NaN (one
+    feature of q is non-finite, that feature of k is positive, the rest of the
+    row is zero); every other logit is finite.  Each kind must set the flag on
+    its own, on the tensor-core path (bf16, d 64) and with argmax."""
+    B, S, H, d = 2, 300, 3, 64
+    q, k, _ = synth.attention_features(B, S, H, d, d, 0, BF16, seed=17)
+    k[:, :, 1, 7] = k[:, :, 1, 7].abs() + 0.5
+    q[1, 211, 1, :] = 0
+    q[1, 211, 1, 7] = {"+inf": float("inf"), "-inf": float("-inf"), "nan": float("nan")}[kind]
+    for argmax in (None, torch.empty(H, dtype=torch.int64, device="cuda")):
+        st = new_status()
+        mc.qk_max_logit(q.cuda(), k.cuda(), status=st, argmax=argmax)
+        torch.cuda.synchronize()
+        assert st.item() & abi.MC_STATUS_NONFINITE_LOGIT, (kind, argmax is not None)
+    st = new_status()
+    q[1, 211, 1, 7] = 1.0
+    mc.qk_max_logit(q.cuda(), k.cuda(), status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+
+
 # ------------------------------------------------------------------ QK-Clip
 def test_clip_mha_parity_and_untouched_heads():
     H, d, D, tau = 8, 16, 40, 100.0
