@@ -664,8 +664,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0;
       uint32_t last_par[8] = {};
       bool used[8] = {};
+      // the first CTA claims one tile ahead of its own loads, so the id of
+      // the next tile is in the ring while this one's stages are loaded
+      int ahead = crank == 0 ? claim(0) : 0;
       for (uint32_t seq = 0; !abort_flag; ++seq) {
-        const int t = crank == 0 ? claim(seq) : take(seq);
+        int t;
+        if (crank == 0) {
+          t = ahead;
+          if (t >= 0) ahead = claim(seq + 1);
+        } else {
+          t = take(seq);
+        }
         if (t == -2) { fail(); break; }
         if (t < 0) break;
         const TileCoord tc = tile_coord<TM_ROWS>(p, t);
