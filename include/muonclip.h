@@ -322,6 +322,42 @@ typedef struct {
 void mc_profiler_enable(int32_t on);
 int32_t mc_profiler_read(mc_kernel_time* out, int32_t max, int32_t reset);
 
+/* ---- Setup (untimed): the attention layer's query/key features on the
+ * library's own kernels ([K2-internals] "MLA 的特殊处理": q^C and the rotary
+ * q^R from the compressed query latent, k^C from the compressed key/value
+ * latent, one rotary k^R shared by every head; MHA: Q = X W_q^T, K = X W_k^T),
+ * so that S_max and its re-measurement after a clip run on the library. ---- */
+
+/* D = A B^T.  A: [M, K] row-major with pitch lda (elements), B: [N, K] with
+ * pitch ldb, D: [M, N] with pitch ldd, all device memory of one dtype.
+ * MC_BF16 runs on the Newton-Schulz phases' tcgen05 GEMM core (one bf16
+ * plane, fp32 accumulation, D rounded to bf16); MC_F32 on the CUDA-core GEMM
+ * (products summed in an unevaluated fp32 pair, D rounded to fp32).  Pointers
+ * and pitches 16-byte aligned; K >= 1; M or N of 0 returns at once.
+ * scratch (MC_BF16 only): device, 16-byte aligned, >= 16 bytes, caller-owned;
+ * the call zeroes it as its launch's tile counter, so one call at a time may
+ * use it.  A NaN/Inf in D ORs MC_STATUS_NONFINITE_UPDATE into *status
+ * (device int32, nullable).  Asynchronous on `stream`. */
+mc_status mc_matmul(const void* A, int64_t lda, const void* B, int64_t ldb, void* D, int64_t ldd,
+                    int32_t M, int32_t N, int32_t K, int32_t dtype, void* scratch, int32_t* status,
+                    mc_stream_t stream);
+
+/* Weightless RMSNorm of each row (the MLA latents): y = x / sqrt(mean(x^2) +
+ * eps) over `cols` values, fp32 arithmetic.  x, y: device, dtype MC_BF16 or
+ * MC_F32, pitches ldx, ldy >= cols; in place when y == x and ldy == ldx;
+ * eps >= 0; rows of 0 returns at once.  Asynchronous on `stream`. */
+mc_status mc_rms_norm(const void* x, int64_t ldx, void* y, int64_t ldy, int64_t rows, int32_t cols,
+                      int32_t dtype, float eps, mc_stream_t stream);
+
+/* Rotary embedding in place on interleaved pairs.  x[b, s, h, 0..d) lives at
+ * element offset b*sb + s*ss + h*sh (device, dtype MC_BF16 or MC_F32); each
+ * pair (x[2k], x[2k+1]) rotates by the angle s * theta^(-2k/d) at position s
+ * (0..S-1): (x0 cos - x1 sin, x0 sin + x1 cos), the angle, its cosine and sine
+ * taken in fp64.  d even, 2..4096; heads nh >= 1; theta > 0.  Asynchronous
+ * on `stream`. */
+mc_status mc_rope(void* x, int32_t B, int32_t S, int32_t nh, int32_t d, int64_t sb, int64_t ss, int64_t sh,
+                  int32_t dtype, double theta, mc_stream_t stream);
+
 /* Diagnostic: exercises the bounded device wait that every tcgen05 kernel of
  * the library uses for its mbarrier phases.  One CTA waits on a phase that
  * nothing completes, for at most budget_ns nanoseconds of %globaltimer

@@ -8,7 +8,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from ctypes import POINTER, c_char_p, c_float, c_int32, c_int64, c_size_t, c_uint64, c_void_p
+from ctypes import POINTER, c_char_p, c_double, c_float, c_int32, c_int64, c_size_t, c_uint64, c_void_p
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmuonclip.so")
 
@@ -87,6 +87,12 @@ SIGNATURES = {
     "muonclip_step": (c_int32, [POINTER(McMat), POINTER(McMat), POINTER(McMat), c_int32,
                                 POINTER(McHparams), POINTER(McClipLayer), c_int32, c_void_p,
                                 c_size_t, c_void_p, c_void_p]),
+    "mc_matmul": (c_int32, [c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_int64, c_int32, c_int32,
+                            c_int32, c_int32, c_void_p, c_void_p, c_void_p]),
+    "mc_rms_norm": (c_int32, [c_void_p, c_int64, c_void_p, c_int64, c_int64, c_int32, c_int32, c_float,
+                              c_void_p]),
+    "mc_rope": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_int32, c_int64, c_int64, c_int64, c_int32,
+                          c_double, c_void_p]),
     "mc_selftest_bounded_wait": (c_int32, [c_uint64, c_uint64, c_void_p, c_void_p, c_void_p]),
     "mc_profiler_enable": (None, [c_int32]),
     "mc_profiler_read": (c_int32, [POINTER(McKernelTime), c_int32, c_int32]),

@@ -254,6 +254,54 @@ def muonclip_step(W, G, M, hp: Hparams | None = None, layers=(), workspace=None,
                                    _stream(stream)), "muonclip_step")
 
 
+def _rows(t, name):
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name}: expected a 2-D tensor with unit column stride")
+    if t.dtype not in _DT:
+        raise ValueError(f"{name}: unsupported dtype {t.dtype}")
+    return max(t.stride(0), t.shape[1])
+
+
+def matmul(A, B, out=None, scratch=None, status=None, stream=None):
+    """Setup: D = A B^T on the library's GEMM core (bf16: tcgen05; fp32: CUDA
+    cores).  A [M, K] and B [N, K] row-major device tensors of one dtype."""
+    lda, ldb = _rows(A, "A"), _rows(B, "B")
+    if A.dtype != B.dtype or A.shape[1] != B.shape[1]:
+        raise ValueError("A and B need one dtype and one K")
+    M, K, N = A.shape[0], A.shape[1], B.shape[0]
+    if out is None:
+        out = torch.empty(M, N, dtype=A.dtype, device=A.device)
+    ldd = _rows(out, "out")
+    if scratch is None and A.dtype == torch.bfloat16:
+        scratch = torch.empty(4, dtype=torch.int32, device=A.device)
+    check(abi.load().mc_matmul(_ptr(A), lda, _ptr(B), ldb, _ptr(out), ldd, M, N, K, _DT[A.dtype],
+                               _ptr(scratch), _ptr(status), _stream(stream)), "mc_matmul")
+    return out
+
+
+def rms_norm(x, out=None, eps: float = 1e-6, stream=None):
+    """Setup: weightless RMSNorm of each row of a 2-D device tensor (out may be x)."""
+    ldx = _rows(x, "x")
+    if out is None:
+        out = torch.empty_like(x)
+    ldy = _rows(out, "out")
+    check(abi.load().mc_rms_norm(_ptr(x), ldx, _ptr(out), ldy, x.shape[0], x.shape[1], _DT[x.dtype],
+                                 float(eps), _stream(stream)), "mc_rms_norm")
+    return out
+
+
+def rope_(x, theta: float = 10000.0, stream=None):
+    """Setup: rotary embedding in place on interleaved pairs of x [B, S, d] or
+    [B, S, heads, d] (unit stride along d), positions 0..S-1."""
+    if x.stride(-1) != 1 or x.dtype not in _DT or x.dim() not in (3, 4):
+        raise ValueError("x: [B, S, d] or [B, S, heads, d] with unit stride along d")
+    B, S, d = x.shape[0], x.shape[1], x.shape[-1]
+    nh, sh = (x.shape[2], x.stride(2)) if x.dim() == 4 else (1, 0)
+    check(abi.load().mc_rope(_ptr(x), B, S, nh, d, x.stride(0), x.stride(1), sh, _DT[x.dtype],
+                             float(theta), _stream(stream)), "mc_rope")
+    return x
+
+
 def profiler_enable(on: bool = True):
     """Bracket every library launch with CUDA events (per kernel class)."""
     abi.load().mc_profiler_enable(1 if on else 0)

@@ -1,59 +1,50 @@
 """Untimed setup: query/key features of an attention layer from its weights.
 
 This is the model forward that produces Q and K (Q^h = X W_q^h, K^h = X W_k^h
-for MHA; the MLA latent projections with RMSNorm and RoPE), run with torch
-matmuls to build inputs for qk_max_logit.  It is not part of the MuonClip
-step: in training, S_max comes from the forward pass.
+for MHA; the MLA latent projections with RMSNorm and RoPE, [K2-internals]
+"MLA 的特殊处理"), run on the library's own kernels (mc_matmul on the tcgen05
+GEMM core for bf16, mc_rms_norm, mc_rope) to build inputs for qk_max_logit
+and to re-measure S_max after a clip.  It is not part of the MuonClip step: in
+training, S_max comes from the forward pass.  Device tensors only.
 """
 from __future__ import annotations
 
-import torch
+from . import binding as mc
+
+
+def _on_device(*ts):
+    for t in ts:
+        if t.device.type != "cuda":
+            raise ValueError("the projection runs on the library's CUDA kernels: pass device tensors")
 
 
 def project_mha(X, Wq, Wk, H: int):
     """Q = X Wq^T, K = X Wk^T as [B, S, H, d] views (fp32 accumulate, X dtype out)."""
+    _on_device(X, Wq, Wk)
     B, S, D = X.shape
     x2 = X.reshape(B * S, D)
-    q = (x2.float() @ Wq.float().t()) if X.device.type == "cpu" else (x2 @ Wq.t())
-    k = (x2.float() @ Wk.float().t()) if X.device.type == "cpu" else (x2 @ Wk.t())
-    return q.to(X.dtype).reshape(B, S, H, -1), k.to(X.dtype).reshape(B, S, H, -1)
+    q = mc.matmul(x2, Wq.contiguous())
+    k = mc.matmul(x2, Wk.contiguous())
+    return q.reshape(B, S, H, -1), k.reshape(B, S, H, -1)
 
 
-def _rms(x, eps=1e-6):
-    x = x.float()
-    return x * torch.rsqrt(x.pow(2).mean(-1, keepdim=True) + eps)
-
-
-def _rope(x, theta=10000.0):
-    """Interleaved-pair rotary embedding along axis 1 (positions 0..S-1)."""
-    S, d = x.shape[1], x.shape[-1]
-    inv = theta ** (-torch.arange(0, d, 2, dtype=torch.float64, device=x.device) / d)
-    ang = torch.arange(S, dtype=torch.float64, device=x.device)[:, None] * inv[None, :]
-    shape = [1, S] + [1] * (x.dim() - 3) + [d // 2]
-    cos, sin = ang.cos().float().reshape(shape), ang.sin().float().reshape(shape)
-    x = x.float()
-    x0, x1 = x[..., 0::2], x[..., 1::2]
-    out = torch.empty_like(x)
-    out[..., 0::2] = x0 * cos - x1 * sin
-    out[..., 1::2] = x0 * sin + x1 * cos
-    return out
-
-
-def project_mla(X, W, H: int, d_nope=128, d_rope=64, d_v=128, chunk=4096, with_v=False):
-    """MLA features: Q [B,S,H,d_nope+d_rope] = [q^C || q^R], K^C a [B,S,H,d_nope]
-    strided view into the [B,S,H,d_nope+d_v] key/value projection, and the
-    shared rotary key K^R [B,S,d_rope]; with_v adds the values V, the other
-    strided view [B,S,H,d_v] of that projection."""
+def project_mla(X, W, H: int, d_nope=128, d_rope=64, d_v=128, with_v=False):
+    """MLA features: Q [B,S,H,d_nope+d_rope] = [q^C || RoPE(q^R)], K^C a
+    [B,S,H,d_nope] strided view into the [B,S,H,d_nope+d_v] key/value
+    projection, and the shared rotary key K^R = RoPE(X W_KR^T) [B,S,d_rope];
+    with_v adds the values V, the other strided view [B,S,H,d_v] of that
+    projection.  The latents c_Q = RMSNorm(X W_DQ^T) and c_KV =
+    RMSNorm(X W_DKV^T) are rounded to X's dtype before their up-projections."""
+    _on_device(X, *W.values())
     B, S, D = X.shape
-    dt = X.dtype
-    mm = (lambda a, w: a.float() @ w.float().t()) if X.device.type == "cpu" else (lambda a, w: a @ w.t())
     x2 = X.reshape(B * S, D)
-    cq = _rms(mm(x2, W["W_DQ"])).to(dt)
-    q = mm(cq, W["W_UQ"]).float().reshape(B, S, H, d_nope + d_rope)
-    q[..., d_nope:] = _rope(q[..., d_nope:])
-    ckv = _rms(mm(x2, W["W_DKV"])).to(dt)
-    kv = mm(ckv, W["W_UKV"]).to(dt).reshape(B, S, H, d_nope + d_v)
-    kr = _rope(mm(x2, W["W_KR"]).float().reshape(B, S, d_rope)).to(dt)
+    cq = mc.rms_norm(mc.matmul(x2, W["W_DQ"].contiguous()))
+    q = mc.matmul(cq, W["W_UQ"].contiguous()).reshape(B, S, H, d_nope + d_rope)
+    mc.rope_(q[..., d_nope:])
+    ckv = mc.rms_norm(mc.matmul(x2, W["W_DKV"].contiguous()))
+    kv = mc.matmul(ckv, W["W_UKV"].contiguous()).reshape(B, S, H, d_nope + d_v)
+    kr = mc.matmul(x2, W["W_KR"].contiguous()).reshape(B, S, d_rope)
+    mc.rope_(kr)
     if with_v:
-        return q.to(dt), kv[..., :d_nope], kr, kv[..., d_nope:]
-    return q.to(dt), kv[..., :d_nope], kr
+        return q, kv[..., :d_nope], kr, kv[..., d_nope:]
+    return q, kv[..., :d_nope], kr

@@ -270,3 +270,49 @@ def test_bounded_wait_selftest_rejects(lib, budget, abort_after, status, needle)
     st = None if status is None else ctypes.c_void_p(status)
     assert lib.mc_selftest_bounded_wait(budget, abort_after, st, None, None) == abi.MC_ERR_INVALID_ARG
     assert needle in lib.mc_last_error().decode()
+
+
+# setup calls (Q/K projection): every rejection happens on the host, before a launch
+P = ctypes.c_void_p(FAKE)
+
+
+@pytest.mark.parametrize("args,needle", [
+    ((P, 64, P, 64, P, 64, 4, 4, 64, 7, P, None, None), "dtype"),
+    ((P, 64, P, 64, P, 64, 4, 4, 0, abi.MC_BF16, P, None, None), "K 0"),
+    ((P, 32, P, 64, P, 64, 4, 4, 64, abi.MC_BF16, P, None, None), "pitch"),
+    ((P, 68, P, 64, P, 64, 4, 4, 64, abi.MC_BF16, P, None, None), "16-byte"),
+    ((ctypes.c_void_p(FAKE + 2), 64, P, 64, P, 64, 4, 4, 64, abi.MC_BF16, P, None, None), "16-byte"),
+    ((P, 64, P, 64, P, 64, 4, 4, 64, abi.MC_BF16, None, None, None), "scratch"),
+    ((None, 64, P, 64, P, 64, 4, 4, 64, abi.MC_F32, None, None, None), "null operand"),
+])
+def test_matmul_rejects(lib, args, needle):
+    assert lib.mc_matmul(*args) == abi.MC_ERR_INVALID_ARG
+    assert needle in lib.mc_last_error().decode()
+
+
+def test_matmul_empty_is_a_no_op(lib):
+    assert lib.mc_matmul(None, 64, None, 64, None, 64, 0, 4, 64, abi.MC_BF16, None, None, None) == abi.MC_OK
+
+
+@pytest.mark.parametrize("args,needle", [
+    ((P, 64, P, 64, 4, 64, 5, 1e-6, None), "dtype"),
+    ((P, 32, P, 64, 4, 64, abi.MC_BF16, 1e-6, None), "pitches"),
+    ((P, 64, P, 64, 4, 0, abi.MC_BF16, 1e-6, None), "cols 0"),
+    ((P, 64, P, 64, 4, 64, abi.MC_BF16, -1.0, None), "eps"),
+    ((None, 64, P, 64, 4, 64, abi.MC_BF16, 1e-6, None), "null"),
+])
+def test_rms_norm_rejects(lib, args, needle):
+    assert lib.mc_rms_norm(*args) == abi.MC_ERR_INVALID_ARG
+    assert needle in lib.mc_last_error().decode()
+
+
+@pytest.mark.parametrize("args,needle", [
+    ((P, 1, 8, 2, 63, 1024, 128, 64, abi.MC_BF16, 1e4, None), "d 63"),
+    ((P, 1, 8, 0, 64, 1024, 128, 64, abi.MC_BF16, 1e4, None), "heads 0"),
+    ((P, 1, 8, 2, 64, 1024, 128, 64, abi.MC_BF16, 0.0, None), "theta"),
+    ((P, 1, 8, 2, 64, 1024, 128, 64, 9, 1e4, None), "dtype"),
+    ((None, 1, 8, 2, 64, 1024, 128, 64, abi.MC_BF16, 1e4, None), "null"),
+])
+def test_rope_rejects(lib, args, needle):
+    assert lib.mc_rope(*args) == abi.MC_ERR_INVALID_ARG
+    assert needle in lib.mc_last_error().decode()

@@ -291,7 +291,7 @@ def test_max_logit_parity(case, with_argmax):
 def test_max_logit_strided_mla_views():
     """K^C as a strided view into the [k^C || v] projection, shared K^R."""
     wl = synth.scaled(synth.workload("k2_mla_layer"), S=80)
-    X, W = synth.attention_inputs(wl, seed=2)
+    X, W = synth.attention_inputs(wl, seed=2, device="cuda")
     q, kc, kr = forward.project_mla(X, W, wl.attention.H)
     q, kc = q[:, :, :6], kc[:, :, :6]
     # device K^C keeps the projection's layout: a view with head stride 256
@@ -524,7 +524,7 @@ def test_tiny_mha_fp32_full_step():
     wl = synth.workload("tiny_mha_fp32")
     X, Wa = synth.attention_inputs(wl)
     Wm, Gm, Mm = synth.muon_inputs(wl)
-    q, k = forward.project_mha(X, Wa["Wq"], Wa["Wk"], wl.attention.H)
+    q, k = forward.project_mha(X.cuda(), Wa["Wq"].cuda(), Wa["Wk"].cuda(), wl.attention.H)
     hp = mc.Hparams()
     smax, _ = mc.qk_max_logit(q.cuda(), k.cuda())
     ref_s, _ = O.max_logit(f64(q), f64(k))
@@ -542,8 +542,9 @@ def test_tiny_mha_fp32_full_step():
     assert_rounded_within(Wq, out["Wq"], 1e-6 * np.abs(out["Wq"]), "Wq")
     assert_rounded_within(Wk, out["Wk"], 1e-6 * np.abs(out["Wk"]), "Wk")
     # re-measured max logit after the clip is min(S, tau)
-    q2, k2 = forward.project_mha(X, Wq.cpu(), Wk.cpu(), 4)
-    s2, _ = mc.qk_max_logit(q2.cuda(), k2.cuda())
+    # on the library: the projection with the clipped weights, then S_max
+    q2, k2 = forward.project_mha(X.cuda(), Wq, Wk, 4)
+    s2, _ = mc.qk_max_logit(q2, k2)
     torch.cuda.synchronize()
     np.testing.assert_allclose(f64(s2), np.minimum(ref_s, 100.0), rtol=1e-5)
 
@@ -555,7 +556,7 @@ def test_tiny_mha_step_tau30():
     wl = synth.scaled(synth.workload("tiny_mha_fp32", "literal"), scaled_heads={1: 12.0, 3: 12.0})
     X, Wa = synth.attention_inputs(wl, seed=5)
     Wm, Gm, Mm = synth.muon_inputs(wl, seed=5)
-    q, k = forward.project_mha(X, Wa["Wq"], Wa["Wk"], wl.attention.H)
+    q, k = forward.project_mha(X.cuda(), Wa["Wq"].cuda(), Wa["Wk"].cuda(), wl.attention.H)
     hp = mc.Hparams(tau=30.0)
     smax, _ = mc.qk_max_logit(q.cuda(), k.cuda())
     ref_s, _ = O.max_logit(f64(q), f64(k))
@@ -575,8 +576,8 @@ def test_tiny_mha_step_tau30():
                              O.mha_segments(4, 64), ref_s, 30.0)
     assert_rounded_within(Wq, out["Wq"], 1e-6 * np.abs(out["Wq"]), "Wq")
     assert_rounded_within(Wk, out["Wk"], 1e-6 * np.abs(out["Wk"]), "Wk")
-    q2, k2 = forward.project_mha(X, Wq.cpu(), Wk.cpu(), 4)
-    s2, _ = mc.qk_max_logit(q2.cuda(), k2.cuda())
+    q2, k2 = forward.project_mha(X.cuda(), Wq, Wk, 4)
+    s2, _ = mc.qk_max_logit(q2, k2)
     torch.cuda.synchronize()
     np.testing.assert_allclose(f64(s2), np.minimum(ref_s, 30.0), rtol=1e-5)
 
@@ -588,7 +589,7 @@ def test_dense_block_step_reduced_tokens():
     wl = synth.scaled(synth.workload("dense_block"), B=1, S=512)
     W, G, M = synth.muon_inputs(wl, seed=12, only=("Wq", "Wk", "W_down"))
     X, _ = synth.attention_inputs(wl, seed=12)
-    q, k = forward.project_mha(X, W["Wq"], W["Wk"], 16)
+    q, k = forward.project_mha(X.cuda(), W["Wq"].cuda(), W["Wk"].cuda(), 16)
     hp = mc.Hparams()
     names = ["Wq", "Wk", "W_down"]
     Wd = [W[n].cuda() for n in names]
