@@ -315,6 +315,37 @@ def test_max_logit_accumulate_over_microbatches():
     assert torch.equal(full, part)
 
 
+def test_max_logit_negative_and_mixed_sign_accumulate():
+    """S_max is max-combined in place as a float: a micro-batch whose logits
+    are all negative (every q feature positive, every k feature negative),
+    then one whose heads 0 and 1 turn positive while heads 2 and 3 stay
+    negative.  Each result equals the oracle's maximum over the batches seen,
+    on the tensor-core path and through the attention forward."""
+    B, S, H, d = 2, 160, 4, 64
+    qa, ka, _ = synth.attention_features(B, S, H, d, d, 0, BF16, seed=23)
+    qb, kb, _ = synth.attention_features(B, S, H, d, d, 0, BF16, seed=24)
+    qa, ka = qa.abs(), -ka.abs()
+    qb, kb = qb.abs(), kb.abs()
+    kb[:, :, 2:] = -kb[:, :, 2:]
+    ra, _ = O.max_logit(f64(qa), f64(ka))
+    rb, _ = O.max_logit(f64(qb), f64(kb))
+    assert np.all(ra < 0) and np.all(rb[:2] > 0) and np.all(rb[2:] < 0)
+    v = torch.zeros(B, S, H, d, dtype=BF16, device="cuda")
+    for run in ("max_logit", "attention"):
+        if run == "max_logit":
+            s, _ = mc.qk_max_logit(qa.cuda(), ka.cuda())
+        else:
+            _, _, s = mc.qk_attention_forward(qa.cuda(), ka.cuda(), v)
+        torch.cuda.synchronize()
+        np.testing.assert_allclose(f64(s), ra, rtol=1e-3)
+        if run == "max_logit":
+            mc.qk_max_logit(qb.cuda(), kb.cuda(), smax=s, accumulate=True)
+        else:
+            mc.qk_attention_forward(qb.cuda(), kb.cuda(), v, smax=s, accumulate=True)
+        torch.cuda.synchronize()
+        np.testing.assert_allclose(f64(s), np.maximum(ra, rb), rtol=1e-3)
+
+
 def test_max_logit_flags_nonfinite():
     q, k, _ = synth.attention_features(1, 32, 2, 64, 64, 0, BF16, seed=7)
     q[0, 5, 1, 3] = float("inf")
