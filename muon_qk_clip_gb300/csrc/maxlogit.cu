@@ -575,7 +575,9 @@ cudaError_t launch_ml_tc(const MaxLogitParams& p, cudaStream_t s, char* err, siz
     if (!encode(&mp.ks, p.ks, 3, dims, st, box)) { snprintf(err, errlen, "tensor map for k_shared failed"); return cudaErrorInvalidValue; }
   }
   const size_t smem = 1024 + 2 * g.nch * Q_CHUNK + g.stages * K_CHUNK + 512;
-  const int grid = (int)(g.units < (uint32_t)sm_count() ? g.units : (uint32_t)sm_count());
+  // one CTA per work unit (a single item in snake order), at most one per SM
+  const uint32_t work = g.snake ? g.items : g.units;
+  const int grid = (int)(work < (uint32_t)sm_count() ? work : (uint32_t)sm_count());
   cudaError_t e;
   if (p.argmax) {
     e = cudaFuncSetAttribute(ml_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
