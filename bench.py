@@ -239,7 +239,9 @@ def ns_products(rows, cols, steps, fast_steps, split=True):
     (up to three, keeping two three-term iterations after them, from a
     smaller side of 256; four with fast_steps >= 4 from 1024, keeping one),
     then one in the Gram and three (hi*hi + hi*lo + lo*hi) in the polynomial
-    and update; matrices with a smaller side under 256 take three everywhere."""
+    and update; matrices with a smaller side under 256 take three everywhere.
+    With two or more three-term iterations, the last update takes two
+    (hi*hi + hi*lo of X) from a smaller side of 512 (iteration 2 onwards)."""
     if not split:
         return [(1, 1, 1)] * steps
     side = min(rows, cols)
@@ -250,7 +252,10 @@ def ns_products(rows, cols, steps, fast_steps, split=True):
     else:
         nf = min(fast_steps, 3, max(0, steps - 2))
     trail = (1, 3, 3) if side >= 256 else (3, 3, 3)
-    return [(1, 1, 1) if it < nf else trail for it in range(steps)]
+    out = [(1, 1, 1) if it < nf else trail for it in range(steps)]
+    if steps >= 2 and nf <= steps - 2 and side >= 512:
+        out[-1] = (out[-1][0], out[-1][1], 2)
+    return out
 
 
 def ns_flops_executed(rows, cols, steps, fast_steps, split=True, symmetric=True):
@@ -753,7 +758,8 @@ def ns_precision_text(hp):
     return (f"16-bit (hi, lo) planes, fp32 accumulate: iteration 1 on bf16 planes, later ones on "
             f"fp16; one product (hi*hi) per k-step in the first {hp.ns_fast_steps} iterations "
             f"(smaller side >= 256) and in the Gram products after them, three "
-            f"(hi*hi+hi*lo+lo*hi) in the later polynomials and updates")
+            f"(hi*hi+hi*lo+lo*hi) in the later polynomials and updates, two (hi*hi+hi*lo of X) "
+            f"in the last update (smaller side >= 512)")
 
 
 def main():

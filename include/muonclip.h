@@ -67,8 +67,9 @@ typedef enum { MC_F32 = 0, MC_BF16 = 1 } mc_dtype;
  *     update normalises by 1/||M|| and every later iterate, Gram and
  *     polynomial matrix is stored as an fp16 (hi, lo) pair (~22 significand
  *     bits; entries stay bounded after the normalisation).  A product takes
- *     one term (hi*hi) or three (hi*hi + hi*lo + lo*hi) per k-step, as
- *     ns_fast_steps below says.  Default for bf16 weights.
+ *     one term (hi*hi), two (hi*hi + hi*lo of X: the last update) or three
+ *     (hi*hi + hi*lo + lo*hi) per k-step, as ns_fast_steps below says.
+ *     Default for bf16 weights.
  *   MC_NS_BF16: tcgen05, one bf16 product, bf16 iterates (fastest, ~1e-1
  *     max-abs / 1e-2 RMS deviation from exact arithmetic).
  *   MC_NS_FP32: CUDA-core fp32 products and fp32 iterates.  Default for fp32
@@ -116,11 +117,13 @@ typedef struct {
                           whose smaller side is at least 256: up to three,
                           each run keeping at least two iterations after it,
                           whose Gram products take one product and whose
-                          polynomial and update take three.  Float64
-                          emulation of this arithmetic gives at most 8.2e-3
-                          of RMS (512 x 16384 Gaussian; 2048 x 7168: 3.9e-3;
-                          adversarial spectra, a few dominant directions over
-                          a 1e-3 rest: at most 6.6e-3).  A value >= 4 allows
+                          polynomial and update take three, except the last
+                          update, which takes two (hi*hi + hi*lo of X) when
+                          the smaller side is at least 512.  Float64
+                          emulation of this arithmetic gives at most 9.3e-3
+                          of RMS (2048 x 7168 adversarial spectrum, a few
+                          dominant directions over a 1e-3 rest; 2048 x 7168
+                          Gaussian: 4.2e-3; 512 x 16384 Gaussian: 8.9e-3).  A value >= 4 allows
                           four (keeping one) for matrices whose smaller side
                           is at least 1024: fewer products, at most 1.0e-2 of
                           RMS (1024 x 1536 Gaussian).  Matrices whose smaller
@@ -197,7 +200,7 @@ mc_status mc_workspace_size(const mc_mat* M, int32_t count, const mc_hparams* hp
  * step; the arithmetic of the split iterate is this library's): for iteration
  * i (0 .. ns_steps - 1), products[3 i + 0], [3 i + 1] and [3 i + 2] are those
  * of the Gram product A = X X^T, the polynomial B = b A + c A^2 and the update,
- * each 1 (hi*hi) or 3 (hi*hi + hi*lo + lo*hi).  products: host int32 array of
+ * each 1 (hi*hi), 2 (hi*hi + hi*lo of X) or 3 (hi*hi + hi*lo + lo*hi).  products: host int32 array of
  * 3 * ns_steps entries, owned by the caller.  Host-only; no GPU work.
  * MC_ERR_INVALID_ARG for a null array, a shape outside 1 .. 2^30 or invalid
  * hyper-parameters. */

@@ -306,9 +306,14 @@ enum Phase { kGram = 1, kPoly = 2, kNext = 3 };
 //     Gaussian; 2048 x 7168: 9.5e-3), 9.8e-3 at 256 and 3.7e-2 at 512 x 16384;
 // so the one-product iterations run from a smaller side of kFastMinSide
 // (three) and kFast4MinSide (four); smaller matrices take three products in
-// every phase (2.8e-3 at 64).
+// every phase (2.8e-3 at 64).  With three leading one-product iterations,
+// the last update may also drop lo(B') x hi(X), the product whose error no
+// later iteration amplifies: at most 9.3e-3 from a smaller side of 512
+// (2048 x 7168 adversarial; 2048 x 7168 Gaussian: 4.2e-3), 1.3e-2 at 256, so
+// it takes two products (hi*hi + hi*lo of X) from kLast2MinSide.
 constexpr int kFastMinSide = 256;
 constexpr int kFast4MinSide = 1024;
+constexpr int kLast2MinSide = 512;
 
 // Leading one-product iterations of a shape group whose smaller side is
 // `side`: up to three with at least two three-term iterations after them,
@@ -320,11 +325,16 @@ int ns_fast_iterations(const mc_hparams* hp, int side) {
   return std::min({hp->ns_fast_steps, 3, std::max(0, hp->ns_steps - 2)});
 }
 
-// Products per k-step (1: hi*hi; 3: hi*hi + hi*lo + lo*hi) of phase `ph` of
-// iteration `it` on the split iterate.
+// Products per k-step (1: hi*hi; 2: hi*hi + hi*lo_B; 3: hi*hi + hi*lo +
+// lo*hi) of phase `ph` of iteration `it` on the split iterate.  Two only in
+// the last update of a plan with at least two three-term iterations, on fp16
+// planes (it >= 1).
 int ns_terms(const mc_hparams* hp, int side, int it, int ph) {
-  if (it < ns_fast_iterations(hp, side)) return 1;
+  const int nf = ns_fast_iterations(hp, side);
+  if (it < nf) return 1;
   if (ph == kGram && side >= kFastMinSide) return 1;
+  if (ph == kNext && it == hp->ns_steps - 1 && it >= 1 && side >= kLast2MinSide && nf <= hp->ns_steps - 2)
+    return 2;
   return 3;
 }
 
@@ -353,7 +363,7 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
     return ns_terms(hp, std::min(P.groups[g].m, P.groups[g].n), it, ph);
   };
   const bool sym_out = P.xmode != kXF32 && (ph == kGram || ph == kPoly);
-  for (int terms : {1, 3}) {
+  for (int terms : {1, 2, 3}) {
     std::vector<int> sub;                    // the groups of this launch kind
     for (int g : order)
       if (terms_of(g) == terms) sub.push_back(g);
@@ -427,10 +437,10 @@ mc_status run_phase(const Plan& P, void* ws, Phase ph, int it, const mc_hparams*
       // plane (its a X term comes from X), so that lo plane is not stored
       gp.d_hi_only = P.xmode == kXSplit && ph == kPoly && terms == 1;
       // Three-term iterations fold a X into the polynomial: B' = c A^2 + b A + a I
-      // and X' = B' X, so the last phase reads no C.  (B' holds ~16 significand
-      // bits there; a one-plane bf16 B' would lose the small singular values, so
-      // the other iterations keep X' = B X + a X.)
-      const bool fold = P.xmode == kXSplit && gp.terms == 3;
+      // and X' = B' X (two or three products), so the last phase reads no C.
+      // (B' holds ~16 significand bits there; a one-plane B' would lose the
+      // small singular values, so the other iterations keep X' = B X + a X.)
+      const bool fold = P.xmode == kXSplit && gp.terms >= 2;
       switch (ph) {
         case kGram:
           gp.alpha = 1.f; gp.beta = 0.f;
@@ -555,13 +565,14 @@ float update_factor(const mc_hparams* hp, int rows, int cols) {
 }
 
 // The last update can apply the step when the iterate is split, every W is
-// bf16, the table holds every matrix and that update takes three products.
+// bf16, the table holds every matrix and that update takes two or three
+// products.
 bool can_fuse_apply(const Plan& P, const mc_mat* W, const mc_hparams* hp) {
   if (P.xmode != kXSplit || hp->ns_steps < 1 || P.count > kMaxFusedApply) return false;
   for (int j = 0; j < P.count; ++j)
     if (W[j].dtype != MC_BF16) return false;
   for (const Group& g : P.groups)
-    if (ns_terms(hp, std::min(g.m, g.n), hp->ns_steps - 1, kNext) != 3) return false;
+    if (ns_terms(hp, std::min(g.m, g.n), hp->ns_steps - 1, kNext) < 2) return false;
   return true;
 }
 

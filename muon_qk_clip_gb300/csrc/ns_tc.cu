@@ -9,10 +9,11 @@
 // All three are D = s_b * (alpha * P + beta * C + diag * I) with
 // P = A_op x B_op^T.  In three-term iterations phase 2 adds a I and phase 3
 // reads no C (X' = s * (B + a I) X).
-// Split mode (default): every operand is a bf16 pair (hi, lo) and
+// Split mode (default): every operand is a 16-bit pair (hi, lo) and
 // P = hi*hi + hi*lo + lo*hi accumulated in fp32 in TMEM, so products carry
-// ~16 significand bits; D is stored again as a (hi, lo) pair.  Plain mode:
-// one bf16 plane, one MMA per k-step.
+// ~16 significand bits (one-product launches take hi*hi alone, the last
+// update of a step may take hi*hi + hi*lo_B); D is stored again as a
+// (hi, lo) pair.  Plain mode: one bf16 plane, one MMA per k-step.
 //
 // Kernel layout (one CTA per SM, persistent over output tiles, CTAs paired
 // into tcgen05 .cta_group::2 clusters of two):
@@ -68,14 +69,18 @@ struct KLayout {
   static constexpr uint32_t kSbo = 8 * kBX * 2;
 };
 
-// TERMS: tensor-core products per k-step (1: hi*hi; 3: hi*hi + hi*lo + lo*hi).
+// TERMS: tensor-core products per k-step (1: hi*hi; 2: hi*hi + hi*lo_B;
+// 3: hi*hi + hi*lo + lo*hi).
 // LO: the iterate is stored as (hi, lo) planes (the epilogue reads and writes
 // both), independently of how many products the k-loop takes.
 template <int TERMS, int AROWS, int BROWS, int BK = BKT>
 struct Stages {
   static constexpr int kABytes = AROWS * BK * 2;
   static constexpr int kBBytes = BROWS * BK * 2;
-  static constexpr int kStageBytes = TERMS == 3 ? 2 * (kABytes + kBBytes) : (kABytes + kBBytes);
+  // three products stage both planes of A and B; two (hi*hi + hi*lo_B)
+  // both planes of B; one the hi planes only
+  static constexpr int kStageBytes =
+      TERMS == 3 ? 2 * (kABytes + kBBytes) : (TERMS == 2 ? kABytes + 2 * kBBytes : kABytes + kBBytes);
   static constexpr int kAvail = kSmemCap - kEpiBytes - 1024 - kBarBytes - 64;
   static constexpr int kStages = kAvail / kStageBytes > 8 ? 8 : kAvail / kStageBytes;
   static constexpr int kSmem = kStages * kStageBytes + kEpiBytes + 1024 + kBarBytes;
@@ -572,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Stages<TERMS, BM, 128, BK>;
   using KL = KLayout<BK>;
   constexpr bool SPLIT = TERMS == 3;     // the A operand's lo plane is staged
-  constexpr bool BLO = TERMS == 3;       // the B operand's lo plane is staged
+  constexpr bool BLO = TERMS >= 2;       // the B operand's lo plane is staged
   constexpr bool IN16 = FMT == kFmtF16;  // fp16 operands (else bf16)
   constexpr bool OUT16 = FMT != kFmtBf16;
   constexpr int TM_ROWS = 2 * BM;
@@ -947,7 +952,7 @@ template <int TERMS, bool LO, int BK, int FMT, class AP = NoApply>
 cudaError_t launch_pairs(const GemmParams& p, const AP& ap, cudaStream_t s, char* err, size_t errlen) {
   TmaArgs tm;
   // each CTA's B box is its 128-row half of the pair's 256 B rows
-  if (!encode_all(p, tm, TERMS == 3, TERMS == 3, LO, FMT == kFmtF16, FMT != kFmtBf16, BM, 128, BK,
+  if (!encode_all(p, tm, TERMS == 3, TERMS >= 2, LO, FMT == kFmtF16, FMT != kFmtBf16, BM, 128, BK,
                   KLayout<BK>::kBX, err, errlen))
     return cudaErrorInvalidValue;
   auto k = ns_gemm_tc_kernel<TERMS, LO, BK, FMT, AP>;
@@ -980,17 +985,27 @@ cudaError_t launch_pairs(const GemmParams& p, const AP& ap, cudaStream_t s, char
 
 // One layout: CTA pairs.  Operand rows are 128-byte swizzled boxes of 64
 // K-elements; three-product launches take 64-deep k-steps (three 64 KB stages,
-// twelve MMAs per stage), one-product launches 128-deep ones (two boxes per
-// operand per stage, eight MMAs, three 64 KB stages): the single issuing
-// thread's per-stage cost is then spread over more MMAs (measured: 32-deep
-// one-product stages took 48 % longer than 64-deep, 128-deep ones 4-9 % less;
-// 64-deep three-product stages 5-9 % less than 32-deep).
+// twelve MMAs per stage), two-product ones 64-deep k-steps too (A's hi plane
+// and both planes of B: four 48 KB stages, eight MMAs per stage), one-product
+// launches 128-deep ones (two boxes per operand per stage, eight MMAs, three
+// 64 KB stages): the single issuing thread's per-stage cost is then spread
+// over more MMAs (measured: 32-deep one-product stages took 48 % longer than
+// 64-deep, 128-deep ones 4-9 % less; 64-deep three-product stages 5-9 % less
+// than 32-deep).  Two products run only on fp16 planes (a last update).
 template <int FMT>
 cudaError_t launch_fmt(const GemmParams& p, const FusedApply* fa, cudaStream_t s, char* err, size_t errlen) {
   if (p.terms == 3) {
     if constexpr (FMT != kFmtBf16)
       if (fa) return launch_pairs<3, true, 64, FMT, FusedApply>(p, *fa, s, err, errlen);
     return launch_pairs<3, true, 64, FMT>(p, NoApply{}, s, err, errlen);
+  }
+  if (p.terms == 2) {
+    if constexpr (FMT == kFmtF16) {
+      if (fa) return launch_pairs<2, true, 64, FMT, FusedApply>(p, *fa, s, err, errlen);
+      return launch_pairs<2, true, 64, FMT>(p, NoApply{}, s, err, errlen);
+    }
+    snprintf(err, errlen, "two products per k-step run on fp16 planes only");
+    return cudaErrorInvalidValue;
   }
   return launch_pairs<1, true, 128, FMT>(p, NoApply{}, s, err, errlen);
 }
@@ -1000,8 +1015,8 @@ cudaError_t launch_fmt(const GemmParams& p, const FusedApply* fa, cudaStream_t s
 cudaError_t launch_ns_gemm_tc(const GemmParams& p, const FusedApply* fa, cudaStream_t s, char* err,
                               size_t errlen) {
   if (p.total_tiles <= 0) return cudaSuccess;
-  if (fa && (p.xmode != kXSplit || p.terms != 3 || p.fmt == kFmtBf16 || p.beta != 0.f || p.g[0].symmetric)) {
-    snprintf(err, errlen, "the fused apply runs in a three-product, fp16-output update launch");
+  if (fa && (p.xmode != kXSplit || p.terms < 2 || p.fmt == kFmtBf16 || p.beta != 0.f || p.g[0].symmetric)) {
+    snprintf(err, errlen, "the fused apply runs in a two- or three-product, fp16-output update launch");
     return cudaErrorInvalidValue;
   }
   if (!p.sched) {
