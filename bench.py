@@ -240,8 +240,9 @@ def ns_products(rows, cols, steps, fast_steps, split=True):
     smaller side of 256; four with fast_steps >= 4 from 1024, keeping one),
     then one in the Gram and three (hi*hi + hi*lo + lo*hi) in the polynomial
     and update; matrices with a smaller side under 256 take three everywhere.
-    With two or more three-term iterations, the last update takes two
-    (hi*hi + hi*lo of X) from a smaller side of 512 (iteration 2 onwards)."""
+    With two or more three-term iterations, the updates of the last two
+    iterations take two (hi*hi + hi*lo of X) from a smaller side of 512
+    (iteration 2 onwards)."""
     if not split:
         return [(1, 1, 1)] * steps
     side = min(rows, cols)
@@ -254,7 +255,8 @@ def ns_products(rows, cols, steps, fast_steps, split=True):
     trail = (1, 3, 3) if side >= 256 else (3, 3, 3)
     out = [(1, 1, 1) if it < nf else trail for it in range(steps)]
     if steps >= 2 and nf <= steps - 2 and side >= 512:
-        out[-1] = (out[-1][0], out[-1][1], 2)
+        for it in range(max(1, steps - 2), steps):
+            out[it] = (out[it][0], out[it][1], 2)
     return out
 
 
@@ -758,8 +760,8 @@ def ns_precision_text(hp):
     return (f"16-bit (hi, lo) planes, fp32 accumulate: iteration 1 on bf16 planes, later ones on "
             f"fp16; one product (hi*hi) per k-step in the first {hp.ns_fast_steps} iterations "
             f"(smaller side >= 256) and in the Gram products after them, three "
-            f"(hi*hi+hi*lo+lo*hi) in the later polynomials and updates, two (hi*hi+hi*lo of X) "
-            f"in the last update (smaller side >= 512)")
+            f"(hi*hi+hi*lo+lo*hi) in the later polynomials, two (hi*hi+hi*lo of X) in the later "
+            f"updates (smaller side >= 512; else three)")
 
 
 def main():

@@ -67,8 +67,8 @@ typedef enum { MC_F32 = 0, MC_BF16 = 1 } mc_dtype;
  *     update normalises by 1/||M|| and every later iterate, Gram and
  *     polynomial matrix is stored as an fp16 (hi, lo) pair (~22 significand
  *     bits; entries stay bounded after the normalisation).  A product takes
- *     one term (hi*hi), two (hi*hi + hi*lo of X: the last update) or three
- *     (hi*hi + hi*lo + lo*hi) per k-step, as ns_fast_steps below says.
+ *     one term (hi*hi), two (hi*hi + hi*lo of X: the trailing updates) or
+ *     three (hi*hi + hi*lo + lo*hi) per k-step, as ns_fast_steps below says.
  *     Default for bf16 weights.
  *   MC_NS_BF16: tcgen05, one bf16 product, bf16 iterates (fastest, ~1e-1
  *     max-abs / 1e-2 RMS deviation from exact arithmetic).
@@ -117,13 +117,13 @@ typedef struct {
                           whose smaller side is at least 256: up to three,
                           each run keeping at least two iterations after it,
                           whose Gram products take one product and whose
-                          polynomial and update take three, except the last
-                          update, which takes two (hi*hi + hi*lo of X) when
-                          the smaller side is at least 512.  Float64
-                          emulation of this arithmetic gives at most 9.3e-3
-                          of RMS (2048 x 7168 adversarial spectrum, a few
-                          dominant directions over a 1e-3 rest; 2048 x 7168
-                          Gaussian: 4.2e-3; 512 x 16384 Gaussian: 8.9e-3).  A value >= 4 allows
+                          polynomial takes three and whose update two
+                          (hi*hi + hi*lo of X; three when the smaller side
+                          is under 512).  Float64 emulation of this
+                          arithmetic gives at most 1.05e-2 of RMS (512 x 2048
+                          adversarial spectrum, a few dominant directions
+                          over a 1e-3 rest; 2048 x 7168 Gaussian: 5.2e-3;
+                          512 x 16384 Gaussian: 9.3e-3).  A value >= 4 allows
                           four (keeping one) for matrices whose smaller side
                           is at least 1024: fewer products, at most 1.0e-2 of
                           RMS (1024 x 1536 Gaussian).  Matrices whose smaller

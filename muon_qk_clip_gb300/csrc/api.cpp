@@ -306,14 +306,14 @@ enum Phase { kGram = 1, kPoly = 2, kNext = 3 };
 //     Gaussian; 2048 x 7168: 9.5e-3), 9.8e-3 at 256 and 3.7e-2 at 512 x 16384;
 // so the one-product iterations run from a smaller side of kFastMinSide
 // (three) and kFast4MinSide (four); smaller matrices take three products in
-// every phase (2.8e-3 at 64).  With three leading one-product iterations,
-// the last update may also drop lo(B') x hi(X), the product whose error no
-// later iteration amplifies: at most 9.3e-3 from a smaller side of 512
-// (2048 x 7168 adversarial; 2048 x 7168 Gaussian: 4.2e-3), 1.3e-2 at 256, so
-// it takes two products (hi*hi + hi*lo of X) from kLast2MinSide.
+// every phase (2.8e-3 at 64).  With two trailing three-term iterations
+// their updates may also drop lo(B') x hi(X), B' = a I + b A + c A^2: at most
+// 1.05e-2 from a smaller side of 512 (512 x 2048 adversarial; 2048 x 7168
+// Gaussian: 5.2e-3), 1.3e-2 at 256, so they take two products (hi*hi + hi*lo
+// of X) from kTrail2MinSide.  Dropping hi(B') x lo(X) instead gives ~2e-2.
 constexpr int kFastMinSide = 256;
 constexpr int kFast4MinSide = 1024;
-constexpr int kLast2MinSide = 512;
+constexpr int kTrail2MinSide = 512;
 
 // Leading one-product iterations of a shape group whose smaller side is
 // `side`: up to three with at least two three-term iterations after them,
@@ -326,14 +326,14 @@ int ns_fast_iterations(const mc_hparams* hp, int side) {
 }
 
 // Products per k-step (1: hi*hi; 2: hi*hi + hi*lo_B; 3: hi*hi + hi*lo +
-// lo*hi) of phase `ph` of iteration `it` on the split iterate.  Two only in
-// the last update of a plan with at least two three-term iterations, on fp16
-// planes (it >= 1).
+// lo*hi) of phase `ph` of iteration `it` on the split iterate.  Two in the
+// updates of the last two iterations of a plan that keeps them three-term,
+// on fp16 planes (it >= 1).
 int ns_terms(const mc_hparams* hp, int side, int it, int ph) {
   const int nf = ns_fast_iterations(hp, side);
   if (it < nf) return 1;
   if (ph == kGram && side >= kFastMinSide) return 1;
-  if (ph == kNext && it == hp->ns_steps - 1 && it >= 1 && side >= kLast2MinSide && nf <= hp->ns_steps - 2)
+  if (ph == kNext && it >= 1 && it >= hp->ns_steps - 2 && side >= kTrail2MinSide && nf <= hp->ns_steps - 2)
     return 2;
   return 3;
 }

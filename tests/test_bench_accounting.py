@@ -47,19 +47,21 @@ def test_counted_flops(bench):
 
 
 def test_products_per_iteration(bench):
-    # G2: the last update of a plan keeping two three-term iterations takes
-    # two products (hi*hi + hi*lo of X) from a smaller side of 512
+    # G2: the updates of the last two iterations of a plan keeping two
+    # three-term iterations take two products (hi*hi + hi*lo of X) from a
+    # smaller side of 512
     F, S, G1, G2 = (1, 1, 1), (3, 3, 3), (1, 3, 3), (1, 3, 2)
     assert bench.ns_products(128, 7168, 5, 3) == [S] * 5              # smaller side < 256
     assert bench.ns_products(256, 7168, 5, 3) == [F, F, F, G1, G1]    # < 512: three
-    assert bench.ns_products(1024, 1536, 5, 3) == [F, F, F, G1, G2]
+    assert bench.ns_products(1024, 1536, 5, 3) == [F, F, F, G2, G2]
     assert bench.ns_products(1024, 1536, 5, 4) == [F, F, F, F, G1]   # a fourth from 1024
-    assert bench.ns_products(512, 1536, 5, 4) == [F, F, F, G1, G2]   # not below it
-    assert bench.ns_products(2048, 5632, 5, 2) == [F, F, G1, G1, G2]
-    assert bench.ns_products(2048, 5632, 4, 3) == [F, F, G1, G2]     # two three-term kept
+    assert bench.ns_products(512, 1536, 5, 4) == [F, F, F, G2, G2]   # not below it
+    assert bench.ns_products(2048, 5632, 5, 2) == [F, F, G1, G2, G2]
+    assert bench.ns_products(2048, 5632, 4, 3) == [F, F, G2, G2]     # two three-term kept
     assert bench.ns_products(2048, 5632, 4, 4) == [F, F, F, G1]      # one kept
-    assert bench.ns_products(2048, 2048, 5, 0) == [G1] * 4 + [G2]
-    assert bench.ns_products(2048, 2048, 1, 0) == [G1]               # iteration 1: bf16 planes
+    assert bench.ns_products(2048, 2048, 5, 0) == [G1] * 3 + [G2] * 2
+    assert bench.ns_products(2048, 2048, 2, 0) == [G1, G2]            # iteration 1: bf16 planes
+    assert bench.ns_products(2048, 2048, 1, 0) == [G1]
     assert bench.ns_products(2048, 2048, 5, 3, split=False) == [F] * 5
 
 
@@ -67,9 +69,9 @@ def test_executed_flops_weight_each_phase_by_its_products(bench):
     m, n = 2048, 5632
     e = bench.ns_sym_entries(m)
     g, p, u = 2.0 * n * e, 2.0 * m * e, 2.0 * m * m * n
-    # iterations: one-product x 3, then one-product Gram + three-term rest,
-    # and last the same with a two-product update
-    want = 3 * (g + p + u) + (g + 3 * p + 3 * u) + (g + 3 * p + 2 * u)
+    # iterations: one-product x 3, then one-product Gram, three-product
+    # polynomial and two-product update x 2
+    want = 3 * (g + p + u) + 2 * (g + 3 * p + 2 * u)
     assert bench.ns_flops_executed(m, n, 5, 3) == want
     assert bench.ns_flops_executed(m, n, 5, 3, split=False) == bench.ns_flops_counted(m, n, 5)
 

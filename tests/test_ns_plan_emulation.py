@@ -1,0 +1,37 @@
+"""The product plan of the split Newton-Schulz, checked by float emulation on
+the CPU (tests/ns_emulation.py): the default plan stays inside the 2e-2 RMS
+bound with room, and the variants the plan avoids are measurably worse."""
+from tests import ns_emulation as E
+
+
+def test_default_plan_within_bound():
+    """Three one-product iterations, then two three-term ones whose updates
+    take two products (hi*hi + hi*lo of X): a Gaussian and two adversarial
+    matrices of smaller side 512 stay near half the 2e-2 bound, within 3x of
+    three products everywhere in the trailing iterations."""
+    for M in (E.gaussian(512, 2048, 1), E.adversarial(512, 2048, 16, 1e-3, 5),
+              E.adversarial(512, 2048, 64, 1e-3, 2)):
+        e2 = E.max_error(E.emulate(M.clone()), M)
+        e3 = E.max_error(E.emulate(M.clone(), last_update=3, trailing_updates=3), M)
+        assert e2 < 1.3e-2, e2
+        assert e2 < 3 * e3, (e2, e3)
+
+
+def test_the_dropped_product_is_the_cheaper_one():
+    """Of the two cross products, dropping lo(B') hi(X) keeps the error near
+    1e-2; dropping hi(B') lo(X) instead roughly doubles it (to the bound) on
+    adversarial spectra."""
+    for M in (E.adversarial(512, 2048, 16, 1e-3, 5), E.adversarial(512, 2048, 64, 1e-3, 2)):
+        e_lib = E.max_error(E.emulate(M.clone()), M)
+        e_other = E.max_error(E.emulate(M.clone(), last_update="2x", trailing_updates="2x"), M)
+        assert e_other > 1.6 * e_lib, (e_other, e_lib)
+
+
+def test_folding_a_i_into_one_product_iterations_fails():
+    """Folding a I into a one-plane polynomial rounds the identity and feeds
+    X's rounding into the small singular directions: an error of order the
+    RMS itself, against ~1e-2 for the default."""
+    M = E.adversarial(256, 1024, 16, 1e-3, 5)
+    e_def = E.max_error(E.emulate(M.clone()), M)
+    e_fold = E.max_error(E.emulate(M.clone(), fold_fast=True), M)
+    assert e_def < 2e-2 and e_fold > 0.2, (e_def, e_fold)
