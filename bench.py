@@ -533,9 +533,9 @@ def gpu_arm(args):
     # region over the K steps: start event, then the first copy, ..., the last
     # step's result read back).  Each step's inputs (G and Q/K) are larger than
     # L2, so no flush runs in this region.
-    Gh = [g.to("cpu").pin_memory() for g in Gl]
     feats = [t for t in (q, k, ks) if t is not None]
-    fh = [t.to("cpu").pin_memory() for t in feats]
+    host_block, host_in = pinned_block(Gl + feats)
+    Gh, fh = host_in[:len(Gl)], host_in[len(Gl):]
     out_h = torch.empty(2 * H + 2, dtype=torch.float32).pin_memory()
     h2d = sum(g.numel() * g.element_size() for g in Gh) + sum(t.numel() * t.element_size() for t in fh)
     d2h = out_h.numel() * 4
@@ -602,10 +602,8 @@ def gpu_arm(args):
                 issue_copies((i + 1) % 2)
             e2e_step(i % 2)
 
-    # warm-up: copies that overlap kernels run far below the link's rate for
-    # the first few hundred ms of such overlap in a process (measured 10-20 vs
-    # 208 GB/s), so the pipeline runs ~1.5 s of steps untimed first (a count
-    # from the max-over-ranks step time, the same on every rank)
+    # warm-up: the pipeline runs ~1.5 s of steps untimed first (a count from
+    # the max-over-ranks step time, the same on every rank)
     e2e_run(max(args.warmup, int(math.ceil(1500.0 / max(ms_per_step, 1e-3)))))
     barrier()
     e2e_t0, e2e_t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -618,7 +616,7 @@ def gpu_arm(args):
         t = torch.tensor([e2e_local], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_local = float(t.item())
-    del Gh, fh, G_slots, F_slots
+    del Gh, fh, host_in, host_block, G_slots, F_slots
 
     pk, pk_src = peaks()
     # a roofline kernel timed inside a second or more of back-to-back steps
@@ -754,6 +752,27 @@ def gpu_arm(args):
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def pinned_block(tensors):
+    """Contiguous host copies of `tensors`, as views into ONE pinned block
+    (each at a 256-byte offset).  Host-to-device copies out of one large
+    pinned allocation run at the link's rate (~210 GB/s measured, alone or
+    beside a GEMM loop); out of 128 separately pinned 59 MB tensors the same
+    copies ran erratically, 12-209 GB/s from one pass to the next."""
+    import torch
+    sizes = [t.numel() * t.element_size() for t in tensors]
+    offs, total = [], 0
+    for n in sizes:
+        offs.append(total)
+        total += (n + 255) // 256 * 256
+    block = torch.empty(max(total, 256), dtype=torch.uint8, pin_memory=True)
+    views = []
+    for t, o, n in zip(tensors, offs, sizes):
+        h = block[o:o + n].view(t.dtype).view(t.shape)
+        h.copy_(t)
+        views.append(h)
+    return block, views
 
 
 def ns_precision_text(hp):
