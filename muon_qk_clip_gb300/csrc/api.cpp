@@ -292,9 +292,9 @@ enum Phase { kGram = 1, kPoly = 2, kNext = 3 };
 // fp16 (hi, lo) planes, and every later iteration works on fp16 planes:
 // entries are then bounded (singular values stay below ~1.2) and fp16's 11
 // significand bits make a one-product (hi*hi) step 8x more accurate than
-// bf16's.  The leading iterations take one product per k-step, the trailing
-// ones three (hi*hi + hi*lo + lo*hi) in the polynomial and the update; the
-// trailing Gram products take one.
+// bf16's.  The leading iterations take one product per k-step; the trailing
+// ones take one in the Gram, three (hi*hi + hi*lo + lo*hi) in the polynomial
+// and two or three in the update (below).
 //
 // Float64 emulation of this arithmetic (max error / RMS of the exact result;
 // the bound is 2e-2) over Gaussian inputs and adversarial spectra (64 or 4
