@@ -277,10 +277,18 @@ TRAFFIC_SOURCES = ("muon_qk_clip_gb300/csrc/ns_tc.cu", "muon_qk_clip_gb300/csrc/
 
 
 def traffic_sources_hash():
+    """Hash of the code of TRAFFIC_SOURCES: comments and blank lines are
+    dropped first, so an edit of a comment keeps the captured traffic."""
+    import re
     h = hashlib.sha256()
     for rel in TRAFFIC_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        code = "\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip())
+        h.update(code.encode())
+        h.update(b"\0")
     return h.hexdigest()[:16]
 
 

@@ -85,7 +85,7 @@ def test_traffic_is_taken_only_for_the_profiled_source(bench, tmp_path, monkeypa
     for rel in bench.TRAFFIC_SOURCES:
         f = tmp_path / rel
         f.parent.mkdir(parents=True, exist_ok=True)
-        f.write_text(f"// {rel}\n")
+        f.write_text(f"// {rel}\nint x = 1;  /* a\n comment */\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     h = bench.traffic_sources_hash()
     (tmp_path / "profiles").mkdir()
@@ -94,11 +94,15 @@ def test_traffic_is_taken_only_for_the_profiled_source(bench, tmp_path, monkeypa
     assert bench.traffic_for("moe_experts", 30) == 100
     assert bench.traffic_for("moe_experts", 0) is None
     assert bench.traffic_for("dense_block", 30) is None           # no capture for it
-    for rel in bench.TRAFFIC_SOURCES:                               # any source change voids it
+    for rel in bench.TRAFFIC_SOURCES:                               # any code change voids it
         f = tmp_path / rel
         old = f.read_text()
-        f.write_text(old + "// changed\n")
+        f.write_text(old + "int changed;\n")
         assert bench.traffic_for("moe_experts", 30) is None, rel
+        f.write_text(old.replace("int x = 1;", "int x = 2;"))
+        assert bench.traffic_for("moe_experts", 30) is None, rel
+        f.write_text(old + "// a comment\n\n/* another */\n")     # comments do not
+        assert bench.traffic_for("moe_experts", 30) == 100, rel
         f.write_text(old)
     assert bench.traffic_for("moe_experts", 30) == 100
 
