@@ -763,11 +763,11 @@ def gpu_arm(args):
 
 
 def pinned_block(tensors):
-    """Contiguous host copies of `tensors`, as views into ONE pinned block
-    (each at a 256-byte offset).  Host-to-device copies out of one large
-    pinned allocation run at the link's rate (~210 GB/s measured, alone or
-    beside a GEMM loop); out of 128 separately pinned 59 MB tensors the same
-    copies ran erratically, 12-209 GB/s from one pass to the next."""
+    """Contiguous host copies of `tensors`, as views into one pinned block
+    (each at a 256-byte offset): one pinned allocation for the whole input
+    set.  Beside a GEMM loop, copies out of it held ~210 GB/s where 128
+    separately pinned 59 MB tensors were measured alternating between 26 and
+    209 GB/s from pass to pass."""
     import torch
     sizes = [t.numel() * t.element_size() for t in tensors]
     offs, total = [], 0
