@@ -237,24 +237,18 @@ def ns_products(rows, cols, steps, fast_steps, split=True):
     """Tensor-core products per k-step of each iteration's (Gram, polynomial,
     update) under the library's plan: one (hi*hi) in the leading iterations
     (up to three, keeping two three-term iterations after them, from a
-    smaller side of 256; four with fast_steps >= 4 from 1024, keeping one),
-    then one in the Gram and three (hi*hi + hi*lo + lo*hi) in the polynomial
-    and update; matrices with a smaller side under 256 take three everywhere.
-    With two or more three-term iterations, the updates of the last two
-    iterations take two (hi*hi + hi*lo of X) from a smaller side of 512
-    (iteration 2 onwards)."""
+    smaller side of 256), then one in the Gram and three (hi*hi + hi*lo +
+    lo*hi) in the polynomial and update; matrices with a smaller side under
+    256 take three everywhere.  The updates of the last two iterations take
+    two (hi*hi + hi*lo of X) from a smaller side of 512 (iteration 2
+    onwards)."""
     if not split:
         return [(1, 1, 1)] * steps
     side = min(rows, cols)
-    if side < 256:
-        nf = 0
-    elif fast_steps >= 4 and side >= 1024:
-        nf = min(fast_steps, max(0, steps - 1))
-    else:
-        nf = min(fast_steps, 3, max(0, steps - 2))
+    nf = 0 if side < 256 else min(fast_steps, 3, max(0, steps - 2))
     trail = (1, 3, 3) if side >= 256 else (3, 3, 3)
     out = [(1, 1, 1) if it < nf else trail for it in range(steps)]
-    if steps >= 2 and nf <= steps - 2 and side >= 512:
+    if steps >= 2 and side >= 512:
         for it in range(max(1, steps - 2), steps):
             out[it] = (out[it][0], out[it][1], 2)
     return out

@@ -114,21 +114,19 @@ typedef struct {
   int32_t ns_precision;/* mc_ns_precision                                    */
   int32_t ns_fast_steps;/* MC_NS_SPLIT_BF16 only: this many leading iterations
                           take one product (hi*hi) per k-step, for matrices
-                          whose smaller side is at least 256: up to three,
-                          each run keeping at least two iterations after it,
-                          whose Gram products take one product and whose
-                          polynomial takes three and whose update two
-                          (hi*hi + hi*lo of X; three when the smaller side
-                          is under 512).  Float64 emulation of this
-                          arithmetic gives at most 1.05e-2 of RMS (512 x 2048
-                          adversarial spectrum, a few dominant directions
-                          over a 1e-3 rest; 2048 x 7168 Gaussian: 5.2e-3;
-                          512 x 16384 Gaussian: 9.3e-3).  A value >= 4 allows
-                          four (keeping one) for matrices whose smaller side
-                          is at least 1024: fewer products, at most 1.0e-2 of
-                          RMS (1024 x 1536 Gaussian).  Matrices whose smaller
-                          side is under 256 take three products everywhere
-                          (1.4e-2 at 64 otherwise).  Default 3. */
+                          whose smaller side is at least 256: up to three
+                          (larger values act as three), each run keeping at
+                          least two iterations after it, whose Gram products
+                          take one product and whose polynomial takes three
+                          and whose update two (hi*hi + hi*lo of X; three
+                          when the smaller side is under 512).  Float64
+                          emulation of this arithmetic gives at most 1.2e-2
+                          of RMS (2048 x 7168 adversarial spectrum, 64
+                          dominant directions over a 1e-3 rest; 2048 x 7168
+                          Gaussian: 3-5e-3; 512 x 16384 Gaussian: 9.3e-3).
+                          Matrices whose smaller side is under 256 take three
+                          products everywhere (1.4e-2 at 64 otherwise).
+                          Default 3. */
   int32_t scale_mode;  /* mc_scale_mode: factor on NewtonSchulz(M)            */
 } mc_hparams;
 

@@ -297,44 +297,40 @@ enum Phase { kGram = 1, kPoly = 2, kNext = 3 };
 // and two or three in the update (below).
 //
 // Float64 emulation of this arithmetic (max error / RMS of the exact result;
-// the bound is 2e-2) over Gaussian inputs and adversarial spectra (64 or 4
-// unit directions over a 1e-3 rest), sides 64 to 2048 x 7168:
-//   - three leading one-product iterations (ns_fast_steps = 3): at most
-//     8.2e-3 from a smaller side of 256 (512 x 16384 Gaussian; 2048 x 7168:
-//     3.9e-3, about what every product split gives there); 1.4e-2 at 64;
-//   - four (ns_fast_steps >= 4): at most 1.0e-2 from 1024 (1024 x 1536
-//     Gaussian; 2048 x 7168: 9.5e-3), 9.8e-3 at 256 and 3.7e-2 at 512 x 16384;
-// so the one-product iterations run from a smaller side of kFastMinSide
-// (three) and kFast4MinSide (four); smaller matrices take three products in
-// every phase (2.8e-3 at 64).  With two trailing three-term iterations
-// their updates may also drop lo(B') x hi(X), B' = a I + b A + c A^2: at most
-// 1.05e-2 from a smaller side of 512 (512 x 2048 adversarial; 2048 x 7168
-// Gaussian: 5.2e-3), 1.3e-2 at 256, so they take two products (hi*hi + hi*lo
-// of X) from kTrail2MinSide.  Dropping hi(B') x lo(X) instead gives ~2e-2.
+// the bound is 2e-2) over Gaussian inputs and adversarial spectra (64, 16 or 4
+// unit directions over a 1e-3 rest), sides 64 to 2048 x 16384:
+//   - three leading one-product iterations (ns_fast_steps = 3) with
+//     three-product trailing iterations: at most 8.2e-3 from a smaller side
+//     of 256 (512 x 16384 Gaussian), 1.4e-2 at 64; so the one-product
+//     iterations run from a smaller side of kFastMinSide and smaller matrices
+//     take three products in every phase (2.8e-3 at 64);
+//   - the updates of the two trailing iterations may then drop lo(B') x hi(X),
+//     B' = a I + b A + c A^2: at most 1.2e-2 from a smaller side of 512
+//     (2048 x 7168 adversarial, 64 directions; 512 x 16384 Gaussian: 9.3e-3),
+//     1.3e-2 at 256, so they take two products (hi*hi + hi*lo of X) from
+//     kTrail2MinSide.  Dropping hi(B') x lo(X) instead gives ~2e-2;
+//   - a fourth one-product iteration is not offered: 2.0-2.3e-2 at 1024 x 4096
+//     and 1024 x 16384 Gaussian, for ~1 % of a call once the trailing updates
+//     take two products.
 constexpr int kFastMinSide = 256;
-constexpr int kFast4MinSide = 1024;
 constexpr int kTrail2MinSide = 512;
 
 // Leading one-product iterations of a shape group whose smaller side is
-// `side`: up to three with at least two three-term iterations after them,
-// or four (ns_fast_steps >= 4, side >= kFast4MinSide) with at least one.
+// `side`: up to three, with at least two three-term iterations after them.
 int ns_fast_iterations(const mc_hparams* hp, int side) {
   if (side < kFastMinSide) return 0;
-  if (hp->ns_fast_steps >= 4 && side >= kFast4MinSide)
-    return std::min(hp->ns_fast_steps, std::max(0, hp->ns_steps - 1));
   return std::min({hp->ns_fast_steps, 3, std::max(0, hp->ns_steps - 2)});
 }
 
 // Products per k-step (1: hi*hi; 2: hi*hi + hi*lo_B; 3: hi*hi + hi*lo +
 // lo*hi) of phase `ph` of iteration `it` on the split iterate.  Two in the
-// updates of the last two iterations of a plan that keeps them three-term,
-// on fp16 planes (it >= 1).
+// updates of the last two iterations (three-term: the leading one-product
+// iterations always leave two), on fp16 planes (it >= 1).
 int ns_terms(const mc_hparams* hp, int side, int it, int ph) {
   const int nf = ns_fast_iterations(hp, side);
   if (it < nf) return 1;
   if (ph == kGram && side >= kFastMinSide) return 1;
-  if (ph == kNext && it >= 1 && it >= hp->ns_steps - 2 && side >= kTrail2MinSide && nf <= hp->ns_steps - 2)
-    return 2;
+  if (ph == kNext && it >= 1 && it >= hp->ns_steps - 2 && side >= kTrail2MinSide) return 2;
   return 3;
 }
 

@@ -54,11 +54,11 @@ def test_products_per_iteration(bench):
     assert bench.ns_products(128, 7168, 5, 3) == [S] * 5              # smaller side < 256
     assert bench.ns_products(256, 7168, 5, 3) == [F, F, F, G1, G1]    # < 512: three
     assert bench.ns_products(1024, 1536, 5, 3) == [F, F, F, G2, G2]
-    assert bench.ns_products(1024, 1536, 5, 4) == [F, F, F, F, G1]   # a fourth from 1024
-    assert bench.ns_products(512, 1536, 5, 4) == [F, F, F, G2, G2]   # not below it
+    assert bench.ns_products(1024, 1536, 5, 4) == [F, F, F, G2, G2]   # at most three
+    assert bench.ns_products(512, 1536, 5, 4) == [F, F, F, G2, G2]
     assert bench.ns_products(2048, 5632, 5, 2) == [F, F, G1, G2, G2]
     assert bench.ns_products(2048, 5632, 4, 3) == [F, F, G2, G2]     # two three-term kept
-    assert bench.ns_products(2048, 5632, 4, 4) == [F, F, F, G1]      # one kept
+    assert bench.ns_products(2048, 5632, 4, 4) == [F, F, G2, G2]
     assert bench.ns_products(2048, 2048, 5, 0) == [G1] * 3 + [G2] * 2
     assert bench.ns_products(2048, 2048, 2, 0) == [G1, G2]            # iteration 1: bf16 planes
     assert bench.ns_products(2048, 2048, 1, 0) == [G1]

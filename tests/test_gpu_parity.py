@@ -118,9 +118,9 @@ def test_ns_split_bf16_parity(case, out_dtype):
 @pytest.mark.parametrize("case", ["batched", "ragged_groups", "large"])
 def test_ns_split_fast_steps(case, fast_steps):
     """Leading iterations with one product (hi operands) per k-step: every
-    setting stays in tolerance.  The 512 x 512 and 256 x 768 matrices take up
-    to three, the 1024 x 1536 one up to four; the ragged groups' matrices
-    (smaller side under 256) keep three products throughout."""
+    setting stays in tolerance.  Every matrix of smaller side 256 or more
+    takes up to three (4 acts as 3); the ragged groups' matrices (smaller side
+    under 256) keep three products throughout."""
     Os, ref = run_ns(NS_CASES[case], abi.MC_NS_SPLIT_BF16, F32, fast_steps=fast_steps)
     for o, want in zip(Os, ref):
         assert_rounded_within(o, want, 2e-2 * rms(want), f"NS fast={fast_steps} {case}")
@@ -727,13 +727,13 @@ def test_step_with_many_shape_groups():
 
 @pytest.mark.parametrize("kind", ["gauss", "few64"])
 def test_ns_fast_iterations_2048(kind):
-    """Three leading one-product iterations (the default) and four (opt-in,
-    smaller side >= 1024) on a 2048 x 2048 input, Gaussian or 64 unit
-    directions over a 1e-3 rest.  float64 emulation of the arithmetic gives
-    2.7e-3 / 5.3e-3 of RMS (three / four one-product iterations) on the
-    Gaussian input and 4.2e-3 / 4.0e-3 with the 64 directions: inside the 2e-2
-    bound.  The two plans must differ,
-    which shows the fourth one-product iteration ran."""
+    """Three leading one-product iterations (the default) on a 2048 x 2048
+    input, Gaussian or 64 unit directions over a 1e-3 rest.  float64
+    emulation of the arithmetic (tests/ns_emulation.py, the same inputs)
+    gives 4.3e-3 and 1.02e-2 of RMS: inside the 2e-2 bound.  A larger
+    ns_fast_steps acts as three (a fourth one-product iteration emulates at
+    2.0-2.3e-2 on 1024 x 4096 and 1024 x 16384 Gaussian inputs), so its
+    output is bit-identical."""
     m = n = 2048
     rng = np.random.default_rng(4096 + len(kind))
     G = rng.standard_normal((m, n))
@@ -753,10 +753,9 @@ def test_ns_fast_iterations_2048(kind):
     ohp = O.Hparams(rms_scale=fp32(hp.rms_scale), ns_coeffs=tuple(fp32(c) for c in hp.ns_coeffs),
                     ns_eps=fp32(hp.ns_eps), ns_steps=hp.ns_steps)
     ref = O.muon_direction(f64(M), ohp)
-    for fast, o in outs.items():
-        err = np.abs(o - ref).max() / rms(ref)
-        assert err <= 2e-2, f"fast={fast}: max |O - O_exact| = {err:.4g} of RMS"
-    assert not np.array_equal(outs[3], outs[4])
+    err = np.abs(outs[3] - ref).max() / rms(ref)
+    assert err <= 2e-2, f"max |O - O_exact| = {err:.4g} of RMS"
+    assert np.array_equal(outs[3], outs[4])
 
 
 @pytest.mark.parametrize("m,n", [(1024, 2048), (256, 512)])
