@@ -120,8 +120,8 @@ typedef struct {
                           take one product and whose polynomial takes three
                           and whose update two (hi*hi + hi*lo of X; three
                           when the smaller side is under 512).  Float64
-                          emulation of this arithmetic gives at most 1.2e-2
-                          of RMS (2048 x 7168 adversarial spectrum, 64
+                          emulation of this arithmetic gives at most 1.4e-2
+                          of RMS (2048 x 16384 adversarial spectrum, 64
                           dominant directions over a 1e-3 rest; 2048 x 7168
                           Gaussian: 3-5e-3; 512 x 16384 Gaussian: 9.3e-3).
                           Matrices whose smaller side is under 256 take three

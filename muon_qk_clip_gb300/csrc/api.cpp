@@ -305,10 +305,11 @@ enum Phase { kGram = 1, kPoly = 2, kNext = 3 };
 //     iterations run from a smaller side of kFastMinSide and smaller matrices
 //     take three products in every phase (2.8e-3 at 64);
 //   - the updates of the two trailing iterations may then drop lo(B') x hi(X),
-//     B' = a I + b A + c A^2: at most 1.2e-2 from a smaller side of 512
-//     (2048 x 7168 adversarial, 64 directions; 512 x 16384 Gaussian: 9.3e-3),
-//     1.3e-2 at 256, so they take two products (hi*hi + hi*lo of X) from
-//     kTrail2MinSide.  Dropping hi(B') x lo(X) instead gives ~2e-2;
+//     B' = a I + b A + c A^2: at most 1.4e-2 from a smaller side of 512
+//     (2048 x 16384 adversarial, 64 directions: 1.37e-2 against 7.9e-3 with
+//     three products; 512 x 16384 Gaussian: 9.3e-3), so they take two
+//     products (hi*hi + hi*lo of X) from kTrail2MinSide (1.3e-2 already at
+//     256 x 2048).  Dropping hi(B') x lo(X) instead gives ~2e-2;
 //   - a fourth one-product iteration is not offered: 2.0-2.3e-2 at 1024 x 4096
 //     and 1024 x 16384 Gaussian, for ~1 % of a call once the trailing updates
 //     take two products.
