@@ -758,19 +758,21 @@ def test_ns_fast_iterations_2048(kind):
     assert np.array_equal(outs[3], outs[4])
 
 
-@pytest.mark.parametrize("m,n", [(1024, 2048), (256, 512)])
-def test_ns_adversarial_spectrum(m, n):
-    """A spectrum of 16 unit directions over a near-null rest (1e-3), an
-    adversarial case for the one-product leading iterations (three run at
-    both sizes).  The directions 1e-3 below the largest are amplified ~500x by
-    the iteration, so their rounding in the first iterations matters most.
-    float64 emulation of the arithmetic gives 4.1e-3 of RMS at 1024 x 2048 and
-    4.6e-3 at 256 x 512: within the 2e-2 bound."""
-    rng = np.random.default_rng(m)
+@pytest.mark.parametrize("m,n,k", [(1024, 2048, 16), (256, 512, 16), (1024, 16384, 64)])
+def test_ns_adversarial_spectrum(m, n, k):
+    """A spectrum of k unit directions over a near-null rest (1e-3), an
+    adversarial case for the split arithmetic (three one-product leading
+    iterations at every size; two-product trailing updates from a smaller
+    side of 512).  The directions 1e-3 below the largest are amplified ~500x
+    by the iteration, so their rounding matters most.  float64 emulation of
+    the arithmetic (tests/ns_emulation.py, the same inputs) gives 8.4e-3 of
+    RMS at 1024 x 2048, 7.7e-3 at 256 x 512 and 1.3e-2 at 1024 x 16384 with
+    64 directions, near the plan's worst case: within the 2e-2 bound."""
+    rng = np.random.default_rng(m if k == 16 else m + n)
     G = rng.standard_normal((m, n))
     U, s, Vt = np.linalg.svd(G, full_matrices=False)
     s2 = np.full(len(s), 1e-3)
-    s2[:16] = 1.0
+    s2[:k] = 1.0
     M = torch.tensor((U * s2) @ Vt, dtype=torch.float32)
     hp = mc.Hparams(ns_precision=abi.MC_NS_SPLIT_BF16)
     O_dev = torch.empty(m, n, dtype=torch.float32, device="cuda")
