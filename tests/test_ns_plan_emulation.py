@@ -17,6 +17,20 @@ def test_default_plan_within_bound():
         assert e2 < 3 * e3, (e2, e3)
 
 
+def test_default_plan_on_a_wide_adversarial_matrix():
+    """The plan's worst inputs are wide matrices with a few dominant
+    directions over a 1e-3 rest (2048 x 16384 with 64: 1.37e-2 of RMS).  At
+    512 x 16384 the default stays under 1.6e-2 (1.16e-2 emulated) and within
+    2x of three-product trailing updates (6.6e-3); the rejected choice of two
+    products (hi(B') lo(X) dropped) breaks the 2e-2 bound (2.8e-2)."""
+    M = E.adversarial(512, 16384, 64, 1e-3, 51)
+    e2 = E.max_error(E.emulate(M.clone()), M)
+    e3 = E.max_error(E.emulate(M.clone(), last_update=3, trailing_updates=3), M)
+    ex = E.max_error(E.emulate(M.clone(), last_update="2x", trailing_updates="2x"), M)
+    assert e2 < 1.6e-2 and e2 < 2 * e3, (e2, e3)
+    assert ex > 2e-2, ex
+
+
 def test_the_dropped_product_is_the_cheaper_one():
     """Of the two cross products, dropping lo(B') hi(X) keeps the error near
     1e-2; dropping hi(B') lo(X) instead roughly doubles it (to the bound) on
