@@ -124,6 +124,88 @@ def _rms_norm_eps_outside(x, eps=1e-6):
     x = np.asarray(x, np.float64)
     return x / (np.sqrt(np.mean(x * x, axis=-1, keepdims=True)) + eps)
 
+def _clip_factors_at_tau(smax, tau):
+    # S = tau clips (the pseudocode skips S <= tau)
+    smax = np.asarray(smax, np.float64)
+    mask = smax >= tau
+    gamma = np.ones_like(smax)
+    gamma[mask] = tau / smax[mask]
+    return gamma, mask
+
+
+def _clip_factors_inverted(smax, tau):
+    smax = np.asarray(smax, np.float64)
+    mask = smax > tau
+    gamma = np.ones_like(smax)
+    gamma[mask] = smax[mask] / tau
+    return gamma, mask
+
+
+def _qk_clip_head_rows_by_height(weights, segments, smax, tau):
+    # head h's block found at h * rows instead of h * stride
+    gamma, mask = O.clip_factors(smax, tau)
+    out = {k: np.array(v, np.float64) for k, v in weights.items()}
+    for seg in segments:
+        W = out[seg.name]
+        for h in np.nonzero(mask)[0]:
+            r0 = seg.offset + h * seg.rows
+            W[r0:r0 + seg.rows] *= gamma[h] ** seg.exponent
+    return out, gamma, mask
+
+
+def _total_clip_smallest_head(smax, tau):
+    s = float(np.min(smax))
+    return tau / s if s > tau else 1.0
+
+
+def _update_scale_spectral_inverted(rows, cols, hp):
+    if hp.scale_mode == "spectral":
+        return np.sqrt(max(1.0, cols / rows))
+    return np.sqrt(max(rows, cols)) * hp.rms_scale
+
+
+def _mha_segments_alpha_swapped(H, d, alpha=0.5):
+    return [O.ClipSegment("Wq", 0, d, d, 1.0 - alpha), O.ClipSegment("Wk", 0, d, d, alpha)]
+
+
+def _newton_schulz_max_abs_normalised(M, steps=5, coeffs=O.DEFAULT_NS_COEFFS, eps=1e-7):
+    M = np.asarray(M, np.float64)
+    t = M.shape[0] > M.shape[1]
+    X = M.T if t else M
+    X = O.ns_iterate(X / (np.abs(X).max() + eps), steps, coeffs)
+    return X.T if t else X
+
+
+def _head_keys_shared_first(K, K_shared, b, h):
+    k = np.asarray(K[b, :, h, :], np.float64)
+    if K_shared is not None:
+        k = np.concatenate([np.asarray(K_shared[b], np.float64), k], axis=1)
+    return k
+
+
+def _muonclip_step_clip_first(weights, grads, moms, hp, layers=()):
+    W = {k: np.array(v, np.float64) for k, v in weights.items()}
+    gammas = []
+    for smax, segs in layers:
+        W, gamma, _ = O.qk_clip(W, segs, smax, hp.tau)
+        gammas.append(gamma)
+    W_new, M_new = {}, {}
+    for name in W:
+        W_new[name], M_new[name], _ = O.muon_step(W[name], grads[name], moms[name], hp)
+    return W_new, M_new, gammas
+
+
+def _momentum_dampened(M_prev, G, mu):
+    return mu * np.asarray(M_prev, np.float64) + (1.0 - mu) * np.asarray(G, np.float64)
+
+
+_max_logit = O.max_logit
+
+
+def _max_logit_scale_one_over_d(Q, K, K_shared=None, causal=True, scale=None, row_chunk=2048):
+    return _max_logit(Q, K, K_shared, causal, 1.0 / Q.shape[-1] if scale is None else scale, row_chunk)
+
+
 MUTATIONS = [
     ("ns_iterate", _ns_dropped_quintic, [P.test_golden_newton_schulz_one_step]),
     ("ns_iterate", _ns_wrong_sign, [P.test_golden_newton_schulz_one_step]),
@@ -141,6 +223,19 @@ MUTATIONS = [
     ("rope", _rope_frequency_over_d_half, [P.test_rope_hand_worked_angles]),
     ("rms_norm", _rms_norm_mean_abs, [P.test_rms_norm_unit_rms_scale_invariance_and_hand_value]),
     ("rms_norm", _rms_norm_eps_outside, [P.test_rms_norm_unit_rms_scale_invariance_and_hand_value]),
+    ("clip_factors", _clip_factors_at_tau, [P.test_clip_factors_edges]),
+    ("clip_factors", _clip_factors_inverted, [P.test_clip_factors_edges]),
+    ("qk_clip", _qk_clip_head_rows_by_height, [P.test_clip_mla_remeasured_and_shared_key_untouched]),
+    ("total_clip_factor", _total_clip_smallest_head, [P.test_total_clip_variant]),
+    ("update_scale", _update_scale_spectral_inverted,
+     [lambda: P.test_spectral_scale_gives_unit_or_aspect_norm((50, 20))]),
+    ("mha_segments", _mha_segments_alpha_swapped, [lambda: P.test_clip_mha_alpha_split(0.25)]),
+    ("newton_schulz", _newton_schulz_max_abs_normalised,
+     [lambda: P.test_ns_svd_closed_form((24, 40), P.QUINTIC, 1)]),
+    ("head_keys", _head_keys_shared_first, [lambda: P.test_max_logit_brute_force(True, True)]),
+    ("muonclip_step", _muonclip_step_clip_first, [P.test_muonclip_step_order_muon_then_clip]),
+    ("momentum", _momentum_dampened, [P.test_momentum_closed_form]),
+    ("max_logit", _max_logit_scale_one_over_d, [P.test_max_logit_single_token]),
 ]
 
 
