@@ -124,6 +124,12 @@ def _rms_norm_eps_outside(x, eps=1e-6):
     x = np.asarray(x, np.float64)
     return x / (np.sqrt(np.mean(x * x, axis=-1, keepdims=True)) + eps)
 
+def _mla_segments_sqrt_gamma_on_qr(H, d_nope=128, d_rope=64, d_v=128):
+    dq, dkv = d_nope + d_rope, d_nope + d_v
+    return [O.ClipSegment("W_UQ", 0, dq, d_nope, 0.5), O.ClipSegment("W_UQ", d_nope, dq, d_rope, 0.5),
+            O.ClipSegment("W_UKV", 0, dkv, d_nope, 0.5)]
+
+
 def _clip_factors_at_tau(smax, tau):
     # S = tau clips (the pseudocode skips S <= tau)
     smax = np.asarray(smax, np.float64)
@@ -223,6 +229,7 @@ MUTATIONS = [
     ("rope", _rope_frequency_over_d_half, [P.test_rope_hand_worked_angles]),
     ("rms_norm", _rms_norm_mean_abs, [P.test_rms_norm_unit_rms_scale_invariance_and_hand_value]),
     ("rms_norm", _rms_norm_eps_outside, [P.test_rms_norm_unit_rms_scale_invariance_and_hand_value]),
+    ("mla_segments", _mla_segments_sqrt_gamma_on_qr, [P.test_clip_mla_remeasured_and_shared_key_untouched]),
     ("clip_factors", _clip_factors_at_tau, [P.test_clip_factors_edges]),
     ("clip_factors", _clip_factors_inverted, [P.test_clip_factors_edges]),
     ("qk_clip", _qk_clip_head_rows_by_height, [P.test_clip_mla_remeasured_and_shared_key_untouched]),
